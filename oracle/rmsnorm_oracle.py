@@ -1,0 +1,179 @@
+"""Plain fp64 CPU oracle for row-wise RMSNorm, forward and backward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this module.  The CUDA
+library never calls it and shares no code with it; the only thing both sides
+share is the seeded input generator in ``synthetic/``.
+
+Every function evaluates the textbook definition directly in float64 on the
+exact values of the (already dtype-rounded) inputs: no blocking, fusion or
+reordering beyond what the definition states.  Library primitives used as
+steps: ``np.mean`` / ``np.sum`` (the row mean and the column sum), ``np.sqrt``.
+
+Sources (web pages on row-wise RMS normalisation):
+
+* [TUT] "Hướng dẫn Triton RMSNorm: kernel, backward…" (partitech.com):
+  - § "Vấn đề và công thức tham chiếu": r = 1/sqrt(mean(x²)+eps),
+    y = x·r·gamma, eps added under the square root;
+  - § "Vì sao cần một lượt đi và một lượt về?": u = dy·gamma,
+    dx = r·u − x·r³·mean(u·x) (mean over the N columns of a row),
+    dgamma = Σ_rows dy·x·r (a sum over the M rows);
+  - § "Lập phương của r từ đâu?": ∂r/∂x_i = −x_i·r³/N;
+  - § "N và BLOCK: hai kích thước không được nhầm": divide by the true N.
+* [UNS] "02 · 手写 Triton kernel:RMSNorm / RoPE / SwiGLU", § 3 (RMSNorm):
+  - the alternative closed form dX = inv_var/n·(n·dY_W − normed·Σ(dY_W·normed));
+  - Gemma weight semantics (1 + W);
+  - § 2 item 3 and § 3: normed is cast to the weight dtype, then multiplied
+    by the weight (the order ``emulate_forward_lowp`` reproduces).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against values
+the pages print, closed forms, invariants, finite differences and
+``torch.nn.functional.rms_norm`` in float64; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def weight(gamma, gemma: int = 0) -> np.ndarray:
+    """Effective per-column weight g: gamma, or 1 + gamma for Gemma ([UNS] § 3)."""
+    g = _f64(gamma)
+    return 1.0 + g if gemma else g
+
+
+def rms_rstd(x, eps: float) -> np.ndarray:
+    """r_i = 1 / sqrt(mean_j x_ij² + eps), mean over the true N ([TUT] reference formula)."""
+    x = _f64(x)
+    ms = np.mean(x * x, axis=-1)
+    return 1.0 / np.sqrt(ms + eps)
+
+
+def rms_forward(x, gamma, eps: float, gemma: int = 0):
+    """y_ij = x_ij · r_i · g_j and r ([TUT] reference formula; [UNS] § 3 for Gemma).
+
+    Returns (y, r) in float64; x is (M, N), gamma is (N,).
+    """
+    x = _f64(x)
+    r = rms_rstd(x, eps)
+    y = x * r[:, None] * weight(gamma, gemma)[None, :]
+    return y, r
+
+
+def rms_backward(x, gamma, dy, eps: float, gemma: int = 0, with_scales: bool = False):
+    """Closed-form gradients of L = Σ dy ⊙ y ([TUT] backward formulas).
+
+    u = dy · g;  c_i = mean_j(u_ij · x_ij);  dx = r·u − x·r³·c;
+    dgamma_j = Σ_i dy_ij · x_ij · r_i  (a sum over rows, not a mean; for
+    Gemma the same, since d(1+gamma)/dgamma = 1).
+
+    With ``with_scales`` it also returns the magnitudes the two outputs are
+    built from, used to scale tolerances where the terms cancel:
+    ``dx_scale = r·|u| + |x|·r³·|c|`` and ``dgamma_scale = Σ_i |dy·x·r|``.
+    """
+    x = _f64(x)
+    dy = _f64(dy)
+    r = rms_rstd(x, eps)
+    u = dy * weight(gamma, gemma)[None, :]
+    c = np.mean(u * x, axis=-1)
+    r3 = r ** 3
+    dx = r[:, None] * u - x * (r3 * c)[:, None]
+    dgamma = np.sum(dy * x * r[:, None], axis=0)
+    if not with_scales:
+        return dx, dgamma
+    dx_scale = r[:, None] * np.abs(u) + np.abs(x) * (r3 * np.abs(c))[:, None]
+    dgamma_scale = np.sum(np.abs(dy * x * r[:, None]), axis=0)
+    return dx, dgamma, dx_scale, dgamma_scale
+
+
+def rms_backward_normed_form(x, gamma, dy, eps: float, gemma: int = 0):
+    """dx in [UNS] § 3's form: inv_var/n · (n·dY_W − normed·Σ_j(dY_W·normed)).
+
+    normed = x·r, dY_W = dy·g.  Algebraically equal to ``rms_backward``'s dx.
+    """
+    x = _f64(x)
+    dy = _f64(dy)
+    n = x.shape[-1]
+    r = rms_rstd(x, eps)
+    normed = x * r[:, None]
+    dyw = dy * weight(gamma, gemma)[None, :]
+    s = np.sum(dyw * normed, axis=-1)
+    return (r / n)[:, None] * (n * dyw - normed * s[:, None])
+
+
+def loss(x, gamma, dy, eps: float, gemma: int = 0) -> float:
+    """Scalar L = Σ_ij dy_ij · y_ij(x, gamma), whose gradients rms_backward gives."""
+    y, _ = rms_forward(x, gamma, eps, gemma)
+    return float(np.sum(_f64(dy) * y))
+
+
+def fd_gradients(x, gamma, dy, eps: float, gemma: int = 0, h_rel: float = 1e-6):
+    """Central differences (L(a+h) − L(a−h)) / 2h of ``loss`` for every entry
+    of x and gamma ([TUT] § "Tham chiếu PyTorch: oracle số học", gradcheck).
+
+    h = h_rel · max(1, |a|).  Pure-Python loops: tiny inputs only.
+    """
+    x = _f64(x).copy()
+    g = _f64(gamma).copy()
+    dx = np.zeros_like(x)
+    dg = np.zeros_like(g)
+    for idx in np.ndindex(*x.shape):
+        a = x[idx]
+        h = h_rel * max(1.0, abs(a))
+        x[idx] = a + h
+        lp = loss(x, g, dy, eps, gemma)
+        x[idx] = a - h
+        lm = loss(x, g, dy, eps, gemma)
+        x[idx] = a
+        dx[idx] = (lp - lm) / (2.0 * h)
+    for j in range(g.shape[0]):
+        a = g[j]
+        h = h_rel * max(1.0, abs(a))
+        g[j] = a + h
+        lp = loss(x, g, dy, eps, gemma)
+        g[j] = a - h
+        lm = loss(x, g, dy, eps, gemma)
+        g[j] = a
+        dg[j] = (lp - lm) / (2.0 * h)
+    return dx, dg
+
+
+# --- low-precision cast-order emulation ------------------------------------
+
+def _round_f32(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64).astype(np.float32)
+
+
+def _round_bf16(a) -> np.ndarray:
+    """float32 values rounded to the nearest bfloat16, ties to even (finite inputs)."""
+    f = np.ascontiguousarray(_round_f32(a))
+    bits = f.view(np.uint32).astype(np.uint64)
+    keep = (bits >> 16) & 1
+    rounded = ((bits + 0x7FFF + keep) >> 16) << 16
+    return rounded.astype(np.uint32).view(np.float32)
+
+
+def emulate_forward_lowp(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf16"):
+    """The forward as a fp32-accumulating kernel with ``dtype`` I/O rounds it.
+
+    Follows the cast order of [UNS] § 3: normed = fp32(x·r) is rounded to the
+    weight dtype first, then multiplied by the weight in fp32 and rounded
+    again.  For Gemma the weight (1+gamma) is formed in fp32 and the product
+    x·r·(1+gamma) is rounded once (the pages state no order there).  r is the
+    fp64 value rounded to fp32.  Returns float64 values of the rounded y.
+    """
+    rnd = _round_bf16 if dtype == "bf16" else _round_f32
+    xf = _round_f32(x)
+    gf = _round_f32(gamma)
+    r32 = _round_f32(rms_rstd(x, eps))
+    xr = _round_f32(xf.astype(np.float64) * r32[:, None])
+    if gemma:
+        w = _round_f32(1.0 + gf.astype(np.float64))
+        y = rnd(_round_f32(xr.astype(np.float64) * w[None, :]))
+    else:
+        normed = rnd(xr)
+        y = rnd(_round_f32(normed.astype(np.float64) * gf[None, :]))
+    return y.astype(np.float64)

@@ -1,0 +1,182 @@
+"""Seeded synthetic inputs for RMSNorm row workloads.
+
+Every tensor is drawn in float64 from numpy's SFC64 bit generator, seeded by
+``SeedSequence([seed, tensor_id])`` so that x, gamma, dy and the row scales
+are independent streams.  Values are drawn row-chunk by row-chunk (a fixed
+chunk size per workload), transformed by the distribution's affine map and
+the optional per-row scale, then rounded to the I/O dtype:
+
+* ``f32``  : float64 -> float32, round to nearest even (numpy ``astype``);
+* ``bf16`` : float64 -> float32 (RNE) -> bfloat16 (RNE on the 16 dropped
+  mantissa bits).  bf16 tensors are returned as their ``uint16`` bit
+  patterns, which is how both the CUDA side (viewed as ``torch.bfloat16``)
+  and the oracle side (decoded exactly with ``storage_to_float64``) read
+  them.
+
+The rounded tensor is the one input both sides see.  Nothing here computes
+any part of the normalisation.
+
+Distributions are written ``("normal", mean, std)``, ``("uniform", lo, hi)``
+and, for the per-row scale, ``("loguniform", a, b)``: ``s_i = exp(U(ln a,
+ln b))`` multiplied into row i of x.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+from typing import Optional, Tuple
+
+import numpy as np
+
+_TENSOR_IDS = {"x": 1, "gamma": 2, "dy": 3, "row_scale": 4}
+_CHUNK_ELEMS = 1 << 22
+
+Dist = Tuple[str, float, float]
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic RMSNorm workload: shapes, dtype, eps, flags and input laws."""
+
+    name: str
+    M: int
+    N: int
+    dtype: str  # "f32" or "bf16"
+    eps: float
+    x: Dist = ("normal", 0.0, 1.0)
+    gamma: Dist = ("uniform", 0.5, 1.5)
+    dy: Dist = ("normal", 0.0, 1.0)
+    row_scale: Optional[Dist] = None
+    gemma: int = 0
+    inplace_dx: int = 0
+    seed: int = 0
+    note: str = field(default="", compare=False)
+
+    @property
+    def elem_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def with_shape(self, M: int, N: Optional[int] = None, name: Optional[str] = None) -> "Workload":
+        return replace(self, M=M, N=self.N if N is None else N,
+                       name=name or f"{self.name}@{M}x{self.N if N is None else N}")
+
+
+def _sweep(N: int) -> Workload:
+    M = (1 << 27) // N  # x is 256 MiB of bf16, rounded down when N does not divide 2^27
+    return Workload(name=f"sweep_bf16_N{N}", M=M, N=N, dtype="bf16", eps=1e-6,
+                    note="row-width sweep, x ~ 256 MiB")
+
+
+# The five workload families of the row-wise RMSNorm benchmark, plus the
+# extra parity shapes the pages single out (N=257 vs 256, M=1 vs 17, the
+# 128x257 fp32 timing shape, the 1151x8192 LayerNorm test shape).
+WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("tiny_f32_64x128", 64, 128, "f32", 1e-6,
+                 note="tiny fp32 fwd+bwd"),
+        Workload("llama7b_bf16_8192x4096", 8192, 4096, "bf16", 1e-6,
+                 gamma=("normal", 1.0, 0.1), dy=("normal", 0.0, 1e-2),
+                 row_scale=("loguniform", 0.1, 10.0),
+                 note="Llama-7B-shaped: 4x2048 tokens, hidden 4096"),
+        Workload("wide_bf16_16384x8192", 16384, 8192, "bf16", 1e-5,
+                 gamma=("normal", 1.0, 0.2), dy=("normal", 0.0, 1.0),
+                 row_scale=("loguniform", 0.01, 100.0),
+                 note="large hidden size; the headline workload"),
+        Workload("gemma_bf16_32768x3072", 32768, 3072, "bf16", 1e-6,
+                 gamma=("normal", 0.0, 0.1), gemma=1, inplace_dx=1,
+                 note="Gemma (1+gamma) weight, dx written into dy"),
+        *[_sweep(n) for n in (512, 1000, 2048, 5120, 11008, 16384)],
+        Workload("timing_f32_128x257", 128, 257, "f32", 1e-6,
+                 note="the tutorial's timing shape, ragged N"),
+        Workload("layernorm_test_bf16_1151x8192", 1151, 8192, "bf16", 1e-5,
+                 note="the LayerNorm chapter's unit-test shape"),
+    ]
+}
+
+
+def workload(name: str) -> Workload:
+    return WORKLOADS[name]
+
+
+def _generator(seed: int, tensor: str) -> np.random.Generator:
+    return np.random.Generator(np.random.SFC64(np.random.SeedSequence([seed, _TENSOR_IDS[tensor]])))
+
+
+def _draw(gen: np.random.Generator, dist: Dist, out: np.ndarray) -> None:
+    kind, a, b = dist
+    if kind == "normal":
+        gen.standard_normal(out=out)
+        if b != 1.0:
+            out *= b
+        if a != 0.0:
+            out += a
+    elif kind == "uniform":
+        out[...] = gen.uniform(a, b, size=out.shape)
+    elif kind == "loguniform":
+        out[...] = np.exp(gen.uniform(math.log(a), math.log(b), size=out.shape))
+    else:
+        raise ValueError(f"unknown distribution {kind!r}")
+
+
+def float_to_bf16_bits(a) -> np.ndarray:
+    """Round float values to bfloat16 bit patterns: float32 RNE, then RNE on 16 bits."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+    u = f.view(np.uint32)
+    lsb = (u >> 16) & np.uint32(1)
+    return ((u + lsb + np.uint32(0x7FFF)) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_float32(bits) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns to float32."""
+    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def storage_to_float64(arr, dtype: str) -> np.ndarray:
+    """Exact float64 values of a stored tensor (float32 array or bf16 bits)."""
+    if dtype == "bf16":
+        return bf16_bits_to_float32(arr).astype(np.float64)
+    return np.asarray(arr, dtype=np.float32).astype(np.float64)
+
+
+def _store(vals64: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return float_to_bf16_bits(vals64)
+    return vals64.astype(np.float32)
+
+
+def _matrix(w: Workload, tensor: str, dist: Dist, row_scale: Optional[np.ndarray]) -> np.ndarray:
+    gen = _generator(w.seed, tensor)
+    out = np.empty((w.M, w.N), dtype=np.uint16 if w.dtype == "bf16" else np.float32)
+    rows = max(1, _CHUNK_ELEMS // max(1, w.N))
+    buf = np.empty((min(rows, max(w.M, 1)), w.N), dtype=np.float64)
+    for r0 in range(0, w.M, rows):
+        r1 = min(w.M, r0 + rows)
+        blk = buf[: r1 - r0]
+        _draw(gen, dist, blk)
+        if row_scale is not None:
+            blk *= row_scale[r0:r1, None]
+        out[r0:r1] = _store(blk, w.dtype)
+    return out
+
+
+def make_inputs(w: Workload) -> dict:
+    """Draw x (M,N), gamma (N,) and dy (M,N) for a workload, in storage form.
+
+    Returns a dict with keys ``x``, ``gamma``, ``dy`` (float32 arrays for f32
+    workloads, uint16 bf16 bit patterns for bf16 ones) and ``row_scale``
+    (float64, or None).
+    """
+    scale = None
+    if w.row_scale is not None:
+        scale = np.empty(w.M, dtype=np.float64)
+        _draw(_generator(w.seed, "row_scale"), w.row_scale, scale)
+    gvals = np.empty(w.N, dtype=np.float64)
+    _draw(_generator(w.seed, "gamma"), w.gamma, gvals)
+    return {
+        "x": _matrix(w, "x", w.x, scale),
+        "gamma": _store(gvals, w.dtype),
+        "dy": _matrix(w, "dy", w.dy, None),
+        "row_scale": scale,
+    }
