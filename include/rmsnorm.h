@@ -1,0 +1,169 @@
+/*
+ * rmsnorm.h — C ABI of the GB300 (sm_103a) fused RMSNorm library
+ * (librmsnorm.so).
+ *
+ * What it computes, per row i of an M x N row-major matrix, with
+ * g_j = gamma_j, or 1 + gamma_j in Gemma mode:
+ *
+ *   forward   r_i  = 1 / sqrt( (1/N) sum_j x_ij^2 + eps )
+ *             y_ij = x_ij * r_i * g_j
+ *   backward  u_ij = dy_ij * g_j
+ *             c_i  = (1/N) sum_j u_ij * x_ij
+ *             dx_ij = r_i * u_ij - x_ij * r_i^3 * c_i
+ *             dgamma_j = sum_i dy_ij * x_ij * r_i      (a sum over rows)
+ *
+ * Sources: "Hướng dẫn Triton RMSNorm: kernel, backward…" (partitech.com),
+ * sections "Vấn đề và công thức tham chiếu" (forward, eps under the square
+ * root), "Vì sao cần một lượt đi và một lượt về?" (backward formulas),
+ * "N và BLOCK: hai kích thước không được nhầm" (the mean divides by the true
+ * N), "Reduce dgamma không có race khi ghi" and "Tổng không phải trung bình"
+ * (dgamma as per-part partial sums reduced in a second pass; a sum, not a
+ * mean); "02 · 手写 Triton kernel:RMSNorm / RoPE / SwiGLU", section 3
+ * (Gemma's (1 + W) weight, the cast of the normalised row to the weight
+ * dtype before the weight multiply, dx written into dy's buffer).
+ *
+ * Conventions shared by every entry point
+ *  - Every tensor argument is a DEVICE pointer owned by the caller.  The
+ *    library allocates nothing and keeps no per-call state; all work is
+ *    enqueued asynchronously on `stream` (a cudaStream_t passed as void*;
+ *    NULL selects the legacy default stream of the current device).
+ *  - Matrices are contiguous row-major with row stride N elements.
+ *    x, gamma, y, dy, dx share the element type `dtype`.  rstd is always
+ *    float32 (M entries), dgamma always float32 (N entries).
+ *  - Arithmetic is float32 throughout (loads widened to float32, float32
+ *    accumulation, one rounding to `dtype` per stored element), except the
+ *    non-Gemma low-precision forward, which rounds x*r to `dtype` before
+ *    multiplying by gamma (the cast order of the source above).
+ *  - Pointers that are not 16-byte aligned, or N*sizeof(dtype) not a
+ *    multiple of 16, select a slower scalar path; they are not an error.
+ *  - Arguments are validated on the host before anything is launched.  On
+ *    any error nothing is enqueued and the status says why.  No CPU
+ *    fallback exists: unsupported shapes are rejected.
+ */
+#ifndef RMSNORM_H_
+#define RMSNORM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of x, gamma, y, dy, dx. */
+typedef enum {
+  RMS_F32 = 0,  /* IEEE float32 */
+  RMS_BF16 = 1  /* bfloat16 (8-bit significand), round-to-nearest-even on store */
+} rms_dtype;
+
+typedef enum {
+  RMS_OK = 0,
+  RMS_ERR_INVALID_ARG = 1, /* null pointer, bad size, eps, flag, dtype, or overlapping buffers */
+  RMS_ERR_UNSUPPORTED = 2, /* N too large for every row mapping on this device */
+  RMS_ERR_ALIGNMENT = 3,   /* an explicitly requested path needs 16-byte aligned rows */
+  RMS_ERR_WORKSPACE = 4,   /* workspace missing or smaller than rms_bwd_workspace_size() */
+  RMS_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed */
+  RMS_ERR_TIMEOUT = 6      /* a device-side bounded wait gave up (see rms_last_device_status) */
+} rms_status;
+
+/* Row mapping, for rms_fwd_ex / rms_bwd_ex.  RMS_PATH_AUTO picks from N and
+ * dtype; the others force one mapping (used to test and time each). */
+typedef enum {
+  RMS_PATH_AUTO = 0,
+  RMS_PATH_REGISTERS = 1, /* a warp or a thread group per row, row held in registers */
+  RMS_PATH_STAGED = 2,    /* persistent CTAs, rows staged in shared memory by cp.async.bulk */
+  RMS_PATH_SCALAR = 3     /* element-wise loads, any alignment */
+} rms_path;
+
+/*
+ * rms_fwd — forward RMSNorm over M rows of N.
+ *   x     [M*N] dtype, read.
+ *   gamma [N]   dtype, read (the weight; used as 1+gamma when gemma=1).
+ *   y     [M*N] dtype, written.  Must not overlap x, gamma or rstd.
+ *   rstd  [M]   float32, written: r_i, kept for rms_bwd.
+ *   M >= 0 (M == 0 is a no-op), N >= 1, eps finite and >= 0, gemma in {0,1}.
+ * Source: the forward formula and worked example of "Hướng dẫn Triton
+ * RMSNorm", section "Vấn đề và công thức tham chiếu"; Gemma weight and cast
+ * order from "02 · 手写 Triton kernel", section 3.
+ * Errors: RMS_ERR_INVALID_ARG, RMS_ERR_UNSUPPORTED, RMS_ERR_CUDA.  With
+ * eps == 0 an all-zero row gives r = +inf and y = NaN (no special case).
+ */
+rms_status rms_fwd(const void* x, const void* gamma, void* y, float* rstd,
+                   int64_t M, int64_t N, float eps, rms_dtype dtype, int gemma,
+                   void* stream);
+
+/* rms_fwd with an explicit row mapping (see rms_path).  A forced mapping
+ * that cannot run the shape returns RMS_ERR_UNSUPPORTED or
+ * RMS_ERR_ALIGNMENT instead of falling back. */
+rms_status rms_fwd_ex(const void* x, const void* gamma, void* y, float* rstd,
+                      int64_t M, int64_t N, float eps, rms_dtype dtype, int gemma,
+                      rms_path path, void* stream);
+
+/*
+ * rms_bwd — backward RMSNorm: dx and dgamma from dy, x, gamma and the rstd
+ * the forward saved (eps enters only through rstd, which is used as given).
+ *   dy     [M*N] dtype, read; overwritten with dx when inplace_dx = 1.
+ *   x      [M*N] dtype, read.      gamma [N] dtype, read.
+ *   rstd   [M]   float32, read.
+ *   dx     [M*N] dtype, written.  With inplace_dx = 1 it must be NULL or
+ *          equal to dy, and dx is written into dy's buffer.
+ *   dgamma [N]   float32, written: sum over rows of dy*x*r (no mean).
+ *   workspace  device scratch of at least rms_bwd_workspace_size(M, N)
+ *          bytes, 256-byte aligned, owned by the caller; holds one float32
+ *          row of column partial sums per persistent CTA.  Contents on entry
+ *          are ignored, on return undefined.  May be NULL only when M == 0.
+ *   dtype, gemma in {0,1}, inplace_dx in {0,1} as for rms_fwd.
+ * dgamma is computed in two deterministic stages (per-CTA partials over a
+ * static row assignment, then a fixed-order column sum; no atomics, no
+ * locks), so it is bitwise identical from run to run on one device.
+ * Written buffers must not overlap any other argument (except dx == dy
+ * with inplace_dx = 1).  M == 0 writes dgamma = 0.
+ * Source: the backward formulas of "Hướng dẫn Triton RMSNorm", sections
+ * "Vì sao cần một lượt đi và một lượt về?", "Backward đầu vào: giữ đúng N",
+ * "Reduce dgamma không có race khi ghi", "Tổng không phải trung bình";
+ * in-place dx from "02 · 手写 Triton kernel", section 3.
+ * Errors: RMS_ERR_INVALID_ARG, RMS_ERR_UNSUPPORTED, RMS_ERR_WORKSPACE,
+ * RMS_ERR_CUDA.
+ */
+rms_status rms_bwd(void* dy, const void* x, const void* gamma, const float* rstd,
+                   void* dx, float* dgamma, void* workspace,
+                   int64_t M, int64_t N, rms_dtype dtype, int gemma, int inplace_dx,
+                   void* stream);
+
+/* rms_bwd with the workspace size stated (checked against the need:
+ * RMS_ERR_WORKSPACE when too small) and an explicit row mapping. */
+rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* rstd,
+                      void* dx, float* dgamma, void* workspace, size_t workspace_bytes,
+                      int64_t M, int64_t N, rms_dtype dtype, int gemma, int inplace_dx,
+                      rms_path path, void* stream);
+
+/* Bytes of workspace rms_bwd needs for M rows of N on the current device
+ * (an upper bound over dtypes and mappings, a multiple of 256).  Returns 0
+ * for M <= 0 or N <= 0, and 0 if the device cannot be queried. */
+size_t rms_bwd_workspace_size(int64_t M, int64_t N);
+
+/* Static, NUL-terminated description of a status code. */
+const char* rms_status_string(rms_status status);
+
+/* Synchronises `stream`, then reports and clears the device-side status
+ * word of the current device: RMS_ERR_TIMEOUT if a bounded wait in the
+ * staged mapping gave up since the last query (that launch's outputs are
+ * then incomplete), RMS_ERR_CUDA if the stream reports an error, else
+ * RMS_OK. */
+rms_status rms_last_device_status(void* stream);
+
+/* Poll limit of the staged mapping's mbarrier waits, for all later launches
+ * in this process; returns the previous value.  A negative value restores
+ * the default.  A limit of 0 makes every wait give up at once, which lets a
+ * test exercise the timeout path without hanging anything. */
+int64_t rms_set_wait_limit(int64_t polls);
+
+/* Number of kernels the library launched since the process started (all
+ * devices), for accounting in benchmarks. */
+uint64_t rms_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_H_ */

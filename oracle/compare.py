@@ -54,7 +54,8 @@ def _check(name: str, got, ref, allowed) -> Check:
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     allowed = np.broadcast_to(np.asarray(allowed, dtype=np.float64), ref.shape)
-    err = np.abs(got - ref)
+    with np.errstate(invalid="ignore"):
+        err = np.abs(got - ref)
     finite = np.isfinite(got) & np.isfinite(ref)
     same_nonfinite = (~np.isfinite(ref)) & (
         (np.isnan(ref) & np.isnan(got)) | (ref == got))

@@ -89,6 +89,22 @@ def rms_backward(x, gamma, dy, eps: float, gemma: int = 0, with_scales: bool = F
     return dx, dgamma, dx_scale, dgamma_scale
 
 
+def rms_dgamma(x, dy, eps: float, with_scales: bool = False):
+    """dgamma_j = Σ_i dy_ij · x_ij · r_i alone ([TUT] § "Tổng không phải trung bình").
+
+    The same sum ``rms_backward`` returns, without forming dx; with
+    ``with_scales`` also Σ_i |dy·x·r| (the size of the summed terms).
+    """
+    x = _f64(x)
+    dy = _f64(dy)
+    r = rms_rstd(x, eps)
+    terms = dy * x * r[:, None]
+    dgamma = np.sum(terms, axis=0)
+    if not with_scales:
+        return dgamma
+    return dgamma, np.sum(np.abs(terms), axis=0)
+
+
 def rms_backward_normed_form(x, gamma, dy, eps: float, gemma: int = 0):
     """dx in [UNS] § 3's form: inv_var/n · (n·dY_W − normed·Σ_j(dY_W·normed)).
 

@@ -1,0 +1,108 @@
+"""Python binding of librmsnorm.so, the GB300 fused RMSNorm library.
+
+Argument marshalling only: every function below derives sizes, dtype codes,
+device pointers and the current CUDA stream from torch tensors and calls the
+C entry point of the same name (declared in include/rmsnorm.h).  All
+computation happens in the library's CUDA kernels; when the library is
+missing, calls raise instead of falling back to anything else.
+
+Forward:  r = 1/sqrt(mean(x^2) + eps),  y = x * r * g  (g = gamma or 1+gamma)
+Backward: u = dy*g,  dx = r*u - x*r^3*mean(u*x),  dgamma = sum_rows dy*x*r
+"""
+from __future__ import annotations
+
+from . import _lib
+
+RMS_F32, RMS_BF16 = 0, 1
+RMS_PATH_AUTO, RMS_PATH_REGISTERS, RMS_PATH_STAGED, RMS_PATH_SCALAR = 0, 1, 2, 3
+(RMS_OK, RMS_ERR_INVALID_ARG, RMS_ERR_UNSUPPORTED, RMS_ERR_ALIGNMENT, RMS_ERR_WORKSPACE,
+ RMS_ERR_CUDA, RMS_ERR_TIMEOUT) = range(7)
+PATHS = {"auto": RMS_PATH_AUTO, "registers": RMS_PATH_REGISTERS, "staged": RMS_PATH_STAGED,
+         "scalar": RMS_PATH_SCALAR}
+
+__all__ = [
+    "RmsError", "lib", "rms_fwd", "rms_bwd", "rms_bwd_workspace_size", "rms_status_string",
+    "rms_last_device_status", "rms_set_wait_limit", "rms_launch_count", "dtype_code",
+]
+
+
+class RmsError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {rms_status_string(status)} (status {status})")
+
+
+def lib():
+    """The raw ctypes library (see _lib.SIGNATURES for the argument types)."""
+    return _lib.load()
+
+
+def rms_status_string(status: int) -> str:
+    return lib().rms_status_string(int(status)).decode()
+
+
+def dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return RMS_F32
+    if t.dtype == torch.bfloat16:
+        return RMS_BF16
+    raise ValueError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous row-major")
+    return t.data_ptr()
+
+
+def _path(path) -> int:
+    return PATHS[path] if isinstance(path, str) else int(path)
+
+
+def rms_fwd(x, gamma, y, rstd, eps: float = 1e-6, gemma: int = 0, stream=None, path="auto"):
+    """y and rstd from x (M,N) and gamma (N,); writes into y (M,N) and rstd (M,) float32."""
+    M, N = x.shape
+    st = lib().rms_fwd_ex(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), M, N, float(eps),
+                          dtype_code(x), int(gemma), _path(path), _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "rms_fwd")
+
+
+def rms_bwd(dy, x, gamma, rstd, dx, dgamma, workspace, gemma: int = 0, inplace_dx: int = 0,
+            stream=None, path="auto"):
+    """dx (M,N) and dgamma (N,) float32; with inplace_dx=1 dx is written into dy (pass dx=None)."""
+    M, N = x.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().rms_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
+                          _ptr(workspace), ws_bytes, M, N, dtype_code(x), int(gemma),
+                          int(inplace_dx), _path(path), _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "rms_bwd")
+
+
+def rms_bwd_workspace_size(M: int, N: int) -> int:
+    return int(lib().rms_bwd_workspace_size(int(M), int(N)))
+
+
+def rms_last_device_status(stream=None) -> int:
+    return int(lib().rms_last_device_status(_stream_handle(stream)))
+
+
+def rms_set_wait_limit(polls: int) -> int:
+    return int(lib().rms_set_wait_limit(int(polls)))
+
+
+def rms_launch_count() -> int:
+    return int(lib().rms_launch_count())

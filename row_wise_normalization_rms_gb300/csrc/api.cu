@@ -1,0 +1,276 @@
+// C ABI of librmsnorm.so: argument validation, row-mapping dispatch,
+// workspace sizing and status reporting.  Nothing here allocates device
+// memory or touches tensor data; every error is found before a launch.
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "rmsnorm.h"
+
+namespace {
+
+using rmsi::BwdArgs;
+using rmsi::DeviceInfo;
+using rmsi::FwdArgs;
+using rmsi::Mapping;
+
+constexpr long long kDefaultWaitLimit = 1ll << 22;
+std::atomic<long long> g_wait_limit{kDefaultWaitLimit};
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ok[kMaxDevices] = {};
+
+bool current_device(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev_ok[dev]) {
+    DeviceInfo d;
+    d.device = dev;
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    d.sms = v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return false;
+    d.smem_optin = (size_t)v;
+    g_dev[dev] = d;
+    g_dev_ok[dev] = true;
+  }
+  *out = g_dev[dev];
+  return true;
+}
+
+int elem_bytes(int dtype) { return dtype == rmsi::kBF16 ? 2 : 4; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Half-open byte ranges [p, p + n) overlap.
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+bool valid_common(int64_t M, int64_t N, rms_dtype dtype, int gemma) {
+  if (dtype != RMS_F32 && dtype != RMS_BF16) return false;
+  if (gemma != 0 && gemma != 1) return false;
+  if (M < 0 || N <= 0) return false;
+  return true;
+}
+
+// Matrix byte count, or 0 when M*N*b does not fit in an int64.
+size_t matrix_bytes(int64_t M, int64_t N, int b) {
+  if (M == 0) return 0;
+  if (N > INT64_MAX / b || M > INT64_MAX / (N * b)) return 0;
+  return (size_t)(M * N * b);
+}
+
+size_t workspace_need(int64_t M, int64_t N, const DeviceInfo& d) {
+  int64_t P = rmsi::max_partials(d.sms);
+  if (P > M) P = M;
+  const size_t bytes = (size_t)P * (size_t)N * sizeof(float);
+  return (bytes + 255) / 256 * 256;
+}
+
+// Picks the row mapping for a call.  A forced path that cannot take the
+// shape is an error, never a silent switch.
+rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const DeviceInfo& d,
+                  Mapping* m) {
+  switch (path) {
+    case RMS_PATH_AUTO:
+      if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m)) return RMS_OK;
+      if (aligned && rmsi::plan_registers(N, dtype, bwd, m)) return RMS_OK;
+      if (rmsi::plan_scalar(N, dtype, bwd, d, m)) return RMS_OK;
+      return RMS_ERR_UNSUPPORTED;
+    case RMS_PATH_REGISTERS:
+      if (!aligned) return RMS_ERR_ALIGNMENT;
+      return rmsi::plan_registers(N, dtype, bwd, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
+    case RMS_PATH_STAGED:
+      if (!aligned) return RMS_ERR_ALIGNMENT;
+      return rmsi::plan_staged(N, dtype, bwd, d, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
+    case RMS_PATH_SCALAR:
+      return rmsi::plan_scalar(N, dtype, bwd, d, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
+    default:
+      return RMS_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rms_status_string(rms_status s) {
+  switch (s) {
+    case RMS_OK: return "ok";
+    case RMS_ERR_INVALID_ARG: return "invalid argument";
+    case RMS_ERR_UNSUPPORTED: return "unsupported shape for the requested row mapping";
+    case RMS_ERR_ALIGNMENT: return "requested row mapping needs 16-byte aligned rows and pointers";
+    case RMS_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case RMS_ERR_CUDA: return "CUDA runtime error";
+    case RMS_ERR_TIMEOUT: return "device-side bounded wait gave up";
+    default: return "unknown status";
+  }
+}
+
+int64_t rms_set_wait_limit(int64_t polls) {
+  const long long v = polls < 0 ? kDefaultWaitLimit : (long long)polls;
+  return (int64_t)g_wait_limit.exchange(v);
+}
+
+uint64_t rms_launch_count(void) { return g_launches.load(); }
+
+size_t rms_bwd_workspace_size(int64_t M, int64_t N) {
+  if (M <= 0 || N <= 0) return 0;
+  DeviceInfo d;
+  if (!current_device(&d)) return 0;
+  return workspace_need(M, N, d);
+}
+
+rms_status rms_fwd_ex(const void* x, const void* gamma, void* y, float* rstd, int64_t M,
+                      int64_t N, float eps, rms_dtype dtype, int gemma, rms_path path,
+                      void* stream) {
+  if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.f) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_SCALAR) return RMS_ERR_INVALID_ARG;
+  if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
+  if (M == 0) return RMS_OK;
+  if (!x || !gamma || !y || !rstd) return RMS_ERR_INVALID_ARG;
+  const int b = elem_bytes(dtype);
+  const size_t xb = matrix_bytes(M, N, b);
+  if (xb == 0) return RMS_ERR_INVALID_ARG;
+  const size_t gb = (size_t)N * b, rb = (size_t)M * sizeof(float);
+  if (overlap(y, xb, x, xb) || overlap(y, xb, gamma, gb) || overlap(y, xb, rstd, rb) ||
+      overlap(rstd, rb, x, xb) || overlap(rstd, rb, gamma, gb))
+    return RMS_ERR_INVALID_ARG;
+
+  DeviceInfo d;
+  if (!current_device(&d)) return RMS_ERR_CUDA;
+  const bool aligned = (N * b) % 16 == 0 && aligned16(x) && aligned16(gamma) && aligned16(y);
+  Mapping m;
+  const rms_status st = choose(path, (int)N, dtype, false, aligned, d, &m);
+  if (st != RMS_OK) return st;
+
+  FwdArgs a{x, gamma, y, rstd, M, (int)N, eps, (int)dtype, gemma};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (m.path) {
+    case rmsi::kRegisters:
+      if ((M + m.rows_per_cta - 1) / m.rows_per_cta > INT32_MAX) return RMS_ERR_UNSUPPORTED;
+      e = rmsi::launch_fwd_registers(a, m, s);
+      break;
+    case rmsi::kStaged:
+      e = rmsi::launch_fwd_staged(a, m, d, g_wait_limit.load(), s);
+      break;
+    default:
+      if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
+      e = rmsi::launch_fwd_scalar(a, m, s);
+      break;
+  }
+  if (e != cudaSuccess) return RMS_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return RMS_OK;
+}
+
+rms_status rms_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t M, int64_t N,
+                   float eps, rms_dtype dtype, int gemma, void* stream) {
+  return rms_fwd_ex(x, gamma, y, rstd, M, N, eps, dtype, gemma, RMS_PATH_AUTO, stream);
+}
+
+rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* rstd, void* dx,
+                      float* dgamma, void* workspace, size_t workspace_bytes, int64_t M,
+                      int64_t N, rms_dtype dtype, int gemma, int inplace_dx, rms_path path,
+                      void* stream) {
+  if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
+  if (inplace_dx != 0 && inplace_dx != 1) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_SCALAR) return RMS_ERR_INVALID_ARG;
+  if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
+  if (inplace_dx) {
+    if (dx && dx != dy) return RMS_ERR_INVALID_ARG;
+    dx = dy;
+  }
+  if (!dgamma) return RMS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    // The sum over zero rows: dgamma = 0.
+    return cudaMemsetAsync(dgamma, 0, (size_t)N * sizeof(float), s) == cudaSuccess ? RMS_OK
+                                                                                    : RMS_ERR_CUDA;
+  }
+  if (!dx || !dy || !x || !gamma || !rstd) return RMS_ERR_INVALID_ARG;
+  const int b = elem_bytes(dtype);
+  const size_t xb = matrix_bytes(M, N, b);
+  if (xb == 0) return RMS_ERR_INVALID_ARG;
+  const size_t gb = (size_t)N * b, rb = (size_t)M * sizeof(float), db = (size_t)N * sizeof(float);
+
+  if (!workspace) return RMS_ERR_WORKSPACE;
+  DeviceInfo d;
+  if (!current_device(&d)) return RMS_ERR_CUDA;
+  const size_t need = workspace_need(M, N, d);
+  if (workspace_bytes < need || ((uintptr_t)workspace & 255u) != 0) return RMS_ERR_WORKSPACE;
+
+  // Written ranges (dx, dgamma, workspace) must not overlap anything else;
+  // dx == dy is the one sanctioned alias.
+  const void* reads[3] = {x, gamma, rstd};
+  const size_t read_n[3] = {xb, gb, rb};
+  for (int i = 0; i < 3; ++i) {
+    if (overlap(dx, xb, reads[i], read_n[i]) || overlap(dgamma, db, reads[i], read_n[i]) ||
+        overlap(workspace, need, reads[i], read_n[i]))
+      return RMS_ERR_INVALID_ARG;
+  }
+  if (dx != dy && overlap(dx, xb, dy, xb)) return RMS_ERR_INVALID_ARG;
+  if (overlap(dgamma, db, dy, xb) || overlap(workspace, need, dy, xb) ||
+      overlap(dgamma, db, dx, xb) || overlap(workspace, need, dx, xb) ||
+      overlap(workspace, need, dgamma, db))
+    return RMS_ERR_INVALID_ARG;
+
+  const bool aligned =
+      (N * b) % 16 == 0 && aligned16(dy) && aligned16(x) && aligned16(gamma) && aligned16(dx);
+  Mapping m;
+  const rms_status st = choose(path, (int)N, dtype, true, aligned, d, &m);
+  if (st != RMS_OK) return st;
+
+  BwdArgs a{dy, x, gamma, rstd, dx, dgamma, static_cast<float*>(workspace), M, (int)N,
+            (int)dtype, gemma};
+  cudaError_t e;
+  switch (m.path) {
+    case rmsi::kRegisters:
+      e = rmsi::size_bwd_registers(a, d, &m);
+      if (e == cudaSuccess) e = rmsi::launch_bwd_registers(a, m, s);
+      break;
+    case rmsi::kStaged:
+      e = rmsi::size_bwd_staged(a, d, &m);
+      if (e == cudaSuccess) e = rmsi::launch_bwd_staged(a, m, d, g_wait_limit.load(), s);
+      break;
+    default:
+      e = rmsi::size_bwd_scalar(a, d, &m);
+      if (e == cudaSuccess) e = rmsi::launch_bwd_scalar(a, m, s);
+      break;
+  }
+  if (e != cudaSuccess) return RMS_ERR_CUDA;
+  if ((size_t)m.blocks * (size_t)N * sizeof(float) > need) return RMS_ERR_WORKSPACE;  // unreachable
+  e = rmsi::launch_colreduce(a.ws, dgamma, m.blocks, (int)N, s);
+  if (e != cudaSuccess) return RMS_ERR_CUDA;
+  g_launches.fetch_add(2);
+  return RMS_OK;
+}
+
+rms_status rms_bwd(void* dy, const void* x, const void* gamma, const float* rstd, void* dx,
+                   float* dgamma, void* workspace, int64_t M, int64_t N, rms_dtype dtype, int gemma,
+                   int inplace_dx, void* stream) {
+  return rms_bwd_ex(dy, x, gamma, rstd, dx, dgamma, workspace, SIZE_MAX, M, N, dtype, gemma,
+                    inplace_dx, RMS_PATH_AUTO, stream);
+}
+
+rms_status rms_last_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return RMS_ERR_CUDA;
+  int v = 0;
+  if (rmsi::take_device_status(&v) != cudaSuccess) return RMS_ERR_CUDA;
+  return v ? RMS_ERR_TIMEOUT : RMS_OK;
+}
+
+}  // extern "C"

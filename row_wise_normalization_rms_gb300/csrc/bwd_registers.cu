@@ -1,0 +1,204 @@
+// Backward RMSNorm, register mapping, persistent grid.
+//
+// A group of G threads owns one row at a time and holds x, dy and the
+// weight in registers as 16-byte vectors:
+//
+//   u  = dy * g                    (g = gamma, or 1 + gamma for Gemma)
+//   c  = sum(u * x) / N            (the true N)
+//   dx = r * u - x * r^3 * c       (r is the forward's saved rstd)
+//
+// dx is stored to dx, or over dy when the caller asks for it in place (the
+// whole row is already in registers when it is overwritten).  The weight
+// gradient is a sum over rows, so each thread also accumulates
+// dy * x * r for the columns it owns, across every row its group visits.
+// Rows are dealt to groups statically (row = group id + k * groups), and at
+// the end each CTA writes one float32 row of column partials to the
+// workspace (groups of a CTA are combined in group order through shared
+// memory).  A second kernel sums the partial rows in a fixed order.  No
+// atomics and no locks: the result depends only on M, N and the grid size.
+//
+// Sources: "Hướng dẫn Triton RMSNorm: kernel, backward…", sections "Vì sao
+// cần một lượt đi và một lượt về?", "Backward đầu vào: giữ đúng N",
+// "Reduce dgamma không có race khi ghi", "Tổng không phải trung bình";
+// "02 · 手写 Triton kernel:RMSNorm / RoPE / SwiGLU", section 3 (dx into dy).
+#include "common.cuh"
+#include "internal.h"
+
+namespace rmsk {
+
+template <typename T, int KV>
+__global__ void __launch_bounds__(512)
+rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restrict__ gamma,
+                         const float* __restrict__ rstd, T* dx, float* __restrict__ ws, int64_t M,
+                         int N, int gemma, int G) {
+  using E = Elem<T>;
+  constexpr int VN = E::kPerVec;
+  __shared__ float red[2][16];
+  extern __shared__ float part[];  // [R][N] when R > 1 groups share the CTA
+
+  const int NV = N / VN;
+  const int R = blockDim.x / G;
+  const int grp = threadIdx.x / G;
+  const int lig = threadIdx.x - grp * G;
+  const int64_t groups = (int64_t)gridDim.x * R;
+  const int64_t gid0 = (int64_t)blockIdx.x * R;  // the CTA's first group: it has the most rows
+  const int64_t gid = gid0 + grp;
+  const int64_t iters = gid0 < M ? (M - gid0 + groups - 1) / groups : 0;
+
+  const uint4* gv = reinterpret_cast<const uint4*>(gamma);
+  uint4 gw[KV];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = lig + k * G;
+    gw[k] = v < NV ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float acc[KV][VN];
+#pragma unroll
+  for (int k = 0; k < KV; ++k)
+#pragma unroll
+    for (int e = 0; e < VN; ++e) acc[k][e] = 0.f;
+
+  for (int64_t it = 0; it < iters; ++it) {
+    const int64_t row = gid + it * groups;
+    const bool active = row < M;
+    const int64_t base = (active ? row : 0) * (int64_t)NV;
+    const uint4* xr = reinterpret_cast<const uint4*>(x) + base;
+    const uint4* dr = reinterpret_cast<const uint4*>(dy) + base;
+    uint4 xv[KV], dv[KV];
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = lig + k * G;
+      const bool in = active && v < NV;
+      xv[k] = in ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+      dv[k] = in ? ld_stream(dr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const float r = active ? rstd[row] : 0.f;
+
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      float f[VN], d[VN], g[VN];
+      E::unpack(xv[k], f);
+      E::unpack(dv[k], d);
+      E::unpack(gw[k], g);
+#pragma unroll
+      for (int e = 0; e < VN; ++e) {
+        const float w = gemma ? 1.0f + g[e] : g[e];
+        s = fmaf(d[e] * w, f[e], s);
+      }
+    }
+    s = group_sum(s, G, grp * (G >> 5), red[it & 1]);
+    const float c = s / (float)N;
+    const float r3c = r * r * r * c;
+
+    if (active) {
+      uint4* out = reinterpret_cast<uint4*>(dx) + base;
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const int v = lig + k * G;
+        if (v < NV) {
+          float f[VN], d[VN], g[VN], o[VN];
+          E::unpack(xv[k], f);
+          E::unpack(dv[k], d);
+          E::unpack(gw[k], g);
+#pragma unroll
+          for (int e = 0; e < VN; ++e) {
+            const float w = gemma ? 1.0f + g[e] : g[e];
+            o[e] = r * (d[e] * w) - f[e] * r3c;
+            acc[k][e] = fmaf(d[e] * f[e], r, acc[k][e]);
+          }
+          st_stream(out + v, E::pack(o));
+        }
+      }
+    }
+  }
+
+  // One workspace row per CTA: this CTA's column partial sums.
+  float* wp = ws + (int64_t)blockIdx.x * N;
+  if (R == 1) {
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = lig + k * G;
+      if (v < NV) {
+        float4* w4 = reinterpret_cast<float4*>(wp + (int64_t)v * VN);
+#pragma unroll
+        for (int q = 0; q < VN / 4; ++q)
+          w4[q] = make_float4(acc[k][4 * q], acc[k][4 * q + 1], acc[k][4 * q + 2], acc[k][4 * q + 3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = lig + k * G;
+      if (v < NV) {
+#pragma unroll
+        for (int e = 0; e < VN; ++e) part[(int64_t)grp * N + v * VN + e] = acc[k][e];
+      }
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < N; j += blockDim.x) {
+      float t = 0.f;
+      for (int q = 0; q < R; ++q) t += part[(int64_t)q * N + j];
+      wp[j] = t;
+    }
+  }
+}
+
+template <typename T, int KV>
+static const void* kernel_ptr() {
+  return reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, KV>);
+}
+
+template <typename T>
+static const void* pick(int kv) {
+  switch (kv) {
+    case 1: return kernel_ptr<T, 1>();
+    case 2: return kernel_ptr<T, 2>();
+    case 4: return kernel_ptr<T, 4>();
+    default: return nullptr;
+  }
+}
+
+template <typename T>
+static cudaError_t launch_t(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
+  const dim3 grid((unsigned)m.blocks), block(m.threads);
+  const T* dy = static_cast<const T*>(a.dy);
+  const T* x = static_cast<const T*>(a.x);
+  const T* g = static_cast<const T*>(a.gamma);
+  T* dx = static_cast<T*>(a.dx);
+  switch (m.kv) {
+    case 1: rms_bwd_registers_kernel<T, 1><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, a.gemma, m.G); break;
+    case 2: rms_bwd_registers_kernel<T, 2><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, a.gemma, m.G); break;
+    case 4: rms_bwd_registers_kernel<T, 4><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, a.gemma, m.G); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace rmsk
+
+namespace rmsi {
+
+cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
+  m->smem = m->rows_per_cta > 1 ? (size_t)m->rows_per_cta * a.N * sizeof(float) : 0;
+  const void* k = a.dtype == kBF16 ? rmsk::pick<__nv_bfloat16>(m->kv) : rmsk::pick<float>(m->kv);
+  if (!k) return cudaErrorInvalidValue;
+  int occ = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, m->threads, m->smem);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  int64_t P = (int64_t)occ * d.sms;
+  if (P > max_partials(d.sms)) P = max_partials(d.sms);
+  const int64_t need = (a.M + m->rows_per_cta - 1) / m->rows_per_cta;
+  if (P > need) P = need;
+  if (P < 1) P = 1;
+  m->blocks = P;
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd_registers(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
+  if (a.dtype == kBF16) return rmsk::launch_t<__nv_bfloat16>(a, m, s);
+  return rmsk::launch_t<float>(a, m, s);
+}
+
+}  // namespace rmsi

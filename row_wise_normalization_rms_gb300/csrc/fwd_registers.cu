@@ -1,0 +1,137 @@
+// Forward RMSNorm, register mapping: a group of G threads (one warp, or
+// several warps up to the whole CTA) owns one row and holds it in registers
+// as 16-byte vectors, so x is read from HBM exactly once and y written once.
+//
+//   r = 1 / sqrt(sum(x^2) / N + eps)        (the true N, never a padded width)
+//   y = round(round(x * r) * gamma)         (non-Gemma: normalised row cast to
+//                                            the weight dtype, then weighted)
+//   y = round(x * r * (1 + gamma))          (Gemma)
+//
+// Sources: "Hướng dẫn Triton RMSNorm: kernel, backward…", sections "Vấn đề
+// và công thức tham chiếu" and "N và BLOCK: hai kích thước không được nhầm";
+// "02 · 手写 Triton kernel:RMSNorm / RoPE / SwiGLU", section 3 (cast order,
+// Gemma weight).
+#include "common.cuh"
+#include "internal.h"
+
+namespace rmsk {
+
+template <typename T, int KV>
+__global__ void __launch_bounds__(1024)
+rms_fwd_registers_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+                         float* __restrict__ rstd, int64_t M, int N, float eps, int gemma, int G) {
+  using E = Elem<T>;
+  constexpr int VN = E::kPerVec;
+  __shared__ float red[32];
+  const int NV = N / VN;
+  const int grp = threadIdx.x / G;
+  const int lig = threadIdx.x - grp * G;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / G) + grp;
+  const bool active = row < M;
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + (active ? row : 0) * (int64_t)NV;
+  const uint4* gv = reinterpret_cast<const uint4*>(gamma);
+
+  uint4 xv[KV];
+  uint4 gw[KV];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = lig + k * G;
+    const bool in = active && v < NV;
+    xv[k] = in ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = lig + k * G;
+    gw[k] = (active && v < NV) ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    float f[VN];
+    E::unpack(xv[k], f);
+#pragma unroll
+    for (int e = 0; e < VN; ++e) ss = fmaf(f[e], f[e], ss);
+  }
+  ss = group_sum(ss, G, grp * (G >> 5), red);
+  const float r = 1.0f / sqrtf(ss / (float)N + eps);
+  if (!active) return;  // no barrier follows
+  if (lig == 0) rstd[row] = r;
+
+  uint4* yr = reinterpret_cast<uint4*>(y) + row * (int64_t)NV;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = lig + k * G;
+    if (v < NV) {
+      float f[VN], g[VN], o[VN];
+      E::unpack(xv[k], f);
+      E::unpack(gw[k], g);
+      if (gemma) {
+#pragma unroll
+        for (int e = 0; e < VN; ++e) o[e] = (f[e] * r) * (1.0f + g[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < VN; ++e) o[e] = E::round(f[e] * r) * g[e];
+      }
+      st_stream(yr + v, E::pack(o));
+    }
+  }
+}
+
+template <typename T>
+static cudaError_t launch_t(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
+  const dim3 grid((unsigned)m.blocks), block(m.threads);
+  const T* x = static_cast<const T*>(a.x);
+  const T* g = static_cast<const T*>(a.gamma);
+  T* y = static_cast<T*>(a.y);
+  switch (m.kv) {
+    case 1: rms_fwd_registers_kernel<T, 1><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, a.gemma, m.G); break;
+    case 2: rms_fwd_registers_kernel<T, 2><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, a.gemma, m.G); break;
+    case 4: rms_fwd_registers_kernel<T, 4><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, a.gemma, m.G); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace rmsk
+
+namespace rmsi {
+
+// Threads per row and vectors per thread for a row of N elements held in
+// registers.  Rows of up to 128 vectors (2 KiB) get one warp each, several
+// rows per CTA; wider rows get ceil(vectors / 4) threads rounded up to a
+// warp multiple, up to 1024 threads (wider rows use the staged mapping).
+bool plan_registers(int N, int dtype, bool bwd, Mapping* m) {
+  const int b = dtype == kBF16 ? 2 : 4;
+  if (N <= 0 || ((int64_t)N * b) % 16 != 0) return false;
+  const int NV = (int)(((int64_t)N * b) / 16);
+  const int max_threads = bwd ? 512 : 1024;
+  int kv, G;
+  if (NV <= 32) {
+    kv = 1; G = 32;
+  } else if (NV <= 64) {
+    kv = 2; G = 32;
+  } else if (NV <= 128) {
+    kv = 4; G = 32;
+  } else {
+    kv = 4;
+    G = ((NV + 3) / 4 + 31) / 32 * 32;
+    if (G > max_threads) return false;
+  }
+  m->path = kRegisters;
+  m->kv = kv;
+  m->G = G;
+  m->rows_per_cta = G >= 256 ? 1 : 256 / G;
+  m->threads = G * m->rows_per_cta;
+  m->smem = 0;
+  return true;
+}
+
+cudaError_t launch_fwd_registers(const FwdArgs& a, const Mapping& m0, cudaStream_t s) {
+  Mapping m = m0;
+  m.blocks = (a.M + m.rows_per_cta - 1) / m.rows_per_cta;
+  if (a.dtype == kBF16) return rmsk::launch_t<__nv_bfloat16>(a, m, s);
+  return rmsk::launch_t<float>(a, m, s);
+}
+
+}  // namespace rmsi

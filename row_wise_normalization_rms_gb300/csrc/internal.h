@@ -1,0 +1,88 @@
+// Host-side interface between the C ABI layer (api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace rmsi {
+
+enum Dtype { kF32 = 0, kBF16 = 1 };
+enum Path { kAuto = 0, kRegisters = 1, kStaged = 2, kScalar = 3 };
+
+struct FwdArgs {
+  const void* x;
+  const void* gamma;
+  void* y;
+  float* rstd;
+  int64_t M;
+  int N;
+  float eps;
+  int dtype;
+  int gemma;
+};
+
+struct BwdArgs {
+  void* dy;
+  const void* x;
+  const void* gamma;
+  const float* rstd;
+  void* dx;  // == dy for in-place dx
+  float* dgamma;
+  float* ws;  // [P][N] float32 column partials
+  int64_t M;
+  int N;
+  int dtype;
+  int gemma;
+};
+
+// How one launch maps rows onto the GPU.
+struct Mapping {
+  int path = kAuto;
+  int G = 0;             // threads per row
+  int kv = 0;            // 16-byte vectors per thread per row (register path)
+  int threads = 0;       // threads per CTA
+  int rows_per_cta = 0;  // rows a CTA works on at once (threads / G)
+  int64_t blocks = 0;    // CTAs launched
+  int stages = 0;        // shared-memory pipeline depth (staged path)
+  size_t smem = 0;       // dynamic shared memory bytes
+};
+
+struct DeviceInfo {
+  int device = 0;
+  int sms = 0;
+  size_t smem_optin = 0;  // max dynamic shared memory per CTA
+};
+
+// Largest number of persistent CTAs a backward launch may use on a device
+// with `sms` SMs; the workspace holds this many float32 rows of N.
+inline int64_t max_partials(int sms) { return 4 * (int64_t)sms; }
+
+// ---- register path (fwd_registers.cu, bwd_registers.cu) ----
+bool plan_registers(int N, int dtype, bool bwd, Mapping* m);
+cudaError_t launch_fwd_registers(const FwdArgs& a, const Mapping& m, cudaStream_t s);
+// Fills m.blocks (= number of partial rows P) for a persistent backward.
+cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m);
+cudaError_t launch_bwd_registers(const BwdArgs& a, const Mapping& m, cudaStream_t s);
+
+// ---- scalar path and the column reduction (scalar.cu) ----
+bool plan_scalar(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m);
+cudaError_t launch_fwd_scalar(const FwdArgs& a, const Mapping& m, cudaStream_t s);
+cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m);
+cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s);
+// dgamma[j] = sum_{p < P} ws[p][j], p in increasing order.
+cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, cudaStream_t s);
+
+// ---- staged path (staged.cu) ----
+bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m);
+cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
+                              long long wait_limit, cudaStream_t s);
+cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m);
+cudaError_t launch_bwd_staged(const BwdArgs& a, const Mapping& m, const DeviceInfo& d,
+                              long long wait_limit, cudaStream_t s);
+// Reads and clears the device status word of the current device
+// (0 = no bounded wait gave up since the last call).
+cudaError_t take_device_status(int* status);
+
+}  // namespace rmsi

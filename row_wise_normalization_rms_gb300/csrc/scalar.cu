@@ -1,0 +1,184 @@
+// Scalar-load RMSNorm kernels for rows that are not 16-byte aligned (odd N,
+// offset pointers), and the column reduction that finishes dgamma for every
+// backward mapping.
+//
+// The scalar kernels compute exactly what the vector kernels compute (same
+// formulas, same cast order, float32 accumulation) but read elements one at
+// a time with a CTA per row, touching x twice (the second read is served by
+// L1/L2).  The backward keeps its dgamma column partials in shared memory,
+// one slot per column owned by one thread, and is persistent with a static
+// row assignment like the register mapping.
+//
+// Sources: "Hướng dẫn Triton RMSNorm: kernel, backward…", sections "Vấn đề
+// và công thức tham chiếu", "Vì sao cần một lượt đi và một lượt về?",
+// "Reduce dgamma không có race khi ghi" (second pass summing the partials
+// column by column), "Tổng không phải trung bình".
+#include "common.cuh"
+#include "internal.h"
+
+namespace rmsk {
+
+constexpr int kScalarThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kScalarThreads)
+rms_fwd_scalar_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+                      float* __restrict__ rstd, int64_t M, int N, float eps, int gemma) {
+  using E = Elem<T>;
+  __shared__ float red[kScalarThreads / 32];
+  const int64_t row = blockIdx.x;
+  const T* xr = x + row * N;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < N; j += kScalarThreads) {
+    const float f = E::to_f(xr[j]);
+    ss = fmaf(f, f, ss);
+  }
+  ss = group_sum(ss, kScalarThreads, 0, red);
+  const float r = 1.0f / sqrtf(ss / (float)N + eps);
+  if (threadIdx.x == 0) rstd[row] = r;
+  T* yr = y + row * N;
+  for (int j = threadIdx.x; j < N; j += kScalarThreads) {
+    const float f = E::to_f(xr[j]);
+    const float g = E::to_f(gamma[j]);
+    const float o = gemma ? (f * r) * (1.0f + g) : E::round(f * r) * g;
+    yr[j] = E::from_f(o);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kScalarThreads)
+rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const T* __restrict__ gamma,
+                      const float* __restrict__ rstd, T* dx, float* __restrict__ ws, int64_t M,
+                      int N, int gemma) {
+  using E = Elem<T>;
+  __shared__ float red[2][kScalarThreads / 32];
+  extern __shared__ float acc[];  // [N]: column j belongs to thread j % kScalarThreads
+  for (int j = threadIdx.x; j < N; j += kScalarThreads) acc[j] = 0.f;
+
+  int it = 0;
+  for (int64_t row = blockIdx.x; row < M; row += gridDim.x, ++it) {
+    const T* xr = x + row * N;
+    const T* dr = dy + row * N;
+    const float r = rstd[row];
+    float s = 0.f;
+    for (int j = threadIdx.x; j < N; j += kScalarThreads) {
+      const float g = E::to_f(gamma[j]);
+      const float w = gemma ? 1.0f + g : g;
+      s = fmaf(E::to_f(dr[j]) * w, E::to_f(xr[j]), s);
+    }
+    s = group_sum(s, kScalarThreads, 0, red[it & 1]);
+    const float r3c = r * r * r * (s / (float)N);
+    T* out = dx + row * N;
+    for (int j = threadIdx.x; j < N; j += kScalarThreads) {
+      const float f = E::to_f(xr[j]);
+      const float d = E::to_f(dr[j]);
+      const float g = E::to_f(gamma[j]);
+      const float w = gemma ? 1.0f + g : g;
+      acc[j] = fmaf(d * f, r, acc[j]);
+      out[j] = E::from_f(r * (d * w) - f * r3c);
+    }
+  }
+  float* wp = ws + (int64_t)blockIdx.x * N;
+  for (int j = threadIdx.x; j < N; j += kScalarThreads) wp[j] = acc[j];
+}
+
+// dgamma[j] = sum over p = 0..P-1 of ws[p][j].  A CTA covers 32 columns with
+// 8 row-strands: strand t sums rows t, t+8, t+16, ... in increasing order,
+// then strand sums are added in strand order.  Fixed order, no atomics.
+__global__ void __launch_bounds__(256)
+rms_dgamma_colreduce_kernel(const float* __restrict__ ws, float* __restrict__ dgamma, int64_t P,
+                            int N) {
+  __shared__ float part[8][33];
+  const int tx = threadIdx.x & 31;
+  const int ty = threadIdx.x >> 5;
+  const int64_t col = (int64_t)blockIdx.x * 32 + tx;
+  float s = 0.f;
+  if (col < N) {
+    for (int64_t p = ty; p < P; p += 8) s += ws[p * N + col];
+  }
+  part[ty][tx] = s;
+  __syncthreads();
+  if (ty == 0 && col < N) {
+    float t = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) t += part[q][tx];
+    dgamma[col] = t;
+  }
+}
+
+}  // namespace rmsk
+
+namespace rmsi {
+
+bool plan_scalar(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
+  (void)dtype;
+  if (N <= 0) return false;
+  m->path = kScalar;
+  m->G = rmsk::kScalarThreads;
+  m->kv = 0;
+  m->threads = rmsk::kScalarThreads;
+  m->rows_per_cta = 1;
+  m->smem = bwd ? (size_t)N * sizeof(float) : 0;
+  if (m->smem > d.smem_optin) return false;
+  return true;
+}
+
+cudaError_t launch_fwd_scalar(const FwdArgs& a, const Mapping& m, cudaStream_t s) {
+  const dim3 grid((unsigned)a.M), block(m.threads);
+  if (a.dtype == kBF16) {
+    rmsk::rms_fwd_scalar_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(a.x), static_cast<const __nv_bfloat16*>(a.gamma),
+        static_cast<__nv_bfloat16*>(a.y), a.rstd, a.M, a.N, a.eps, a.gemma);
+  } else {
+    rmsk::rms_fwd_scalar_kernel<float><<<grid, block, 0, s>>>(
+        static_cast<const float*>(a.x), static_cast<const float*>(a.gamma),
+        static_cast<float*>(a.y), a.rstd, a.M, a.N, a.eps, a.gemma);
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+static const void* bwd_scalar_ptr() {
+  return reinterpret_cast<const void*>(&rmsk::rms_bwd_scalar_kernel<T>);
+}
+
+cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
+  const void* k = a.dtype == kBF16 ? bwd_scalar_ptr<__nv_bfloat16>() : bwd_scalar_ptr<float>();
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)m->smem);
+  if (e != cudaSuccess) return e;
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, m->threads, m->smem);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  int64_t P = (int64_t)occ * d.sms;
+  if (P > max_partials(d.sms)) P = max_partials(d.sms);
+  if (P > a.M) P = a.M;
+  if (P < 1) P = 1;
+  m->blocks = P;
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
+  const dim3 grid((unsigned)m.blocks), block(m.threads);
+  if (a.dtype == kBF16) {
+    rmsk::rms_bwd_scalar_kernel<__nv_bfloat16><<<grid, block, m.smem, s>>>(
+        static_cast<const __nv_bfloat16*>(a.dy), static_cast<const __nv_bfloat16*>(a.x),
+        static_cast<const __nv_bfloat16*>(a.gamma), a.rstd, static_cast<__nv_bfloat16*>(a.dx),
+        a.ws, a.M, a.N, a.gemma);
+  } else {
+    rmsk::rms_bwd_scalar_kernel<float><<<grid, block, m.smem, s>>>(
+        static_cast<const float*>(a.dy), static_cast<const float*>(a.x),
+        static_cast<const float*>(a.gamma), a.rstd, static_cast<float*>(a.dx), a.ws, a.M, a.N,
+        a.gemma);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, cudaStream_t s) {
+  const dim3 grid((unsigned)((N + 31) / 32)), block(256);
+  rmsk::rms_dgamma_colreduce_kernel<<<grid, block, 0, s>>>(ws, dgamma, P, N);
+  return cudaGetLastError();
+}
+
+}  // namespace rmsi

@@ -1,0 +1,143 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI on
+seeded inputs and compare with the fp64 oracle on the same inputs."""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+import row_wise_normalization_rms_gb300 as rms
+from oracle import compare
+from oracle import rmsnorm_oracle as orc
+from synthetic import make_inputs, storage_to_float64
+
+PAD = 64  # guard elements on each side of every output buffer
+_SENTINEL = {"bf16": 0x7FC1, "f32": 0x7FC00001}  # NaN payloads nothing else writes
+
+
+def tdtype(dtype: str):
+    return torch.bfloat16 if dtype == "bf16" else torch.float32
+
+
+def to_device(arr: np.ndarray, dtype: str) -> torch.Tensor:
+    a = np.ascontiguousarray(arr)
+    if dtype == "bf16":
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(a).cuda()
+
+
+def to_host64(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy().astype(np.float64)
+
+
+class Guarded:
+    """A device tensor with sentinel-filled guard regions on both sides."""
+
+    def __init__(self, shape, torch_dtype, sentinel_bits: int):
+        n = int(np.prod(shape)) if len(shape) else 1
+        self.bits_dtype = torch.int16 if torch_dtype == torch.bfloat16 else torch.int32
+        self.buf = torch.empty(n + 2 * PAD, dtype=torch_dtype, device="cuda")
+        # both sentinels are positive in their signed view (0x7FC1, 0x7FC00001)
+        self.buf.view(self.bits_dtype).fill_(sentinel_bits)
+        self.sentinel = sentinel_bits
+        self.t = self.buf[PAD:PAD + n].view(*shape)
+
+    def guards_intact(self) -> bool:
+        b = self.buf.view(self.bits_dtype)
+        return bool((b[:PAD] == self.sentinel).all() and (b[-PAD:] == self.sentinel).all())
+
+
+@dataclass
+class GpuResult:
+    y: torch.Tensor
+    rstd: torch.Tensor
+    dx: torch.Tensor
+    dgamma: torch.Tensor
+    guards_ok: bool
+
+
+def run_gpu(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None) -> GpuResult:
+    """Forward then backward through the C ABI on device copies of ``inp``."""
+    dt = tdtype(w.dtype)
+    M, N = w.M, w.N
+    inplace = w.inplace_dx if inplace is None else inplace
+    x = to_device(inp["x"], w.dtype)
+    g = to_device(inp["gamma"], w.dtype)
+    dy = to_device(inp["dy"], w.dtype)
+    y = Guarded((M, N), dt, _SENTINEL[w.dtype])
+    rstd = Guarded((M,), torch.float32, _SENTINEL["f32"])
+    dg = Guarded((N,), torch.float32, _SENTINEL["f32"])
+    dx = None if inplace else Guarded((M, N), dt, _SENTINEL[w.dtype])
+    ws_bytes = rms.rms_bwd_workspace_size(M, N)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda")
+    rms.rms_fwd(x, g, y.t, rstd.t, w.eps, w.gemma, path=fwd_path or path)
+    rms.rms_bwd(dy, x, g, rstd.t, None if inplace else dx.t, dg.t, ws, w.gemma, inplace,
+                path=bwd_path or path)
+    torch.cuda.synchronize()
+    assert rms.rms_last_device_status() == rms.RMS_OK
+    guards = y.guards_intact() and rstd.guards_intact() and dg.guards_intact() and (
+        inplace or dx.guards_intact())
+    return GpuResult(y.t, rstd.t, dy if inplace else dx.t, dg.t, guards)
+
+
+def oracle_rows(w, inp, rows):
+    """Oracle y, r, dx and the dx tolerance scale for the given rows."""
+    x = storage_to_float64(inp["x"][rows], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.dtype)
+    dy = storage_to_float64(inp["dy"][rows], w.dtype)
+    y, r = orc.rms_forward(x, g, w.eps, w.gemma)
+    dx, _, dxs, _ = orc.rms_backward(x, g, dy, w.eps, w.gemma, with_scales=True)
+    return y, r, dx, dxs
+
+
+def oracle_dgamma(w, inp, block_rows: int = 1024):
+    """Oracle dgamma over all M rows; the test sums it over row blocks to
+    bound host memory (each block is the oracle's plain column sum)."""
+    N = w.N
+    total = np.zeros(N)
+    scale = np.zeros(N)
+    for r0 in range(0, w.M, block_rows):
+        r1 = min(w.M, r0 + block_rows)
+        x = storage_to_float64(inp["x"][r0:r1], w.dtype)
+        dy = storage_to_float64(inp["dy"][r0:r1], w.dtype)
+        d, s = orc.rms_dgamma(x, dy, w.eps, with_scales=True)
+        total += d
+        scale += s
+    return total, scale
+
+
+def sample_rows(M: int, n: int = 48, seed: int = 0) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    rows = set(np.linspace(0, M - 1, num=min(M, n // 2), dtype=np.int64).tolist())
+    rows.update(rng.integers(0, M, size=min(M, n // 2)).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+def check_against_oracle(w, inp, res: GpuResult, rows=None):
+    """All tolerance checks; ``rows`` None compares every row."""
+    rows = np.arange(w.M) if rows is None else rows
+    y_ref, r_ref, dx_ref, dxs = oracle_rows(w, inp, rows)
+    dg_ref, dgs = oracle_dgamma(w, inp)
+    idx = torch.as_tensor(rows, device=res.y.device)
+    checks = [
+        compare.check_y(to_host64(res.y.index_select(0, idx)), y_ref, w.dtype),
+        compare.check_rstd(to_host64(res.rstd.index_select(0, idx)), r_ref),
+        compare.check_dx(to_host64(res.dx.index_select(0, idx)), dx_ref, dxs, w.dtype),
+        compare.check_dgamma(to_host64(res.dgamma), dg_ref, dgs, w.dtype),
+    ]
+    return checks
+
+
+def assert_parity(w, inp, res: GpuResult, rows=None):
+    assert res.guards_ok, "a kernel wrote outside its output buffer"
+    checks = check_against_oracle(w, inp, res, rows)
+    bad = [str(c) for c in checks if not c.ok]
+    assert not bad, f"{w.name}: " + "; ".join(bad)
+    return checks
+
+
+def inputs_for(w):
+    return make_inputs(w)

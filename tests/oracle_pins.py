@@ -97,6 +97,14 @@ def pin_sum_not_mean(impl):
     _, dg1 = impl.rms_backward(x1, g, dy1, 1e-6)
     _, dg17 = impl.rms_backward(np.repeat(x1, 17, 0), g, np.repeat(dy1, 17, 0), 1e-6)
     assert np.allclose(dg17, 17.0 * dg1, rtol=1e-13, atol=1e-15)
+    # The dgamma-only sum: the table, and agreement with the full backward.
+    assert np.array_equal(impl.rms_dgamma(x, contrib, 0.0), np.array(c["expected_sum"]))
+    xs = rng.standard_normal((23, 11)) * rng.uniform(0.1, 10.0, (23, 1))
+    dys = rng.standard_normal((23, 11))
+    _, dgf = impl.rms_backward(xs, rng.uniform(0.5, 1.5, 11), dys, 1e-5)
+    dgo, sc = impl.rms_dgamma(xs, dys, 1e-5, with_scales=True)
+    assert np.allclose(dgo, dgf, rtol=1e-14, atol=1e-14 * sc.max())
+    assert np.all(sc >= np.abs(dgo))
 
 
 def _fd_loss_grads(impl, x, g, dy, eps, gemma, h_rel=1e-6):

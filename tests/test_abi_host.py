@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects invalid arguments on the host before any CUDA call.
+
+The pointers passed here are never dereferenced: every case fails
+validation, which runs before the library touches CUDA.
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = ROOT / "include" / "rmsnorm.h"
+
+(OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA, TIMEOUT) = range(7)
+A = 1 << 24  # fake, 256-byte aligned addresses A, 2A, ... that are never dereferenced
+FAKE = A
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from row_wise_normalization_rms_gb300 import build
+
+    build.build()
+    from row_wise_normalization_rms_gb300 import _lib
+
+    return _lib.load()
+
+
+def declared_functions():
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rms_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in rmsnorm.h but not exported"
+    from row_wise_normalization_rms_gb300 import _lib
+
+    assert sorted(_lib.SIGNATURES) == names
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.rms_status_string(s)
+    assert b"unknown" in lib.rms_status_string(99)
+
+
+def fwd(lib, x=A, g=2 * A, y=3 * A, r=4 * A, M=4, N=8, eps=1e-6,
+        dtype=1, gemma=0, path=0):
+    return lib.rms_fwd_ex(x, g, y, r, M, N, eps, dtype, gemma, path, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    nan, inf = float("nan"), float("inf")
+    assert fwd(lib, dtype=2) == INVALID
+    assert fwd(lib, dtype=-1) == INVALID
+    assert fwd(lib, gemma=2) == INVALID
+    assert fwd(lib, M=-1) == INVALID
+    assert fwd(lib, N=0) == INVALID
+    assert fwd(lib, N=-5) == INVALID
+    assert fwd(lib, eps=nan) == INVALID
+    assert fwd(lib, eps=inf) == INVALID
+    assert fwd(lib, eps=-1e-6) == INVALID
+    assert fwd(lib, path=7) == INVALID
+    assert fwd(lib, x=None) == INVALID
+    assert fwd(lib, g=None) == INVALID
+    assert fwd(lib, y=None) == INVALID
+    assert fwd(lib, r=None) == INVALID
+    assert fwd(lib, N=1 << 40) == UNSUPPORTED
+    assert fwd(lib, M=1 << 62, N=1 << 20) == INVALID  # size overflows int64
+
+
+def test_fwd_rejects_overlap(lib):
+    assert fwd(lib, y=A + 16) == INVALID          # y inside x
+    assert fwd(lib, y=2 * A - 16) == INVALID      # y's tail runs into gamma
+    assert fwd(lib, r=A + 8) == INVALID           # rstd inside x
+    assert fwd(lib, r=3 * A + 60) == INVALID      # rstd inside y
+
+
+def test_fwd_empty_batch_is_a_noop(lib):
+    assert fwd(lib, M=0, x=None, g=None, y=None, r=None) == OK
+
+
+def bwd(lib, dy=A, x=2 * A, g=3 * A, r=4 * A, dx=5 * A, dg=6 * A, ws=7 * A, wsb=1 << 30, M=4,
+        N=8, dtype=1, gemma=0, inplace=0,
+        path=0):
+    return lib.rms_bwd_ex(dy, x, g, r, dx, dg, ws, wsb, M, N, dtype, gemma, inplace, path, None)
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    assert bwd(lib, dtype=5) == INVALID
+    assert bwd(lib, gemma=-1) == INVALID
+    assert bwd(lib, inplace=2) == INVALID
+    assert bwd(lib, M=-3) == INVALID
+    assert bwd(lib, N=0) == INVALID
+    assert bwd(lib, path=-1) == INVALID
+    assert bwd(lib, dg=None) == INVALID
+    assert bwd(lib, dx=None) == INVALID
+    assert bwd(lib, x=None) == INVALID
+    assert bwd(lib, dy=None) == INVALID
+    assert bwd(lib, g=None) == INVALID
+    assert bwd(lib, r=None) == INVALID
+    # in place: dx must be NULL or dy itself
+    assert bwd(lib, inplace=1, dx=9 * A) == INVALID
+    # the workspace is required when there are rows
+    assert bwd(lib, ws=None) == WORKSPACE
+
+
+def test_set_wait_limit_roundtrip(lib):
+    prev = lib.rms_set_wait_limit(123)
+    assert lib.rms_set_wait_limit(-1) == 123
+    assert lib.rms_set_wait_limit(prev) > 0
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from row_wise_normalization_rms_gb300 import _lib
+
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.load()

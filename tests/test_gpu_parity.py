@@ -1,0 +1,279 @@
+"""CUDA path versus the fp64 oracle, element by element, through the C ABI.
+
+Small shapes are compared in full (every row, every column); the full-size
+workloads are compared on sampled rows for y, rstd and dx and in full for
+dgamma (the oracle sums all M rows).  Tolerances are those of
+``oracle.compare``.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import row_wise_normalization_rms_gb300 as rms
+    from oracle import rmsnorm_oracle as orc
+    from synthetic import WORKLOADS, Workload, storage_to_float64
+
+
+def _w(M, N, dtype, gemma=0, inplace=0, eps=1e-6, seed=0, **kw):
+    from synthetic import Workload
+
+    return Workload(name=f"t{M}x{N}_{dtype}_g{gemma}_i{inplace}", M=M, N=N, dtype=dtype, eps=eps,
+                    gemma=gemma, inplace_dx=inplace, seed=seed,
+                    gamma=("normal", 0.0, 0.1) if gemma else ("uniform", 0.5, 1.5),
+                    row_scale=("loguniform", 0.01, 100.0), **kw)
+
+
+SMALL_SHAPES = [
+    (1, 1), (3, 7), (17, 8), (5, 64), (64, 128), (33, 256), (31, 257), (128, 257), (40, 1000),
+    (9, 1024), (2000, 512), (1200, 1000), (7, 2048), (6, 3072), (900, 4096), (4, 5120),
+    (700, 8192), (3, 11008), (300, 16384), (2, 32768),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N", SMALL_SHAPES, ids=[f"{m}x{n}" for m, n in SMALL_SHAPES])
+@pytest.mark.parametrize("path", ["auto", "registers", "scalar"])
+def test_small_shapes_full_parity(M, N, dtype, path):
+    w = _w(M, N, dtype, seed=M + N)
+    b = 2 if dtype == "bf16" else 4
+    inp = H.inputs_for(w)
+    if path == "registers" and (N * b) % 16 != 0:
+        with pytest.raises(rms.RmsError) as ei:
+            H.run_gpu(w, inp, path=path)
+        assert ei.value.status == rms.RMS_ERR_ALIGNMENT
+        return
+    try:
+        res = H.run_gpu(w, inp, path=path)
+    except rms.RmsError as e:
+        assert e.status == rms.RMS_ERR_UNSUPPORTED and path != "auto", str(e)
+        pytest.skip(f"{path} mapping does not take N={N}")
+    H.assert_parity(w, inp, res)
+
+
+@pytest.mark.parametrize("gemma,inplace", [(0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("M,N", [(257, 3072), (65, 1000), (31, 257)])
+def test_gemma_and_inplace(M, N, dtype, gemma, inplace):
+    w = _w(M, N, dtype, gemma=gemma, inplace=inplace, seed=7)
+    inp = H.inputs_for(w)
+    H.assert_parity(w, inp, H.run_gpu(w, inp))
+
+
+FULL = [n for n in WORKLOADS] if torch.cuda.is_available() else []
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_workload_full_size(name):
+    """Every workload at its full size, in the mapping the benchmark uses."""
+    w = WORKLOADS[name]
+    inp = H.inputs_for(w)
+    res = H.run_gpu(w, inp)
+    rows = None if w.M * w.N <= (1 << 20) else H.sample_rows(w.M)
+    H.assert_parity(w, inp, res, rows)
+
+
+def test_dgamma_bitwise_reproducible():
+    w = WORKLOADS["llama7b_bf16_8192x4096"]
+    inp = H.inputs_for(w)
+    a = H.run_gpu(w, inp)
+    b = H.run_gpu(w, inp)
+    c = H.run_gpu(w, inp)
+    assert torch.equal(a.dgamma.view(torch.int32), b.dgamma.view(torch.int32))
+    assert torch.equal(a.dgamma.view(torch.int32), c.dgamma.view(torch.int32))
+    assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("path", ["auto", "registers", "scalar"])
+def test_inplace_matches_out_of_place_bitwise(dtype, path):
+    w = _w(1500, 2048, dtype, seed=3)
+    inp = H.inputs_for(w)
+    a = H.run_gpu(w, inp, path=path, inplace=0)
+    b = H.run_gpu(w, inp, path=path, inplace=1)
+    bits = torch.int16 if dtype == "bf16" else torch.int32
+    assert torch.equal(a.dx.view(bits), b.dx.view(bits))
+    assert torch.equal(a.dgamma.view(torch.int32), b.dgamma.view(torch.int32))
+
+
+@pytest.mark.parametrize("N", [1000, 4096, 8192])
+def test_bf16_cast_order(N):
+    """y rounds x*r to bf16 before the weight multiply: nearly every element
+    equals the oracle's emulation of that order bit for bit (the rest differ
+    by one bf16 step where the fp32 rstd rounds differently), and many
+    elements differ from a single rounding of the exact product."""
+    w = _w(256, N, "bf16", seed=N)
+    inp = H.inputs_for(w)
+    res = H.run_gpu(w, inp)
+    x = storage_to_float64(inp["x"], "bf16")
+    g = storage_to_float64(inp["gamma"], "bf16")
+    emu = orc.emulate_forward_lowp(x, g, w.eps, 0, "bf16")
+    got = H.to_host64(res.y)
+    same = np.mean(got == emu)
+    assert same >= 0.999, same
+    diff = got != emu
+    assert np.all(np.abs(got[diff] - emu[diff]) <= 2.0 ** -7 * np.abs(emu[diff]))
+    exact, _ = orc.rms_forward(x, g, w.eps)
+    once = torch.tensor(exact).float().to(torch.bfloat16).double().numpy()
+    assert np.mean(got != once) > 0.01
+
+
+def test_gemma_equals_plain_with_shifted_weight_f32():
+    w = _w(300, 1024, "f32", gemma=1, seed=5)
+    inp = H.inputs_for(w)
+    a = H.run_gpu(w, inp)
+    shifted = dict(inp)
+    shifted["gamma"] = (1.0 + inp["gamma"].astype(np.float32)).astype(np.float32)
+    b = H.run_gpu(dataclasses.replace(w, gemma=0), shifted)
+    assert torch.equal(a.y, b.y) and torch.equal(a.dx, b.dx) and torch.equal(a.dgamma, b.dgamma)
+
+
+def test_printed_worked_examples_fp32():
+    """The tutorial's hand-worked rows through the CUDA path."""
+    x = torch.tensor([[3.0, 4.0]], device="cuda")
+    y = torch.empty_like(x)
+    r = torch.empty(1, device="cuda")
+    for gamma, expect in (([1.0, 1.0], [0.848528, 1.131371]), ([2.0, 0.5], [1.697056, 0.565685])):
+        g = torch.tensor(gamma, device="cuda")
+        rms.rms_fwd(x, g, y, r, 1e-6)
+        torch.cuda.synchronize()
+        assert np.all(np.abs(y.cpu().numpy()[0] - expect) <= 5e-7 + 1e-6 * np.abs(expect))
+    assert abs(r.item() - 0.282843) <= 5e-7
+    g = torch.ones(2, device="cuda")
+    rms.rms_fwd(x, g, y, r, 1e-6)
+    dy = torch.tensor([[1.0, 2.0]], device="cuda")
+    dx = torch.empty_like(x)
+    dg = torch.empty(2, device="cuda")
+    ws = torch.empty(rms.rms_bwd_workspace_size(1, 2), dtype=torch.uint8, device="cuda")
+    rms.rms_bwd(dy, x, g, r, dx, dg, ws)
+    torch.cuda.synchronize()
+    assert np.all(np.abs(dx.cpu().numpy()[0] - [-0.090510, 0.067882]) <= 5e-7 + 1e-6)
+    # 257 ones: divide by N = 257, not by a padded 512.
+    ones = torch.ones(1, 257, device="cuda")
+    y1 = torch.empty_like(ones)
+    rms.rms_fwd(ones, torch.ones(257, device="cuda"), y1, r, 1e-6)
+    torch.cuda.synchronize()
+    assert torch.all((y1 - 0.9999995).abs() <= 5e-7)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sum_not_mean_on_gpu(dtype):
+    dt = H.tdtype(dtype)
+    x = torch.ones(2, 8, device="cuda", dtype=dt)
+    dy = torch.tensor([[1.0, 2.0] * 4, [3.0, 4.0] * 4], device="cuda", dtype=dt)
+    g = torch.ones(8, device="cuda", dtype=dt)
+    r = torch.ones(2, device="cuda")  # eps = 0 on rows of ones
+    dx = torch.empty_like(x)
+    dg = torch.empty(8, device="cuda")
+    ws = torch.empty(rms.rms_bwd_workspace_size(2, 8), dtype=torch.uint8, device="cuda")
+    rms.rms_bwd(dy, x, g, r, dx, dg, ws)
+    torch.cuda.synchronize()
+    assert dg.tolist() == [4.0, 6.0] * 4
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_edge_rows(dtype):
+    dt = H.tdtype(dtype)
+    eps = 1e-4
+    x = torch.zeros(3, 64, device="cuda", dtype=dt)
+    x[1] = torch.linspace(-2, 2, 64, device="cuda").to(dt)
+    x[2, 5] = float("nan")
+    g = torch.full((64,), 1.5, device="cuda", dtype=dt)
+    y = torch.empty_like(x)
+    r = torch.empty(3, device="cuda")
+    rms.rms_fwd(x, g, y, r, eps)
+    dy = torch.ones_like(x)
+    dx = torch.empty_like(x)
+    dg = torch.empty(64, device="cuda")
+    ws = torch.empty(rms.rms_bwd_workspace_size(3, 64), dtype=torch.uint8, device="cuda")
+    rms.rms_bwd(dy, x, g, r, dx, dg, ws)
+    torch.cuda.synchronize()
+    assert torch.all(y[0] == 0) and abs(r[0].item() - 100.0) < 1e-4
+    assert torch.allclose(dx[0].float(), torch.full((64,), 150.0, device="cuda"), rtol=1e-2)
+    assert torch.isnan(y[2]).all() and torch.isnan(r[2])
+    # eps = 0 on a zero row: r = inf and y = NaN, no special case.
+    rms.rms_fwd(x[:1].contiguous(), g, y[:1], r[:1], 0.0)
+    torch.cuda.synchronize()
+    assert torch.isinf(r[0]) and torch.isnan(y[0]).all()
+
+
+def test_empty_batch():
+    x = torch.empty(0, 128, device="cuda")
+    g = torch.ones(128, device="cuda")
+    rms.rms_fwd(x, g, torch.empty_like(x), torch.empty(0, device="cuda"))
+    dg = torch.full((128,), 7.0, device="cuda")
+    rms.rms_bwd(x, x, g, torch.empty(0, device="cuda"), torch.empty_like(x), dg,
+                torch.empty(0, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.all(dg == 0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_misaligned_pointers_use_scalar_path(dtype):
+    """Views offset by one element are legal inputs; a forced vector mapping
+    refuses them instead of reading unaligned vectors."""
+    w = _w(100, 1024, dtype, seed=9)
+    inp = H.inputs_for(w)
+    dt = H.tdtype(dtype)
+    M, N = w.M, w.N
+    xb = torch.empty(M * N + 1, dtype=dt, device="cuda")
+    x = xb[1:].view(M, N)
+    x.copy_(H.to_device(inp["x"], dtype))
+    g = H.to_device(inp["gamma"], dtype)
+    yb = torch.empty(M * N + 1, dtype=dt, device="cuda")
+    y = yb[1:].view(M, N)
+    r = torch.empty(M, device="cuda")
+    with pytest.raises(rms.RmsError) as ei:
+        rms.rms_fwd(x, g, y, r, w.eps, path="registers")
+    assert ei.value.status == rms.RMS_ERR_ALIGNMENT
+    rms.rms_fwd(x, g, y, r, w.eps)
+    dy = H.to_device(inp["dy"], dtype)
+    dx = torch.empty(M * N + 1, dtype=dt, device="cuda")[1:].view(M, N)
+    dg = torch.empty(N, device="cuda")
+    ws = torch.empty(rms.rms_bwd_workspace_size(M, N), dtype=torch.uint8, device="cuda")
+    rms.rms_bwd(dy, x, g, r, dx, dg, ws)
+    torch.cuda.synchronize()
+    res = H.GpuResult(y, r, dx, dg, True)
+    H.assert_parity(w, inp, res)
+
+
+def test_workspace_checks():
+    M, N = 4096, 1024
+    x = torch.randn(M, N, device="cuda")
+    g = torch.ones(N, device="cuda")
+    r = torch.ones(M, device="cuda")
+    need = rms.rms_bwd_workspace_size(M, N)
+    assert need > 0 and need % 256 == 0
+    small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(rms.RmsError) as ei:
+        rms.rms_bwd(x, x.clone(), g, r, torch.empty_like(x), torch.empty(N, device="cuda"), small)
+    assert ei.value.status == rms.RMS_ERR_WORKSPACE
+    odd = torch.empty(need + 512, dtype=torch.uint8, device="cuda")[16:]
+    with pytest.raises(rms.RmsError) as ei:
+        rms.rms_bwd(x, x.clone(), g, r, torch.empty_like(x), torch.empty(N, device="cuda"), odd)
+    assert ei.value.status == rms.RMS_ERR_WORKSPACE
+
+
+def test_overlapping_outputs_rejected_on_device_buffers():
+    M, N = 64, 256
+    buf = torch.randn(2 * M * N, device="cuda")
+    x = buf[: M * N].view(M, N)
+    y = buf[M * N // 2: M * N // 2 + M * N].view(M, N)
+    with pytest.raises(rms.RmsError) as ei:
+        rms.rms_fwd(x, torch.ones(N, device="cuda"), y, torch.empty(M, device="cuda"))
+    assert ei.value.status == rms.RMS_ERR_INVALID_ARG
+
+
+def test_launch_count_and_status():
+    before = rms.rms_launch_count()
+    w = _w(64, 128, "f32")
+    inp = H.inputs_for(w)
+    H.run_gpu(w, inp)
+    assert rms.rms_launch_count() - before == 3
+    assert rms.rms_last_device_status() == rms.RMS_OK

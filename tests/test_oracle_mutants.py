@@ -76,6 +76,11 @@ def mutant(name):
         m.rms_rstd = lambda x, eps: 1.0 / np.sqrt(np.mean(np.asarray(x, np.float64) ** 2, axis=-1))
     elif name == "rms_not_mean_square":
         m.rms_rstd = lambda x, eps: 1.0 / np.sqrt(np.mean(np.abs(np.asarray(x, np.float64)), axis=-1) + eps)
+    elif name == "dgamma_only_mean":
+        orig = m.rms_dgamma
+        m.rms_dgamma = lambda x, dy, eps, with_scales=False, _o=orig: (
+            (lambda r: (r[0] / np.shape(x)[0], r[1]) if with_scales else r / np.shape(x)[0])(
+                _o(x, dy, eps, with_scales)))
     elif name == "gemma_ignored":
         m.weight = lambda gamma, gemma=0: np.asarray(gamma, np.float64)
     elif name == "gamma_reversed":
@@ -124,6 +129,7 @@ MUTANTS = [
     "dgamma_mean",
     "dgamma_without_r",
     "dgamma_times_weight",
+    "dgamma_only_mean",
     "normed_form_missing_n",
     "emulation_single_rounding",
     "emulation_weight_first",
