@@ -15,7 +15,8 @@ from, because dx and dgamma are differences/sums of signed terms that can
 cancel to ~0 (where a plain |err|/|ref| is ill-posed):
 
 * y:      |e| <= tol * |ref|
-* dx:     |e| <= tol * (|ref| + r|u| + |x| r^3 |c|)
+* dx:     |e| <= tol * (|ref| + r|u| + |x| r^3 mean|u x|)   (c = mean(u x) is
+          itself a sum of signed terms)
 * dgamma: |e| <= tol * (|ref| + sum_i |dy x r|)
 
 Each check also reports the plain max abs / max rel error and the normwise

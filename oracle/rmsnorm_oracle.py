@@ -72,7 +72,9 @@ def rms_backward(x, gamma, dy, eps: float, gemma: int = 0, with_scales: bool = F
 
     With ``with_scales`` it also returns the magnitudes the two outputs are
     built from, used to scale tolerances where the terms cancel:
-    ``dx_scale = r·|u| + |x|·r³·|c|`` and ``dgamma_scale = Σ_i |dy·x·r|``.
+    ``dx_scale = r·|u| + |x|·r³·mean_j|u·x|`` (c is itself a mean of signed
+    terms, so its rounding error scales with the mean of their sizes) and
+    ``dgamma_scale = Σ_i |dy·x·r|``.
     """
     x = _f64(x)
     dy = _f64(dy)
@@ -84,7 +86,7 @@ def rms_backward(x, gamma, dy, eps: float, gemma: int = 0, with_scales: bool = F
     dgamma = np.sum(dy * x * r[:, None], axis=0)
     if not with_scales:
         return dx, dgamma
-    dx_scale = r[:, None] * np.abs(u) + np.abs(x) * (r3 * np.abs(c))[:, None]
+    dx_scale = r[:, None] * np.abs(u) + np.abs(x) * (r3 * np.mean(np.abs(u * x), axis=-1))[:, None]
     dgamma_scale = np.sum(np.abs(dy * x * r[:, None]), axis=0)
     return dx, dgamma, dx_scale, dgamma_scale
 

@@ -60,7 +60,7 @@ def _bwd_factory(variant):
             dgamma = np.sum(dy * x * r[:, None], axis=0)
         if not with_scales:
             return dx, dgamma
-        dxs = r[:, None] * np.abs(u) + np.abs(x) * (r ** 3 * np.abs(c))[:, None]
+        dxs = r[:, None] * np.abs(u) + np.abs(x) * (r ** 3 * np.mean(np.abs(u * x), axis=-1))[:, None]
         return dx, dgamma, dxs, np.sum(np.abs(dy * x * r[:, None]), axis=0)
     return rms_backward
 
