@@ -78,14 +78,25 @@ size_t workspace_need(int64_t M, int64_t N, const DeviceInfo& d) {
   return (bytes + 255) / 256 * 256;
 }
 
+// Row bytes above which the automatic choice stages rows in shared memory
+// instead of holding them in registers.
+constexpr int64_t kAutoStagedRowBytes = 16384;
+
+bool prefer_staged(int N, int dtype, bool bwd) {
+  (void)bwd;
+  return (int64_t)N * elem_bytes(dtype) > kAutoStagedRowBytes;
+}
+
 // Picks the row mapping for a call.  A forced path that cannot take the
 // shape is an error, never a silent switch.
 rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const DeviceInfo& d,
                   Mapping* m) {
   switch (path) {
     case RMS_PATH_AUTO:
-      if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m)) return RMS_OK;
+      if (aligned && prefer_staged(N, dtype, bwd) && rmsi::plan_staged(N, dtype, bwd, d, m))
+        return RMS_OK;
       if (aligned && rmsi::plan_registers(N, dtype, bwd, m)) return RMS_OK;
+      if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m)) return RMS_OK;
       if (rmsi::plan_scalar(N, dtype, bwd, d, m)) return RMS_OK;
       return RMS_ERR_UNSUPPORTED;
     case RMS_PATH_REGISTERS:

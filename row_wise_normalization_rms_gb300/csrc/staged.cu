@@ -1,34 +1,571 @@
-// Staged mapping (rows staged in shared memory by cp.async.bulk) and the
-// device status word its bounded waits report through.
+// Staged mapping: persistent CTAs stream tiles of R consecutive rows
+// (R * N contiguous elements) from HBM into an S-deep ring of shared-memory
+// stages with bulk TMA copies (cp.async.bulk + mbarrier), so S-1 tiles are
+// always in flight no matter how long the math on the current tile takes.
+// A group of G threads owns one row of the tile; each thread moves its
+// 16-byte vectors from the stage into registers, the group reduces, and the
+// results go straight to global memory.  The stage is handed back to the
+// copy engine as soon as every thread has read it (one barrier per tile,
+// which the row reduction needs anyway).
+//
+// Forward computes r and y exactly as the register mapping does; backward
+// stages x and dy together and accumulates dgamma column partials in
+// registers across the CTA's tiles (static tile order), one workspace row
+// per CTA.
+//
+// Every mbarrier wait is bounded.  If a wait gives up, the CTA stops
+// consuming tiles, waits (again bounded) for the copies it has in flight,
+// sets the device status word and exits; the host reads that word through
+// rms_last_device_status().  Nothing spins without a limit.
+//
+// Sources: "Hướng dẫn Triton RMSNorm: kernel, backward…" (formulas, true-N
+// mean, per-part dgamma partials reduced in a second pass); "第 07 章:
+// LayerNorm——反向传播与原子锁", step 3 (a row too wide for one block is
+// walked through in chunks; here it is staged whole in shared memory).
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace rmsk {
 
 // Nonzero once a bounded wait gave up; read and cleared by the host.
 __device__ int g_rms_device_status = 0;
 
+constexpr int kHeaderBytes = 1024;  // barriers, reduction slots, abort flags
+
+struct StagedParams {
+  const void* x;
+  const void* gamma;
+  const float* rstd_in;  // backward: saved r
+  float* rstd_out;       // forward: r
+  void* y;               // forward output
+  const void* dy;        // backward input
+  void* dx;              // backward output (may equal dy)
+  float* ws;             // backward: [gridDim.x][N] column partials
+  int64_t M;
+  int N;
+  float eps;
+  int gemma;
+  int G;  // threads per row
+  int R;  // rows per tile
+  int S;  // stages
+  int64_t ntiles;
+  uint32_t tile_bytes;   // R * N * sizeof(T)
+  uint32_t stage_bytes;  // tile_bytes (forward) or 2 * tile_bytes (backward)
+  long long wait_limit;
+};
+
+struct StageHeader {
+  uint64_t* full;
+  float* red;           // [2][32]
+  volatile int* abort;  // [2]
+  uint8_t* stages;
+};
+
+__device__ __forceinline__ StageHeader header(uint8_t* smem) {
+  StageHeader h;
+  h.full = reinterpret_cast<uint64_t*>(smem);
+  h.red = reinterpret_cast<float*>(smem + 64);
+  h.abort = reinterpret_cast<volatile int*>(smem + 64 + 2 * 32 * sizeof(float));
+  h.stages = smem + kHeaderBytes;
+  return h;
+}
+
+// Thread 0: start the copy of local tile i (tile blockIdx.x + i*gridDim.x)
+// into stage i % S: x, and for the backward dy right after it.
+template <typename T, bool BWD>
+__device__ __forceinline__ void issue_tile(const StagedParams& p, const StageHeader& h, int64_t i,
+                                           uint64_t pol) {
+  const int64_t t = blockIdx.x + i * gridDim.x;
+  const int64_t row0 = t * p.R;
+  const int64_t rows = min((int64_t)p.R, p.M - row0);
+  const int64_t row_bytes = (int64_t)p.N * sizeof(T);
+  const uint32_t bytes = (uint32_t)(rows * row_bytes);
+  const int s = (int)(i % p.S);
+  const uint32_t bar = smem_u32(&h.full[s]);
+  const uint32_t dst = smem_u32(h.stages + (size_t)s * p.stage_bytes);
+  mbar_arrive_expect_tx(bar, BWD ? 2 * bytes : bytes);
+  tma_load_1d(dst, static_cast<const char*>(p.x) + row0 * row_bytes, bytes, bar, pol);
+  if (BWD)
+    tma_load_1d(dst + p.tile_bytes, static_cast<const char*>(p.dy) + row0 * row_bytes, bytes, bar,
+                pol);
+}
+
+// After an abort at local tile i: wait (bounded) for the copies this CTA
+// issued and has not consumed (tiles i .. issued-1), then raise the device
+// status.  Thread 0 only.
+__device__ __forceinline__ void drain_and_flag(const StagedParams& p, const StageHeader& h,
+                                               int64_t i, int64_t issued) {
+  for (int64_t j = i; j < issued; ++j)
+    mbar_wait(smem_u32(&h.full[j % p.S]), (uint32_t)((j / p.S) & 1), kDrainPolls);
+  g_rms_device_status = 1;
+  __threadfence();
+}
+
+__device__ __forceinline__ void init_barriers(const StagedParams& p, const StageHeader& h) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.S; ++s) mbar_init(smem_u32(&h.full[s]), 1);
+    h.abort[0] = 0;
+    h.abort[1] = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+// Pipeline shared by both kernels.  Local tile i lives in stage i % S.
+// Iteration i: wait for tile i, first pass over it (row partial sums),
+// barrier, second pass (outputs).  The barrier of iteration i also proves
+// every thread finished the second pass of tile i-1, so right after it
+// thread 0 refills that stage with tile i-1+S: S-2 tiles stay in flight
+// while tile i is processed, and no row slice has to stay in registers
+// across the barrier.
+
+template <typename T, int KV>
+__global__ void __launch_bounds__(1024)
+rms_fwd_staged_kernel(const StagedParams p) {
+  using E = Elem<T>;
+  constexpr int VN = E::kPerVec;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const StageHeader h = header(smem);
+  const int NV = p.N / VN;
+  const int q = threadIdx.x / p.G;
+  const int lig = threadIdx.x - q * p.G;
+  const int warp = threadIdx.x >> 5;
+  const int first_warp = q * (p.G >> 5);
+  const int nw = p.G >> 5;
+  const int64_t my_tiles = (p.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  const uint32_t row_off = (uint32_t)(q * p.N * (int)sizeof(T));
+
+  init_barriers(p, h);
+  uint64_t pol = 0;
+  int64_t issued = 0;  // thread 0 only
+  if (threadIdx.x == 0) {
+    pol = l2_evict_first_policy();
+    const int64_t pre = min((int64_t)p.S, my_tiles);
+    for (; issued < pre; ++issued) issue_tile<T, false>(p, h, issued, pol);
+  }
+
+  const uint4* gv = reinterpret_cast<const uint4*>(p.gamma);
+  uint4 gw[KV];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = lig + k * p.G;
+    gw[k] = v < NV ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  int64_t i = 0;
+  bool aborted = false;
+  for (; i < my_tiles; ++i) {
+    const int s = (int)(i % p.S);
+    const int buf = (int)(i & 1);
+    const int64_t row = (blockIdx.x + i * gridDim.x) * p.R + q;
+    const bool active = row < p.M;
+    if (!mbar_wait(smem_u32(&h.full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) h.abort[buf] = 1;
+
+    const uint32_t xs = smem_u32(h.stages + (size_t)s * p.stage_bytes) + row_off;
+    float ss = 0.f;
+    if (active) {
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const int v = lig + k * p.G;
+        if (v < NV) {
+          float f[VN];
+          E::unpack(lds128(xs + 16u * v), f);
+#pragma unroll
+          for (int e = 0; e < VN; ++e) ss = fmaf(f[e], f[e], ss);
+        }
+      }
+    }
+    ss = warp_sum(ss);
+    if ((threadIdx.x & 31) == 0) h.red[buf * 32 + warp] = ss;
+    __syncthreads();  // partial sums visible; tile i-1 fully consumed
+    if (h.abort[buf]) {
+      aborted = true;
+      break;
+    }
+    if (threadIdx.x == 0 && i >= 1 && issued < my_tiles) issue_tile<T, false>(p, h, issued++, pol);
+
+    float tot = 0.f;
+    for (int w = 0; w < nw; ++w) tot += h.red[buf * 32 + first_warp + w];
+    const float r = 1.0f / sqrtf(tot / (float)p.N + p.eps);
+    if (active) {
+      if (lig == 0) p.rstd_out[row] = r;
+      uint4* yr = reinterpret_cast<uint4*>(p.y) + row * (int64_t)NV;
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const int v = lig + k * p.G;
+        if (v < NV) {
+          float f[VN], g[VN], o[VN];
+          E::unpack(lds128(xs + 16u * v), f);
+          E::unpack(gw[k], g);
+          if (p.gemma) {
+#pragma unroll
+            for (int e = 0; e < VN; ++e) o[e] = (f[e] * r) * (1.0f + g[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < VN; ++e) o[e] = E::round(f[e] * r) * g[e];
+          }
+          st_stream(yr + v, E::pack(o));
+        }
+      }
+    }
+  }
+  if (aborted && threadIdx.x == 0) drain_and_flag(p, h, i, issued);
+}
+
+template <typename T, int KV>
+__global__ void __launch_bounds__(512)
+rms_bwd_staged_kernel(const StagedParams p) {
+  using E = Elem<T>;
+  constexpr int VN = E::kPerVec;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const StageHeader h = header(smem);
+  const int NV = p.N / VN;
+  const int q = threadIdx.x / p.G;
+  const int lig = threadIdx.x - q * p.G;
+  const int warp = threadIdx.x >> 5;
+  const int first_warp = q * (p.G >> 5);
+  const int nw = p.G >> 5;
+  const int64_t my_tiles = (p.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+  const uint32_t row_off = (uint32_t)(q * p.N * (int)sizeof(T));
+
+  init_barriers(p, h);
+  uint64_t pol = 0;
+  int64_t issued = 0;  // thread 0 only
+  if (threadIdx.x == 0) {
+    pol = l2_evict_first_policy();
+    const int64_t pre = min((int64_t)p.S, my_tiles);
+    for (; issued < pre; ++issued) issue_tile<T, true>(p, h, issued, pol);
+  }
+
+  const uint4* gv = reinterpret_cast<const uint4*>(p.gamma);
+  uint4 gw[KV];
+  float acc[KV][VN];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = lig + k * p.G;
+    gw[k] = v < NV ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int e = 0; e < VN; ++e) acc[k][e] = 0.f;
+  }
+
+  int64_t i = 0;
+  bool aborted = false;
+  for (; i < my_tiles; ++i) {
+    const int s = (int)(i % p.S);
+    const int buf = (int)(i & 1);
+    const int64_t row = (blockIdx.x + i * gridDim.x) * p.R + q;
+    const bool active = row < p.M;
+    const float r = active ? p.rstd_in[row] : 0.f;
+    if (!mbar_wait(smem_u32(&h.full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) h.abort[buf] = 1;
+
+    const uint32_t xs = smem_u32(h.stages + (size_t)s * p.stage_bytes) + row_off;
+    const uint32_t ds = xs + p.tile_bytes;
+    // First pass: sum(u*x) for the row, and this row's dgamma terms dy*x*r.
+    float sux = 0.f;
+    if (active) {
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const int v = lig + k * p.G;
+        if (v < NV) {
+          float f[VN], d[VN], g[VN];
+          E::unpack(lds128(xs + 16u * v), f);
+          E::unpack(lds128(ds + 16u * v), d);
+          E::unpack(gw[k], g);
+#pragma unroll
+          for (int e = 0; e < VN; ++e) {
+            const float w = p.gemma ? 1.0f + g[e] : g[e];
+            sux = fmaf(d[e] * w, f[e], sux);
+            acc[k][e] = fmaf(d[e] * f[e], r, acc[k][e]);
+          }
+        }
+      }
+    }
+    sux = warp_sum(sux);
+    if ((threadIdx.x & 31) == 0) h.red[buf * 32 + warp] = sux;
+    __syncthreads();  // partial sums visible; tile i-1 fully consumed
+    if (h.abort[buf]) {
+      aborted = true;
+      break;
+    }
+    if (threadIdx.x == 0 && i >= 1 && issued < my_tiles) issue_tile<T, true>(p, h, issued++, pol);
+
+    float tot = 0.f;
+    for (int w = 0; w < nw; ++w) tot += h.red[buf * 32 + first_warp + w];
+    const float r3c = r * r * r * (tot / (float)p.N);
+    // Second pass: dx = r*u - x*r^3*c.
+    if (active) {
+      uint4* out = reinterpret_cast<uint4*>(p.dx) + row * (int64_t)NV;
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const int v = lig + k * p.G;
+        if (v < NV) {
+          float f[VN], d[VN], g[VN], o[VN];
+          E::unpack(lds128(xs + 16u * v), f);
+          E::unpack(lds128(ds + 16u * v), d);
+          E::unpack(gw[k], g);
+#pragma unroll
+          for (int e = 0; e < VN; ++e) {
+            const float w = p.gemma ? 1.0f + g[e] : g[e];
+            o[e] = r * (d[e] * w) - f[e] * r3c;
+          }
+          st_stream(out + v, E::pack(o));
+        }
+      }
+    }
+  }
+  if (aborted) {
+    if (threadIdx.x == 0) drain_and_flag(p, h, i, issued);
+    return;  // the partial row stays unwritten; the status word reports it
+  }
+
+  // This CTA's column partials: one workspace row, groups combined in
+  // group order through the (now idle) stage memory.
+  float* wp = p.ws + (int64_t)blockIdx.x * p.N;
+  if (p.R == 1) {
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = lig + k * p.G;
+      if (v < NV) {
+        float4* w4 = reinterpret_cast<float4*>(wp + (int64_t)v * VN);
+#pragma unroll
+        for (int c = 0; c < VN / 4; ++c)
+          w4[c] = make_float4(acc[k][4 * c], acc[k][4 * c + 1], acc[k][4 * c + 2], acc[k][4 * c + 3]);
+      }
+    }
+  } else {
+    float* part = reinterpret_cast<float*>(h.stages);  // [R][N] fits in the stage ring
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = lig + k * p.G;
+      if (v < NV) {
+#pragma unroll
+        for (int e = 0; e < VN; ++e) part[(int64_t)q * p.N + v * VN + e] = acc[k][e];
+      }
+    }
+    __syncthreads();
+    for (int j = threadIdx.x; j < p.N; j += blockDim.x) {
+      float t = 0.f;
+      for (int qq = 0; qq < p.R; ++qq) t += part[(int64_t)qq * p.N + j];
+      wp[j] = t;
+    }
+  }
+}
+
+template <typename T, bool BWD>
+static const void* staged_ptr(int kv) {
+  if (BWD) {
+    switch (kv) {
+      case 1: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 1>);
+      case 2: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 2>);
+      case 4: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 4>);
+    }
+  } else {
+    switch (kv) {
+      case 1: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 1>);
+      case 2: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 2>);
+      case 4: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 4>);
+    }
+  }
+  return nullptr;
+}
+
 }  // namespace rmsk
 
 namespace rmsi {
 
+namespace {
+
+#ifndef RMS_STAGED_SMEM_PER_SM
+#define RMS_STAGED_SMEM_PER_SM (200 * 1024)
+#endif
+
+const void* staged_kernel(int dtype, bool bwd, int kv) {
+  if (dtype == kBF16)
+    return bwd ? rmsk::staged_ptr<__nv_bfloat16, true>(kv) : rmsk::staged_ptr<__nv_bfloat16, false>(kv);
+  return bwd ? rmsk::staged_ptr<float, true>(kv) : rmsk::staged_ptr<float, false>(kv);
+}
+
+// Per (kernel, device): dynamic shared memory opted in and the occupancy
+// for a (threads, smem) pair, so repeated calls do no driver queries.
+struct OccEntry {
+  const void* k;
+  int dev, threads;
+  size_t smem;
+  int occ;
+};
+std::mutex g_occ_mu;
+OccEntry g_occ[64];
+int g_occ_n = 0;
+
+cudaError_t occupancy(const void* k, int dev, int threads, size_t smem, int* occ) {
+  std::lock_guard<std::mutex> lk(g_occ_mu);
+  for (int i = 0; i < g_occ_n; ++i) {
+    const OccEntry& e = g_occ[i];
+    if (e.k == k && e.dev == dev && e.threads == threads && e.smem == smem) {
+      *occ = e.occ;
+      return cudaSuccess;
+    }
+  }
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{k, dev, threads, smem, *occ};
+  return cudaSuccess;
+}
+
+}  // namespace
+
+// Tiles of R rows (about 16 KiB of x, at most 16 rows), G threads per row
+// with up to 4 vectors each, and as many stages as fit in the per-SM
+// shared-memory budget: two CTAs per SM when each can keep three stages,
+// else one CTA with at least three.
 bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
-  (void)N; (void)dtype; (void)bwd; (void)d; (void)m;
-  return false;
+  const int b = dtype == kBF16 ? 2 : 4;
+  if (N <= 0 || ((int64_t)N * b) % 16 != 0) return false;
+  const int64_t row_bytes = (int64_t)N * b;
+  const int NV = (int)(row_bytes / 16);
+  const int max_threads = bwd ? 512 : 1024;
+  int kv, G;
+  if (NV <= 32) {
+    kv = 1; G = 32;
+  } else if (NV <= 64) {
+    kv = 2; G = 32;
+  } else {
+    kv = 4;
+    G = ((NV + 3) / 4 + 31) / 32 * 32;
+    if (G > max_threads) return false;
+  }
+  int R = (int)(16384 / row_bytes);
+  if (R < 1) R = 1;
+  if (R > 16) R = 16;
+  while (R > 1 && G * R > max_threads) --R;
+  const int64_t tile = R * row_bytes;
+  const int64_t stage = bwd ? 2 * tile : tile;
+  const int64_t budget = RMS_STAGED_SMEM_PER_SM;
+  const int64_t cap = (int64_t)d.smem_optin - rmsk::kHeaderBytes;
+  // At least three stages: one being processed, one whose refill waits for
+  // the next barrier, and at least one more in flight.
+  int cps, S;
+  if (2 * 3 * stage <= budget && budget / 2 <= cap) {
+    cps = 2;
+    S = (int)((budget / 2) / stage);
+  } else if (3 * stage <= std::min(budget, cap)) {
+    cps = 1;
+    S = (int)(std::min(budget, cap) / stage);
+  } else {
+    return false;
+  }
+  if (S > 8) S = 8;
+  m->path = kStaged;
+  m->kv = kv;
+  m->G = G;
+  m->rows_per_cta = R;
+  m->threads = G * R;
+  m->stages = S;
+  m->smem = rmsk::kHeaderBytes + (size_t)S * stage;
+  m->blocks = cps;  // CTAs per SM wanted; the launcher turns it into a grid
+  return true;
 }
 
-cudaError_t launch_fwd_staged(const FwdArgs&, const Mapping&, const DeviceInfo&, long long,
-                              cudaStream_t) {
-  return cudaErrorNotSupported;
+static cudaError_t grid_for(const void* k, const Mapping& m, const DeviceInfo& d, int64_t ntiles,
+                            int64_t* grid) {
+  int occ = 0;
+  cudaError_t e = occupancy(k, d.device, m.threads, m.smem, &occ);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  const int64_t per_sm = std::min<int64_t>(occ, m.blocks);
+  int64_t g = per_sm * d.sms;
+  if (g > ntiles) g = ntiles;
+  if (g < 1) g = 1;
+  *grid = g;
+  return cudaSuccess;
 }
 
-cudaError_t size_bwd_staged(const BwdArgs&, const DeviceInfo&, Mapping*) {
-  return cudaErrorNotSupported;
+static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, int b, bool bwd,
+                                 long long wait_limit) {
+  rmsk::StagedParams p{};
+  p.M = M;
+  p.N = N;
+  p.G = m.G;
+  p.R = m.rows_per_cta;
+  p.S = m.stages;
+  p.ntiles = (M + p.R - 1) / p.R;
+  p.tile_bytes = (uint32_t)((int64_t)p.R * N * b);
+  p.stage_bytes = bwd ? 2 * p.tile_bytes : p.tile_bytes;
+  p.wait_limit = wait_limit;
+  return p;
 }
 
-cudaError_t launch_bwd_staged(const BwdArgs&, const Mapping&, const DeviceInfo&, long long,
-                              cudaStream_t) {
-  return cudaErrorNotSupported;
+template <typename T>
+static cudaError_t launch_fwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
+                                cudaStream_t s) {
+  switch (m.kv) {
+    case 1: rmsk::rms_fwd_staged_kernel<T, 1><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 2: rmsk::rms_fwd_staged_kernel<T, 2><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 4: rmsk::rms_fwd_staged_kernel<T, 4><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_bwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
+                                cudaStream_t s) {
+  switch (m.kv) {
+    case 1: rmsk::rms_bwd_staged_kernel<T, 1><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 2: rmsk::rms_bwd_staged_kernel<T, 2><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 4: rmsk::rms_bwd_staged_kernel<T, 4><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
+                              long long wait_limit, cudaStream_t s) {
+  const int b = a.dtype == kBF16 ? 2 : 4;
+  rmsk::StagedParams p = params(m, a.M, a.N, b, false, wait_limit);
+  p.x = a.x;
+  p.gamma = a.gamma;
+  p.y = a.y;
+  p.rstd_out = a.rstd;
+  p.eps = a.eps;
+  p.gemma = a.gemma;
+  int64_t grid = 0;
+  cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv), m, d, p.ntiles, &grid);
+  if (e != cudaSuccess) return e;
+  if (a.dtype == kBF16) return launch_fwd_t<__nv_bfloat16>(p, m, grid, s);
+  return launch_fwd_t<float>(p, m, grid, s);
+}
+
+cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
+  const int64_t ntiles = (a.M + m->rows_per_cta - 1) / m->rows_per_cta;
+  int64_t grid = 0;
+  cudaError_t e = grid_for(staged_kernel(a.dtype, true, m->kv), *m, d, ntiles, &grid);
+  if (e != cudaSuccess) return e;
+  m->blocks = grid;  // = number of partial rows
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd_staged(const BwdArgs& a, const Mapping& m, const DeviceInfo& d,
+                              long long wait_limit, cudaStream_t s) {
+  (void)d;
+  const int b = a.dtype == kBF16 ? 2 : 4;
+  rmsk::StagedParams p = params(m, a.M, a.N, b, true, wait_limit);
+  p.x = a.x;
+  p.gamma = a.gamma;
+  p.rstd_in = a.rstd;
+  p.dy = a.dy;
+  p.dx = a.dx;
+  p.ws = a.ws;
+  p.gemma = a.gemma;
+  if (a.dtype == kBF16) return launch_bwd_t<__nv_bfloat16>(p, m, m.blocks, s);
+  return launch_bwd_t<float>(p, m, m.blocks, s);
 }
 
 cudaError_t take_device_status(int* status) {

@@ -39,12 +39,12 @@ SMALL_SHAPES = [
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("M,N", SMALL_SHAPES, ids=[f"{m}x{n}" for m, n in SMALL_SHAPES])
-@pytest.mark.parametrize("path", ["auto", "registers", "scalar"])
+@pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar"])
 def test_small_shapes_full_parity(M, N, dtype, path):
     w = _w(M, N, dtype, seed=M + N)
     b = 2 if dtype == "bf16" else 4
     inp = H.inputs_for(w)
-    if path == "registers" and (N * b) % 16 != 0:
+    if path in ("registers", "staged") and (N * b) % 16 != 0:
         with pytest.raises(rms.RmsError) as ei:
             H.run_gpu(w, inp, path=path)
         assert ei.value.status == rms.RMS_ERR_ALIGNMENT
@@ -91,7 +91,7 @@ def test_dgamma_bitwise_reproducible():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("path", ["auto", "registers", "scalar"])
+@pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar"])
 def test_inplace_matches_out_of_place_bitwise(dtype, path):
     w = _w(1500, 2048, dtype, seed=3)
     inp = H.inputs_for(w)
@@ -277,3 +277,44 @@ def test_launch_count_and_status():
     H.run_gpu(w, inp)
     assert rms.rms_launch_count() - before == 3
     assert rms.rms_last_device_status() == rms.RMS_OK
+
+
+@pytest.mark.parametrize("N", [8192, 16384])
+def test_both_vector_mappings_on_wide_rows(N):
+    """Rows of 16 and 32 KiB run through both the register and the staged
+    mapping, each checked against the oracle."""
+    w = _w(2048, N, "bf16", seed=N + 1)
+    inp = H.inputs_for(w)
+    for path in ("registers", "staged"):
+        H.assert_parity(w, inp, H.run_gpu(w, inp, path=path), H.sample_rows(w.M, 64))
+
+
+@pytest.mark.parametrize("bwd", [False, True])
+def test_staged_wait_timeout_reports_status(bwd):
+    """With the poll limit at 0 every staged wait gives up at once: the
+    kernel drains its copies, raises the device status and returns; the
+    host sees RMS_ERR_TIMEOUT and the context stays usable."""
+    w = _w(600, 4096, "bf16", seed=11)
+    inp = H.inputs_for(w)
+    x = H.to_device(inp["x"], "bf16")
+    g = H.to_device(inp["gamma"], "bf16")
+    dy = H.to_device(inp["dy"], "bf16")
+    y = torch.empty_like(x)
+    r = torch.empty(w.M, device="cuda")
+    dx = torch.empty_like(x)
+    dg = torch.empty(w.N, device="cuda")
+    ws = torch.empty(rms.rms_bwd_workspace_size(w.M, w.N), dtype=torch.uint8, device="cuda")
+    rms.rms_fwd(x, g, y, r, w.eps, path="staged")
+    torch.cuda.synchronize()
+    assert rms.rms_last_device_status() == rms.RMS_OK
+    prev = rms.rms_set_wait_limit(0)
+    try:
+        if bwd:
+            rms.rms_bwd(dy, x, g, r, dx, dg, ws, path="staged")
+        else:
+            rms.rms_fwd(x, g, y, r, w.eps, path="staged")
+        assert rms.rms_last_device_status() == rms.RMS_ERR_TIMEOUT
+        assert rms.rms_last_device_status() == rms.RMS_OK  # cleared by the read
+    finally:
+        rms.rms_set_wait_limit(prev)
+    H.assert_parity(w, inp, H.run_gpu(w, inp, path="staged"))
