@@ -46,6 +46,14 @@ bool current_device(DeviceInfo* out) {
   return true;
 }
 
+struct OptIn {
+  const void* k;
+  int dev;
+};
+std::mutex g_optin_mu;
+OptIn g_optin[64];
+int g_optin_n = 0;
+
 int elem_bytes(int dtype) { return dtype == rmsi::kBF16 ? 2 : 4; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
@@ -79,12 +87,16 @@ size_t workspace_need(int64_t M, int64_t N, const DeviceInfo& d) {
 }
 
 // Row bytes above which the automatic choice stages rows in shared memory
-// instead of holding them in registers.
-constexpr int64_t kAutoStagedRowBytes = 16384;
+// instead of holding them in registers, from GB300 timings over N = 512 ..
+// 16384 bf16: the forward (one stream in, one out) is fastest in registers
+// up to 16 KiB rows; the backward (two streams in) gains from the deeper
+// copy pipeline as soon as rows exceed 1 KiB.
+constexpr int64_t kAutoStagedRowBytesFwd = 16384;
+constexpr int64_t kAutoStagedRowBytesBwd = 1024;
 
 bool prefer_staged(int N, int dtype, bool bwd) {
-  (void)bwd;
-  return (int64_t)N * elem_bytes(dtype) > kAutoStagedRowBytes;
+  const int64_t row = (int64_t)N * elem_bytes(dtype);
+  return row > (bwd ? kAutoStagedRowBytesBwd : kAutoStagedRowBytesFwd);
 }
 
 // Picks the row mapping for a call.  A forced path that cannot take the
@@ -113,6 +125,25 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
 }
 
 }  // namespace
+
+namespace rmsi {
+
+cudaError_t opt_in_max_smem(const void* kernel, const DeviceInfo& d) {
+  std::lock_guard<std::mutex> lk(g_optin_mu);
+  for (int i = 0; i < g_optin_n; ++i)
+    if (g_optin[i].k == kernel && g_optin[i].dev == d.device) return cudaSuccess;
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return e;
+  // Static plus dynamic shared memory may not exceed the opt-in maximum.
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(d.smem_optin - fa.sharedSizeBytes));
+  if (e != cudaSuccess) return e;
+  if (g_optin_n < 64) g_optin[g_optin_n++] = OptIn{kernel, d.device};
+  return cudaSuccess;
+}
+
+}  // namespace rmsi
 
 extern "C" {
 

@@ -26,13 +26,14 @@
 
 namespace rmsk {
 
-template <typename T, int KV>
+template <typename T, int KV, bool GEMMA>
 __global__ void __launch_bounds__(512)
 rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restrict__ gamma,
                          const float* __restrict__ rstd, T* dx, float* __restrict__ ws, int64_t M,
-                         int N, int gemma, int G) {
-  using E = Elem<T>;
-  constexpr int VN = E::kPerVec;
+                         int N, int G) {
+  using Math = RowMath<T, GEMMA>;
+  constexpr int VN = Elem<T>::kPerVec;
+  constexpr int NP = Math::kPairs;
   __shared__ float red[2][16];
   extern __shared__ float part[];  // [R][N] when R > 1 groups share the CTA
 
@@ -47,16 +48,14 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restri
 
   const uint4* gv = reinterpret_cast<const uint4*>(gamma);
   uint4 gw[KV];
+  f32x2 acc[KV][NP];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * G;
     gw[k] = v < NV ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < NP; ++i) acc[k][i] = 0ull;
   }
-  float acc[KV][VN];
-#pragma unroll
-  for (int k = 0; k < KV; ++k)
-#pragma unroll
-    for (int e = 0; e < VN; ++e) acc[k][e] = 0.f;
 
   for (int64_t it = 0; it < iters; ++it) {
     const int64_t row = gid + it * groups;
@@ -74,41 +73,19 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restri
     }
     const float r = active ? rstd[row] : 0.f;
 
-    float s = 0.f;
+    // Zero vectors (inactive rows, columns past N) add nothing to either sum.
+    f32x2 sux2 = 0ull;
 #pragma unroll
-    for (int k = 0; k < KV; ++k) {
-      float f[VN], d[VN], g[VN];
-      E::unpack(xv[k], f);
-      E::unpack(dv[k], d);
-      E::unpack(gw[k], g);
-#pragma unroll
-      for (int e = 0; e < VN; ++e) {
-        const float w = gemma ? 1.0f + g[e] : g[e];
-        s = fmaf(d[e] * w, f[e], s);
-      }
-    }
-    s = group_sum(s, G, grp * (G >> 5), red[it & 1]);
-    const float c = s / (float)N;
-    const float r3c = r * r * r * c;
+    for (int k = 0; k < KV; ++k) Math::backward_sums(xv[k], dv[k], gw[k], r, sux2, acc[k]);
+    const float sux = group_sum(lo2(sux2) + hi2(sux2), G, grp * (G >> 5), red[it & 1]);
+    const float kc = sux / (float)N;  // r * mean(u*x)
 
     if (active) {
       uint4* out = reinterpret_cast<uint4*>(dx) + base;
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * G;
-        if (v < NV) {
-          float f[VN], d[VN], g[VN], o[VN];
-          E::unpack(xv[k], f);
-          E::unpack(dv[k], d);
-          E::unpack(gw[k], g);
-#pragma unroll
-          for (int e = 0; e < VN; ++e) {
-            const float w = gemma ? 1.0f + g[e] : g[e];
-            o[e] = r * (d[e] * w) - f[e] * r3c;
-            acc[k][e] = fmaf(d[e] * f[e], r, acc[k][e]);
-          }
-          st_stream(out + v, E::pack(o));
-        }
+        if (v < NV) st_stream(out + v, Math::backward_dx(xv[k], dv[k], gw[k], r, kc));
       }
     }
   }
@@ -122,8 +99,9 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restri
       if (v < NV) {
         float4* w4 = reinterpret_cast<float4*>(wp + (int64_t)v * VN);
 #pragma unroll
-        for (int q = 0; q < VN / 4; ++q)
-          w4[q] = make_float4(acc[k][4 * q], acc[k][4 * q + 1], acc[k][4 * q + 2], acc[k][4 * q + 3]);
+        for (int q = 0; q < NP / 2; ++q)
+          w4[q] = make_float4(lo2(acc[k][2 * q]), hi2(acc[k][2 * q]), lo2(acc[k][2 * q + 1]),
+                              hi2(acc[k][2 * q + 1]));
       }
     }
   } else {
@@ -132,7 +110,10 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restri
       const int v = lig + k * G;
       if (v < NV) {
 #pragma unroll
-        for (int e = 0; e < VN; ++e) part[(int64_t)grp * N + v * VN + e] = acc[k][e];
+        for (int i = 0; i < NP; ++i) {
+          part[(int64_t)grp * N + v * VN + 2 * i] = lo2(acc[k][i]);
+          part[(int64_t)grp * N + v * VN + 2 * i + 1] = hi2(acc[k][i]);
+        }
       }
     }
     __syncthreads();
@@ -145,34 +126,40 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restri
 }
 
 template <typename T, int KV>
-static const void* kernel_ptr() {
-  return reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, KV>);
+static const void* kernel_ptr(bool gemma) {
+  return gemma ? reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, KV, true>)
+               : reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, KV, false>);
 }
 
 template <typename T>
-static const void* pick(int kv) {
+static const void* pick(int kv, bool gemma) {
   switch (kv) {
-    case 1: return kernel_ptr<T, 1>();
-    case 2: return kernel_ptr<T, 2>();
-    case 4: return kernel_ptr<T, 4>();
+    case 1: return kernel_ptr<T, 1>(gemma);
+    case 2: return kernel_ptr<T, 2>(gemma);
+    case 4: return kernel_ptr<T, 4>(gemma);
     default: return nullptr;
   }
 }
 
-template <typename T>
-static cudaError_t launch_t(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
+template <typename T, bool GEMMA>
+static cudaError_t launch_g(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)m.blocks), block(m.threads);
   const T* dy = static_cast<const T*>(a.dy);
   const T* x = static_cast<const T*>(a.x);
   const T* g = static_cast<const T*>(a.gamma);
   T* dx = static_cast<T*>(a.dx);
   switch (m.kv) {
-    case 1: rms_bwd_registers_kernel<T, 1><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, a.gemma, m.G); break;
-    case 2: rms_bwd_registers_kernel<T, 2><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, a.gemma, m.G); break;
-    case 4: rms_bwd_registers_kernel<T, 4><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, a.gemma, m.G); break;
+    case 1: rms_bwd_registers_kernel<T, 1, GEMMA><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
+    case 2: rms_bwd_registers_kernel<T, 2, GEMMA><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
+    case 4: rms_bwd_registers_kernel<T, 4, GEMMA><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_t(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
+  return a.gemma ? launch_g<T, true>(a, m, s) : launch_g<T, false>(a, m, s);
 }
 
 }  // namespace rmsk
@@ -181,7 +168,8 @@ namespace rmsi {
 
 cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   m->smem = m->rows_per_cta > 1 ? (size_t)m->rows_per_cta * a.N * sizeof(float) : 0;
-  const void* k = a.dtype == kBF16 ? rmsk::pick<__nv_bfloat16>(m->kv) : rmsk::pick<float>(m->kv);
+  const void* k = a.dtype == kBF16 ? rmsk::pick<__nv_bfloat16>(m->kv, a.gemma)
+                                    : rmsk::pick<float>(m->kv, a.gemma);
   if (!k) return cudaErrorInvalidValue;
   int occ = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, m->threads, m->smem);

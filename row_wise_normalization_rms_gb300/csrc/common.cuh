@@ -62,6 +62,167 @@ struct Elem<__nv_bfloat16> {
   }
 };
 
+// ---- packed float pairs ------------------------------------------------------
+// Blackwell issues two float32 FMAs/multiplies per instruction on register
+// pairs (fma.rn.f32x2 / mul.rn.f32x2): each lane is an ordinary IEEE float32
+// operation with a single rounding, so results equal the scalar forms.
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 pk2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float lo2(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float hi2(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 splat2(float v) { return pk2(v, v); }
+
+// Two bf16 (one 32-bit word, low half first) widened exactly to a pair.
+__device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
+  return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// A pair rounded to two bf16 (round to nearest even), low half first.
+__device__ __forceinline__ uint32_t f2_to_bf2(f32x2 v) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo2(v), hi2(v));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Product of two bf16 pairs rounded once to bf16.  The exact product of two
+// 8-bit significands fits a float32, so this equals rounding the float32
+// product of the widened values.
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// A 16-byte vector as float pairs: 4 pairs for bf16, 2 for float32.
+template <typename T>
+struct Pairs;
+template <>
+struct Pairs<__nv_bfloat16> {
+  static constexpr int n = 4;
+  __device__ static __forceinline__ f32x2 get(const uint4& v, int i) {
+    return bf2_to_f2(i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w);
+  }
+};
+template <>
+struct Pairs<float> {
+  static constexpr int n = 2;
+  __device__ static __forceinline__ f32x2 get(const uint4& v, int i) {
+    return i == 0 ? pk2(__uint_as_float(v.x), __uint_as_float(v.y))
+                  : pk2(__uint_as_float(v.z), __uint_as_float(v.w));
+  }
+};
+
+// ---- per-vector arithmetic ---------------------------------------------------
+// Shared by every vector kernel, so all mappings compute identical bits.
+template <typename T, bool GEMMA>
+struct RowMath {
+  using P = Pairs<T>;
+  static constexpr int kPairs = P::n;
+
+  // Effective weight pair: gamma, or 1 + gamma (Gemma).
+  __device__ static __forceinline__ f32x2 weight(const uint4& g, int i) {
+    const f32x2 w = P::get(g, i);
+    return GEMMA ? add2(w, splat2(1.0f)) : w;
+  }
+
+  // ss += x^2 over the vector.
+  __device__ static __forceinline__ void sumsq(const uint4& x, f32x2& ss) {
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) {
+      const f32x2 f = P::get(x, i);
+      ss = fma2(f, f, ss);
+    }
+  }
+
+  // y for one vector.  Non-Gemma: (x*r) rounded to the I/O type, then times
+  // gamma, rounded again.  Gemma: x*r*(1+gamma) rounded once.
+  __device__ static __forceinline__ uint4 forward(const uint4& x, const uint4& g, float r) {
+    const f32x2 rr = splat2(r);
+    uint32_t o[4];
+    if (sizeof(T) == 2) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const f32x2 xr = mul2(P::get(x, i), rr);
+        if (GEMMA) {
+          o[i] = f2_to_bf2(mul2(xr, weight(g, i)));
+        } else {
+          const uint32_t gw = i == 0 ? g.x : i == 1 ? g.y : i == 2 ? g.z : g.w;
+          o[i] = bf2_mul(f2_to_bf2(xr), gw);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const f32x2 y = mul2(mul2(P::get(x, i), rr), weight(g, i));
+        o[2 * i] = __float_as_uint(lo2(y));
+        o[2 * i + 1] = __float_as_uint(hi2(y));
+      }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+
+  // Backward first pass over one vector, with xn = x*r and u = dy*w:
+  // sux += u*xn (the row's r*sum(u*x)) and acc += dy*xn (dgamma terms).
+  __device__ static __forceinline__ void backward_sums(const uint4& x, const uint4& dy,
+                                                       const uint4& g, float r, f32x2& sux,
+                                                       f32x2* acc) {
+    const f32x2 rr = splat2(r);
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) {
+      const f32x2 xn = mul2(P::get(x, i), rr);
+      const f32x2 d = P::get(dy, i);
+      sux = fma2(mul2(d, weight(g, i)), xn, sux);
+      acc[i] = fma2(d, xn, acc[i]);
+    }
+  }
+
+  // dx for one vector: r*u - x*r^3*c = r*(u - xn*k) with k = r*c.
+  __device__ static __forceinline__ uint4 backward_dx(const uint4& x, const uint4& dy,
+                                                      const uint4& g, float r, float k) {
+    const f32x2 rr = splat2(r);
+    const f32x2 nk = splat2(-k);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) {
+      const f32x2 xn = mul2(P::get(x, i), rr);
+      const f32x2 u = mul2(P::get(dy, i), weight(g, i));
+      const f32x2 dx = mul2(fma2(xn, nk, u), rr);
+      if (sizeof(T) == 2) {
+        o[i] = f2_to_bf2(dx);
+      } else {
+        o[2 * i] = __float_as_uint(lo2(dx));
+        o[2 * i + 1] = __float_as_uint(hi2(dx));
+      }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+};
+
 // ---- memory ----------------------------------------------------------------
 // Rows are touched once per kernel: load and store them evict-first so they
 // do not push gamma and the partial sums out of L2.

@@ -16,12 +16,12 @@
 
 namespace rmsk {
 
-template <typename T, int KV>
+template <typename T, int KV, bool GEMMA>
 __global__ void __launch_bounds__(1024)
 rms_fwd_registers_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
-                         float* __restrict__ rstd, int64_t M, int N, float eps, int gemma, int G) {
-  using E = Elem<T>;
-  constexpr int VN = E::kPerVec;
+                         float* __restrict__ rstd, int64_t M, int N, float eps, int G) {
+  using Math = RowMath<T, GEMMA>;
+  constexpr int VN = Elem<T>::kPerVec;
   __shared__ float red[32];
   const int NV = N / VN;
   const int grp = threadIdx.x / G;
@@ -32,28 +32,15 @@ rms_fwd_registers_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T
   const uint4* gv = reinterpret_cast<const uint4*>(gamma);
 
   uint4 xv[KV];
-  uint4 gw[KV];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * G;
-    const bool in = active && v < NV;
-    xv[k] = in ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    xv[k] = (active && v < NV) ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
   }
+  f32x2 ss2 = 0ull;
 #pragma unroll
-  for (int k = 0; k < KV; ++k) {
-    const int v = lig + k * G;
-    gw[k] = (active && v < NV) ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
-  }
-
-  float ss = 0.f;
-#pragma unroll
-  for (int k = 0; k < KV; ++k) {
-    float f[VN];
-    E::unpack(xv[k], f);
-#pragma unroll
-    for (int e = 0; e < VN; ++e) ss = fmaf(f[e], f[e], ss);
-  }
-  ss = group_sum(ss, G, grp * (G >> 5), red);
+  for (int k = 0; k < KV; ++k) Math::sumsq(xv[k], ss2);
+  const float ss = group_sum(lo2(ss2) + hi2(ss2), G, grp * (G >> 5), red);
   const float r = 1.0f / sqrtf(ss / (float)N + eps);
   if (!active) return;  // no barrier follows
   if (lig == 0) rstd[row] = r;
@@ -62,35 +49,28 @@ rms_fwd_registers_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * G;
-    if (v < NV) {
-      float f[VN], g[VN], o[VN];
-      E::unpack(xv[k], f);
-      E::unpack(gw[k], g);
-      if (gemma) {
-#pragma unroll
-        for (int e = 0; e < VN; ++e) o[e] = (f[e] * r) * (1.0f + g[e]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < VN; ++e) o[e] = E::round(f[e] * r) * g[e];
-      }
-      st_stream(yr + v, E::pack(o));
-    }
+    if (v < NV) st_stream(yr + v, Math::forward(xv[k], ld_keep(gv + v), r));
   }
 }
 
-template <typename T>
-static cudaError_t launch_t(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
+template <typename T, bool GEMMA>
+static cudaError_t launch_g(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)m.blocks), block(m.threads);
   const T* x = static_cast<const T*>(a.x);
   const T* g = static_cast<const T*>(a.gamma);
   T* y = static_cast<T*>(a.y);
   switch (m.kv) {
-    case 1: rms_fwd_registers_kernel<T, 1><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, a.gemma, m.G); break;
-    case 2: rms_fwd_registers_kernel<T, 2><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, a.gemma, m.G); break;
-    case 4: rms_fwd_registers_kernel<T, 4><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, a.gemma, m.G); break;
+    case 1: rms_fwd_registers_kernel<T, 1, GEMMA><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
+    case 2: rms_fwd_registers_kernel<T, 2, GEMMA><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
+    case 4: rms_fwd_registers_kernel<T, 4, GEMMA><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_t(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
+  return a.gemma ? launch_g<T, true>(a, m, s) : launch_g<T, false>(a, m, s);
 }
 
 }  // namespace rmsk

@@ -55,6 +55,10 @@ struct DeviceInfo {
   size_t smem_optin = 0;  // max dynamic shared memory per CTA
 };
 
+// Raises a kernel's dynamic shared memory limit to the device maximum
+// (once per kernel and device; thread-safe).  Defined in api.cu.
+cudaError_t opt_in_max_smem(const void* kernel, const DeviceInfo& d);
+
 // Largest number of persistent CTAs a backward launch may use on a device
 // with `sms` SMs; the workspace holds this many float32 rows of N.
 inline int64_t max_partials(int sms) { return 4 * (int64_t)sms; }

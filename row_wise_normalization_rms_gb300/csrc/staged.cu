@@ -123,11 +123,11 @@ __device__ __forceinline__ void init_barriers(const StagedParams& p, const Stage
 // while tile i is processed, and no row slice has to stay in registers
 // across the barrier.
 
-template <typename T, int KV>
+template <typename T, int KV, bool GEMMA>
 __global__ void __launch_bounds__(1024)
 rms_fwd_staged_kernel(const StagedParams p) {
-  using E = Elem<T>;
-  constexpr int VN = E::kPerVec;
+  using Math = RowMath<T, GEMMA>;
+  constexpr int VN = Elem<T>::kPerVec;
   extern __shared__ __align__(128) uint8_t smem[];
   const StageHeader h = header(smem);
   const int NV = p.N / VN;
@@ -166,20 +166,15 @@ rms_fwd_staged_kernel(const StagedParams p) {
     if (!mbar_wait(smem_u32(&h.full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) h.abort[buf] = 1;
 
     const uint32_t xs = smem_u32(h.stages + (size_t)s * p.stage_bytes) + row_off;
-    float ss = 0.f;
+    f32x2 ss2 = 0ull;
     if (active) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < NV) {
-          float f[VN];
-          E::unpack(lds128(xs + 16u * v), f);
-#pragma unroll
-          for (int e = 0; e < VN; ++e) ss = fmaf(f[e], f[e], ss);
-        }
+        if (v < NV) Math::sumsq(lds128(xs + 16u * v), ss2);
       }
     }
-    ss = warp_sum(ss);
+    const float ss = warp_sum(lo2(ss2) + hi2(ss2));
     if ((threadIdx.x & 31) == 0) h.red[buf * 32 + warp] = ss;
     __syncthreads();  // partial sums visible; tile i-1 fully consumed
     if (h.abort[buf]) {
@@ -197,30 +192,19 @@ rms_fwd_staged_kernel(const StagedParams p) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < NV) {
-          float f[VN], g[VN], o[VN];
-          E::unpack(lds128(xs + 16u * v), f);
-          E::unpack(gw[k], g);
-          if (p.gemma) {
-#pragma unroll
-            for (int e = 0; e < VN; ++e) o[e] = (f[e] * r) * (1.0f + g[e]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < VN; ++e) o[e] = E::round(f[e] * r) * g[e];
-          }
-          st_stream(yr + v, E::pack(o));
-        }
+        if (v < NV) st_stream(yr + v, Math::forward(lds128(xs + 16u * v), gw[k], r));
       }
     }
   }
   if (aborted && threadIdx.x == 0) drain_and_flag(p, h, i, issued);
 }
 
-template <typename T, int KV>
+template <typename T, int KV, bool GEMMA>
 __global__ void __launch_bounds__(512)
 rms_bwd_staged_kernel(const StagedParams p) {
-  using E = Elem<T>;
-  constexpr int VN = E::kPerVec;
+  using Math = RowMath<T, GEMMA>;
+  constexpr int VN = Elem<T>::kPerVec;
+  constexpr int NP = Math::kPairs;
   extern __shared__ __align__(128) uint8_t smem[];
   const StageHeader h = header(smem);
   const int NV = p.N / VN;
@@ -243,13 +227,13 @@ rms_bwd_staged_kernel(const StagedParams p) {
 
   const uint4* gv = reinterpret_cast<const uint4*>(p.gamma);
   uint4 gw[KV];
-  float acc[KV][VN];
+  f32x2 acc[KV][NP];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * p.G;
     gw[k] = v < NV ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int e = 0; e < VN; ++e) acc[k][e] = 0.f;
+    for (int e = 0; e < NP; ++e) acc[k][e] = 0ull;
   }
 
   int64_t i = 0;
@@ -264,27 +248,17 @@ rms_bwd_staged_kernel(const StagedParams p) {
 
     const uint32_t xs = smem_u32(h.stages + (size_t)s * p.stage_bytes) + row_off;
     const uint32_t ds = xs + p.tile_bytes;
-    // First pass: sum(u*x) for the row, and this row's dgamma terms dy*x*r.
-    float sux = 0.f;
+    // First pass: r*sum(u*x) for the row, and this row's dgamma terms dy*x*r.
+    f32x2 sux2 = 0ull;
     if (active) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < NV) {
-          float f[VN], d[VN], g[VN];
-          E::unpack(lds128(xs + 16u * v), f);
-          E::unpack(lds128(ds + 16u * v), d);
-          E::unpack(gw[k], g);
-#pragma unroll
-          for (int e = 0; e < VN; ++e) {
-            const float w = p.gemma ? 1.0f + g[e] : g[e];
-            sux = fmaf(d[e] * w, f[e], sux);
-            acc[k][e] = fmaf(d[e] * f[e], r, acc[k][e]);
-          }
-        }
+        if (v < NV)
+          Math::backward_sums(lds128(xs + 16u * v), lds128(ds + 16u * v), gw[k], r, sux2, acc[k]);
       }
     }
-    sux = warp_sum(sux);
+    const float sux = warp_sum(lo2(sux2) + hi2(sux2));
     if ((threadIdx.x & 31) == 0) h.red[buf * 32 + warp] = sux;
     __syncthreads();  // partial sums visible; tile i-1 fully consumed
     if (h.abort[buf]) {
@@ -295,25 +269,15 @@ rms_bwd_staged_kernel(const StagedParams p) {
 
     float tot = 0.f;
     for (int w = 0; w < nw; ++w) tot += h.red[buf * 32 + first_warp + w];
-    const float r3c = r * r * r * (tot / (float)p.N);
-    // Second pass: dx = r*u - x*r^3*c.
+    const float kc = tot / (float)p.N;  // r * mean(u*x)
+    // Second pass: dx = r*(u - x*r*kc).
     if (active) {
       uint4* out = reinterpret_cast<uint4*>(p.dx) + row * (int64_t)NV;
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < NV) {
-          float f[VN], d[VN], g[VN], o[VN];
-          E::unpack(lds128(xs + 16u * v), f);
-          E::unpack(lds128(ds + 16u * v), d);
-          E::unpack(gw[k], g);
-#pragma unroll
-          for (int e = 0; e < VN; ++e) {
-            const float w = p.gemma ? 1.0f + g[e] : g[e];
-            o[e] = r * (d[e] * w) - f[e] * r3c;
-          }
-          st_stream(out + v, E::pack(o));
-        }
+        if (v < NV)
+          st_stream(out + v, Math::backward_dx(lds128(xs + 16u * v), lds128(ds + 16u * v), gw[k], r, kc));
       }
     }
   }
@@ -332,8 +296,9 @@ rms_bwd_staged_kernel(const StagedParams p) {
       if (v < NV) {
         float4* w4 = reinterpret_cast<float4*>(wp + (int64_t)v * VN);
 #pragma unroll
-        for (int c = 0; c < VN / 4; ++c)
-          w4[c] = make_float4(acc[k][4 * c], acc[k][4 * c + 1], acc[k][4 * c + 2], acc[k][4 * c + 3]);
+        for (int c = 0; c < NP / 2; ++c)
+          w4[c] = make_float4(lo2(acc[k][2 * c]), hi2(acc[k][2 * c]), lo2(acc[k][2 * c + 1]),
+                              hi2(acc[k][2 * c + 1]));
       }
     }
   } else {
@@ -344,7 +309,10 @@ rms_bwd_staged_kernel(const StagedParams p) {
       const int v = lig + k * p.G;
       if (v < NV) {
 #pragma unroll
-        for (int e = 0; e < VN; ++e) part[(int64_t)q * p.N + v * VN + e] = acc[k][e];
+        for (int e = 0; e < NP; ++e) {
+          part[(int64_t)q * p.N + v * VN + 2 * e] = lo2(acc[k][e]);
+          part[(int64_t)q * p.N + v * VN + 2 * e + 1] = hi2(acc[k][e]);
+        }
       }
     }
     __syncthreads();
@@ -356,22 +324,27 @@ rms_bwd_staged_kernel(const StagedParams p) {
   }
 }
 
-template <typename T, bool BWD>
-static const void* staged_ptr(int kv) {
+template <typename T, bool BWD, bool GEMMA>
+static const void* staged_ptr_g(int kv) {
   if (BWD) {
     switch (kv) {
-      case 1: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 1>);
-      case 2: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 2>);
-      case 4: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 4>);
+      case 1: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 1, GEMMA>);
+      case 2: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 2, GEMMA>);
+      case 4: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 4, GEMMA>);
     }
   } else {
     switch (kv) {
-      case 1: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 1>);
-      case 2: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 2>);
-      case 4: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 4>);
+      case 1: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 1, GEMMA>);
+      case 2: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 2, GEMMA>);
+      case 4: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 4, GEMMA>);
     }
   }
   return nullptr;
+}
+
+template <typename T, bool BWD>
+static const void* staged_ptr(int kv, bool gemma) {
+  return gemma ? staged_ptr_g<T, BWD, true>(kv) : staged_ptr_g<T, BWD, false>(kv);
 }
 
 }  // namespace rmsk
@@ -380,18 +353,32 @@ namespace rmsi {
 
 namespace {
 
+// Measured on GB300 over N = 512 .. 16384 bf16: up to four CTAs per SM
+// sharing 224 KiB of stages is as fast or faster than fewer, larger rings.
 #ifndef RMS_STAGED_SMEM_PER_SM
-#define RMS_STAGED_SMEM_PER_SM (200 * 1024)
+#define RMS_STAGED_SMEM_PER_SM (224 * 1024)
+#endif
+#ifndef RMS_STAGED_MAX_CTAS_PER_SM
+#define RMS_STAGED_MAX_CTAS_PER_SM 4
+#endif
+#ifndef RMS_STAGED_TILE_BYTES
+#define RMS_STAGED_TILE_BYTES 16384
+#endif
+#ifndef RMS_STAGED_MAX_STAGES
+#define RMS_STAGED_MAX_STAGES 8
 #endif
 
-const void* staged_kernel(int dtype, bool bwd, int kv) {
+const void* staged_kernel(int dtype, bool bwd, int kv, bool gemma) {
   if (dtype == kBF16)
-    return bwd ? rmsk::staged_ptr<__nv_bfloat16, true>(kv) : rmsk::staged_ptr<__nv_bfloat16, false>(kv);
-  return bwd ? rmsk::staged_ptr<float, true>(kv) : rmsk::staged_ptr<float, false>(kv);
+    return bwd ? rmsk::staged_ptr<__nv_bfloat16, true>(kv, gemma)
+               : rmsk::staged_ptr<__nv_bfloat16, false>(kv, gemma);
+  return bwd ? rmsk::staged_ptr<float, true>(kv, gemma) : rmsk::staged_ptr<float, false>(kv, gemma);
 }
 
-// Per (kernel, device): dynamic shared memory opted in and the occupancy
-// for a (threads, smem) pair, so repeated calls do no driver queries.
+// Occupancy per (kernel, device, threads, smem), so repeated calls make no
+// driver queries.  Each kernel is opted in to the device's full dynamic
+// shared memory once (the attribute is per kernel, last writer wins, so it
+// is never lowered for a smaller configuration).
 struct OccEntry {
   const void* k;
   int dev, threads;
@@ -399,23 +386,23 @@ struct OccEntry {
   int occ;
 };
 std::mutex g_occ_mu;
-OccEntry g_occ[64];
+OccEntry g_occ[128];
 int g_occ_n = 0;
 
-cudaError_t occupancy(const void* k, int dev, int threads, size_t smem, int* occ) {
+cudaError_t occupancy(const void* k, const DeviceInfo& d, int threads, size_t smem, int* occ) {
   std::lock_guard<std::mutex> lk(g_occ_mu);
   for (int i = 0; i < g_occ_n; ++i) {
     const OccEntry& e = g_occ[i];
-    if (e.k == k && e.dev == dev && e.threads == threads && e.smem == smem) {
+    if (e.k == k && e.dev == d.device && e.threads == threads && e.smem == smem) {
       *occ = e.occ;
       return cudaSuccess;
     }
   }
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = opt_in_max_smem(k, d);
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, k, threads, smem);
   if (e != cudaSuccess) return e;
-  if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{k, dev, threads, smem, *occ};
+  if (g_occ_n < 128) g_occ[g_occ_n++] = OccEntry{k, d.device, threads, smem, *occ};
   return cudaSuccess;
 }
 
@@ -423,8 +410,7 @@ cudaError_t occupancy(const void* k, int dev, int threads, size_t smem, int* occ
 
 // Tiles of R rows (about 16 KiB of x, at most 16 rows), G threads per row
 // with up to 4 vectors each, and as many stages as fit in the per-SM
-// shared-memory budget: two CTAs per SM when each can keep three stages,
-// else one CTA with at least three.
+// shared-memory budget (at least three per CTA).
 bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
   const int b = dtype == kBF16 ? 2 : 4;
   if (N <= 0 || ((int64_t)N * b) % 16 != 0) return false;
@@ -441,7 +427,7 @@ bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
     G = ((NV + 3) / 4 + 31) / 32 * 32;
     if (G > max_threads) return false;
   }
-  int R = (int)(16384 / row_bytes);
+  int R = (int)(RMS_STAGED_TILE_BYTES / row_bytes);
   if (R < 1) R = 1;
   if (R > 16) R = 16;
   while (R > 1 && G * R > max_threads) --R;
@@ -449,19 +435,20 @@ bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
   const int64_t stage = bwd ? 2 * tile : tile;
   const int64_t budget = RMS_STAGED_SMEM_PER_SM;
   const int64_t cap = (int64_t)d.smem_optin - rmsk::kHeaderBytes;
-  // At least three stages: one being processed, one whose refill waits for
-  // the next barrier, and at least one more in flight.
-  int cps, S;
-  if (2 * 3 * stage <= budget && budget / 2 <= cap) {
-    cps = 2;
-    S = (int)((budget / 2) / stage);
-  } else if (3 * stage <= std::min(budget, cap)) {
-    cps = 1;
-    S = (int)(std::min(budget, cap) / stage);
-  } else {
-    return false;
+  // At least three stages per CTA: one being processed, one whose refill
+  // waits for the next barrier, and at least one more in flight.  The most
+  // CTAs per SM (up to the cap) whose three stages fit the budget.
+  int cps = 0, S = 0;
+  for (int c = RMS_STAGED_MAX_CTAS_PER_SM; c >= 1; --c) {
+    const int64_t per_cta = std::min(budget / c, cap);
+    if (3 * stage <= per_cta) {
+      cps = c;
+      S = (int)(per_cta / stage);
+      break;
+    }
   }
-  if (S > 8) S = 8;
+  if (cps == 0) return false;
+  if (S > RMS_STAGED_MAX_STAGES) S = RMS_STAGED_MAX_STAGES;
   m->path = kStaged;
   m->kv = kv;
   m->G = G;
@@ -476,7 +463,7 @@ bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
 static cudaError_t grid_for(const void* k, const Mapping& m, const DeviceInfo& d, int64_t ntiles,
                             int64_t* grid) {
   int occ = 0;
-  cudaError_t e = occupancy(k, d.device, m.threads, m.smem, &occ);
+  cudaError_t e = occupancy(k, d, m.threads, m.smem, &occ);
   if (e != cudaSuccess) return e;
   if (occ < 1) return cudaErrorInvalidConfiguration;
   const int64_t per_sm = std::min<int64_t>(occ, m.blocks);
@@ -502,28 +489,40 @@ static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, int b, bool
   return p;
 }
 
-template <typename T>
-static cudaError_t launch_fwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
+template <typename T, bool GEMMA>
+static cudaError_t launch_fwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
   switch (m.kv) {
-    case 1: rmsk::rms_fwd_staged_kernel<T, 1><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    case 2: rmsk::rms_fwd_staged_kernel<T, 2><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    case 4: rmsk::rms_fwd_staged_kernel<T, 4><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 1: rmsk::rms_fwd_staged_kernel<T, 1, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 2: rmsk::rms_fwd_staged_kernel<T, 2, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 4: rmsk::rms_fwd_staged_kernel<T, 4, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <typename T, bool GEMMA>
+static cudaError_t launch_bwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
+                                cudaStream_t s) {
+  switch (m.kv) {
+    case 1: rmsk::rms_bwd_staged_kernel<T, 1, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 2: rmsk::rms_bwd_staged_kernel<T, 2, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 4: rmsk::rms_bwd_staged_kernel<T, 4, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }
 
 template <typename T>
+static cudaError_t launch_fwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
+                                cudaStream_t s) {
+  return p.gemma ? launch_fwd_g<T, true>(p, m, grid, s) : launch_fwd_g<T, false>(p, m, grid, s);
+}
+
+template <typename T>
 static cudaError_t launch_bwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
-  switch (m.kv) {
-    case 1: rmsk::rms_bwd_staged_kernel<T, 1><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    case 2: rmsk::rms_bwd_staged_kernel<T, 2><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    case 4: rmsk::rms_bwd_staged_kernel<T, 4><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  return p.gemma ? launch_bwd_g<T, true>(p, m, grid, s) : launch_bwd_g<T, false>(p, m, grid, s);
 }
 
 cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
@@ -537,7 +536,7 @@ cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceIn
   p.eps = a.eps;
   p.gemma = a.gemma;
   int64_t grid = 0;
-  cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv), m, d, p.ntiles, &grid);
+  cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv, a.gemma), m, d, p.ntiles, &grid);
   if (e != cudaSuccess) return e;
   if (a.dtype == kBF16) return launch_fwd_t<__nv_bfloat16>(p, m, grid, s);
   return launch_fwd_t<float>(p, m, grid, s);
@@ -546,7 +545,7 @@ cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceIn
 cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   const int64_t ntiles = (a.M + m->rows_per_cta - 1) / m->rows_per_cta;
   int64_t grid = 0;
-  cudaError_t e = grid_for(staged_kernel(a.dtype, true, m->kv), *m, d, ntiles, &grid);
+  cudaError_t e = grid_for(staged_kernel(a.dtype, true, m->kv, a.gemma), *m, d, ntiles, &grid);
   if (e != cudaSuccess) return e;
   m->blocks = grid;  // = number of partial rows
   return cudaSuccess;

@@ -79,6 +79,14 @@ def test_workload_full_size(name):
     H.assert_parity(w, inp, res, rows)
 
 
+@pytest.mark.parametrize("path", ["registers", "staged"])
+def test_headline_workload_both_mappings(path):
+    """16384 x 8192 bf16 through each vector mapping, full size."""
+    w = WORKLOADS["wide_bf16_16384x8192"]
+    inp = H.inputs_for(w)
+    H.assert_parity(w, inp, H.run_gpu(w, inp, path=path), H.sample_rows(w.M))
+
+
 def test_dgamma_bitwise_reproducible():
     w = WORKLOADS["llama7b_bf16_8192x4096"]
     inp = H.inputs_for(w)
