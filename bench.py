@@ -1,0 +1,459 @@
+"""Benchmark: RMSNorm forward + backward on one GB300, through the C ABI.
+
+One step = rms_fwd + rms_bwd (forward, backward rows, dgamma column
+reduction) over the 16384 x 8192 bf16 workload, inputs resident in HBM.
+Prints ONE JSON line (rank 0):
+
+  value      whole-job algorithmic HBM GB/s of the step, summed over ranks
+  roofline   the backward call (the dominant one) against the measured HBM peak
+  e2e        the same metric with host buffers: pinned H2D of x, dy, gamma and
+             D2H of y, rstd, dx, dgamma inside every timed step
+  cpu_baseline  the fp64 oracle on a bounded row sample, on the host cores
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+For N > 1 launch one process per GPU with torch.distributed.run; every rank
+runs the same workload on its own GPU (replicas: the rows of independent
+batches need no exchange), timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "wide_bf16_16384x8192"
+METRIC = "RMSNorm fwd+bwd achieved HBM GB/s and % of GB300 peak at M×N bf16; rows/s"
+L2_BYTES = 129 * 1000 * 1000
+FALLBACK_HBM_GBS = 6800.0
+
+
+def step_bytes(M: int, N: int, b: int):
+    """Algorithmic bytes: fwd reads x, writes y and rstd; bwd reads dy, x and
+    rstd, writes dx; plus gamma (read once per call) and dgamma (written once)."""
+    fwd = 2 * M * N * b + 4 * M + N * b
+    bwd = 3 * M * N * b + 4 * M + N * b + 4 * N
+    return fwd, bwd
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """Max of a float over all ranks (the whole job ends with the slowest)."""
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.window = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.first = threading.Event()
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        self.first.wait(5.0)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [c.strip() for c in line.split(",")]))
+            self.first.set()
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.window = (self.t0, time.time())
+
+    def close(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.window is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        t0, t1 = self.window
+        inside = [s for t, s in self.samples if t0 - 0.1 <= t <= t1 + 0.25]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            try:
+                sm.append(float(s[1]))
+                smax = float(s[2])
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, s[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+def cpu_oracle_throughput(w, inp, seconds: float = 10.0, rows: int = 256):
+    """The fp64 oracle's fwd+bwd on a fixed row sample, repeated for about
+    ``seconds``; GB/s on the same algorithmic-byte formula as the GPU."""
+    from oracle import rmsnorm_oracle as orc
+    from synthetic import storage_to_float64
+
+    rows = min(rows, w.M)
+    x = storage_to_float64(inp["x"][:rows], w.dtype)
+    dy = storage_to_float64(inp["dy"][:rows], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.dtype)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        orc.rms_forward(x, g, w.eps, w.gemma)
+        orc.rms_backward(x, g, dy, w.eps, w.gemma)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    f, b = step_bytes(rows, w.N, w.elem_bytes)
+    per_rep = el / reps
+    return {
+        "value": round((f + b) / per_rep / 1e9, 3),
+        "unit": "GB/s",
+        "rows_per_s": round(rows / per_rep, 1),
+        "cores": 1,
+        "kind": "oracle",
+        "sample": (f"fp64 numpy oracle fwd+bwd on the first {rows} rows of the {w.M}x{w.N} "
+                   f"{w.dtype} workload, repeated {reps} times in {el:.1f} s (one thread: "
+                   "numpy elementwise ops and reductions)"),
+    }
+
+
+# ------------------------------------------------------------------ reference
+def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, one bounded row
+    sample of the same workload per step, rank 0 only."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    from oracle import rmsnorm_oracle as orc
+    from synthetic import make_inputs, storage_to_float64, workload
+
+    w = workload(WORKLOAD)
+    rows = 32
+    sub = w.with_shape(rows)
+    inp = make_inputs(sub)
+    x = storage_to_float64(inp["x"], w.dtype)
+    dy = storage_to_float64(inp["dy"], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.dtype)
+
+    def step():
+        orc.rms_forward(x, g, w.eps, w.gemma)
+        orc.rms_backward(x, g, dy, w.eps, w.gemma)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    f, b = step_bytes(rows, w.N, w.elem_bytes)
+    value = (f + b) * args.steps / el / 1e9
+    sample = (f"fp64 numpy oracle fwd+bwd on {rows} rows x {w.N} per step (seeded rows of the "
+              f"{w.M}x{w.N} {w.dtype} workload), one thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w),
+        "rows_per_s": round(rows * args.steps / el, 2),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w):
+    return {
+        "workload": f"RMSNorm fwd+bwd, M={w.M} rows x N={w.N} hidden, {w.dtype} I/O, "
+                    f"eps={w.eps}, large-hidden synthetic rows (x ~ N(0,1) x log-uniform "
+                    "row scale [0.01, 100], gamma ~ N(1, 0.2), dy ~ N(0, 1), seed 0)",
+        "M": w.M, "N": w.N, "eps": w.eps, "gemma": w.gemma, "inplace_dx": w.inplace_dx,
+        "l2": "inputs larger than L2: x, dy, y, dx are 256 MiB each (L2 is 129 MB)",
+    }
+
+
+# ------------------------------------------------------------------------ GPU
+def run_gpu(args):
+    import numpy as np
+    import torch
+
+    import row_wise_normalization_rms_gb300 as rms
+    from synthetic import make_inputs, workload
+
+    rank, local, world = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    w = workload(WORKLOAD)
+    M, N, b = w.M, w.N, w.elem_bytes
+    fwd_b, bwd_b = step_bytes(M, N, b)
+
+    inp = make_inputs(w)
+
+    def pinned(a):
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    hx, hdy, hg = pinned(inp["x"]), pinned(inp["dy"]), pinned(inp["gamma"])
+    x = hx.to(dev)
+    dy = hdy.to(dev)
+    g = hg.to(dev)
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    rstd = torch.empty(M, device=dev)
+    dg = torch.empty(N, device=dev)
+    ws = torch.empty(rms.rms_bwd_workspace_size(M, N), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        rms.rms_fwd(x, g, y, rstd, w.eps, w.gemma, stream=stream)
+        rms.rms_bwd(dy, x, g, rstd, dx, dg, ws, w.gemma, w.inplace_dx, stream=stream)
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    torch.cuda.synchronize(dev)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    launches0 = rms.rms_launch_count()
+    if clocks:
+        clocks.start()
+    ev[0].record(stream)
+    for i in range(args.steps):
+        rms.rms_fwd(x, g, y, rstd, w.eps, w.gemma, stream=stream)
+        ev[2 * i + 1].record(stream)
+        rms.rms_bwd(dy, x, g, rstd, dx, dg, ws, w.gemma, w.inplace_dx, stream=stream)
+        ev[2 * i + 2].record(stream)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.stop()
+    launches = rms.rms_launch_count() - launches0
+    total_ms = ev[0].elapsed_time(ev[-1])
+    fwd_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    bwd_ms = [ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.steps)]
+    barrier(dist, dev)
+    total_ms = max_over_ranks(total_ms, dist, dev)
+    ms_step = total_ms / args.steps
+    value = (fwd_b + bwd_b) * world / (ms_step * 1e-3) / 1e9
+
+    # End to end through the same API with host buffers.
+    e2e_steps = max(3, min(args.steps, 20))
+    hy = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    hdx = torch.empty_like(hy).pin_memory()
+    hr = torch.empty(M).pin_memory()
+    hdg = torch.empty(N).pin_memory()
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        dy.copy_(hdy, non_blocking=True)
+        g.copy_(hg, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+        hdx.copy_(dx, non_blocking=True)
+        hr.copy_(rstd, non_blocking=True)
+        hdg.copy_(dg, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dist, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / e2e_steps
+    h2d = (hx.numel() + hdy.numel() + hg.numel()) * 2
+    d2h = (hy.numel() + hdx.numel()) * 2 + (hr.numel() + hdg.numel()) * 4
+
+    if clocks:
+        clocks.close()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = measured_peaks()
+    fwd_avg = statistics.fmean(fwd_ms)
+    bwd_avg = statistics.fmean(bwd_ms)
+    bwd_gbs = bwd_b / (bwd_avg * 1e-3) / 1e9
+    fwd_gbs = fwd_b / (fwd_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": config_dict(w),
+        "rows_per_s": round(M * world / (ms_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100.0 * value / (peak * world), 2),
+        "per_call": {
+            "fwd_us": round(fwd_avg * 1e3, 2), "fwd_gbs": round(fwd_gbs, 1),
+            "fwd_frac": round(fwd_gbs / peak, 4),
+            "bwd_us": round(bwd_avg * 1e3, 2), "bwd_gbs": round(bwd_gbs, 1),
+            "bwd_frac": round(bwd_gbs / peak, 4),
+            "note": "bwd = backward rows kernel + dgamma column reduction (two launches)",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(bwd_gbs, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(bwd_gbs / peak, 4),
+            "traffic": captured_traffic("bwd"),
+            "kernel": "rms_bwd (rms_bwd_staged_kernel + rms_dgamma_colreduce_kernel)",
+            "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind}, burst copy)",
+        },
+        "roofline_fwd": {
+            "bound": "hbm", "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(fwd_gbs / peak, 4), "traffic": captured_traffic("fwd"),
+            "kernel": "rms_fwd (rms_fwd_registers_kernel)",
+        },
+        "e2e": {
+            "value": round((fwd_b + bwd_b) * world / (e2e_ms * 1e-3) / 1e9, 2),
+            "unit": "GB/s",
+            "ms_per_step": round(e2e_ms, 4),
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+        },
+        "gpu_launches": launches,
+        "clocks": clocks.summary() if clocks else None,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_throughput(w, inp)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+# DRAM bytes per call from one ncu capture of these kernels at this workload
+# (dram__bytes_read.sum + dram__bytes_write.sum of one timed step, summed
+# over the call's launches; profiles/rms_launch_list_wide_bf16_16384x8192.md).
+# They are reported only while the kernel sources hash to the value they were
+# captured with; after any kernel change the traffic reads null.
+TRAFFIC_CAPTURE = {
+    "src_sha256_16": "b97d9a30d993c9a2",
+    "bwd": 537081088 + 233487104 + 9968128,  # staged rows kernel + column reduction
+    "fwd": 268470528 + 215680256,            # register-mapping forward
+}
+
+
+def kernel_source_hash() -> str:
+    import glob
+    import hashlib
+
+    csrc = os.path.join(ROOT, "row_wise_normalization_rms_gb300", "csrc")
+    files = sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))
+                   + glob.glob(os.path.join(csrc, "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(which: str):
+    if kernel_source_hash() != TRAFFIC_CAPTURE["src_sha256_16"]:
+        return None
+    return TRAFFIC_CAPTURE[which]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

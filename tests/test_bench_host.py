@@ -1,0 +1,69 @@
+"""bench.py's host logic without a GPU: the multi-rank reduction over gloo
+(world size 2), the byte formula, and the reference (oracle) arm."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+
+    r, lr, w = bench.dist_env()
+    dist = bench.init_dist(w, "gloo")
+    bench.barrier(dist)
+    m = bench.max_over_ranks(10.0 + 5.0 * r, dist)
+    out[r] = (r, lr, w, m)
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    port = 29500 + os.getpid() % 1000
+    with mp.Manager() as man:
+        out = man.dict()
+        mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
+        res = dict(out)
+    assert res[0] == (0, 0, 2, 15.0) and res[1] == (1, 1, 2, 15.0)
+
+
+def test_step_bytes_formula():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    f, b = bench.step_bytes(16384, 8192, 2)
+    assert f == 2 * 16384 * 8192 * 2 + 4 * 16384 + 8192 * 2
+    assert b == 3 * 16384 * 8192 * 2 + 4 * 16384 + 8192 * 2 + 4 * 8192
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["config"]["M"] == 16384 and d["config"]["N"] == 8192
+
+
+def test_reference_arm_other_ranks_are_silent():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "3",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300,
+                       env=env)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_warmup_floor():
+    r = subprocess.run([sys.executable, "bench.py", "--warmup", "2"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
