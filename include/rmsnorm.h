@@ -137,6 +137,33 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
                       int64_t M, int64_t N, rms_dtype dtype, int gemma, int inplace_dx,
                       rms_path path, void* stream);
 
+/*
+ * rms_bwd_noalloc — rms_bwd without a caller-provided workspace.  The paper
+ * has no counterpart: this entry point exists for callers, not for the
+ * method.  It is for callers that cannot obtain device scratch memory
+ * themselves: a plugin inside a host program whose allocator owns all device
+ * memory and offers no way to request scratch, or a latency-critical loop
+ * that must not pay cudaMalloc's device-wide synchronisation.  It allocates
+ * nothing and calls no allocating routine; the caller still passes every
+ * input and output, with the meanings, layouts and errors of rms_bwd.
+ *   Scratch: a fixed array of RMS_NOALLOC_SCRATCH_BYTES (32 MiB) inside this
+ *   library, held by every device that loads the library until the process
+ *   exits.  Shapes whose workspace need, rms_bwd_workspace_size(M, N) =
+ *   min(M, 4 * SMs) * N * 4 bytes rounded up to 256, exceeds it are
+ *   rejected with RMS_ERR_WORKSPACE (on a 152-SM GB300: any M with
+ *   N <= 13797, or M * N <= 8388608).
+ *   The first call on each device looks up the array's device address with
+ *   that device current; make that first call before any stream capture.
+ *   All calls on a device share the array and it keeps the last call's
+ *   contents (nothing in it needs clearing): calls whose executions overlap
+ *   on the GPU (other streams, other host threads) race and must be
+ *   serialised by the caller.
+ */
+#define RMS_NOALLOC_SCRATCH_BYTES (32u << 20)
+rms_status rms_bwd_noalloc(void* dy, const void* x, const void* gamma, const float* rstd,
+                           void* dx, float* dgamma, int64_t M, int64_t N, rms_dtype dtype,
+                           int gemma, int inplace_dx, void* stream);
+
 /* Bytes of workspace rms_bwd needs for M rows of N on the current device
  * (an upper bound over dtypes and mappings, a multiple of 256).  Returns 0
  * for M <= 0 or N <= 0, and 0 if the device cannot be queried. */

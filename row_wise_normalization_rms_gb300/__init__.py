@@ -21,7 +21,8 @@ PATHS = {"auto": RMS_PATH_AUTO, "registers": RMS_PATH_REGISTERS, "staged": RMS_P
          "scalar": RMS_PATH_SCALAR}
 
 __all__ = [
-    "RmsError", "lib", "rms_fwd", "rms_bwd", "rms_bwd_workspace_size", "rms_status_string",
+    "RmsError", "lib", "rms_fwd", "rms_bwd", "rms_bwd_noalloc", "rms_bwd_workspace_size",
+    "rms_status_string",
     "rms_last_device_status", "rms_set_wait_limit", "rms_launch_count", "dtype_code",
 ]
 
@@ -90,6 +91,19 @@ def rms_bwd(dy, x, gamma, rstd, dx, dgamma, workspace, gemma: int = 0, inplace_d
                           int(inplace_dx), _path(path), _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_bwd")
+
+
+def rms_bwd_noalloc(dy, x, gamma, rstd, dx, dgamma, gemma: int = 0, inplace_dx: int = 0,
+                    stream=None):
+    """rms_bwd with the library's built-in scratch instead of a workspace
+    argument, for callers that cannot allocate device scratch themselves
+    (see include/rmsnorm.h for the size limit and the sharing rules)."""
+    M, N = x.shape
+    st = lib().rms_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
+                               M, N, dtype_code(x), int(gemma), int(inplace_dx),
+                               _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "rms_bwd_noalloc")
 
 
 def rms_bwd_workspace_size(M: int, N: int) -> int:
