@@ -287,27 +287,44 @@ def run_gpu(args):
     barrier(dist, dev)
     torch.cuda.synchronize(dev)
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps + 1)]
+    # Timed region: K steps back to back, events only at its ends (events
+    # between calls would serialise the kernels' programmatic overlap).
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
     launches0 = rms.rms_launch_count()
     if clocks:
         clocks.start()
-    ev[0].record(stream)
-    for i in range(args.steps):
-        rms.rms_fwd(x, g, y, rstd, w.eps, w.gemma, stream=stream)
-        ev[2 * i + 1].record(stream)
-        rms.rms_bwd(dy, x, g, rstd, dx, dg, ws, w.gemma, w.inplace_dx, stream=stream)
-        ev[2 * i + 2].record(stream)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        step()
+    e_end.record(stream)
     torch.cuda.synchronize(dev)
     if clocks:
         clocks.stop()
     launches = rms.rms_launch_count() - launches0
-    total_ms = ev[0].elapsed_time(ev[-1])
-    fwd_ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
-    bwd_ms = [ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.steps)]
+    total_ms = e_start.elapsed_time(e_end)
     barrier(dist, dev)
     total_ms = max_over_ranks(total_ms, dist, dev)
     ms_step = total_ms / args.steps
     value = (fwd_b + bwd_b) * world / (ms_step * 1e-3) / 1e9
+
+    # Per-call durations: the same calls, K of one kind back to back, on the
+    # same stream; average = elapsed / K.
+    def per_call(fn, k):
+        for _ in range(3):
+            fn()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(z) / k
+
+    k_call = max(10, args.steps // 2)
+    fwd_avg = per_call(lambda: rms.rms_fwd(x, g, y, rstd, w.eps, w.gemma, stream=stream), k_call)
+    bwd_avg = per_call(lambda: rms.rms_bwd(dy, x, g, rstd, dx, dg, ws, w.gemma, w.inplace_dx,
+                                           stream=stream), k_call)
 
     # End to end through the same API with host buffers.
     e2e_steps = max(3, min(args.steps, 20))
@@ -347,8 +364,6 @@ def run_gpu(args):
         return 0
 
     peak, peak_kind = measured_peaks()
-    fwd_avg = statistics.fmean(fwd_ms)
-    bwd_avg = statistics.fmean(bwd_ms)
     bwd_gbs = bwd_b / (bwd_avg * 1e-3) / 1e9
     fwd_gbs = fwd_b / (fwd_avg * 1e-3) / 1e9
     line = {
@@ -372,7 +387,8 @@ def run_gpu(args):
             "fwd_frac": round(fwd_gbs / peak, 4),
             "bwd_us": round(bwd_avg * 1e3, 2), "bwd_gbs": round(bwd_gbs, 1),
             "bwd_frac": round(bwd_gbs / peak, 4),
-            "note": "bwd = backward rows kernel + dgamma column reduction (two launches)",
+            "note": ("average over back-to-back calls of one kind (CUDA events around the "
+                     "loop); bwd = backward rows kernel + dgamma column reduction"),
         },
         "roofline": {
             "bound": "hbm",
@@ -413,9 +429,9 @@ def run_gpu(args):
 # They are reported only while the kernel sources hash to the value they were
 # captured with; after any kernel change the traffic reads null.
 TRAFFIC_CAPTURE = {
-    "src_sha256_16": "20d508676230af24",
-    "bwd": 537081088 + 233487104 + 9968128,  # staged rows kernel + column reduction
-    "fwd": 268470528 + 215680256,            # register-mapping forward
+    "src_sha256_16": "0afed5f8f19ac3ba",
+    "bwd": 537005312 + 233666048 + 9975552,  # staged rows kernel + column reduction
+    "fwd": 268471552 + 215691776,            # register-mapping forward
 }
 
 
@@ -443,6 +459,93 @@ def captured_traffic(which: str):
     return TRAFFIC_CAPTURE[which]
 
 
+def run_sweep(args):
+    """Per-call forward and backward timing of every workload (not the
+    contract line): one JSON line per workload and mapping.  Calls of one
+    kind run back to back over k rotating buffer sets, k chosen so the sets
+    together exceed three times the L2 (at most 64 sets); CUDA events around
+    each loop, average per call.  (In-place workloads overwrite dy with dx in
+    every backward call; the timing does not depend on the values.)"""
+    import numpy as np
+    import torch
+
+    import row_wise_normalization_rms_gb300 as rms
+    from synthetic import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    peak, peak_kind = measured_peaks()
+    names = args.workloads.split(",") if args.workloads else list(WORKLOADS)
+    paths = args.paths.split(",")
+    for name in names:
+        w = WORKLOADS[name]
+        M, N, b = w.M, w.N, w.elem_bytes
+        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+        inp = make_inputs(w)
+
+        def dev_t(a):
+            if w.dtype == "bf16":
+                return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            return torch.from_numpy(a).to(dev)
+
+        set_bytes = 4 * M * N * b
+        k = int(min(64, max(1, -(-3 * L2_BYTES // set_bytes))))
+        x0, dy0, g = dev_t(inp["x"]), dev_t(inp["dy"]), dev_t(inp["gamma"])
+        sets = []
+        for i in range(k):
+            sets.append((x0 if i == 0 else x0.clone(), dy0 if i == 0 else dy0.clone(),
+                         torch.empty_like(x0), torch.empty_like(x0),
+                         torch.empty(M, device=dev)))
+        dg = torch.empty(N, device=dev)
+        ws = torch.empty(max(256, rms.rms_bwd_workspace_size(M, N)), dtype=torch.uint8, device=dev)
+        fwd_b, bwd_b = step_bytes(M, N, b)
+        calls = max(args.steps, 2 * k)
+        for path in paths:
+            def fwd_call(i):
+                x, dy, y, dx, r = sets[i % k]
+                rms.rms_fwd(x, g, y, r, w.eps, w.gemma, path=path)
+
+            def bwd_call(i):
+                x, dy, y, dx, r = sets[i % k]
+                rms.rms_bwd(dy, x, g, r, None if w.inplace_dx else dx, dg, ws, w.gemma,
+                            w.inplace_dx, path=path)
+
+            def timed(fn, n):
+                for i in range(max(3, args.warmup)):
+                    fn(i)
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for i in range(n):
+                    fn(i)
+                z.record()
+                torch.cuda.synchronize()
+                return a.elapsed_time(z) / n
+
+            try:
+                for i in range(k):
+                    fwd_call(i)  # every set gets its rstd before the backward loop
+                f_ms = timed(fwd_call, calls)
+                b_ms = timed(bwd_call, calls)
+            except rms.RmsError as e:
+                print(json.dumps({"workload": name, "path": path, "error": str(e)}), flush=True)
+                continue
+            fg = fwd_b / (f_ms * 1e-3) / 1e9
+            bg = bwd_b / (b_ms * 1e-3) / 1e9
+            print(json.dumps({
+                "workload": name, "M": M, "N": N, "dtype": w.dtype, "gemma": w.gemma,
+                "inplace_dx": w.inplace_dx, "path": path, "calls": calls, "buffer_sets": k,
+                "l2": ("rotating sets exceed 3x L2" if k * set_bytes >= 3 * L2_BYTES
+                       else "sets fit in L2: launch-bound shape"),
+                "fwd_us": round(f_ms * 1e3, 2), "fwd_gbs": round(fg, 1),
+                "fwd_frac": round(fg / peak, 4),
+                "bwd_us": round(b_ms * 1e3, 2), "bwd_gbs": round(bg, 1),
+                "bwd_frac": round(bg / peak, 4),
+                "peak_gbs": peak, "peak_source": peak_kind}), flush=True)
+        del sets, x0, dy0
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -450,11 +553,19 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="per-call timing of every workload instead of the benchmark line")
+    ap.add_argument("--workloads", default="", help="comma-separated workload names (--sweep)")
+    ap.add_argument("--paths", default="auto", help="comma-separated row mappings (--sweep)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sweep:
+        if args.steps == 4000:
+            args.steps = 50
+        return run_sweep(args)
     return run_gpu(args)
 
 

@@ -45,6 +45,9 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restri
   const int64_t gid0 = (int64_t)blockIdx.x * R;  // the CTA's first group: it has the most rows
   const int64_t gid = gid0 + grp;
   const int64_t iters = gid0 < M ? (M - gid0 + groups - 1) / groups : 0;
+  // Let the column reduction (a programmatic dependent) launch into SMs this
+  // grid frees; it waits for this grid's completion before reading.
+  pdl_wait();
 
   const uint4* gv = reinterpret_cast<const uint4*>(gamma);
   uint4 gw[KV];
@@ -148,13 +151,14 @@ static cudaError_t launch_g(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cuda
   const T* x = static_cast<const T*>(a.x);
   const T* g = static_cast<const T*>(a.gamma);
   T* dx = static_cast<T*>(a.dx);
+  cudaError_t e;
   switch (m.kv) {
-    case 1: rms_bwd_registers_kernel<T, 1, GEMMA><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
-    case 2: rms_bwd_registers_kernel<T, 2, GEMMA><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
-    case 4: rms_bwd_registers_kernel<T, 4, GEMMA><<<grid, block, m.smem, s>>>(dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
+    case 1: e = launch_pdl(rms_bwd_registers_kernel<T, 1, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
+    case 2: e = launch_pdl(rms_bwd_registers_kernel<T, 2, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
+    case 4: e = launch_pdl(rms_bwd_registers_kernel<T, 4, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 template <typename T>

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace rmsk {
 
 // ---- element traits --------------------------------------------------------
@@ -230,6 +232,20 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 __device__ __forceinline__ uint4 ld_keep(const uint4* p) { return __ldg(p); }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Every kernel is launched with programmatic stream serialisation allowed,
+// so it may be scheduled while its predecessor in the stream is finishing,
+// and waits for the predecessor's completion and memory (pdl_wait) before it
+// reads or writes any global memory.  Only the non-persistent forward
+// kernels let their dependents be scheduled early (pdl_trigger, once every
+// CTA has started); the persistent kernels trigger implicitly at exit: an
+// early trigger there let dependents take SM slots mid-run and cost up to
+// 50 % at some shapes.  Both are no-ops without such a dependency.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- reductions ------------------------------------------------------------
 // Butterfly sum over a warp.  a+b == b+a exactly, so every lane ends with the
 // same bits and the order depends on nothing but the lane layout.
@@ -255,6 +271,23 @@ __device__ __forceinline__ float group_sum(float v, int G, int first_warp, float
   const int nw = G >> 5;
   for (int w = 0; w < nw; ++w) s += red[first_warp + w];
   return s;
+}
+
+// Host side: launch `kernel` with programmatic stream serialisation allowed.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace rmsk

@@ -30,6 +30,8 @@ rms_fwd_registers_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T
   const bool active = row < M;
   const uint4* xr = reinterpret_cast<const uint4*>(x) + (active ? row : 0) * (int64_t)NV;
   const uint4* gv = reinterpret_cast<const uint4*>(gamma);
+  pdl_trigger();
+  pdl_wait();
 
   uint4 xv[KV];
 #pragma unroll
@@ -59,13 +61,14 @@ static cudaError_t launch_g(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cuda
   const T* x = static_cast<const T*>(a.x);
   const T* g = static_cast<const T*>(a.gamma);
   T* y = static_cast<T*>(a.y);
+  cudaError_t e;
   switch (m.kv) {
-    case 1: rms_fwd_registers_kernel<T, 1, GEMMA><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
-    case 2: rms_fwd_registers_kernel<T, 2, GEMMA><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
-    case 4: rms_fwd_registers_kernel<T, 4, GEMMA><<<grid, block, 0, s>>>(x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
+    case 1: e = launch_pdl(rms_fwd_registers_kernel<T, 1, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
+    case 2: e = launch_pdl(rms_fwd_registers_kernel<T, 2, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
+    case 4: e = launch_pdl(rms_fwd_registers_kernel<T, 4, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 template <typename T>

@@ -140,6 +140,7 @@ rms_fwd_staged_kernel(const StagedParams p) {
   const uint32_t row_off = (uint32_t)(q * p.N * (int)sizeof(T));
 
   init_barriers(p, h);
+  pdl_wait();
   uint64_t pol = 0;
   int64_t issued = 0;  // thread 0 only
   if (threadIdx.x == 0) {
@@ -217,6 +218,7 @@ rms_bwd_staged_kernel(const StagedParams p) {
   const uint32_t row_off = (uint32_t)(q * p.N * (int)sizeof(T));
 
   init_barriers(p, h);
+  pdl_wait();
   uint64_t pol = 0;
   int64_t issued = 0;  // thread 0 only
   if (threadIdx.x == 0) {
@@ -367,6 +369,9 @@ namespace {
 #ifndef RMS_STAGED_MAX_STAGES
 #define RMS_STAGED_MAX_STAGES 8
 #endif
+#ifndef RMS_STAGED_KV_MAX
+#define RMS_STAGED_KV_MAX 4
+#endif
 
 const void* staged_kernel(int dtype, bool bwd, int kv, bool gemma) {
   if (dtype == kBF16)
@@ -423,8 +428,12 @@ bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
   } else if (NV <= 64) {
     kv = 2; G = 32;
   } else {
-    kv = 4;
-    G = ((NV + 3) / 4 + 31) / 32 * 32;
+    kv = RMS_STAGED_KV_MAX;
+    G = ((NV + kv - 1) / kv + 31) / 32 * 32;
+    if (G > max_threads) {
+      kv = 4;
+      G = ((NV + 3) / 4 + 31) / 32 * 32;
+    }
     if (G > max_threads) return false;
   }
   int R = (int)(RMS_STAGED_TILE_BYTES / row_bytes);
@@ -492,25 +501,27 @@ static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, int b, bool
 template <typename T, bool GEMMA>
 static cudaError_t launch_fwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
+  cudaError_t e;
   switch (m.kv) {
-    case 1: rmsk::rms_fwd_staged_kernel<T, 1, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    case 2: rmsk::rms_fwd_staged_kernel<T, 2, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    case 4: rmsk::rms_fwd_staged_kernel<T, 4, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 1: e = rmsk::launch_pdl(rmsk::rms_fwd_staged_kernel<T, 1, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
+    case 2: e = rmsk::launch_pdl(rmsk::rms_fwd_staged_kernel<T, 2, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
+    case 4: e = rmsk::launch_pdl(rmsk::rms_fwd_staged_kernel<T, 4, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 template <typename T, bool GEMMA>
 static cudaError_t launch_bwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
+  cudaError_t e;
   switch (m.kv) {
-    case 1: rmsk::rms_bwd_staged_kernel<T, 1, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    case 2: rmsk::rms_bwd_staged_kernel<T, 2, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
-    case 4: rmsk::rms_bwd_staged_kernel<T, 4, GEMMA><<<(unsigned)grid, m.threads, m.smem, s>>>(p); break;
+    case 1: e = rmsk::launch_pdl(rmsk::rms_bwd_staged_kernel<T, 1, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
+    case 2: e = rmsk::launch_pdl(rmsk::rms_bwd_staged_kernel<T, 2, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
+    case 4: e = rmsk::launch_pdl(rmsk::rms_bwd_staged_kernel<T, 4, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 template <typename T>
