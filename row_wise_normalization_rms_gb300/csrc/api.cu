@@ -294,8 +294,8 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
       break;
   }
   if (e != cudaSuccess) return RMS_ERR_CUDA;
-  if ((size_t)m.blocks * (size_t)N * sizeof(float) > need) return RMS_ERR_WORKSPACE;  // unreachable
-  e = rmsi::launch_colreduce(a.ws, dgamma, m.blocks, (int)N, s);
+  if ((size_t)m.partials * (size_t)N * sizeof(float) > need) return RMS_ERR_WORKSPACE;  // unreachable
+  e = rmsi::launch_colreduce(a.ws, dgamma, m.partials, (int)N, s);
   if (e != cudaSuccess) return RMS_ERR_CUDA;
   g_launches.fetch_add(2);
   return RMS_OK;

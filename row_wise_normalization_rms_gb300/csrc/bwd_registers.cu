@@ -185,6 +185,7 @@ cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m
   if (P > need) P = need;
   if (P < 1) P = 1;
   m->blocks = P;
+  m->partials = P;
   return cudaSuccess;
 }
 

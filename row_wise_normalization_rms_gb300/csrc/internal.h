@@ -45,7 +45,10 @@ struct Mapping {
   int threads = 0;       // threads per CTA
   int rows_per_cta = 0;  // rows a CTA works on at once (threads / G)
   int64_t blocks = 0;    // CTAs launched
+  int64_t partials = 0;  // backward: workspace rows of column partials (one per CTA or cluster)
   int stages = 0;        // shared-memory pipeline depth (staged path)
+  int cluster = 1;       // CTAs per cluster sharing one row (staged path)
+  int sv = 0;            // 16-byte vectors per CTA's column slice (staged path)
   size_t smem = 0;       // dynamic shared memory bytes
 };
 
@@ -66,7 +69,7 @@ inline int64_t max_partials(int sms) { return 4 * (int64_t)sms; }
 // ---- register path (fwd_registers.cu, bwd_registers.cu) ----
 bool plan_registers(int N, int dtype, bool bwd, Mapping* m);
 cudaError_t launch_fwd_registers(const FwdArgs& a, const Mapping& m, cudaStream_t s);
-// Fills m.blocks (= number of partial rows P) for a persistent backward.
+// Fill m.blocks (CTAs) and m.partials (workspace rows) for a persistent backward.
 cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m);
 cudaError_t launch_bwd_registers(const BwdArgs& a, const Mapping& m, cudaStream_t s);
 

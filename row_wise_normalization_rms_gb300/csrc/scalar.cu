@@ -199,6 +199,7 @@ cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   if (P > a.M) P = a.M;
   if (P < 1) P = 1;
   m->blocks = P;
+  m->partials = P;
   return cudaSuccess;
 }
 

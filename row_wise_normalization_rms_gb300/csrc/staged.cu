@@ -44,24 +44,28 @@ struct StagedParams {
   void* y;               // forward output
   const void* dy;        // backward input
   void* dx;              // backward output (may equal dy)
-  float* ws;             // backward: [gridDim.x][N] column partials
+  float* ws;             // backward: [units][N] column partials
   int64_t M;
   int N;
   float eps;
   int gemma;
-  int G;  // threads per row
-  int R;  // rows per tile
-  int S;  // stages
+  int G;   // threads per row slice
+  int R;   // rows per tile (1 when C > 1)
+  int S;   // stages
+  int C;   // CTAs per cluster sharing one row (1: no cluster)
+  int SV;  // 16-byte vectors per CTA's column slice (the whole row when C == 1)
   int64_t ntiles;
-  uint32_t tile_bytes;   // R * N * sizeof(T)
+  uint32_t tile_bytes;   // R * SV * 16
   uint32_t stage_bytes;  // tile_bytes (forward) or 2 * tile_bytes (backward)
   long long wait_limit;
 };
 
 struct StageHeader {
   uint64_t* full;
-  float* red;           // [2][32]
-  volatile int* abort;  // [2]
+  float* red;             // [2][32] warp partial sums
+  volatile int* abort;    // [2] a wait of this CTA gave up
+  float* cta_sum;         // [2] this CTA's partial of the row (clusters)
+  int* cta_abort;         // [2] this CTA's abort flag, as read by its peers
   uint8_t* stages;
 };
 
@@ -69,29 +73,50 @@ __device__ __forceinline__ StageHeader header(uint8_t* smem) {
   StageHeader h;
   h.full = reinterpret_cast<uint64_t*>(smem);
   h.red = reinterpret_cast<float*>(smem + 64);
-  h.abort = reinterpret_cast<volatile int*>(smem + 64 + 2 * 32 * sizeof(float));
+  h.abort = reinterpret_cast<volatile int*>(smem + 320);
+  h.cta_sum = reinterpret_cast<float*>(smem + 336);
+  h.cta_abort = reinterpret_cast<int*>(smem + 352);
   h.stages = smem + kHeaderBytes;
   return h;
 }
 
-// Thread 0: start the copy of local tile i (tile blockIdx.x + i*gridDim.x)
-// into stage i % S: x, and for the backward dy right after it.
+// Which part of which rows this CTA works on.  Without clusters a unit is a
+// CTA and its slice is the whole row; with clusters of C CTAs a unit is a
+// cluster and CTA rank c owns vectors [c*SV, c*SV + nvs) of each row.
+struct Slice {
+  int64_t unit, units;  // this work unit and how many there are
+  int rank;             // CTA rank in the cluster (0 without clusters)
+  int v0, nvs;          // first vector and vector count of this CTA's slice
+};
+
+__device__ __forceinline__ Slice my_slice(const StagedParams& p, int NV) {
+  Slice sl;
+  sl.rank = p.C > 1 ? (int)cluster_rank() : 0;
+  sl.unit = blockIdx.x / p.C;
+  sl.units = gridDim.x / p.C;
+  sl.v0 = sl.rank * p.SV;
+  sl.nvs = min(p.SV, NV - sl.v0);
+  return sl;
+}
+
+// Thread 0: start the copy of local tile i (rows of tile unit + i*units,
+// this CTA's slice) into stage i % S: x, and for the backward dy after it.
 template <typename T, bool BWD>
-__device__ __forceinline__ void issue_tile(const StagedParams& p, const StageHeader& h, int64_t i,
-                                           uint64_t pol) {
-  const int64_t t = blockIdx.x + i * gridDim.x;
+__device__ __forceinline__ void issue_tile(const StagedParams& p, const StageHeader& h,
+                                           const Slice& sl, int64_t i, uint64_t pol) {
+  const int64_t t = sl.unit + i * sl.units;
   const int64_t row0 = t * p.R;
   const int64_t rows = min((int64_t)p.R, p.M - row0);
   const int64_t row_bytes = (int64_t)p.N * sizeof(T);
-  const uint32_t bytes = (uint32_t)(rows * row_bytes);
+  // Without clusters nvs*16 == row_bytes and the R rows are contiguous.
+  const uint32_t bytes = (uint32_t)(rows * sl.nvs * 16);
+  const int64_t src = row0 * row_bytes + (int64_t)sl.v0 * 16;
   const int s = (int)(i % p.S);
   const uint32_t bar = smem_u32(&h.full[s]);
   const uint32_t dst = smem_u32(h.stages + (size_t)s * p.stage_bytes);
   mbar_arrive_expect_tx(bar, BWD ? 2 * bytes : bytes);
-  tma_load_1d(dst, static_cast<const char*>(p.x) + row0 * row_bytes, bytes, bar, pol);
-  if (BWD)
-    tma_load_1d(dst + p.tile_bytes, static_cast<const char*>(p.dy) + row0 * row_bytes, bytes, bar,
-                pol);
+  tma_load_1d(dst, static_cast<const char*>(p.x) + src, bytes, bar, pol);
+  if (BWD) tma_load_1d(dst + p.tile_bytes, static_cast<const char*>(p.dy) + src, bytes, bar, pol);
 }
 
 // After an abort at local tile i: wait (bounded) for the copies this CTA
@@ -115,13 +140,46 @@ __device__ __forceinline__ void init_barriers(const StagedParams& p, const Stage
   __syncthreads();
 }
 
+// The row's total of a per-thread partial, after the stage barrier of
+// iteration i.  Without clusters: the group's warp partials in warp order.
+// With clusters: each CTA's sum (warps in order) exchanged through
+// distributed shared memory, added in rank order; the abort decision is made
+// the same way, so every CTA of a cluster leaves the loop together.  Returns
+// the total; *abort tells whether any CTA (of the cluster) gave up a wait.
+__device__ __forceinline__ float row_total(const StagedParams& p, const StageHeader& h, int buf,
+                                           int first_warp, int nw, bool* abort) {
+  float tot = 0.f;
+  for (int w = 0; w < nw; ++w) tot += h.red[buf * 32 + first_warp + w];
+  if (p.C == 1) {
+    *abort = h.abort[buf] != 0;
+    return tot;
+  }
+  if (threadIdx.x == 0) {
+    h.cta_sum[buf] = tot;
+    h.cta_abort[buf] = h.abort[buf];
+  }
+  cluster_sync();
+  const uint32_t sa = smem_u32(&h.cta_sum[buf]);
+  const uint32_t aa = smem_u32(&h.cta_abort[buf]);
+  float all = 0.f;
+  int ab = 0;
+  for (int c = 0; c < p.C; ++c) {
+    all += ld_cluster_f32(map_to_rank(sa, (uint32_t)c));
+    ab |= ld_cluster_s32(map_to_rank(aa, (uint32_t)c));
+  }
+  *abort = ab != 0;
+  return all;
+}
+
 // Pipeline shared by both kernels.  Local tile i lives in stage i % S.
 // Iteration i: wait for tile i, first pass over it (row partial sums),
 // barrier, second pass (outputs).  The barrier of iteration i also proves
-// every thread finished the second pass of tile i-1, so right after it
-// thread 0 refills that stage with tile i-1+S: S-2 tiles stay in flight
-// while tile i is processed, and no row slice has to stay in registers
-// across the barrier.
+// every thread of the CTA finished the second pass of tile i-1, so right
+// after it thread 0 refills that stage with the next tile: S-2 tiles stay in
+// flight while tile i is processed, and no row slice has to stay in
+// registers across the barrier.  With clusters a cluster barrier follows for
+// the exchange of row partials, and a last one before exit keeps every CTA's
+// shared memory alive while its peers may still read it.
 
 template <typename T, int KV, bool GEMMA>
 __global__ void __launch_bounds__(1024)
@@ -131,13 +189,14 @@ rms_fwd_staged_kernel(const StagedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const StageHeader h = header(smem);
   const int NV = p.N / VN;
+  const Slice sl = my_slice(p, NV);
   const int q = threadIdx.x / p.G;
   const int lig = threadIdx.x - q * p.G;
   const int warp = threadIdx.x >> 5;
   const int first_warp = q * (p.G >> 5);
   const int nw = p.G >> 5;
-  const int64_t my_tiles = (p.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
-  const uint32_t row_off = (uint32_t)(q * p.N * (int)sizeof(T));
+  const int64_t my_tiles = (p.ntiles - sl.unit + sl.units - 1) / sl.units;
+  const uint32_t row_off = (uint32_t)(q * p.SV * 16);
 
   init_barriers(p, h);
   pdl_wait();
@@ -146,15 +205,15 @@ rms_fwd_staged_kernel(const StagedParams p) {
   if (threadIdx.x == 0) {
     pol = l2_evict_first_policy();
     const int64_t pre = min((int64_t)p.S, my_tiles);
-    for (; issued < pre; ++issued) issue_tile<T, false>(p, h, issued, pol);
+    for (; issued < pre; ++issued) issue_tile<T, false>(p, h, sl, issued, pol);
   }
 
-  const uint4* gv = reinterpret_cast<const uint4*>(p.gamma);
+  const uint4* gv = reinterpret_cast<const uint4*>(p.gamma) + sl.v0;
   uint4 gw[KV];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * p.G;
-    gw[k] = v < NV ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+    gw[k] = v < sl.nvs ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
   }
 
   int64_t i = 0;
@@ -162,7 +221,7 @@ rms_fwd_staged_kernel(const StagedParams p) {
   for (; i < my_tiles; ++i) {
     const int s = (int)(i % p.S);
     const int buf = (int)(i & 1);
-    const int64_t row = (blockIdx.x + i * gridDim.x) * p.R + q;
+    const int64_t row = (sl.unit + i * sl.units) * p.R + q;
     const bool active = row < p.M;
     if (!mbar_wait(smem_u32(&h.full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) h.abort[buf] = 1;
 
@@ -172,32 +231,33 @@ rms_fwd_staged_kernel(const StagedParams p) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < NV) Math::sumsq(lds128(xs + 16u * v), ss2);
+        if (v < sl.nvs) Math::sumsq(lds128(xs + 16u * v), ss2);
       }
     }
     const float ss = warp_sum(lo2(ss2) + hi2(ss2));
     if ((threadIdx.x & 31) == 0) h.red[buf * 32 + warp] = ss;
     __syncthreads();  // partial sums visible; tile i-1 fully consumed
-    if (h.abort[buf]) {
+    if (threadIdx.x == 0 && i >= 1 && issued < my_tiles && !h.abort[buf])
+      issue_tile<T, false>(p, h, sl, issued++, pol);
+    bool abort;
+    const float tot = row_total(p, h, buf, first_warp, nw, &abort);
+    if (abort) {
       aborted = true;
       break;
     }
-    if (threadIdx.x == 0 && i >= 1 && issued < my_tiles) issue_tile<T, false>(p, h, issued++, pol);
-
-    float tot = 0.f;
-    for (int w = 0; w < nw; ++w) tot += h.red[buf * 32 + first_warp + w];
     const float r = 1.0f / sqrtf(tot / (float)p.N + p.eps);
     if (active) {
-      if (lig == 0) p.rstd_out[row] = r;
-      uint4* yr = reinterpret_cast<uint4*>(p.y) + row * (int64_t)NV;
+      if (lig == 0 && sl.rank == 0) p.rstd_out[row] = r;
+      uint4* yr = reinterpret_cast<uint4*>(p.y) + row * (int64_t)NV + sl.v0;
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < NV) st_stream(yr + v, Math::forward(lds128(xs + 16u * v), gw[k], r));
+        if (v < sl.nvs) st_stream(yr + v, Math::forward(lds128(xs + 16u * v), gw[k], r));
       }
     }
   }
   if (aborted && threadIdx.x == 0) drain_and_flag(p, h, i, issued);
+  if (p.C > 1) cluster_sync();
 }
 
 template <typename T, int KV, bool GEMMA>
@@ -209,13 +269,14 @@ rms_bwd_staged_kernel(const StagedParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const StageHeader h = header(smem);
   const int NV = p.N / VN;
+  const Slice sl = my_slice(p, NV);
   const int q = threadIdx.x / p.G;
   const int lig = threadIdx.x - q * p.G;
   const int warp = threadIdx.x >> 5;
   const int first_warp = q * (p.G >> 5);
   const int nw = p.G >> 5;
-  const int64_t my_tiles = (p.ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
-  const uint32_t row_off = (uint32_t)(q * p.N * (int)sizeof(T));
+  const int64_t my_tiles = (p.ntiles - sl.unit + sl.units - 1) / sl.units;
+  const uint32_t row_off = (uint32_t)(q * p.SV * 16);
 
   init_barriers(p, h);
   pdl_wait();
@@ -224,16 +285,16 @@ rms_bwd_staged_kernel(const StagedParams p) {
   if (threadIdx.x == 0) {
     pol = l2_evict_first_policy();
     const int64_t pre = min((int64_t)p.S, my_tiles);
-    for (; issued < pre; ++issued) issue_tile<T, true>(p, h, issued, pol);
+    for (; issued < pre; ++issued) issue_tile<T, true>(p, h, sl, issued, pol);
   }
 
-  const uint4* gv = reinterpret_cast<const uint4*>(p.gamma);
+  const uint4* gv = reinterpret_cast<const uint4*>(p.gamma) + sl.v0;
   uint4 gw[KV];
   f32x2 acc[KV][NP];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * p.G;
-    gw[k] = v < NV ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+    gw[k] = v < sl.nvs ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int e = 0; e < NP; ++e) acc[k][e] = 0ull;
   }
@@ -243,59 +304,61 @@ rms_bwd_staged_kernel(const StagedParams p) {
   for (; i < my_tiles; ++i) {
     const int s = (int)(i % p.S);
     const int buf = (int)(i & 1);
-    const int64_t row = (blockIdx.x + i * gridDim.x) * p.R + q;
+    const int64_t row = (sl.unit + i * sl.units) * p.R + q;
     const bool active = row < p.M;
     const float r = active ? p.rstd_in[row] : 0.f;
     if (!mbar_wait(smem_u32(&h.full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) h.abort[buf] = 1;
 
     const uint32_t xs = smem_u32(h.stages + (size_t)s * p.stage_bytes) + row_off;
     const uint32_t ds = xs + p.tile_bytes;
-    // First pass: r*sum(u*x) for the row, and this row's dgamma terms dy*x*r.
+    // First pass: r*sum(u*x) over the slice, and the slice's dgamma terms.
     f32x2 sux2 = 0ull;
     if (active) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < NV)
+        if (v < sl.nvs)
           Math::backward_sums(lds128(xs + 16u * v), lds128(ds + 16u * v), gw[k], r, sux2, acc[k]);
       }
     }
     const float sux = warp_sum(lo2(sux2) + hi2(sux2));
     if ((threadIdx.x & 31) == 0) h.red[buf * 32 + warp] = sux;
     __syncthreads();  // partial sums visible; tile i-1 fully consumed
-    if (h.abort[buf]) {
+    if (threadIdx.x == 0 && i >= 1 && issued < my_tiles && !h.abort[buf])
+      issue_tile<T, true>(p, h, sl, issued++, pol);
+    bool abort;
+    const float tot = row_total(p, h, buf, first_warp, nw, &abort);
+    if (abort) {
       aborted = true;
       break;
     }
-    if (threadIdx.x == 0 && i >= 1 && issued < my_tiles) issue_tile<T, true>(p, h, issued++, pol);
-
-    float tot = 0.f;
-    for (int w = 0; w < nw; ++w) tot += h.red[buf * 32 + first_warp + w];
     const float kc = tot / (float)p.N;  // r * mean(u*x)
     // Second pass: dx = r*(u - x*r*kc).
     if (active) {
-      uint4* out = reinterpret_cast<uint4*>(p.dx) + row * (int64_t)NV;
+      uint4* out = reinterpret_cast<uint4*>(p.dx) + row * (int64_t)NV + sl.v0;
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < NV)
+        if (v < sl.nvs)
           st_stream(out + v, Math::backward_dx(lds128(xs + 16u * v), lds128(ds + 16u * v), gw[k], r, kc));
       }
     }
   }
   if (aborted) {
     if (threadIdx.x == 0) drain_and_flag(p, h, i, issued);
+    if (p.C > 1) cluster_sync();
     return;  // the partial row stays unwritten; the status word reports it
   }
 
-  // This CTA's column partials: one workspace row, groups combined in
-  // group order through the (now idle) stage memory.
-  float* wp = p.ws + (int64_t)blockIdx.x * p.N;
+  // This unit's column partials: one workspace row per unit; this CTA writes
+  // its slice; groups of a CTA (several rows per tile) are combined in group
+  // order through the (now idle) stage memory.
+  float* wp = p.ws + sl.unit * (int64_t)p.N + (int64_t)sl.v0 * VN;
   if (p.R == 1) {
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
       const int v = lig + k * p.G;
-      if (v < NV) {
+      if (v < sl.nvs) {
         float4* w4 = reinterpret_cast<float4*>(wp + (int64_t)v * VN);
 #pragma unroll
         for (int c = 0; c < NP / 2; ++c)
@@ -309,7 +372,7 @@ rms_bwd_staged_kernel(const StagedParams p) {
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
       const int v = lig + k * p.G;
-      if (v < NV) {
+      if (v < sl.nvs) {
 #pragma unroll
         for (int e = 0; e < NP; ++e) {
           part[(int64_t)q * p.N + v * VN + 2 * e] = lo2(acc[k][e]);
@@ -324,6 +387,7 @@ rms_bwd_staged_kernel(const StagedParams p) {
       wp[j] = t;
     }
   }
+  if (p.C > 1) cluster_sync();
 }
 
 template <typename T, bool BWD, bool GEMMA>
@@ -372,6 +436,9 @@ namespace {
 #ifndef RMS_STAGED_KV_MAX
 #define RMS_STAGED_KV_MAX 4
 #endif
+#ifndef RMS_STAGED_MIN_CPS
+#define RMS_STAGED_MIN_CPS 1
+#endif
 
 const void* staged_kernel(int dtype, bool bwd, int kv, bool gemma) {
   if (dtype == kBF16)
@@ -413,40 +480,42 @@ cudaError_t occupancy(const void* k, const DeviceInfo& d, int threads, size_t sm
 
 }  // namespace
 
-// Tiles of R rows (about 16 KiB of x, at most 16 rows), G threads per row
-// with up to 4 vectors each, and as many stages as fit in the per-SM
-// shared-memory budget (at least three per CTA).
-bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
-  const int b = dtype == kBF16 ? 2 : 4;
-  if (N <= 0 || ((int64_t)N * b) % 16 != 0) return false;
-  const int64_t row_bytes = (int64_t)N * b;
-  const int NV = (int)(row_bytes / 16);
+// One plan for a cluster size C: the row split into C slices of SV vectors
+// (C = 1: whole rows, tiles of R rows of about 16 KiB, at most 16 rows), G
+// threads per row slice with up to 4 vectors each, and as many stages as fit
+// in the per-SM shared-memory budget, at least three per CTA (one being
+// processed, one whose refill waits for the next barrier, one in flight):
+// the most CTAs per SM, up to the cap, whose three stages fit.
+static bool plan_for_cluster(int C, int NV, int64_t row_bytes, bool bwd, const DeviceInfo& d,
+                             Mapping* m) {
+  if (C > 1 && NV < 64 * C) return false;  // rows this short never need a cluster
+  const int SV = (NV + C - 1) / C;
   const int max_threads = bwd ? 512 : 1024;
   int kv, G;
-  if (NV <= 32) {
+  if (SV <= 32) {
     kv = 1; G = 32;
-  } else if (NV <= 64) {
+  } else if (SV <= 64) {
     kv = 2; G = 32;
   } else {
     kv = RMS_STAGED_KV_MAX;
-    G = ((NV + kv - 1) / kv + 31) / 32 * 32;
+    G = ((SV + kv - 1) / kv + 31) / 32 * 32;
     if (G > max_threads) {
       kv = 4;
-      G = ((NV + 3) / 4 + 31) / 32 * 32;
+      G = ((SV + 3) / 4 + 31) / 32 * 32;
     }
     if (G > max_threads) return false;
   }
-  int R = (int)(RMS_STAGED_TILE_BYTES / row_bytes);
-  if (R < 1) R = 1;
-  if (R > 16) R = 16;
-  while (R > 1 && G * R > max_threads) --R;
-  const int64_t tile = R * row_bytes;
+  int R = 1;
+  if (C == 1) {
+    R = (int)(RMS_STAGED_TILE_BYTES / row_bytes);
+    if (R < 1) R = 1;
+    if (R > 16) R = 16;
+    while (R > 1 && G * R > max_threads) --R;
+  }
+  const int64_t tile = (int64_t)R * SV * 16;
   const int64_t stage = bwd ? 2 * tile : tile;
   const int64_t budget = RMS_STAGED_SMEM_PER_SM;
   const int64_t cap = (int64_t)d.smem_optin - rmsk::kHeaderBytes;
-  // At least three stages per CTA: one being processed, one whose refill
-  // waits for the next barrier, and at least one more in flight.  The most
-  // CTAs per SM (up to the cap) whose three stages fit the budget.
   int cps = 0, S = 0;
   for (int c = RMS_STAGED_MAX_CTAS_PER_SM; c >= 1; --c) {
     const int64_t per_cta = std::min(budget / c, cap);
@@ -464,26 +533,78 @@ bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
   m->rows_per_cta = R;
   m->threads = G * R;
   m->stages = S;
+  m->cluster = C;
+  m->sv = SV;
   m->smem = rmsk::kHeaderBytes + (size_t)S * stage;
   m->blocks = cps;  // CTAs per SM wanted; the launcher turns it into a grid
   return true;
 }
 
+// The smallest cluster (1, 2, 4 or 8 CTAs) whose plan fits: rows up to
+// 16 KiB (backward) or 64 KiB (forward) per CTA, so clusters take rows of
+// up to 128 K bf16 elements in the backward and 256 K in the forward.
+bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
+  const int b = dtype == kBF16 ? 2 : 4;
+  if (N <= 0 || ((int64_t)N * b) % 16 != 0) return false;
+  const int64_t row_bytes = (int64_t)N * b;
+  const int NV = (int)(row_bytes / 16);
+  for (int C = 1; C <= 8; C *= 2)
+    if (plan_for_cluster(C, NV, row_bytes, bwd, d, m) && m->blocks >= RMS_STAGED_MIN_CPS)
+      return true;
+  for (int C = 1; C <= 8; C *= 2)
+    if (plan_for_cluster(C, NV, row_bytes, bwd, d, m)) return true;
+  return false;
+}
+
+// Launch config with programmatic serialisation and, for C > 1, the cluster
+// dimension.
+struct StagedLaunch {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  StagedLaunch(const Mapping& m, int64_t grid, cudaStream_t s) {
+    cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(m.threads);
+    cfg.dynamicSmemBytes = m.smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+    if (m.cluster > 1) {
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = m.cluster;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      cfg.numAttrs = 2;
+    }
+    cfg.attrs = attr;
+  }
+};
+
+// Persistent grid: as many work units (CTAs, or clusters of C CTAs) as fit
+// on the device at once, at most the planned CTAs per SM, at most the tiles.
 static cudaError_t grid_for(const void* k, const Mapping& m, const DeviceInfo& d, int64_t ntiles,
                             int64_t* grid) {
   int occ = 0;
   cudaError_t e = occupancy(k, d, m.threads, m.smem, &occ);
   if (e != cudaSuccess) return e;
   if (occ < 1) return cudaErrorInvalidConfiguration;
-  const int64_t per_sm = std::min<int64_t>(occ, m.blocks);
-  int64_t g = per_sm * d.sms;
-  if (g > ntiles) g = ntiles;
-  if (g < 1) g = 1;
-  *grid = g;
+  int64_t units = std::min<int64_t>(occ, m.blocks) * d.sms / m.cluster;
+  if (m.cluster > 1) {
+    StagedLaunch L(m, m.cluster, nullptr);
+    int nc = 0;
+    e = cudaOccupancyMaxActiveClusters(&nc, k, &L.cfg);
+    if (e != cudaSuccess) return e;
+    if (nc < 1) return cudaErrorInvalidConfiguration;
+    units = std::min<int64_t>(units, nc);
+  }
+  if (units > ntiles) units = ntiles;
+  if (units < 1) units = 1;
+  *grid = units * m.cluster;
   return cudaSuccess;
 }
 
-static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, int b, bool bwd,
+static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, bool bwd,
                                  long long wait_limit) {
   rmsk::StagedParams p{};
   p.M = M;
@@ -491,8 +612,10 @@ static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, int b, bool
   p.G = m.G;
   p.R = m.rows_per_cta;
   p.S = m.stages;
+  p.C = m.cluster;
+  p.SV = m.sv;
   p.ntiles = (M + p.R - 1) / p.R;
-  p.tile_bytes = (uint32_t)((int64_t)p.R * N * b);
+  p.tile_bytes = (uint32_t)((int64_t)p.R * p.SV * 16);
   p.stage_bytes = bwd ? 2 * p.tile_bytes : p.tile_bytes;
   p.wait_limit = wait_limit;
   return p;
@@ -501,27 +624,25 @@ static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, int b, bool
 template <typename T, bool GEMMA>
 static cudaError_t launch_fwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
-  cudaError_t e;
+  StagedLaunch L(m, grid, s);
   switch (m.kv) {
-    case 1: e = rmsk::launch_pdl(rmsk::rms_fwd_staged_kernel<T, 1, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
-    case 2: e = rmsk::launch_pdl(rmsk::rms_fwd_staged_kernel<T, 2, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
-    case 4: e = rmsk::launch_pdl(rmsk::rms_fwd_staged_kernel<T, 4, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
+    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, 1, GEMMA>, p);
+    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, 2, GEMMA>, p);
+    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, 4, GEMMA>, p);
     default: return cudaErrorInvalidValue;
   }
-  return e;
 }
 
 template <typename T, bool GEMMA>
 static cudaError_t launch_bwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
-  cudaError_t e;
+  StagedLaunch L(m, grid, s);
   switch (m.kv) {
-    case 1: e = rmsk::launch_pdl(rmsk::rms_bwd_staged_kernel<T, 1, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
-    case 2: e = rmsk::launch_pdl(rmsk::rms_bwd_staged_kernel<T, 2, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
-    case 4: e = rmsk::launch_pdl(rmsk::rms_bwd_staged_kernel<T, 4, GEMMA>, dim3((unsigned)grid), dim3(m.threads), m.smem, s, p); break;
+    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, 1, GEMMA>, p);
+    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, 2, GEMMA>, p);
+    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, 4, GEMMA>, p);
     default: return cudaErrorInvalidValue;
   }
-  return e;
 }
 
 template <typename T>
@@ -538,8 +659,7 @@ static cudaError_t launch_bwd_t(const rmsk::StagedParams& p, const Mapping& m, i
 
 cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
                               long long wait_limit, cudaStream_t s) {
-  const int b = a.dtype == kBF16 ? 2 : 4;
-  rmsk::StagedParams p = params(m, a.M, a.N, b, false, wait_limit);
+  rmsk::StagedParams p = params(m, a.M, a.N, false, wait_limit);
   p.x = a.x;
   p.gamma = a.gamma;
   p.y = a.y;
@@ -558,15 +678,15 @@ cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   int64_t grid = 0;
   cudaError_t e = grid_for(staged_kernel(a.dtype, true, m->kv, a.gemma), *m, d, ntiles, &grid);
   if (e != cudaSuccess) return e;
-  m->blocks = grid;  // = number of partial rows
+  m->blocks = grid;
+  m->partials = grid / m->cluster;  // one workspace row per unit
   return cudaSuccess;
 }
 
 cudaError_t launch_bwd_staged(const BwdArgs& a, const Mapping& m, const DeviceInfo& d,
                               long long wait_limit, cudaStream_t s) {
   (void)d;
-  const int b = a.dtype == kBF16 ? 2 : 4;
-  rmsk::StagedParams p = params(m, a.M, a.N, b, true, wait_limit);
+  rmsk::StagedParams p = params(m, a.M, a.N, true, wait_limit);
   p.x = a.x;
   p.gamma = a.gamma;
   p.rstd_in = a.rstd;

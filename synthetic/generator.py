@@ -87,6 +87,9 @@ WORKLOADS = {
                  gamma=("normal", 0.0, 0.1), gemma=1, inplace_dx=1,
                  note="Gemma (1+gamma) weight, dx written into dy"),
         *[_sweep(n) for n in (512, 1000, 2048, 5120, 11008, 16384)],
+        *[Workload(f"widerows_bf16_N{n}", (1 << 27) // n, n, "bf16", 1e-6,
+                   note="rows wider than one CTA's shared memory (cluster split)")
+          for n in (32768, 65536, 131072)],
         Workload("timing_f32_128x257", 128, 257, "f32", 1e-6,
                  note="the tutorial's timing shape, ragged N"),
         Workload("layernorm_test_bf16_1151x8192", 1151, 8192, "bf16", 1e-5,

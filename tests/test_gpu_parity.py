@@ -297,12 +297,25 @@ def test_both_vector_mappings_on_wide_rows(N):
         H.assert_parity(w, inp, H.run_gpu(w, inp, path=path), H.sample_rows(w.M, 64))
 
 
+@pytest.mark.parametrize("dtype,N", [("bf16", 32768), ("bf16", 65536), ("bf16", 131072),
+                                     ("bf16", 22024), ("f32", 16384), ("f32", 32768)])
+@pytest.mark.parametrize("gemma,inplace", [(0, 0), (1, 1)])
+def test_cluster_split_rows(dtype, N, gemma, inplace):
+    """Rows wider than one CTA's stages are split across a thread-block
+    cluster (column slices, row sums exchanged through distributed shared
+    memory).  N = 22024 bf16 gives slices of unequal length."""
+    w = _w(48, N, dtype, gemma=gemma, inplace=inplace, seed=N + gemma)
+    inp = H.inputs_for(w)
+    H.assert_parity(w, inp, H.run_gpu(w, inp, path="staged"))
+
+
 @pytest.mark.parametrize("bwd", [False, True])
-def test_staged_wait_timeout_reports_status(bwd):
+@pytest.mark.parametrize("N", [4096, 65536])
+def test_staged_wait_timeout_reports_status(bwd, N):
     """With the poll limit at 0 every staged wait gives up at once: the
     kernel drains its copies, raises the device status and returns; the
     host sees RMS_ERR_TIMEOUT and the context stays usable."""
-    w = _w(600, 4096, "bf16", seed=11)
+    w = _w(600 if N <= 4096 else 40, N, "bf16", seed=11)
     inp = H.inputs_for(w)
     x = H.to_device(inp["x"], "bf16")
     g = H.to_device(inp["gamma"], "bf16")
@@ -326,3 +339,82 @@ def test_staged_wait_timeout_reports_status(bwd):
     finally:
         rms.rms_set_wait_limit(prev)
     H.assert_parity(w, inp, H.run_gpu(w, inp, path="staged"))
+
+
+def test_more_than_2_31_elements():
+    """2,097,157 x 1024 bf16 (2^31 + 5120 elements per matrix): 64-bit
+    indexing in every kernel.  Inputs are drawn on the device with a seeded
+    torch generator; sampled rows (including the last ones) are copied back
+    and checked against the oracle; dgamma is checked by additivity: the
+    full-matrix result equals the sum of three row blocks' results."""
+    from oracle import compare
+
+    M, N = (1 << 21) + 5, 1024
+    gen = torch.Generator(device="cuda").manual_seed(0)
+    x = torch.randn(M, N, device="cuda", generator=gen).to(torch.bfloat16)
+    dy = torch.randn(M, N, device="cuda", generator=gen).to(torch.bfloat16)
+    g = (torch.rand(N, device="cuda", generator=gen) + 0.5).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    r = torch.empty(M, device="cuda")
+    dx = torch.empty_like(x)
+    dg = torch.empty(N, device="cuda")
+    ws = torch.empty(rms.rms_bwd_workspace_size(M, N), dtype=torch.uint8, device="cuda")
+    eps = 1e-6
+    rms.rms_fwd(x, g, y, r, eps)
+    rms.rms_bwd(dy, x, g, r, dx, dg, ws)
+    torch.cuda.synchronize()
+    rows = torch.tensor([0, 1, 2097151, 2097152, 2097153, M - 2, M - 1] + list(range(1000, M, 99991)),
+                        device="cuda")
+    xs = H.to_host64(x.index_select(0, rows))
+    dys = H.to_host64(dy.index_select(0, rows))
+    gs = H.to_host64(g)
+    y_ref, r_ref = orc.rms_forward(xs, gs, eps)
+    dx_ref, _, dxs, _ = orc.rms_backward(xs, gs, dys, eps, with_scales=True)
+    for c in (compare.check_y(H.to_host64(y.index_select(0, rows)), y_ref, "bf16"),
+              compare.check_rstd(H.to_host64(r.index_select(0, rows)), r_ref),
+              compare.check_dx(H.to_host64(dx.index_select(0, rows)), dx_ref, dxs, "bf16")):
+        assert c.ok, str(c)
+    parts = np.zeros(N)
+    for a, b in ((0, 700001), (700001, 2097152), (2097152, M)):
+        dgb = torch.empty(N, device="cuda")
+        wsb = torch.empty(rms.rms_bwd_workspace_size(b - a, N), dtype=torch.uint8, device="cuda")
+        rms.rms_bwd(dy[a:b], x[a:b], g, r[a:b], dx[a:b], dgb, wsb)
+        torch.cuda.synchronize()
+        parts += H.to_host64(dgb)
+    full = H.to_host64(dg)
+    assert np.all(np.abs(full - parts) <= 2e-5 * (np.abs(full) + np.sqrt(M))), np.abs(full - parts).max()
+
+
+@pytest.mark.parametrize("N,fwd_ok,bwd_ok", [(32768, True, True), (65536, True, True),
+                                             (131072, True, True), (262144, True, False)])
+def test_widest_rows_and_unsupported(N, fwd_ok, bwd_ok):
+    """The widest rows each direction accepts (bf16), and a clear
+    RMS_ERR_UNSUPPORTED beyond them (nothing is launched)."""
+    M = 64
+    w = _w(M, N, "bf16", seed=N)
+    inp = H.inputs_for(w)
+    x = H.to_device(inp["x"], "bf16")
+    g = H.to_device(inp["gamma"], "bf16")
+    y = torch.empty_like(x)
+    r = torch.empty(M, device="cuda")
+    rms.rms_fwd(x, g, y, r, w.eps)
+    dy = H.to_device(inp["dy"], "bf16")
+    dx = torch.empty_like(x)
+    dg = torch.empty(N, device="cuda")
+    ws = torch.empty(rms.rms_bwd_workspace_size(M, N), dtype=torch.uint8, device="cuda")
+    if bwd_ok:
+        rms.rms_bwd(dy, x, g, r, dx, dg, ws)
+        torch.cuda.synchronize()
+        H.assert_parity(w, inp, H.GpuResult(y, r, dx, dg, True))
+    else:
+        with pytest.raises(rms.RmsError) as ei:
+            rms.rms_bwd(dy, x, g, r, dx, dg, ws)
+        assert ei.value.status == rms.RMS_ERR_UNSUPPORTED
+        torch.cuda.synchronize()
+        from oracle import compare
+
+        xf = storage_to_float64(inp["x"], "bf16")
+        gf = storage_to_float64(inp["gamma"], "bf16")
+        y_ref, r_ref = orc.rms_forward(xf, gf, w.eps)
+        assert compare.check_y(H.to_host64(y), y_ref, "bf16").ok
+        assert compare.check_rstd(H.to_host64(r), r_ref).ok
