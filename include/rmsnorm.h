@@ -53,7 +53,8 @@ extern "C" {
 /* Element type of x, gamma, y, dy, dx. */
 typedef enum {
   RMS_F32 = 0,  /* IEEE float32 */
-  RMS_BF16 = 1  /* bfloat16 (8-bit significand), round-to-nearest-even on store */
+  RMS_BF16 = 1, /* bfloat16 (8-bit significand), round-to-nearest-even on store */
+  RMS_F16 = 2   /* IEEE float16 (11-bit significand), round-to-nearest-even on store */
 } rms_dtype;
 
 typedef enum {

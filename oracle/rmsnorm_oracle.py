@@ -174,6 +174,11 @@ def _round_bf16(a) -> np.ndarray:
     return rounded.astype(np.uint32).view(np.float32)
 
 
+def _round_f16(a) -> np.ndarray:
+    """float32 values rounded to the nearest float16, ties to even (numpy's conversion)."""
+    return _round_f32(a).astype(np.float16).astype(np.float32)
+
+
 def emulate_forward_lowp(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf16"):
     """The forward as a fp32-accumulating kernel with ``dtype`` I/O rounds it.
 
@@ -183,7 +188,7 @@ def emulate_forward_lowp(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf1
     x·r·(1+gamma) is rounded once (the pages state no order there).  r is the
     fp64 value rounded to fp32.  Returns float64 values of the rounded y.
     """
-    rnd = _round_bf16 if dtype == "bf16" else _round_f32
+    rnd = {"bf16": _round_bf16, "f16": _round_f16}.get(dtype, _round_f32)
     xf = _round_f32(x)
     gf = _round_f32(gamma)
     r32 = _round_f32(rms_rstd(x, eps))

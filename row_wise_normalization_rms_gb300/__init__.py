@@ -13,7 +13,7 @@ from __future__ import annotations
 
 from . import _lib
 
-RMS_F32, RMS_BF16 = 0, 1
+RMS_F32, RMS_BF16, RMS_F16 = 0, 1, 2
 RMS_PATH_AUTO, RMS_PATH_REGISTERS, RMS_PATH_STAGED, RMS_PATH_SCALAR = 0, 1, 2, 3
 (RMS_OK, RMS_ERR_INVALID_ARG, RMS_ERR_UNSUPPORTED, RMS_ERR_ALIGNMENT, RMS_ERR_WORKSPACE,
  RMS_ERR_CUDA, RMS_ERR_TIMEOUT) = range(7)
@@ -49,7 +49,9 @@ def dtype_code(t) -> int:
         return RMS_F32
     if t.dtype == torch.bfloat16:
         return RMS_BF16
-    raise ValueError(f"unsupported dtype {t.dtype}: float32 or bfloat16")
+    if t.dtype == torch.float16:
+        return RMS_F16
+    raise ValueError(f"unsupported dtype {t.dtype}: float32, bfloat16 or float16")
 
 
 def _stream_handle(stream):

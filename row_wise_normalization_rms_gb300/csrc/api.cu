@@ -54,7 +54,7 @@ std::mutex g_optin_mu;
 OptIn g_optin[64];
 int g_optin_n = 0;
 
-int elem_bytes(int dtype) { return dtype == rmsi::kBF16 ? 2 : 4; }
+int elem_bytes(int dtype) { return rmsi::dtype_bytes(dtype); }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -66,7 +66,7 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 bool valid_common(int64_t M, int64_t N, rms_dtype dtype, int gemma) {
-  if (dtype != RMS_F32 && dtype != RMS_BF16) return false;
+  if (dtype != RMS_F32 && dtype != RMS_BF16 && dtype != RMS_F16) return false;
   if (gemma != 0 && gemma != 1) return false;
   if (M < 0 || N <= 0) return false;
   return true;

@@ -172,7 +172,8 @@ namespace rmsi {
 
 cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   m->smem = m->rows_per_cta > 1 ? (size_t)m->rows_per_cta * a.N * sizeof(float) : 0;
-  const void* k = a.dtype == kBF16 ? rmsk::pick<__nv_bfloat16>(m->kv, a.gemma)
+  const void* k = a.dtype == kBF16  ? rmsk::pick<__nv_bfloat16>(m->kv, a.gemma)
+                  : a.dtype == kF16 ? rmsk::pick<__half>(m->kv, a.gemma)
                                     : rmsk::pick<float>(m->kv, a.gemma);
   if (!k) return cudaErrorInvalidValue;
   int occ = 0;
@@ -191,6 +192,7 @@ cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m
 
 cudaError_t launch_bwd_registers(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
   if (a.dtype == kBF16) return rmsk::launch_t<__nv_bfloat16>(a, m, s);
+  if (a.dtype == kF16) return rmsk::launch_t<__half>(a, m, s);
   return rmsk::launch_t<float>(a, m, s);
 }
 

@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -58,6 +59,32 @@ struct Elem<__nv_bfloat16> {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+template <>
+struct Elem<__half> {
+  static constexpr int kPerVec = 8;
+  __device__ static __forceinline__ float to_f(__half v) { return __half2float(v); }
+  __device__ static __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+  __device__ static __forceinline__ float round(float v) { return __half2float(__float2half_rn(v)); }
+  __device__ static __forceinline__ void unpack(const uint4& v, float* f) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ static __forceinline__ uint4 pack(const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
       w[i] = *reinterpret_cast<uint32_t*>(&h);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
@@ -120,7 +147,41 @@ __device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
-// A 16-byte vector as float pairs: 4 pairs for bf16, 2 for float32.
+// Two fp16 (one 32-bit word, low half first) widened exactly to a pair.
+__device__ __forceinline__ f32x2 h2_to_f2(uint32_t w) {
+  const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w));
+  return pk2(t.x, t.y);
+}
+__device__ __forceinline__ uint32_t f2_to_h2(f32x2 v) {
+  __half2 h = __floats2half2_rn(lo2(v), hi2(v));
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+// Product of two fp16 pairs rounded once to fp16.  The exact product of two
+// 11-bit significands (and any fp16 exponents) fits a float32 exactly, so
+// this equals rounding the float32 product of the widened values.
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Pair conversion and the rounding weight multiply for the 16-bit types.
+template <typename T>
+struct Half2Ops;
+template <>
+struct Half2Ops<__nv_bfloat16> {
+  __device__ static __forceinline__ f32x2 widen(uint32_t w) { return bf2_to_f2(w); }
+  __device__ static __forceinline__ uint32_t narrow(f32x2 v) { return f2_to_bf2(v); }
+  __device__ static __forceinline__ uint32_t mul(uint32_t a, uint32_t b) { return bf2_mul(a, b); }
+};
+template <>
+struct Half2Ops<__half> {
+  __device__ static __forceinline__ f32x2 widen(uint32_t w) { return h2_to_f2(w); }
+  __device__ static __forceinline__ uint32_t narrow(f32x2 v) { return f2_to_h2(v); }
+  __device__ static __forceinline__ uint32_t mul(uint32_t a, uint32_t b) { return h2_mul(a, b); }
+};
+
+// A 16-byte vector as float pairs: 4 pairs for bf16 and fp16, 2 for float32.
 template <typename T>
 struct Pairs;
 template <>
@@ -128,6 +189,13 @@ struct Pairs<__nv_bfloat16> {
   static constexpr int n = 4;
   __device__ static __forceinline__ f32x2 get(const uint4& v, int i) {
     return bf2_to_f2(i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w);
+  }
+};
+template <>
+struct Pairs<__half> {
+  static constexpr int n = 4;
+  __device__ static __forceinline__ f32x2 get(const uint4& v, int i) {
+    return h2_to_f2(i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w);
   }
 };
 template <>
@@ -166,15 +234,16 @@ struct RowMath {
   __device__ static __forceinline__ uint4 forward(const uint4& x, const uint4& g, float r) {
     const f32x2 rr = splat2(r);
     uint32_t o[4];
-    if (sizeof(T) == 2) {
+    if constexpr (sizeof(T) == 2) {
+      using H = Half2Ops<T>;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const f32x2 xr = mul2(P::get(x, i), rr);
         if (GEMMA) {
-          o[i] = f2_to_bf2(mul2(xr, weight(g, i)));
+          o[i] = H::narrow(mul2(xr, weight(g, i)));
         } else {
           const uint32_t gw = i == 0 ? g.x : i == 1 ? g.y : i == 2 ? g.z : g.w;
-          o[i] = bf2_mul(f2_to_bf2(xr), gw);
+          o[i] = H::mul(H::narrow(xr), gw);
         }
       }
     } else {
@@ -214,8 +283,8 @@ struct RowMath {
       const f32x2 xn = mul2(P::get(x, i), rr);
       const f32x2 u = mul2(P::get(dy, i), weight(g, i));
       const f32x2 dx = mul2(fma2(xn, nk, u), rr);
-      if (sizeof(T) == 2) {
-        o[i] = f2_to_bf2(dx);
+      if constexpr (sizeof(T) == 2) {
+        o[i] = Half2Ops<T>::narrow(dx);
       } else {
         o[2 * i] = __float_as_uint(lo2(dx));
         o[2 * i + 1] = __float_as_uint(hi2(dx));

@@ -85,7 +85,7 @@ namespace rmsi {
 // rows per CTA; wider rows get ceil(vectors / 4) threads rounded up to a
 // warp multiple, up to 1024 threads (wider rows use the staged mapping).
 bool plan_registers(int N, int dtype, bool bwd, Mapping* m) {
-  const int b = dtype == kBF16 ? 2 : 4;
+  const int b = dtype_bytes(dtype);
   if (N <= 0 || ((int64_t)N * b) % 16 != 0) return false;
   const int NV = (int)(((int64_t)N * b) / 16);
   const int max_threads = bwd ? 512 : 1024;
@@ -114,6 +114,7 @@ cudaError_t launch_fwd_registers(const FwdArgs& a, const Mapping& m0, cudaStream
   Mapping m = m0;
   m.blocks = (a.M + m.rows_per_cta - 1) / m.rows_per_cta;
   if (a.dtype == kBF16) return rmsk::launch_t<__nv_bfloat16>(a, m, s);
+  if (a.dtype == kF16) return rmsk::launch_t<__half>(a, m, s);
   return rmsk::launch_t<float>(a, m, s);
 }
 

@@ -8,7 +8,9 @@
 
 namespace rmsi {
 
-enum Dtype { kF32 = 0, kBF16 = 1 };
+enum Dtype { kF32 = 0, kBF16 = 1, kF16 = 2 };
+
+inline int dtype_bytes(int dtype) { return dtype == kF32 ? 4 : 2; }
 enum Path { kAuto = 0, kRegisters = 1, kStaged = 2, kScalar = 3 };
 
 struct FwdArgs {

@@ -169,16 +169,18 @@ bool plan_scalar(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
   return true;
 }
 
+template <typename T>
+static cudaError_t launch_fwd_scalar_t(const FwdArgs& a, dim3 grid, dim3 block, cudaStream_t s) {
+  return rmsk::launch_pdl(rmsk::rms_fwd_scalar_kernel<T>, grid, block, 0, s,
+                          static_cast<const T*>(a.x), static_cast<const T*>(a.gamma),
+                          static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps, a.gemma);
+}
+
 cudaError_t launch_fwd_scalar(const FwdArgs& a, const Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)a.M), block(m.threads);
-  if (a.dtype == kBF16)
-    return rmsk::launch_pdl(rmsk::rms_fwd_scalar_kernel<__nv_bfloat16>, grid, block, 0, s,
-                            static_cast<const __nv_bfloat16*>(a.x),
-                            static_cast<const __nv_bfloat16*>(a.gamma),
-                            static_cast<__nv_bfloat16*>(a.y), a.rstd, a.M, a.N, a.eps, a.gemma);
-  return rmsk::launch_pdl(rmsk::rms_fwd_scalar_kernel<float>, grid, block, 0, s,
-                          static_cast<const float*>(a.x), static_cast<const float*>(a.gamma),
-                          static_cast<float*>(a.y), a.rstd, a.M, a.N, a.eps, a.gemma);
+  if (a.dtype == kBF16) return launch_fwd_scalar_t<__nv_bfloat16>(a, grid, block, s);
+  if (a.dtype == kF16) return launch_fwd_scalar_t<__half>(a, grid, block, s);
+  return launch_fwd_scalar_t<float>(a, grid, block, s);
 }
 
 template <typename T>
@@ -187,7 +189,9 @@ static const void* bwd_scalar_ptr() {
 }
 
 cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
-  const void* k = a.dtype == kBF16 ? bwd_scalar_ptr<__nv_bfloat16>() : bwd_scalar_ptr<float>();
+  const void* k = a.dtype == kBF16  ? bwd_scalar_ptr<__nv_bfloat16>()
+                  : a.dtype == kF16 ? bwd_scalar_ptr<__half>()
+                                    : bwd_scalar_ptr<float>();
   cudaError_t e = opt_in_max_smem(k, d);
   if (e != cudaSuccess) return e;
   int occ = 0;
@@ -203,18 +207,19 @@ cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   return cudaSuccess;
 }
 
-cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
+template <typename T>
+static cudaError_t launch_bwd_scalar_t(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)m.blocks), block(m.threads);
-  if (a.dtype == kBF16)
-    return rmsk::launch_pdl(rmsk::rms_bwd_scalar_kernel<__nv_bfloat16>, grid, block, m.smem, s,
-                            static_cast<const __nv_bfloat16*>(a.dy),
-                            static_cast<const __nv_bfloat16*>(a.x),
-                            static_cast<const __nv_bfloat16*>(a.gamma), a.rstd,
-                            static_cast<__nv_bfloat16*>(a.dx), a.ws, a.M, a.N, a.gemma);
-  return rmsk::launch_pdl(rmsk::rms_bwd_scalar_kernel<float>, grid, block, m.smem, s,
-                          static_cast<const float*>(a.dy), static_cast<const float*>(a.x),
-                          static_cast<const float*>(a.gamma), a.rstd, static_cast<float*>(a.dx),
-                          a.ws, a.M, a.N, a.gemma);
+  return rmsk::launch_pdl(rmsk::rms_bwd_scalar_kernel<T>, grid, block, m.smem, s,
+                          static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
+                          static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.ws,
+                          a.M, a.N, a.gemma);
+}
+
+cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
+  if (a.dtype == kBF16) return launch_bwd_scalar_t<__nv_bfloat16>(a, m, s);
+  if (a.dtype == kF16) return launch_bwd_scalar_t<__half>(a, m, s);
+  return launch_bwd_scalar_t<float>(a, m, s);
 }
 
 cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, cudaStream_t s) {

@@ -444,6 +444,8 @@ const void* staged_kernel(int dtype, bool bwd, int kv, bool gemma) {
   if (dtype == kBF16)
     return bwd ? rmsk::staged_ptr<__nv_bfloat16, true>(kv, gemma)
                : rmsk::staged_ptr<__nv_bfloat16, false>(kv, gemma);
+  if (dtype == kF16)
+    return bwd ? rmsk::staged_ptr<__half, true>(kv, gemma) : rmsk::staged_ptr<__half, false>(kv, gemma);
   return bwd ? rmsk::staged_ptr<float, true>(kv, gemma) : rmsk::staged_ptr<float, false>(kv, gemma);
 }
 
@@ -544,7 +546,7 @@ static bool plan_for_cluster(int C, int NV, int64_t row_bytes, bool bwd, const D
 // 16 KiB (backward) or 64 KiB (forward) per CTA, so clusters take rows of
 // up to 128 K bf16 elements in the backward and 256 K in the forward.
 bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
-  const int b = dtype == kBF16 ? 2 : 4;
+  const int b = dtype_bytes(dtype);
   if (N <= 0 || ((int64_t)N * b) % 16 != 0) return false;
   const int64_t row_bytes = (int64_t)N * b;
   const int NV = (int)(row_bytes / 16);
@@ -670,6 +672,7 @@ cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceIn
   cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv, a.gemma), m, d, p.ntiles, &grid);
   if (e != cudaSuccess) return e;
   if (a.dtype == kBF16) return launch_fwd_t<__nv_bfloat16>(p, m, grid, s);
+  if (a.dtype == kF16) return launch_fwd_t<__half>(p, m, grid, s);
   return launch_fwd_t<float>(p, m, grid, s);
 }
 
@@ -695,6 +698,7 @@ cudaError_t launch_bwd_staged(const BwdArgs& a, const Mapping& m, const DeviceIn
   p.ws = a.ws;
   p.gemma = a.gemma;
   if (a.dtype == kBF16) return launch_bwd_t<__nv_bfloat16>(p, m, m.blocks, s);
+  if (a.dtype == kF16) return launch_bwd_t<__half>(p, m, m.blocks, s);
   return launch_bwd_t<float>(p, m, m.blocks, s);
 }
 

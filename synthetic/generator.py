@@ -7,6 +7,7 @@ chunk size per workload), transformed by the distribution's affine map and
 the optional per-row scale, then rounded to the I/O dtype:
 
 * ``f32``  : float64 -> float32, round to nearest even (numpy ``astype``);
+* ``f16``  : float64 -> float16, round to nearest even (numpy ``astype``);
 * ``bf16`` : float64 -> float32 (RNE) -> bfloat16 (RNE on the 16 dropped
   mantissa bits).  bf16 tensors are returned as their ``uint16`` bit
   patterns, which is how both the CUDA side (viewed as ``torch.bfloat16``)
@@ -41,7 +42,7 @@ class Workload:
     name: str
     M: int
     N: int
-    dtype: str  # "f32" or "bf16"
+    dtype: str  # "f32", "bf16" or "f16"
     eps: float
     x: Dist = ("normal", 0.0, 1.0)
     gamma: Dist = ("uniform", 0.5, 1.5)
@@ -90,6 +91,10 @@ WORKLOADS = {
         *[Workload(f"widerows_bf16_N{n}", (1 << 27) // n, n, "bf16", 1e-6,
                    note="rows wider than one CTA's shared memory (cluster split)")
           for n in (32768, 65536, 131072)],
+        Workload("wide_f16_16384x8192", 16384, 8192, "f16", 1e-5,
+                 gamma=("normal", 1.0, 0.2), dy=("normal", 0.0, 1.0),
+                 row_scale=("loguniform", 0.01, 100.0),
+                 note="the large-hidden workload with fp16 I/O"),
         Workload("timing_f32_128x257", 128, 257, "f32", 1e-6,
                  note="the tutorial's timing shape, ragged N"),
         Workload("layernorm_test_bf16_1151x8192", 1151, 8192, "bf16", 1e-5,
@@ -140,18 +145,22 @@ def storage_to_float64(arr, dtype: str) -> np.ndarray:
     """Exact float64 values of a stored tensor (float32 array or bf16 bits)."""
     if dtype == "bf16":
         return bf16_bits_to_float32(arr).astype(np.float64)
+    if dtype == "f16":
+        return np.asarray(arr, dtype=np.float16).astype(np.float64)
     return np.asarray(arr, dtype=np.float32).astype(np.float64)
 
 
 def _store(vals64: np.ndarray, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return float_to_bf16_bits(vals64)
+    if dtype == "f16":
+        return vals64.astype(np.float16)
     return vals64.astype(np.float32)
 
 
 def _matrix(w: Workload, tensor: str, dist: Dist, row_scale: Optional[np.ndarray]) -> np.ndarray:
     gen = _generator(w.seed, tensor)
-    out = np.empty((w.M, w.N), dtype=np.uint16 if w.dtype == "bf16" else np.float32)
+    out = np.empty((w.M, w.N), dtype={"bf16": np.uint16, "f16": np.float16}.get(w.dtype, np.float32))
     rows = max(1, _CHUNK_ELEMS // max(1, w.N))
     buf = np.empty((min(rows, max(w.M, 1)), w.N), dtype=np.float64)
     for r0 in range(0, w.M, rows):
@@ -168,7 +177,8 @@ def make_inputs(w: Workload) -> dict:
     """Draw x (M,N), gamma (N,) and dy (M,N) for a workload, in storage form.
 
     Returns a dict with keys ``x``, ``gamma``, ``dy`` (float32 arrays for f32
-    workloads, uint16 bf16 bit patterns for bf16 ones) and ``row_scale``
+    workloads, float16 arrays for f16 ones, uint16 bf16 bit patterns for bf16
+    ones) and ``row_scale``
     (float64, or None).
     """
     scale = None

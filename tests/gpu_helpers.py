@@ -13,22 +13,22 @@ from oracle import rmsnorm_oracle as orc
 from synthetic import make_inputs, storage_to_float64
 
 PAD = 64  # guard elements on each side of every output buffer
-_SENTINEL = {"bf16": 0x7FC1, "f32": 0x7FC00001}  # NaN payloads nothing else writes
+_SENTINEL = {"bf16": 0x7FC1, "f16": 0x7E01, "f32": 0x7FC00001}  # NaN payloads nothing else writes
 
 
 def tdtype(dtype: str):
-    return torch.bfloat16 if dtype == "bf16" else torch.float32
+    return {"bf16": torch.bfloat16, "f16": torch.float16}.get(dtype, torch.float32)
 
 
 def to_device(arr: np.ndarray, dtype: str) -> torch.Tensor:
     a = np.ascontiguousarray(arr)
     if dtype == "bf16":
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
-    return torch.from_numpy(a).cuda()
+    return torch.from_numpy(a).cuda()  # float32 or float16 arrays map directly
 
 
 def to_host64(t: torch.Tensor) -> np.ndarray:
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.float().cpu().numpy().astype(np.float64)
     return t.cpu().numpy().astype(np.float64)
 
@@ -38,9 +38,9 @@ class Guarded:
 
     def __init__(self, shape, torch_dtype, sentinel_bits: int):
         n = int(np.prod(shape)) if len(shape) else 1
-        self.bits_dtype = torch.int16 if torch_dtype == torch.bfloat16 else torch.int32
+        self.bits_dtype = torch.int32 if torch_dtype == torch.float32 else torch.int16
         self.buf = torch.empty(n + 2 * PAD, dtype=torch_dtype, device="cuda")
-        # both sentinels are positive in their signed view (0x7FC1, 0x7FC00001)
+        # the sentinels are positive in their signed view (0x7FC1, 0x7E01, 0x7FC00001)
         self.buf.view(self.bits_dtype).fill_(sentinel_bits)
         self.sentinel = sentinel_bits
         self.t = self.buf[PAD:PAD + n].view(*shape)

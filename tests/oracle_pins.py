@@ -279,6 +279,13 @@ def pin_lowp_emulation(impl):
     assert np.all(np.abs(got - exact) <= (2.0 ** -7 + 2.0 ** -16) * np.abs(exact) + 1e-30)
     once = torch.tensor(exact).float().to(torch.bfloat16).double().numpy()
     assert not np.array_equal(got, once)
+    # float16 I/O: the same order with torch's float16 conversions.
+    xh = torch.tensor(rng.standard_normal((M, N)) * 3.0, dtype=torch.float32).to(torch.float16).float()
+    gh = torch.tensor(rng.uniform(0.5, 1.5, N), dtype=torch.float32).to(torch.float16).float()
+    r16 = torch.tensor(impl.rms_rstd(xh.double().numpy(), eps), dtype=torch.float32)
+    ref_h = ((xh * r16[:, None]).to(torch.float16).float() * gh[None, :]).to(torch.float16)
+    got_h = impl.emulate_forward_lowp(xh.double().numpy(), gh.double().numpy(), eps, 0, "f16")
+    assert np.array_equal(got_h, ref_h.double().numpy())
 
 
 ALL_PINS = [

@@ -37,12 +37,12 @@ SMALL_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("M,N", SMALL_SHAPES, ids=[f"{m}x{n}" for m, n in SMALL_SHAPES])
 @pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar"])
 def test_small_shapes_full_parity(M, N, dtype, path):
     w = _w(M, N, dtype, seed=M + N)
-    b = 2 if dtype == "bf16" else 4
+    b = 4 if dtype == "f32" else 2
     inp = H.inputs_for(w)
     if path in ("registers", "staged") and (N * b) % 16 != 0:
         with pytest.raises(rms.RmsError) as ei:
@@ -58,7 +58,7 @@ def test_small_shapes_full_parity(M, N, dtype, path):
 
 
 @pytest.mark.parametrize("gemma,inplace", [(0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("M,N", [(257, 3072), (65, 1000), (31, 257)])
 def test_gemma_and_inplace(M, N, dtype, gemma, inplace):
     w = _w(M, N, dtype, gemma=gemma, inplace=inplace, seed=7)
@@ -98,37 +98,41 @@ def test_dgamma_bitwise_reproducible():
     assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar"])
 def test_inplace_matches_out_of_place_bitwise(dtype, path):
     w = _w(1500, 2048, dtype, seed=3)
     inp = H.inputs_for(w)
     a = H.run_gpu(w, inp, path=path, inplace=0)
     b = H.run_gpu(w, inp, path=path, inplace=1)
-    bits = torch.int16 if dtype == "bf16" else torch.int32
+    bits = torch.int32 if dtype == "f32" else torch.int16
     assert torch.equal(a.dx.view(bits), b.dx.view(bits))
     assert torch.equal(a.dgamma.view(torch.int32), b.dgamma.view(torch.int32))
 
 
 @pytest.mark.parametrize("N", [1000, 4096, 8192])
-def test_bf16_cast_order(N):
-    """y rounds x*r to bf16 before the weight multiply: nearly every element
-    equals the oracle's emulation of that order bit for bit (the rest differ
-    by one bf16 step where the fp32 rstd rounds differently), and many
-    elements differ from a single rounding of the exact product."""
-    w = _w(256, N, "bf16", seed=N)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_lowp_cast_order(N, dtype):
+    """y rounds x*r to the I/O type before the weight multiply: nearly every
+    element equals the oracle's emulation of that order bit for bit, and many
+    elements differ from a single rounding of the exact product.  Where the
+    device's fp32 rstd rounds differently from the oracle's, the rounded x*r
+    moves by one unit in the last place, and the weight (up to ~1.5) carries
+    that into at most two units of y."""
+    w = _w(256, N, dtype, seed=N)
     inp = H.inputs_for(w)
     res = H.run_gpu(w, inp)
-    x = storage_to_float64(inp["x"], "bf16")
-    g = storage_to_float64(inp["gamma"], "bf16")
-    emu = orc.emulate_forward_lowp(x, g, w.eps, 0, "bf16")
+    x = storage_to_float64(inp["x"], dtype)
+    g = storage_to_float64(inp["gamma"], dtype)
+    emu = orc.emulate_forward_lowp(x, g, w.eps, 0, dtype)
     got = H.to_host64(res.y)
     same = np.mean(got == emu)
     assert same >= 0.999, same
     diff = got != emu
-    assert np.all(np.abs(got[diff] - emu[diff]) <= 2.0 ** -7 * np.abs(emu[diff]))
+    step = 2.0 ** -6 if dtype == "bf16" else 2.0 ** -9  # two units in the last place, relative
+    assert np.all(np.abs(got[diff] - emu[diff]) <= step * np.abs(emu[diff]))
     exact, _ = orc.rms_forward(x, g, w.eps)
-    once = torch.tensor(exact).float().to(torch.bfloat16).double().numpy()
+    once = torch.tensor(exact).float().to(H.tdtype(dtype)).double().numpy()
     assert np.mean(got != once) > 0.01
 
 
@@ -170,7 +174,7 @@ def test_printed_worked_examples_fp32():
     assert torch.all((y1 - 0.9999995).abs() <= 5e-7)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_sum_not_mean_on_gpu(dtype):
     dt = H.tdtype(dtype)
     x = torch.ones(2, 8, device="cuda", dtype=dt)
@@ -185,7 +189,7 @@ def test_sum_not_mean_on_gpu(dtype):
     assert dg.tolist() == [4.0, 6.0] * 4
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_edge_rows(dtype):
     dt = H.tdtype(dtype)
     eps = 1e-4
@@ -222,7 +226,7 @@ def test_empty_batch():
     assert torch.all(dg == 0)
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_misaligned_pointers_use_scalar_path(dtype):
     """Views offset by one element are legal inputs; a forced vector mapping
     refuses them instead of reading unaligned vectors."""
@@ -298,7 +302,8 @@ def test_both_vector_mappings_on_wide_rows(N):
 
 
 @pytest.mark.parametrize("dtype,N", [("bf16", 32768), ("bf16", 65536), ("bf16", 131072),
-                                     ("bf16", 22024), ("f32", 16384), ("f32", 32768)])
+                                     ("bf16", 22024), ("f32", 16384), ("f32", 32768),
+                                     ("f16", 32768)])
 @pytest.mark.parametrize("gemma,inplace", [(0, 0), (1, 1)])
 def test_cluster_split_rows(dtype, N, gemma, inplace):
     """Rows wider than one CTA's stages are split across a thread-block
