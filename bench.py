@@ -161,7 +161,7 @@ def cpu_oracle_throughput(w, inp, seconds: float = 10.0, rows: int = 256):
     rows = min(rows, w.M)
     x = storage_to_float64(inp["x"][:rows], w.dtype)
     dy = storage_to_float64(inp["dy"][:rows], w.dtype)
-    g = storage_to_float64(inp["gamma"], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.wdtype)
     reps = 0
     t0 = time.perf_counter()
     while True:
@@ -201,7 +201,7 @@ def run_reference(args):
     inp = make_inputs(sub)
     x = storage_to_float64(inp["x"], w.dtype)
     dy = storage_to_float64(inp["dy"], w.dtype)
-    g = storage_to_float64(inp["gamma"], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.wdtype)
 
     def step():
         orc.rms_forward(x, g, w.eps, w.gemma)
@@ -480,17 +480,16 @@ def run_sweep(args):
     for name in names:
         w = WORKLOADS[name]
         M, N, b = w.M, w.N, w.elem_bytes
-        dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
         inp = make_inputs(w)
 
-        def dev_t(a):
-            if w.dtype == "bf16":
+        def dev_t(a, dtype=w.dtype):
+            if dtype == "bf16":
                 return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
             return torch.from_numpy(a).to(dev)
 
         set_bytes = 4 * M * N * b
         k = int(min(64, max(1, -(-3 * L2_BYTES // set_bytes))))
-        x0, dy0, g = dev_t(inp["x"]), dev_t(inp["dy"]), dev_t(inp["gamma"])
+        x0, dy0, g = dev_t(inp["x"]), dev_t(inp["dy"]), dev_t(inp["gamma"], w.wdtype)
         sets = []
         for i in range(k):
             sets.append((x0 if i == 0 else x0.clone(), dy0 if i == 0 else dy0.clone(),
@@ -532,7 +531,8 @@ def run_sweep(args):
             fg = fwd_b / (f_ms * 1e-3) / 1e9
             bg = bwd_b / (b_ms * 1e-3) / 1e9
             print(json.dumps({
-                "workload": name, "M": M, "N": N, "dtype": w.dtype, "gemma": w.gemma,
+                "workload": name, "M": M, "N": N, "dtype": w.dtype, "weight_dtype": w.wdtype,
+                "gemma": w.gemma,
                 "inplace_dx": w.inplace_dx, "path": path, "calls": calls, "buffer_sets": k,
                 "l2": ("rotating sets exceed 3x L2" if k * set_bytes >= 3 * L2_BYTES
                        else "sets fit in L2: launch-bound shape"),

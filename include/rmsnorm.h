@@ -28,8 +28,9 @@
  *    enqueued asynchronously on `stream` (a cudaStream_t passed as void*;
  *    NULL selects the legacy default stream of the current device).
  *  - Matrices are contiguous row-major with row stride N elements.
- *    x, gamma, y, dy, dx share the element type `dtype`.  rstd is always
- *    float32 (M entries), dgamma always float32 (N entries).
+ *    x, y, dy, dx share the activation type of `dtype`, gamma its weight
+ *    type (see rms_dtype).  rstd is always float32 (M entries), dgamma
+ *    always float32 (N entries).
  *  - Arithmetic is float32 throughout (loads widened to float32, float32
  *    accumulation, one rounding to `dtype` per stored element), except the
  *    non-Gemma low-precision forward, which rounds x*r to `dtype` before
@@ -50,11 +51,16 @@
 extern "C" {
 #endif
 
-/* Element type of x, gamma, y, dy, dx. */
+/* Element types of a call.  The first three use one type for activations
+ * (x, y, dy, dx) and weight (gamma); the _W32 codes pair 16-bit activations
+ * with a float32 gamma (the normalised row is then "cast" to float32, which
+ * is exact, and y is one rounding of x*r*gamma). */
 typedef enum {
-  RMS_F32 = 0,  /* IEEE float32 */
-  RMS_BF16 = 1, /* bfloat16 (8-bit significand), round-to-nearest-even on store */
-  RMS_F16 = 2   /* IEEE float16 (11-bit significand), round-to-nearest-even on store */
+  RMS_F32 = 0,      /* IEEE float32 */
+  RMS_BF16 = 1,     /* bfloat16 (8-bit significand), round-to-nearest-even on store */
+  RMS_F16 = 2,      /* IEEE float16 (11-bit significand), round-to-nearest-even on store */
+  RMS_BF16_W32 = 3, /* bfloat16 activations, float32 gamma */
+  RMS_F16_W32 = 4   /* float16 activations, float32 gamma */
 } rms_dtype;
 
 typedef enum {

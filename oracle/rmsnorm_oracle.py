@@ -179,16 +179,21 @@ def _round_f16(a) -> np.ndarray:
     return _round_f32(a).astype(np.float16).astype(np.float32)
 
 
-def emulate_forward_lowp(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf16"):
+def emulate_forward_lowp(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf16",
+                         weight_dtype: str = ""):
     """The forward as a fp32-accumulating kernel with ``dtype`` I/O rounds it.
 
     Follows the cast order of [UNS] § 3: normed = fp32(x·r) is rounded to the
-    weight dtype first, then multiplied by the weight in fp32 and rounded
-    again.  For Gemma the weight (1+gamma) is formed in fp32 and the product
-    x·r·(1+gamma) is rounded once (the pages state no order there).  r is the
-    fp64 value rounded to fp32.  Returns float64 values of the rounded y.
+    weight dtype (``weight_dtype``, default ``dtype``; float32 makes this
+    rounding exact) first, then multiplied by the weight in fp32 and rounded
+    to ``dtype``.  For Gemma the weight (1+gamma) is formed in fp32 and the
+    product x·r·(1+gamma) is rounded once (the pages state no order there).
+    r is the fp64 value rounded to fp32.  Returns float64 values of the
+    rounded y.
     """
-    rnd = {"bf16": _round_bf16, "f16": _round_f16}.get(dtype, _round_f32)
+    rounders = {"bf16": _round_bf16, "f16": _round_f16}
+    rnd = rounders.get(dtype, _round_f32)
+    rnd_w = rounders.get(weight_dtype or dtype, _round_f32)
     xf = _round_f32(x)
     gf = _round_f32(gamma)
     r32 = _round_f32(rms_rstd(x, eps))
@@ -197,6 +202,6 @@ def emulate_forward_lowp(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf1
         w = _round_f32(1.0 + gf.astype(np.float64))
         y = rnd(_round_f32(xr.astype(np.float64) * w[None, :]))
     else:
-        normed = rnd(xr)
+        normed = rnd_w(xr)
         y = rnd(_round_f32(normed.astype(np.float64) * gf[None, :]))
     return y.astype(np.float64)

@@ -13,7 +13,7 @@ from __future__ import annotations
 
 from . import _lib
 
-RMS_F32, RMS_BF16, RMS_F16 = 0, 1, 2
+RMS_F32, RMS_BF16, RMS_F16, RMS_BF16_W32, RMS_F16_W32 = 0, 1, 2, 3, 4
 RMS_PATH_AUTO, RMS_PATH_REGISTERS, RMS_PATH_STAGED, RMS_PATH_SCALAR = 0, 1, 2, 3
 (RMS_OK, RMS_ERR_INVALID_ARG, RMS_ERR_UNSUPPORTED, RMS_ERR_ALIGNMENT, RMS_ERR_WORKSPACE,
  RMS_ERR_CUDA, RMS_ERR_TIMEOUT) = range(7)
@@ -42,16 +42,18 @@ def rms_status_string(status: int) -> str:
     return lib().rms_status_string(int(status)).decode()
 
 
-def dtype_code(t) -> int:
+def dtype_code(t, gamma=None) -> int:
+    """The rms_dtype code of activations ``t`` and weight ``gamma`` (default: same type)."""
     import torch
 
-    if t.dtype == torch.float32:
-        return RMS_F32
-    if t.dtype == torch.bfloat16:
-        return RMS_BF16
-    if t.dtype == torch.float16:
-        return RMS_F16
-    raise ValueError(f"unsupported dtype {t.dtype}: float32, bfloat16 or float16")
+    act = {torch.float32: RMS_F32, torch.bfloat16: RMS_BF16, torch.float16: RMS_F16}.get(t.dtype)
+    if act is None:
+        raise ValueError(f"unsupported dtype {t.dtype}: float32, bfloat16 or float16")
+    if gamma is None or gamma.dtype == t.dtype:
+        return act
+    if gamma.dtype == torch.float32 and act in (RMS_BF16, RMS_F16):
+        return RMS_BF16_W32 if act == RMS_BF16 else RMS_F16_W32
+    raise ValueError(f"unsupported weight dtype {gamma.dtype} for {t.dtype} activations")
 
 
 def _stream_handle(stream):
@@ -78,7 +80,7 @@ def rms_fwd(x, gamma, y, rstd, eps: float = 1e-6, gemma: int = 0, stream=None, p
     """y and rstd from x (M,N) and gamma (N,); writes into y (M,N) and rstd (M,) float32."""
     M, N = x.shape
     st = lib().rms_fwd_ex(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), M, N, float(eps),
-                          dtype_code(x), int(gemma), _path(path), _stream_handle(stream))
+                          dtype_code(x, gamma), int(gemma), _path(path), _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_fwd")
 
@@ -89,7 +91,7 @@ def rms_bwd(dy, x, gamma, rstd, dx, dgamma, workspace, gemma: int = 0, inplace_d
     M, N = x.shape
     ws_bytes = workspace.numel() * workspace.element_size()
     st = lib().rms_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
-                          _ptr(workspace), ws_bytes, M, N, dtype_code(x), int(gemma),
+                          _ptr(workspace), ws_bytes, M, N, dtype_code(x, gamma), int(gemma),
                           int(inplace_dx), _path(path), _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_bwd")
@@ -102,7 +104,7 @@ def rms_bwd_noalloc(dy, x, gamma, rstd, dx, dgamma, gemma: int = 0, inplace_dx: 
     (see include/rmsnorm.h for the size limit and the sharing rules)."""
     M, N = x.shape
     st = lib().rms_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
-                               M, N, dtype_code(x), int(gemma), int(inplace_dx),
+                               M, N, dtype_code(x, gamma), int(gemma), int(inplace_dx),
                                _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_bwd_noalloc")

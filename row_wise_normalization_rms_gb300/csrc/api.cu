@@ -66,7 +66,7 @@ bool overlap(const void* a, size_t na, const void* b, size_t nb) {
 }
 
 bool valid_common(int64_t M, int64_t N, rms_dtype dtype, int gemma) {
-  if (dtype != RMS_F32 && dtype != RMS_BF16 && dtype != RMS_F16) return false;
+  if (dtype < RMS_F32 || dtype > RMS_F16_W32) return false;
   if (gemma != 0 && gemma != 1) return false;
   if (M < 0 || N <= 0) return false;
   return true;
@@ -186,7 +186,7 @@ rms_status rms_fwd_ex(const void* x, const void* gamma, void* y, float* rstd, in
   const int b = elem_bytes(dtype);
   const size_t xb = matrix_bytes(M, N, b);
   if (xb == 0) return RMS_ERR_INVALID_ARG;
-  const size_t gb = (size_t)N * b, rb = (size_t)M * sizeof(float);
+  const size_t gb = (size_t)N * rmsi::weight_bytes(dtype), rb = (size_t)M * sizeof(float);
   if (overlap(y, xb, x, xb) || overlap(y, xb, gamma, gb) || overlap(y, xb, rstd, rb) ||
       overlap(rstd, rb, x, xb) || overlap(rstd, rb, gamma, gb))
     return RMS_ERR_INVALID_ARG;
@@ -247,7 +247,8 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
   const int b = elem_bytes(dtype);
   const size_t xb = matrix_bytes(M, N, b);
   if (xb == 0) return RMS_ERR_INVALID_ARG;
-  const size_t gb = (size_t)N * b, rb = (size_t)M * sizeof(float), db = (size_t)N * sizeof(float);
+  const size_t gb = (size_t)N * rmsi::weight_bytes(dtype), rb = (size_t)M * sizeof(float),
+               db = (size_t)N * sizeof(float);
 
   if (!workspace) return RMS_ERR_WORKSPACE;
   DeviceInfo d;

@@ -26,12 +26,13 @@
 
 namespace rmsk {
 
-template <typename T, int KV, bool GEMMA>
+template <typename T, typename W, int KV, bool GEMMA>
 __global__ void __launch_bounds__(512)
-rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restrict__ gamma,
+rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__ gamma,
                          const float* __restrict__ rstd, T* dx, float* __restrict__ ws, int64_t M,
                          int N, int G) {
-  using Math = RowMath<T, GEMMA>;
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
   constexpr int NP = Math::kPairs;
   __shared__ float red[2][16];
@@ -49,13 +50,12 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restri
   // grid frees; it waits for this grid's completion before reading.
   pdl_wait();
 
-  const uint4* gv = reinterpret_cast<const uint4*>(gamma);
-  uint4 gw[KV];
+  GV gw[KV];
   f32x2 acc[KV][NP];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * G;
-    gw[k] = v < NV ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+    gw[k] = v < NV ? GV::load(gamma, v) : GV::zero();
 #pragma unroll
     for (int i = 0; i < NP; ++i) acc[k][i] = 0ull;
   }
@@ -128,42 +128,40 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const T* __restri
   }
 }
 
-template <typename T, int KV>
+template <typename T, typename W, int KV>
 static const void* kernel_ptr(bool gemma) {
-  return gemma ? reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, KV, true>)
-               : reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, KV, false>);
+  return gemma ? reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, W, KV, true>)
+               : reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, W, KV, false>);
 }
 
-template <typename T>
+template <typename T, typename W>
 static const void* pick(int kv, bool gemma) {
   switch (kv) {
-    case 1: return kernel_ptr<T, 1>(gemma);
-    case 2: return kernel_ptr<T, 2>(gemma);
-    case 4: return kernel_ptr<T, 4>(gemma);
+    case 1: return kernel_ptr<T, W, 1>(gemma);
+    case 2: return kernel_ptr<T, W, 2>(gemma);
+    case 4: return kernel_ptr<T, W, 4>(gemma);
     default: return nullptr;
   }
 }
 
-template <typename T, bool GEMMA>
+template <typename T, typename W, bool GEMMA>
 static cudaError_t launch_g(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)m.blocks), block(m.threads);
   const T* dy = static_cast<const T*>(a.dy);
   const T* x = static_cast<const T*>(a.x);
-  const T* g = static_cast<const T*>(a.gamma);
+  const W* g = static_cast<const W*>(a.gamma);
   T* dx = static_cast<T*>(a.dx);
-  cudaError_t e;
   switch (m.kv) {
-    case 1: e = launch_pdl(rms_bwd_registers_kernel<T, 1, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
-    case 2: e = launch_pdl(rms_bwd_registers_kernel<T, 2, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
-    case 4: e = launch_pdl(rms_bwd_registers_kernel<T, 4, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G); break;
+    case 1: return launch_pdl(rms_bwd_registers_kernel<T, W, 1, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G);
+    case 2: return launch_pdl(rms_bwd_registers_kernel<T, W, 2, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G);
+    case 4: return launch_pdl(rms_bwd_registers_kernel<T, W, 4, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G);
     default: return cudaErrorInvalidValue;
   }
-  return e;
 }
 
-template <typename T>
+template <typename T, typename W>
 static cudaError_t launch_t(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
-  return a.gemma ? launch_g<T, true>(a, m, s) : launch_g<T, false>(a, m, s);
+  return a.gemma ? launch_g<T, W, true>(a, m, s) : launch_g<T, W, false>(a, m, s);
 }
 
 }  // namespace rmsk
@@ -172,9 +170,14 @@ namespace rmsi {
 
 cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   m->smem = m->rows_per_cta > 1 ? (size_t)m->rows_per_cta * a.N * sizeof(float) : 0;
-  const void* k = a.dtype == kBF16  ? rmsk::pick<__nv_bfloat16>(m->kv, a.gemma)
-                  : a.dtype == kF16 ? rmsk::pick<__half>(m->kv, a.gemma)
-                                    : rmsk::pick<float>(m->kv, a.gemma);
+  const void* k;
+  switch (a.dtype) {
+    case kBF16: k = rmsk::pick<__nv_bfloat16, __nv_bfloat16>(m->kv, a.gemma); break;
+    case kF16: k = rmsk::pick<__half, __half>(m->kv, a.gemma); break;
+    case kBF16W32: k = rmsk::pick<__nv_bfloat16, float>(m->kv, a.gemma); break;
+    case kF16W32: k = rmsk::pick<__half, float>(m->kv, a.gemma); break;
+    default: k = rmsk::pick<float, float>(m->kv, a.gemma); break;
+  }
   if (!k) return cudaErrorInvalidValue;
   int occ = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, m->threads, m->smem);
@@ -191,9 +194,13 @@ cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m
 }
 
 cudaError_t launch_bwd_registers(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
-  if (a.dtype == kBF16) return rmsk::launch_t<__nv_bfloat16>(a, m, s);
-  if (a.dtype == kF16) return rmsk::launch_t<__half>(a, m, s);
-  return rmsk::launch_t<float>(a, m, s);
+  switch (a.dtype) {
+    case kBF16: return rmsk::launch_t<__nv_bfloat16, __nv_bfloat16>(a, m, s);
+    case kF16: return rmsk::launch_t<__half, __half>(a, m, s);
+    case kBF16W32: return rmsk::launch_t<__nv_bfloat16, float>(a, m, s);
+    case kF16W32: return rmsk::launch_t<__half, float>(a, m, s);
+    default: return rmsk::launch_t<float, float>(a, m, s);
+  }
 }
 
 }  // namespace rmsi

@@ -207,16 +207,69 @@ struct Pairs<float> {
   }
 };
 
+// ---- the weight beside one activation vector ----------------------------------
+// The weight values of the columns of one 16-byte activation vector: one
+// vector when the weight has the activations' type, two float32 vectors when
+// a 16-bit activation comes with a float32 weight.
+template <typename T>
+struct GammaSame {
+  uint4 v;
+  __device__ static __forceinline__ GammaSame load(const void* gamma, int vec) {
+    return GammaSame{__ldg(reinterpret_cast<const uint4*>(gamma) + vec)};
+  }
+  __device__ static __forceinline__ GammaSame zero() { return GammaSame{make_uint4(0u, 0u, 0u, 0u)}; }
+  __device__ __forceinline__ f32x2 pair(int i) const { return Pairs<T>::get(v, i); }
+  // 32-bit word i: two 16-bit weights, for the packed 16-bit multiply.
+  __device__ __forceinline__ uint32_t word(int i) const {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+  }
+};
+
+// Eight float32 weights beside one vector of eight 16-bit activations.
+struct GammaW32 {
+  uint4 a, b;  // weights of elements 0..3 and 4..7
+  __device__ static __forceinline__ GammaW32 load(const void* gamma, int vec) {
+    const uint4* g = reinterpret_cast<const uint4*>(gamma) + 2 * vec;
+    return GammaW32{__ldg(g), __ldg(g + 1)};
+  }
+  __device__ static __forceinline__ GammaW32 zero() {
+    return GammaW32{make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+  }
+  __device__ __forceinline__ f32x2 pair(int i) const {
+    const uint4& q = i < 2 ? a : b;
+    return (i & 1) ? pk2(__uint_as_float(q.z), __uint_as_float(q.w))
+                   : pk2(__uint_as_float(q.x), __uint_as_float(q.y));
+  }
+  __device__ __forceinline__ uint32_t word(int) const { return 0u; }  // not used with W32
+};
+
+template <typename T, typename W>
+struct GammaSel {
+  using type = GammaSame<T>;
+};
+template <>
+struct GammaSel<__nv_bfloat16, float> {
+  using type = GammaW32;
+};
+template <>
+struct GammaSel<__half, float> {
+  using type = GammaW32;
+};
+template <typename T, typename W>
+using GammaVec = typename GammaSel<T, W>::type;
+
 // ---- per-vector arithmetic ---------------------------------------------------
 // Shared by every vector kernel, so all mappings compute identical bits.
-template <typename T, bool GEMMA>
+// T: activation type; W: weight type (T, or float with 16-bit T).
+template <typename T, typename W, bool GEMMA>
 struct RowMath {
   using P = Pairs<T>;
+  using G = GammaVec<T, W>;
   static constexpr int kPairs = P::n;
 
   // Effective weight pair: gamma, or 1 + gamma (Gemma).
-  __device__ static __forceinline__ f32x2 weight(const uint4& g, int i) {
-    const f32x2 w = P::get(g, i);
+  __device__ static __forceinline__ f32x2 weight(const G& g, int i) {
+    const f32x2 w = g.pair(i);
     return GEMMA ? add2(w, splat2(1.0f)) : w;
   }
 
@@ -229,9 +282,10 @@ struct RowMath {
     }
   }
 
-  // y for one vector.  Non-Gemma: (x*r) rounded to the I/O type, then times
-  // gamma, rounded again.  Gemma: x*r*(1+gamma) rounded once.
-  __device__ static __forceinline__ uint4 forward(const uint4& x, const uint4& g, float r) {
+  // y for one vector.  Non-Gemma: (x*r) rounded to the weight type, then
+  // times gamma, rounded to the output type (with a float32 weight the first
+  // rounding is exact).  Gemma: x*r*(1+gamma) rounded once.
+  __device__ static __forceinline__ uint4 forward(const uint4& x, const G& g, float r) {
     const f32x2 rr = splat2(r);
     uint32_t o[4];
     if constexpr (sizeof(T) == 2) {
@@ -239,11 +293,10 @@ struct RowMath {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const f32x2 xr = mul2(P::get(x, i), rr);
-        if (GEMMA) {
+        if constexpr (GEMMA || sizeof(W) == 4) {
           o[i] = H::narrow(mul2(xr, weight(g, i)));
         } else {
-          const uint32_t gw = i == 0 ? g.x : i == 1 ? g.y : i == 2 ? g.z : g.w;
-          o[i] = H::mul(H::narrow(xr), gw);
+          o[i] = H::mul(H::narrow(xr), g.word(i));
         }
       }
     } else {
@@ -259,9 +312,8 @@ struct RowMath {
 
   // Backward first pass over one vector, with xn = x*r and u = dy*w:
   // sux += u*xn (the row's r*sum(u*x)) and acc += dy*xn (dgamma terms).
-  __device__ static __forceinline__ void backward_sums(const uint4& x, const uint4& dy,
-                                                       const uint4& g, float r, f32x2& sux,
-                                                       f32x2* acc) {
+  __device__ static __forceinline__ void backward_sums(const uint4& x, const uint4& dy, const G& g,
+                                                       float r, f32x2& sux, f32x2* acc) {
     const f32x2 rr = splat2(r);
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
@@ -273,8 +325,8 @@ struct RowMath {
   }
 
   // dx for one vector: r*u - x*r^3*c = r*(u - xn*k) with k = r*c.
-  __device__ static __forceinline__ uint4 backward_dx(const uint4& x, const uint4& dy,
-                                                      const uint4& g, float r, float k) {
+  __device__ static __forceinline__ uint4 backward_dx(const uint4& x, const uint4& dy, const G& g,
+                                                      float r, float k) {
     const f32x2 rr = splat2(r);
     const f32x2 nk = splat2(-k);
     uint32_t o[4];

@@ -16,11 +16,12 @@
 
 namespace rmsk {
 
-template <typename T, int KV, bool GEMMA>
+template <typename T, typename W, int KV, bool GEMMA>
 __global__ void __launch_bounds__(1024)
-rms_fwd_registers_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+rms_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T* __restrict__ y,
                          float* __restrict__ rstd, int64_t M, int N, float eps, int G) {
-  using Math = RowMath<T, GEMMA>;
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
   __shared__ float red[32];
   const int NV = N / VN;
@@ -29,7 +30,6 @@ rms_fwd_registers_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / G) + grp;
   const bool active = row < M;
   const uint4* xr = reinterpret_cast<const uint4*>(x) + (active ? row : 0) * (int64_t)NV;
-  const uint4* gv = reinterpret_cast<const uint4*>(gamma);
   pdl_trigger();
   pdl_wait();
 
@@ -51,29 +51,27 @@ rms_fwd_registers_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * G;
-    if (v < NV) st_stream(yr + v, Math::forward(xv[k], ld_keep(gv + v), r));
+    if (v < NV) st_stream(yr + v, Math::forward(xv[k], GV::load(gamma, v), r));
   }
 }
 
-template <typename T, bool GEMMA>
+template <typename T, typename W, bool GEMMA>
 static cudaError_t launch_g(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)m.blocks), block(m.threads);
   const T* x = static_cast<const T*>(a.x);
-  const T* g = static_cast<const T*>(a.gamma);
+  const W* g = static_cast<const W*>(a.gamma);
   T* y = static_cast<T*>(a.y);
-  cudaError_t e;
   switch (m.kv) {
-    case 1: e = launch_pdl(rms_fwd_registers_kernel<T, 1, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
-    case 2: e = launch_pdl(rms_fwd_registers_kernel<T, 2, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
-    case 4: e = launch_pdl(rms_fwd_registers_kernel<T, 4, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G); break;
+    case 1: return launch_pdl(rms_fwd_registers_kernel<T, W, 1, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G);
+    case 2: return launch_pdl(rms_fwd_registers_kernel<T, W, 2, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G);
+    case 4: return launch_pdl(rms_fwd_registers_kernel<T, W, 4, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G);
     default: return cudaErrorInvalidValue;
   }
-  return e;
 }
 
-template <typename T>
+template <typename T, typename W>
 static cudaError_t launch_t(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
-  return a.gemma ? launch_g<T, true>(a, m, s) : launch_g<T, false>(a, m, s);
+  return a.gemma ? launch_g<T, W, true>(a, m, s) : launch_g<T, W, false>(a, m, s);
 }
 
 }  // namespace rmsk
@@ -113,9 +111,13 @@ bool plan_registers(int N, int dtype, bool bwd, Mapping* m) {
 cudaError_t launch_fwd_registers(const FwdArgs& a, const Mapping& m0, cudaStream_t s) {
   Mapping m = m0;
   m.blocks = (a.M + m.rows_per_cta - 1) / m.rows_per_cta;
-  if (a.dtype == kBF16) return rmsk::launch_t<__nv_bfloat16>(a, m, s);
-  if (a.dtype == kF16) return rmsk::launch_t<__half>(a, m, s);
-  return rmsk::launch_t<float>(a, m, s);
+  switch (a.dtype) {
+    case kBF16: return rmsk::launch_t<__nv_bfloat16, __nv_bfloat16>(a, m, s);
+    case kF16: return rmsk::launch_t<__half, __half>(a, m, s);
+    case kBF16W32: return rmsk::launch_t<__nv_bfloat16, float>(a, m, s);
+    case kF16W32: return rmsk::launch_t<__half, float>(a, m, s);
+    default: return rmsk::launch_t<float, float>(a, m, s);
+  }
 }
 
 }  // namespace rmsi

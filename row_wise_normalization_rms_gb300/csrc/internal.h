@@ -8,9 +8,12 @@
 
 namespace rmsi {
 
-enum Dtype { kF32 = 0, kBF16 = 1, kF16 = 2 };
+// Element types of a call: activations (x, y, dy, dx) and weight (gamma).
+enum Dtype { kF32 = 0, kBF16 = 1, kF16 = 2, kBF16W32 = 3, kF16W32 = 4 };
 
+// Bytes of one activation element / one weight element.
 inline int dtype_bytes(int dtype) { return dtype == kF32 ? 4 : 2; }
+inline int weight_bytes(int dtype) { return (dtype == kBF16 || dtype == kF16) ? 2 : 4; }
 enum Path { kAuto = 0, kRegisters = 1, kStaged = 2, kScalar = 3 };
 
 struct FwdArgs {

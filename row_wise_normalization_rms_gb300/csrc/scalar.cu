@@ -20,9 +20,9 @@ namespace rmsk {
 
 constexpr int kScalarThreads = 256;
 
-template <typename T>
+template <typename T, typename W>
 __global__ void __launch_bounds__(kScalarThreads)
-rms_fwd_scalar_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T* __restrict__ y,
+rms_fwd_scalar_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T* __restrict__ y,
                       float* __restrict__ rstd, int64_t M, int N, float eps, int gemma) {
   using E = Elem<T>;
   __shared__ float red[kScalarThreads / 32];
@@ -41,15 +41,15 @@ rms_fwd_scalar_kernel(const T* __restrict__ x, const T* __restrict__ gamma, T* _
   T* yr = y + row * N;
   for (int j = threadIdx.x; j < N; j += kScalarThreads) {
     const float f = E::to_f(xr[j]);
-    const float g = E::to_f(gamma[j]);
-    const float o = gemma ? (f * r) * (1.0f + g) : E::round(f * r) * g;
+    const float g = Elem<W>::to_f(gamma[j]);
+    const float o = gemma ? (f * r) * (1.0f + g) : Elem<W>::round(f * r) * g;
     yr[j] = E::from_f(o);
   }
 }
 
-template <typename T>
+template <typename T, typename W>
 __global__ void __launch_bounds__(kScalarThreads)
-rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const T* __restrict__ gamma,
+rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__ gamma,
                       const float* __restrict__ rstd, T* dx, float* __restrict__ ws, int64_t M,
                       int N, int gemma) {
   using E = Elem<T>;
@@ -66,7 +66,7 @@ rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const T* __restrict_
     // xn = x*r, u = dy*w:  k = mean(u*xn) = r*c,  dx = r*(u - xn*k).
     float s = 0.f;
     for (int j = threadIdx.x; j < N; j += kScalarThreads) {
-      const float g = E::to_f(gamma[j]);
+      const float g = Elem<W>::to_f(gamma[j]);
       const float w = gemma ? 1.0f + g : g;
       s = fmaf(E::to_f(dr[j]) * w, E::to_f(xr[j]) * r, s);
     }
@@ -76,7 +76,7 @@ rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const T* __restrict_
     for (int j = threadIdx.x; j < N; j += kScalarThreads) {
       const float xn = E::to_f(xr[j]) * r;
       const float d = E::to_f(dr[j]);
-      const float g = E::to_f(gamma[j]);
+      const float g = Elem<W>::to_f(gamma[j]);
       const float w = gemma ? 1.0f + g : g;
       acc[j] = fmaf(d, xn, acc[j]);
       out[j] = E::from_f(fmaf(-xn, k, d * w) * r);
@@ -169,29 +169,38 @@ bool plan_scalar(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
   return true;
 }
 
-template <typename T>
+template <typename T, typename W>
 static cudaError_t launch_fwd_scalar_t(const FwdArgs& a, dim3 grid, dim3 block, cudaStream_t s) {
-  return rmsk::launch_pdl(rmsk::rms_fwd_scalar_kernel<T>, grid, block, 0, s,
-                          static_cast<const T*>(a.x), static_cast<const T*>(a.gamma),
+  return rmsk::launch_pdl(rmsk::rms_fwd_scalar_kernel<T, W>, grid, block, 0, s,
+                          static_cast<const T*>(a.x), static_cast<const W*>(a.gamma),
                           static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps, a.gemma);
 }
 
 cudaError_t launch_fwd_scalar(const FwdArgs& a, const Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)a.M), block(m.threads);
-  if (a.dtype == kBF16) return launch_fwd_scalar_t<__nv_bfloat16>(a, grid, block, s);
-  if (a.dtype == kF16) return launch_fwd_scalar_t<__half>(a, grid, block, s);
-  return launch_fwd_scalar_t<float>(a, grid, block, s);
+  switch (a.dtype) {
+    case kBF16: return launch_fwd_scalar_t<__nv_bfloat16, __nv_bfloat16>(a, grid, block, s);
+    case kF16: return launch_fwd_scalar_t<__half, __half>(a, grid, block, s);
+    case kBF16W32: return launch_fwd_scalar_t<__nv_bfloat16, float>(a, grid, block, s);
+    case kF16W32: return launch_fwd_scalar_t<__half, float>(a, grid, block, s);
+    default: return launch_fwd_scalar_t<float, float>(a, grid, block, s);
+  }
 }
 
-template <typename T>
+template <typename T, typename W>
 static const void* bwd_scalar_ptr() {
-  return reinterpret_cast<const void*>(&rmsk::rms_bwd_scalar_kernel<T>);
+  return reinterpret_cast<const void*>(&rmsk::rms_bwd_scalar_kernel<T, W>);
 }
 
 cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
-  const void* k = a.dtype == kBF16  ? bwd_scalar_ptr<__nv_bfloat16>()
-                  : a.dtype == kF16 ? bwd_scalar_ptr<__half>()
-                                    : bwd_scalar_ptr<float>();
+  const void* k;
+  switch (a.dtype) {
+    case kBF16: k = bwd_scalar_ptr<__nv_bfloat16, __nv_bfloat16>(); break;
+    case kF16: k = bwd_scalar_ptr<__half, __half>(); break;
+    case kBF16W32: k = bwd_scalar_ptr<__nv_bfloat16, float>(); break;
+    case kF16W32: k = bwd_scalar_ptr<__half, float>(); break;
+    default: k = bwd_scalar_ptr<float, float>(); break;
+  }
   cudaError_t e = opt_in_max_smem(k, d);
   if (e != cudaSuccess) return e;
   int occ = 0;
@@ -207,19 +216,23 @@ cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   return cudaSuccess;
 }
 
-template <typename T>
+template <typename T, typename W>
 static cudaError_t launch_bwd_scalar_t(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)m.blocks), block(m.threads);
-  return rmsk::launch_pdl(rmsk::rms_bwd_scalar_kernel<T>, grid, block, m.smem, s,
+  return rmsk::launch_pdl(rmsk::rms_bwd_scalar_kernel<T, W>, grid, block, m.smem, s,
                           static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
-                          static_cast<const T*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.ws,
+                          static_cast<const W*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.ws,
                           a.M, a.N, a.gemma);
 }
 
 cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s) {
-  if (a.dtype == kBF16) return launch_bwd_scalar_t<__nv_bfloat16>(a, m, s);
-  if (a.dtype == kF16) return launch_bwd_scalar_t<__half>(a, m, s);
-  return launch_bwd_scalar_t<float>(a, m, s);
+  switch (a.dtype) {
+    case kBF16: return launch_bwd_scalar_t<__nv_bfloat16, __nv_bfloat16>(a, m, s);
+    case kF16: return launch_bwd_scalar_t<__half, __half>(a, m, s);
+    case kBF16W32: return launch_bwd_scalar_t<__nv_bfloat16, float>(a, m, s);
+    case kF16W32: return launch_bwd_scalar_t<__half, float>(a, m, s);
+    default: return launch_bwd_scalar_t<float, float>(a, m, s);
+  }
 }
 
 cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, cudaStream_t s) {

@@ -181,10 +181,11 @@ __device__ __forceinline__ float row_total(const StagedParams& p, const StageHea
 // the exchange of row partials, and a last one before exit keeps every CTA's
 // shared memory alive while its peers may still read it.
 
-template <typename T, int KV, bool GEMMA>
+template <typename T, typename W, int KV, bool GEMMA>
 __global__ void __launch_bounds__(1024)
 rms_fwd_staged_kernel(const StagedParams p) {
-  using Math = RowMath<T, GEMMA>;
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
   extern __shared__ __align__(128) uint8_t smem[];
   const StageHeader h = header(smem);
@@ -208,12 +209,11 @@ rms_fwd_staged_kernel(const StagedParams p) {
     for (; issued < pre; ++issued) issue_tile<T, false>(p, h, sl, issued, pol);
   }
 
-  const uint4* gv = reinterpret_cast<const uint4*>(p.gamma) + sl.v0;
-  uint4 gw[KV];
+  GV gw[KV];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * p.G;
-    gw[k] = v < sl.nvs ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+    gw[k] = v < sl.nvs ? GV::load(p.gamma, sl.v0 + v) : GV::zero();
   }
 
   int64_t i = 0;
@@ -260,10 +260,11 @@ rms_fwd_staged_kernel(const StagedParams p) {
   if (p.C > 1) cluster_sync();
 }
 
-template <typename T, int KV, bool GEMMA>
+template <typename T, typename W, int KV, bool GEMMA>
 __global__ void __launch_bounds__(512)
 rms_bwd_staged_kernel(const StagedParams p) {
-  using Math = RowMath<T, GEMMA>;
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
   constexpr int NP = Math::kPairs;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -288,13 +289,12 @@ rms_bwd_staged_kernel(const StagedParams p) {
     for (; issued < pre; ++issued) issue_tile<T, true>(p, h, sl, issued, pol);
   }
 
-  const uint4* gv = reinterpret_cast<const uint4*>(p.gamma) + sl.v0;
-  uint4 gw[KV];
+  GV gw[KV];
   f32x2 acc[KV][NP];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * p.G;
-    gw[k] = v < sl.nvs ? ld_keep(gv + v) : make_uint4(0u, 0u, 0u, 0u);
+    gw[k] = v < sl.nvs ? GV::load(p.gamma, sl.v0 + v) : GV::zero();
 #pragma unroll
     for (int e = 0; e < NP; ++e) acc[k][e] = 0ull;
   }
@@ -390,27 +390,27 @@ rms_bwd_staged_kernel(const StagedParams p) {
   if (p.C > 1) cluster_sync();
 }
 
-template <typename T, bool BWD, bool GEMMA>
+template <typename T, typename W, bool BWD, bool GEMMA>
 static const void* staged_ptr_g(int kv) {
   if (BWD) {
     switch (kv) {
-      case 1: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 1, GEMMA>);
-      case 2: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 2, GEMMA>);
-      case 4: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, 4, GEMMA>);
+      case 1: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 1, GEMMA>);
+      case 2: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 2, GEMMA>);
+      case 4: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 4, GEMMA>);
     }
   } else {
     switch (kv) {
-      case 1: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 1, GEMMA>);
-      case 2: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 2, GEMMA>);
-      case 4: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, 4, GEMMA>);
+      case 1: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 1, GEMMA>);
+      case 2: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 2, GEMMA>);
+      case 4: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 4, GEMMA>);
     }
   }
   return nullptr;
 }
 
-template <typename T, bool BWD>
+template <typename T, typename W, bool BWD>
 static const void* staged_ptr(int kv, bool gemma) {
-  return gemma ? staged_ptr_g<T, BWD, true>(kv) : staged_ptr_g<T, BWD, false>(kv);
+  return gemma ? staged_ptr_g<T, W, BWD, true>(kv) : staged_ptr_g<T, W, BWD, false>(kv);
 }
 
 }  // namespace rmsk
@@ -441,12 +441,23 @@ namespace {
 #endif
 
 const void* staged_kernel(int dtype, bool bwd, int kv, bool gemma) {
-  if (dtype == kBF16)
-    return bwd ? rmsk::staged_ptr<__nv_bfloat16, true>(kv, gemma)
-               : rmsk::staged_ptr<__nv_bfloat16, false>(kv, gemma);
-  if (dtype == kF16)
-    return bwd ? rmsk::staged_ptr<__half, true>(kv, gemma) : rmsk::staged_ptr<__half, false>(kv, gemma);
-  return bwd ? rmsk::staged_ptr<float, true>(kv, gemma) : rmsk::staged_ptr<float, false>(kv, gemma);
+  switch (dtype) {
+    case kBF16:
+      return bwd ? rmsk::staged_ptr<__nv_bfloat16, __nv_bfloat16, true>(kv, gemma)
+                 : rmsk::staged_ptr<__nv_bfloat16, __nv_bfloat16, false>(kv, gemma);
+    case kF16:
+      return bwd ? rmsk::staged_ptr<__half, __half, true>(kv, gemma)
+                 : rmsk::staged_ptr<__half, __half, false>(kv, gemma);
+    case kBF16W32:
+      return bwd ? rmsk::staged_ptr<__nv_bfloat16, float, true>(kv, gemma)
+                 : rmsk::staged_ptr<__nv_bfloat16, float, false>(kv, gemma);
+    case kF16W32:
+      return bwd ? rmsk::staged_ptr<__half, float, true>(kv, gemma)
+                 : rmsk::staged_ptr<__half, float, false>(kv, gemma);
+    default:
+      return bwd ? rmsk::staged_ptr<float, float, true>(kv, gemma)
+                 : rmsk::staged_ptr<float, float, false>(kv, gemma);
+  }
 }
 
 // Occupancy per (kernel, device, threads, smem), so repeated calls make no
@@ -623,40 +634,40 @@ static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, bool bwd,
   return p;
 }
 
-template <typename T, bool GEMMA>
+template <typename T, typename W, bool GEMMA>
 static cudaError_t launch_fwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
   StagedLaunch L(m, grid, s);
   switch (m.kv) {
-    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, 1, GEMMA>, p);
-    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, 2, GEMMA>, p);
-    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, 4, GEMMA>, p);
+    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 1, GEMMA>, p);
+    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 2, GEMMA>, p);
+    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 4, GEMMA>, p);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <typename T, bool GEMMA>
+template <typename T, typename W, bool GEMMA>
 static cudaError_t launch_bwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
   StagedLaunch L(m, grid, s);
   switch (m.kv) {
-    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, 1, GEMMA>, p);
-    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, 2, GEMMA>, p);
-    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, 4, GEMMA>, p);
+    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 1, GEMMA>, p);
+    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 2, GEMMA>, p);
+    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 4, GEMMA>, p);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <typename T>
+template <typename T, typename W>
 static cudaError_t launch_fwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
-  return p.gemma ? launch_fwd_g<T, true>(p, m, grid, s) : launch_fwd_g<T, false>(p, m, grid, s);
+  return p.gemma ? launch_fwd_g<T, W, true>(p, m, grid, s) : launch_fwd_g<T, W, false>(p, m, grid, s);
 }
 
-template <typename T>
+template <typename T, typename W>
 static cudaError_t launch_bwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
-  return p.gemma ? launch_bwd_g<T, true>(p, m, grid, s) : launch_bwd_g<T, false>(p, m, grid, s);
+  return p.gemma ? launch_bwd_g<T, W, true>(p, m, grid, s) : launch_bwd_g<T, W, false>(p, m, grid, s);
 }
 
 cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
@@ -671,9 +682,13 @@ cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceIn
   int64_t grid = 0;
   cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv, a.gemma), m, d, p.ntiles, &grid);
   if (e != cudaSuccess) return e;
-  if (a.dtype == kBF16) return launch_fwd_t<__nv_bfloat16>(p, m, grid, s);
-  if (a.dtype == kF16) return launch_fwd_t<__half>(p, m, grid, s);
-  return launch_fwd_t<float>(p, m, grid, s);
+  switch (a.dtype) {
+    case kBF16: return launch_fwd_t<__nv_bfloat16, __nv_bfloat16>(p, m, grid, s);
+    case kF16: return launch_fwd_t<__half, __half>(p, m, grid, s);
+    case kBF16W32: return launch_fwd_t<__nv_bfloat16, float>(p, m, grid, s);
+    case kF16W32: return launch_fwd_t<__half, float>(p, m, grid, s);
+    default: return launch_fwd_t<float, float>(p, m, grid, s);
+  }
 }
 
 cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
@@ -697,9 +712,13 @@ cudaError_t launch_bwd_staged(const BwdArgs& a, const Mapping& m, const DeviceIn
   p.dx = a.dx;
   p.ws = a.ws;
   p.gemma = a.gemma;
-  if (a.dtype == kBF16) return launch_bwd_t<__nv_bfloat16>(p, m, m.blocks, s);
-  if (a.dtype == kF16) return launch_bwd_t<__half>(p, m, m.blocks, s);
-  return launch_bwd_t<float>(p, m, m.blocks, s);
+  switch (a.dtype) {
+    case kBF16: return launch_bwd_t<__nv_bfloat16, __nv_bfloat16>(p, m, m.blocks, s);
+    case kF16: return launch_bwd_t<__half, __half>(p, m, m.blocks, s);
+    case kBF16W32: return launch_bwd_t<__nv_bfloat16, float>(p, m, m.blocks, s);
+    case kF16W32: return launch_bwd_t<__half, float>(p, m, m.blocks, s);
+    default: return launch_bwd_t<float, float>(p, m, m.blocks, s);
+  }
 }
 
 cudaError_t take_device_status(int* status) {

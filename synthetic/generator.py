@@ -51,11 +51,17 @@ class Workload:
     gemma: int = 0
     inplace_dx: int = 0
     seed: int = 0
+    weight_dtype: str = ""  # "" (the activations' dtype) or "f32"
     note: str = field(default="", compare=False)
 
     @property
     def elem_bytes(self) -> int:
         return 4 if self.dtype == "f32" else 2
+
+    @property
+    def wdtype(self) -> str:
+        """The weight's dtype."""
+        return self.weight_dtype or self.dtype
 
     def with_shape(self, M: int, N: Optional[int] = None, name: Optional[str] = None) -> "Workload":
         return replace(self, M=M, N=self.N if N is None else N,
@@ -95,6 +101,10 @@ WORKLOADS = {
                  gamma=("normal", 1.0, 0.2), dy=("normal", 0.0, 1.0),
                  row_scale=("loguniform", 0.01, 100.0),
                  note="the large-hidden workload with fp16 I/O"),
+        Workload("llama7b_bf16w32_8192x4096", 8192, 4096, "bf16", 1e-6,
+                 gamma=("normal", 1.0, 0.1), dy=("normal", 0.0, 1e-2),
+                 row_scale=("loguniform", 0.1, 10.0), weight_dtype="f32",
+                 note="the Llama-7B shape with a float32 weight (mixed precision)"),
         Workload("timing_f32_128x257", 128, 257, "f32", 1e-6,
                  note="the tutorial's timing shape, ragged N"),
         Workload("layernorm_test_bf16_1151x8192", 1151, 8192, "bf16", 1e-5,
@@ -174,7 +184,8 @@ def _matrix(w: Workload, tensor: str, dist: Dist, row_scale: Optional[np.ndarray
 
 
 def make_inputs(w: Workload) -> dict:
-    """Draw x (M,N), gamma (N,) and dy (M,N) for a workload, in storage form.
+    """Draw x (M,N), gamma (N,) and dy (M,N) for a workload, in storage form
+    (gamma in the weight dtype).
 
     Returns a dict with keys ``x``, ``gamma``, ``dy`` (float32 arrays for f32
     workloads, float16 arrays for f16 ones, uint16 bf16 bit patterns for bf16
@@ -189,7 +200,7 @@ def make_inputs(w: Workload) -> dict:
     _draw(_generator(w.seed, "gamma"), w.gamma, gvals)
     return {
         "x": _matrix(w, "x", w.x, scale),
-        "gamma": _store(gvals, w.dtype),
+        "gamma": _store(gvals, w.wdtype),
         "dy": _matrix(w, "dy", w.dy, None),
         "row_scale": scale,
     }

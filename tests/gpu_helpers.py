@@ -65,7 +65,7 @@ def run_gpu(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None) -> 
     M, N = w.M, w.N
     inplace = w.inplace_dx if inplace is None else inplace
     x = to_device(inp["x"], w.dtype)
-    g = to_device(inp["gamma"], w.dtype)
+    g = to_device(inp["gamma"], w.wdtype)
     dy = to_device(inp["dy"], w.dtype)
     y = Guarded((M, N), dt, _SENTINEL[w.dtype])
     rstd = Guarded((M,), torch.float32, _SENTINEL["f32"])
@@ -86,7 +86,7 @@ def run_gpu(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None) -> 
 def oracle_rows(w, inp, rows):
     """Oracle y, r, dx and the dx tolerance scale for the given rows."""
     x = storage_to_float64(inp["x"][rows], w.dtype)
-    g = storage_to_float64(inp["gamma"], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.wdtype)
     dy = storage_to_float64(inp["dy"][rows], w.dtype)
     y, r = orc.rms_forward(x, g, w.eps, w.gemma)
     dx, _, dxs, _ = orc.rms_backward(x, g, dy, w.eps, w.gemma, with_scales=True)

@@ -286,6 +286,11 @@ def pin_lowp_emulation(impl):
     ref_h = ((xh * r16[:, None]).to(torch.float16).float() * gh[None, :]).to(torch.float16)
     got_h = impl.emulate_forward_lowp(xh.double().numpy(), gh.double().numpy(), eps, 0, "f16")
     assert np.array_equal(got_h, ref_h.double().numpy())
+    # bf16 activations with a float32 weight: x*r stays float32, one rounding at the end.
+    gw = torch.tensor(rng.uniform(0.5, 1.5, N), dtype=torch.float32)
+    ref_w = ((x * r32[:, None]) * gw[None, :]).to(torch.bfloat16).double().numpy()
+    got_w = impl.emulate_forward_lowp(x.double().numpy(), gw.double().numpy(), eps, 0, "bf16", "f32")
+    assert np.array_equal(got_w, ref_w)
 
 
 ALL_PINS = [

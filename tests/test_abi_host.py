@@ -57,7 +57,7 @@ def fwd(lib, x=A, g=2 * A, y=3 * A, r=4 * A, M=4, N=8, eps=1e-6,
 
 def test_fwd_rejects_bad_arguments(lib):
     nan, inf = float("nan"), float("inf")
-    assert fwd(lib, dtype=3) == INVALID
+    assert fwd(lib, dtype=5) == INVALID
     assert fwd(lib, dtype=-1) == INVALID
     assert fwd(lib, gemma=2) == INVALID
     assert fwd(lib, M=-1) == INVALID

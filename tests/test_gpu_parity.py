@@ -22,10 +22,14 @@ if torch.cuda.is_available():
 
 
 def _w(M, N, dtype, gemma=0, inplace=0, eps=1e-6, seed=0, **kw):
+    """A test workload; dtype "bf16w32"/"f16w32" means 16-bit activations, float32 weight."""
     from synthetic import Workload
 
-    return Workload(name=f"t{M}x{N}_{dtype}_g{gemma}_i{inplace}", M=M, N=N, dtype=dtype, eps=eps,
-                    gemma=gemma, inplace_dx=inplace, seed=seed,
+    wd = ""
+    if dtype.endswith("w32"):
+        dtype, wd = dtype[:-3], "f32"
+    return Workload(name=f"t{M}x{N}_{dtype}{wd}_g{gemma}_i{inplace}", M=M, N=N, dtype=dtype,
+                    eps=eps, gemma=gemma, inplace_dx=inplace, seed=seed, weight_dtype=wd,
                     gamma=("normal", 0.0, 0.1) if gemma else ("uniform", 0.5, 1.5),
                     row_scale=("loguniform", 0.01, 100.0), **kw)
 
@@ -37,12 +41,12 @@ SMALL_SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "bf16w32", "f16w32"])
 @pytest.mark.parametrize("M,N", SMALL_SHAPES, ids=[f"{m}x{n}" for m, n in SMALL_SHAPES])
 @pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar"])
 def test_small_shapes_full_parity(M, N, dtype, path):
     w = _w(M, N, dtype, seed=M + N)
-    b = 4 if dtype == "f32" else 2
+    b = 4 if w.dtype == "f32" else 2
     inp = H.inputs_for(w)
     if path in ("registers", "staged") and (N * b) % 16 != 0:
         with pytest.raises(rms.RmsError) as ei:
@@ -58,7 +62,7 @@ def test_small_shapes_full_parity(M, N, dtype, path):
 
 
 @pytest.mark.parametrize("gemma,inplace", [(0, 1), (1, 0), (1, 1)])
-@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "bf16w32", "f16w32"])
 @pytest.mark.parametrize("M,N", [(257, 3072), (65, 1000), (31, 257)])
 def test_gemma_and_inplace(M, N, dtype, gemma, inplace):
     w = _w(M, N, dtype, gemma=gemma, inplace=inplace, seed=7)
@@ -111,7 +115,7 @@ def test_inplace_matches_out_of_place_bitwise(dtype, path):
 
 
 @pytest.mark.parametrize("N", [1000, 4096, 8192])
-@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "bf16w32", "f16w32"])
 def test_lowp_cast_order(N, dtype):
     """y rounds x*r to the I/O type before the weight multiply: nearly every
     element equals the oracle's emulation of that order bit for bit, and many
@@ -122,18 +126,19 @@ def test_lowp_cast_order(N, dtype):
     w = _w(256, N, dtype, seed=N)
     inp = H.inputs_for(w)
     res = H.run_gpu(w, inp)
-    x = storage_to_float64(inp["x"], dtype)
-    g = storage_to_float64(inp["gamma"], dtype)
-    emu = orc.emulate_forward_lowp(x, g, w.eps, 0, dtype)
+    x = storage_to_float64(inp["x"], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.wdtype)
+    emu = orc.emulate_forward_lowp(x, g, w.eps, 0, w.dtype, w.wdtype)
     got = H.to_host64(res.y)
     same = np.mean(got == emu)
     assert same >= 0.999, same
     diff = got != emu
-    step = 2.0 ** -6 if dtype == "bf16" else 2.0 ** -9  # two units in the last place, relative
+    step = 2.0 ** -6 if w.dtype == "bf16" else 2.0 ** -9  # two units in the last place, relative
     assert np.all(np.abs(got[diff] - emu[diff]) <= step * np.abs(emu[diff]))
-    exact, _ = orc.rms_forward(x, g, w.eps)
-    once = torch.tensor(exact).float().to(H.tdtype(dtype)).double().numpy()
-    assert np.mean(got != once) > 0.01
+    if not w.weight_dtype:  # with a float32 weight there is only one rounding
+        exact, _ = orc.rms_forward(x, g, w.eps)
+        once = torch.tensor(exact).float().to(H.tdtype(w.dtype)).double().numpy()
+        assert np.mean(got != once) > 0.01
 
 
 def test_gemma_equals_plain_with_shifted_weight_f32():
