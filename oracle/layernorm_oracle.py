@@ -1,0 +1,100 @@
+"""Plain fp64 CPU oracle for row-wise LayerNorm, forward and backward.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+the CPU-baseline leg of ``bench.py`` may import this module.  It shares no
+code with the CUDA library.
+
+Source: "第 07 章:LayerNorm——反向传播与原子锁" ([LN]):
+  - step 3 (forward): per row mean = Σx/N, var = Σ(x − mean)²/N (a second
+    pass over the centred values), rstd = 1/sqrt(var + eps),
+    y = (x − mean)·rstd·w + b; mean and rstd are kept for the backward;
+  - § 3.0 (backward): x̂ = (x − mean)·rstd, ĝ = w·dy, c1 = Σ x̂·ĝ / N,
+    c2 = Σ ĝ / N, dx = (ĝ − (x̂·c1 + c2))·rstd; the weight and bias
+    gradients are the row contributions dy·x̂ and dy summed over all rows.
+
+Every function evaluates those definitions directly in float64 on the exact
+values of the (dtype-rounded) inputs.  Library primitives used as steps:
+``np.mean`` / ``np.sum``, ``np.sqrt``.  Every function is pinned by
+``tests/test_layernorm_oracle.py`` (torch's float64 layer_norm and autograd,
+central differences, closed forms, invariants); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def ln_stats(x, eps: float):
+    """(mean, rstd) per row: mean = Σx/N, var = Σ(x − mean)²/N, rstd = 1/sqrt(var + eps)."""
+    x = _f64(x)
+    mean = np.mean(x, axis=-1)
+    d = x - mean[:, None]
+    var = np.mean(d * d, axis=-1)
+    return mean, 1.0 / np.sqrt(var + eps)
+
+
+def ln_forward(x, w, b, eps: float):
+    """y = (x − mean)·rstd·w + b (b may be None: no bias).  Returns (y, mean, rstd)."""
+    x = _f64(x)
+    mean, rstd = ln_stats(x, eps)
+    xhat = (x - mean[:, None]) * rstd[:, None]
+    y = xhat * _f64(w)[None, :]
+    if b is not None:
+        y = y + _f64(b)[None, :]
+    return y, mean, rstd
+
+
+def ln_backward(x, w, dy, eps: float, with_scales: bool = False):
+    """Gradients of L = Σ dy ⊙ y: (dx, dw, db), from the [LN] § 3.0 closed form.
+
+    With ``with_scales`` also the sizes of the terms each output is built
+    from, for tolerances where they cancel: ``dx_scale = rstd·(|ĝ| + |c2| +
+    |x̂|·mean|x̂ ĝ| + mean|ĝ|)`` and ``dw_scale = Σ_i |dy·x̂|``,
+    ``db_scale = Σ_i |dy|``.
+    """
+    x = _f64(x)
+    dy = _f64(dy)
+    mean, rstd = ln_stats(x, eps)
+    xhat = (x - mean[:, None]) * rstd[:, None]
+    gh = dy * _f64(w)[None, :]
+    c1 = np.mean(xhat * gh, axis=-1)
+    c2 = np.mean(gh, axis=-1)
+    dx = (gh - (xhat * c1[:, None] + c2[:, None])) * rstd[:, None]
+    dw = np.sum(dy * xhat, axis=0)
+    db = np.sum(dy, axis=0)
+    if not with_scales:
+        return dx, dw, db
+    dx_scale = rstd[:, None] * (np.abs(gh) + np.mean(np.abs(gh), axis=-1)[:, None]
+                                + np.abs(xhat) * np.mean(np.abs(xhat * gh), axis=-1)[:, None])
+    dw_scale = np.sum(np.abs(dy * xhat), axis=0)
+    db_scale = np.sum(np.abs(dy), axis=0)
+    return dx, dw, db, dx_scale, dw_scale, db_scale
+
+
+def ln_loss(x, w, b, dy, eps: float) -> float:
+    y, _, _ = ln_forward(x, w, b, eps)
+    return float(np.sum(_f64(dy) * y))
+
+
+def ln_fd_gradients(x, w, b, dy, eps: float, h_rel: float = 1e-6):
+    """Central differences of ``ln_loss`` for every entry of x, w and b (tiny inputs)."""
+    x = _f64(x).copy()
+    w = _f64(w).copy()
+    b = _f64(b).copy()
+    grads = []
+    for arr in (x, w, b):
+        g = np.zeros_like(arr)
+        for idx in np.ndindex(*arr.shape):
+            a = arr[idx]
+            h = h_rel * max(1.0, abs(a))
+            arr[idx] = a + h
+            lp = ln_loss(x, w, b, dy, eps)
+            arr[idx] = a - h
+            lm = ln_loss(x, w, b, dy, eps)
+            arr[idx] = a
+            g[idx] = (lp - lm) / (2.0 * h)
+        grads.append(g)
+    return tuple(grads)
