@@ -171,6 +171,54 @@ rms_status rms_bwd_noalloc(void* dy, const void* x, const void* gamma, const flo
                            void* dx, float* dgamma, int64_t M, int64_t N, rms_dtype dtype,
                            int gemma, int inplace_dx, void* stream);
 
+/*
+ * ln_fwd — forward LayerNorm over M rows of N, on the same engine.
+ *   mean_i = (1/N) sum_j x_ij,  var_i = (1/N) sum_j (x_ij - mean_i)^2,
+ *   rstd_i = 1/sqrt(var_i + eps),  y_ij = (x_ij - mean_i) * rstd_i * w_j + b_j
+ *   x [M*N], w [N], b [N] (or NULL: no bias), y [M*N]; mean, rstd [M] float32,
+ *   written for ln_bwd.  Types as rms_dtype (w and b share the weight type).
+ *   Arithmetic float32, the variance from the centred values (two passes
+ *   over the row held on chip), one rounding per stored y.
+ * Source: "第 07 章:LayerNorm——反向传播与原子锁", step 3 (forward kernel).
+ * Errors: RMS_ERR_INVALID_ARG, RMS_ERR_UNSUPPORTED, RMS_ERR_CUDA.
+ */
+rms_status ln_fwd(const void* x, const void* w, const void* b, void* y, float* mean, float* rstd,
+                  int64_t M, int64_t N, float eps, rms_dtype dtype, void* stream);
+
+/* ln_fwd with an explicit mapping (RMS_PATH_REGISTERS or RMS_PATH_SCALAR). */
+rms_status ln_fwd_ex(const void* x, const void* w, const void* b, void* y, float* mean,
+                     float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype, rms_path path,
+                     void* stream);
+
+/*
+ * ln_bwd — backward LayerNorm from the saved mean and rstd.
+ *   xhat = (x - mean)*rstd, g = dy*w, c1 = mean_j(xhat*g), c2 = mean_j(g),
+ *   dx = (g - (xhat*c1 + c2)) * rstd,
+ *   dw_j = sum_i dy_ij*xhat_ij,  db_j = sum_i dy_ij   (sums over rows)
+ *   dy, x [M*N]; w [N]; mean, rstd [M] float32; dx [M*N] (NULL or dy with
+ *   inplace_dx = 1); dw [N] float32; db [N] float32 or NULL (not computed);
+ *   workspace of ln_bwd_workspace_size(M, N) bytes, 256-byte aligned.
+ * dw and db come from per-CTA partials over a static row assignment and a
+ * fixed-order column sum (no atomics, no locks): bitwise reproducible.
+ * Source: "第 07 章:LayerNorm——反向传播与原子锁", § 3.0 (backward formulas,
+ * row contributions summed over rows).
+ * Errors: as rms_bwd.
+ */
+rms_status ln_bwd(void* dy, const void* x, const void* w, const float* mean, const float* rstd,
+                  void* dx, float* dw, float* db, void* workspace, int64_t M, int64_t N,
+                  rms_dtype dtype, int inplace_dx, void* stream);
+
+/* ln_bwd with the workspace size stated and an explicit mapping
+ * (RMS_PATH_STAGED or RMS_PATH_SCALAR). */
+rms_status ln_bwd_ex(void* dy, const void* x, const void* w, const float* mean,
+                     const float* rstd, void* dx, float* dw, float* db, void* workspace,
+                     size_t workspace_bytes, int64_t M, int64_t N, rms_dtype dtype, int inplace_dx,
+                     rms_path path, void* stream);
+
+/* Bytes of workspace ln_bwd needs for M rows of N on the current device
+ * (two rows of partials per CTA: dw and db; a multiple of 256). */
+size_t ln_bwd_workspace_size(int64_t M, int64_t N);
+
 /* Bytes of workspace rms_bwd needs for M rows of N on the current device
  * (an upper bound over dtypes and mappings, a multiple of 256).  Returns 0
  * for M <= 0 or N <= 0, and 0 if the device cannot be queried. */
@@ -180,8 +228,8 @@ size_t rms_bwd_workspace_size(int64_t M, int64_t N);
 const char* rms_status_string(rms_status status);
 
 /* Synchronises `stream`, then reports and clears the device-side status
- * word of the current device: RMS_ERR_TIMEOUT if a bounded wait in the
- * staged mapping gave up since the last query (that launch's outputs are
+ * words of the current device: RMS_ERR_TIMEOUT if a bounded wait in a
+ * staged mapping (RMSNorm or LayerNorm) gave up since the last query (that launch's outputs are
  * then incomplete), RMS_ERR_CUDA if the stream reports an error, else
  * RMS_OK. */
 rms_status rms_last_device_status(void* stream);

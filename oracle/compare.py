@@ -22,6 +22,22 @@ cancel to ~0 (where a plain |err|/|ref| is ill-posed):
           itself a sum of signed terms)
 * dgamma: |e| <= tol * (|ref| + sum_i |dy x r|)
 
+LayerNorm keeps the per-dtype bars and adds a float32 term for what the
+method's float32 mean costs: x - mean cancels, so the rounding of the mean
+(relative to |x| + |mean|) reaches xhat multiplied by rstd.  With X = (|x| +
+|mean|) rstd standing for xhat before that cancellation (the fp64 LayerNorm
+oracle reports these scales):
+
+* y:      |e| <= bar(y) + 1e-5 (X |w| + |b|)
+* dx:     |e| <= bar(dx) + 1e-5 rstd (|g| + mean|g| + X mean(X |g|))
+* dw, db: the dgamma bar with scales sum_i |dy| X and sum_i |dy|
+* mean:   |e| <= 1e-5 (|ref| + mean|x|), rstd: rel <= 1e-5.  Both are float32
+          sums of up to a few hundred terms in sequence (a thread's share of
+          a row, then the tree): (L + depth) u <= ~1e-5 relative to the sum of
+          magnitudes, with u = 2^-24.
+
+bar() is RMSNorm's y/dx bar for the dtype (for f32: 1e-5 |ref|).
+
 Each check also reports the plain max abs / max rel error and the normwise
 relative error ||e|| / ||ref|| for information.
 """
@@ -113,3 +129,44 @@ def check_dgamma(got, ref, scale, dtype: str) -> Check:
     ref = np.asarray(ref, np.float64)
     tol = TOL[dtype]["dgamma"]
     return _check("dgamma", got, ref, tol * (np.abs(ref) + np.asarray(scale, np.float64)))
+
+
+# ---- LayerNorm ----
+LN_STAT_TOL = 1e-5
+
+
+def check_ln_y(got, ref, scale, dtype: str) -> Check:
+    ref = np.asarray(ref, np.float64)
+    extra = TOL["f32"]["y"] * np.asarray(scale, np.float64)
+    return _check("y", got, ref, _bar(ref, dtype, "y") + extra)
+
+
+def check_ln_mean(got, ref, abs_mean) -> Check:
+    ref = np.asarray(ref, np.float64)
+    return _check("mean", got, ref, LN_STAT_TOL * (np.abs(ref) + np.asarray(abs_mean, np.float64)))
+
+
+def check_ln_rstd(got, ref) -> Check:
+    ref = np.asarray(ref, np.float64)
+    return _check("rstd", got, ref, LN_STAT_TOL * np.abs(ref))
+
+
+def check_ln_dx(got, ref, scale, dtype: str) -> Check:
+    ref = np.asarray(ref, np.float64)
+    extra = TOL["f32"]["dx"] * np.asarray(scale, np.float64)
+    return _check("dx", got, ref, _bar(ref, dtype, "dx") + extra)
+
+
+def _bar(ref, dtype: str, what: str):
+    if dtype == "bf16":
+        return TOL["bf16"][what] * np.maximum(1.0, np.abs(ref))
+    if dtype == "f16":
+        return TOL["f16"][what] * (1.0 + np.abs(ref))
+    return TOL["f32"][what] * np.abs(ref)
+
+
+def check_ln_wsum(name: str, got, ref, scale, dtype: str) -> Check:
+    """dw or db (float32 sums over rows), at the dgamma bar."""
+    c = check_dgamma(got, ref, scale, dtype)
+    c.name = name
+    return c

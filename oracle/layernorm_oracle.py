@@ -36,24 +36,37 @@ def ln_stats(x, eps: float):
     return mean, 1.0 / np.sqrt(var + eps)
 
 
-def ln_forward(x, w, b, eps: float):
-    """y = (x − mean)·rstd·w + b (b may be None: no bias).  Returns (y, mean, rstd)."""
+def ln_forward(x, w, b, eps: float, with_scales: bool = False):
+    """y = (x − mean)·rstd·w + b (b may be None: no bias).  Returns (y, mean, rstd).
+
+    With ``with_scales`` also ``y_scale = X·|w| + |b|`` with ``X = (|x| +
+    |mean|)·rstd`` (the magnitudes of the terms y is made of before
+    x − mean and the bias cancel, for tolerances) and ``abs_mean = Σ|x|/N``
+    per row (the size of the terms of the mean).
+    """
     x = _f64(x)
     mean, rstd = ln_stats(x, eps)
     xhat = (x - mean[:, None]) * rstd[:, None]
     y = xhat * _f64(w)[None, :]
     if b is not None:
         y = y + _f64(b)[None, :]
-    return y, mean, rstd
+    if not with_scales:
+        return y, mean, rstd
+    X = (np.abs(x) + np.abs(mean)[:, None]) * rstd[:, None]
+    y_scale = X * np.abs(_f64(w))[None, :]
+    if b is not None:
+        y_scale = y_scale + np.abs(_f64(b))[None, :]
+    return y, mean, rstd, y_scale, np.mean(np.abs(x), axis=-1)
 
 
 def ln_backward(x, w, dy, eps: float, with_scales: bool = False):
     """Gradients of L = Σ dy ⊙ y: (dx, dw, db), from the [LN] § 3.0 closed form.
 
     With ``with_scales`` also the sizes of the terms each output is built
-    from, for tolerances where they cancel: ``dx_scale = rstd·(|ĝ| + |c2| +
-    |x̂|·mean|x̂ ĝ| + mean|ĝ|)`` and ``dw_scale = Σ_i |dy·x̂|``,
-    ``db_scale = Σ_i |dy|``.
+    from, for tolerances where they cancel, with ``X = (|x| + |mean|)·rstd``
+    standing for x̂ before x − mean cancels: ``dx_scale = rstd·(|ĝ| +
+    mean|ĝ| + X·mean(X·|ĝ|))``, ``dw_scale = Σ_i |dy|·X`` and ``db_scale =
+    Σ_i |dy|``.
     """
     x = _f64(x)
     dy = _f64(dy)
@@ -67,9 +80,10 @@ def ln_backward(x, w, dy, eps: float, with_scales: bool = False):
     db = np.sum(dy, axis=0)
     if not with_scales:
         return dx, dw, db
+    X = (np.abs(x) + np.abs(mean)[:, None]) * rstd[:, None]
     dx_scale = rstd[:, None] * (np.abs(gh) + np.mean(np.abs(gh), axis=-1)[:, None]
-                                + np.abs(xhat) * np.mean(np.abs(xhat * gh), axis=-1)[:, None])
-    dw_scale = np.sum(np.abs(dy * xhat), axis=0)
+                                + X * np.mean(X * np.abs(gh), axis=-1)[:, None])
+    dw_scale = np.sum(np.abs(dy) * X, axis=0)
     db_scale = np.sum(np.abs(dy), axis=0)
     return dx, dw, db, dx_scale, dw_scale, db_scale
 

@@ -8,6 +8,11 @@ missing, calls raise instead of falling back to anything else.
 
 Forward:  r = 1/sqrt(mean(x^2) + eps),  y = x * r * g  (g = gamma or 1+gamma)
 Backward: u = dy*g,  dx = r*u - x*r^3*mean(u*x),  dgamma = sum_rows dy*x*r
+
+LayerNorm on the same engine (ln_fwd / ln_bwd):
+  xhat = (x - mean)*rstd,  y = xhat*w + b
+  g = dy*w,  dx = (g - (xhat*mean(xhat*g) + mean(g)))*rstd,
+  dw = sum_rows dy*xhat,  db = sum_rows dy
 """
 from __future__ import annotations
 
@@ -108,6 +113,35 @@ def rms_bwd_noalloc(dy, x, gamma, rstd, dx, dgamma, gemma: int = 0, inplace_dx: 
                                _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_bwd_noalloc")
+
+
+def ln_fwd(x, w, b, y, mean, rstd, eps: float = 1e-5, stream=None, path="auto"):
+    """LayerNorm forward: y (M,N), mean and rstd (M,) float32 from x (M,N),
+    w (N,) and b (N,) or None (no bias)."""
+    M, N = x.shape
+    if b is not None and b.dtype != w.dtype:
+        raise ValueError("w and b must share one dtype")
+    st = lib().ln_fwd_ex(_ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(mean), _ptr(rstd), M, N,
+                         float(eps), dtype_code(x, w), _path(path), _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "ln_fwd")
+
+
+def ln_bwd(dy, x, w, mean, rstd, dx, dw, db, workspace, inplace_dx: int = 0, stream=None,
+           path="auto"):
+    """LayerNorm backward: dx (M,N); dw and db (N,) float32 (db may be None);
+    with inplace_dx=1 dx is written into dy (pass dx=None)."""
+    M, N = x.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().ln_bwd_ex(_ptr(dy), _ptr(x), _ptr(w), _ptr(mean), _ptr(rstd), _ptr(dx), _ptr(dw),
+                         _ptr(db), _ptr(workspace), ws_bytes, M, N, dtype_code(x, w),
+                         int(inplace_dx), _path(path), _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "ln_bwd")
+
+
+def ln_bwd_workspace_size(M: int, N: int) -> int:
+    return int(lib().ln_bwd_workspace_size(int(M), int(N)))
 
 
 def rms_bwd_workspace_size(M: int, N: int) -> int:

@@ -26,6 +26,14 @@ SIGNATURES = {
                            c_int, c_int, c_int, c_vp]),
     "rms_bwd_noalloc": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_int, c_int,
                                 c_int, c_vp]),
+    "ln_fwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_float, c_int, c_vp]),
+    "ln_fwd_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_float, c_int, c_int,
+                          c_vp]),
+    "ln_bwd": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_int,
+                       c_int, c_vp]),
+    "ln_bwd_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_i64,
+                          c_i64, c_int, c_int, c_int, c_vp]),
+    "ln_bwd_workspace_size": (c_size, [c_i64, c_i64]),
     "rms_bwd_workspace_size": (c_size, [c_i64, c_i64]),
     "rms_status_string": (ctypes.c_char_p, [c_int]),
     "rms_last_device_status": (c_int, [c_vp]),

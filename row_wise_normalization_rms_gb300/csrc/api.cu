@@ -311,9 +311,135 @@ rms_status rms_bwd(void* dy, const void* x, const void* gamma, const float* rstd
 
 rms_status rms_last_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return RMS_ERR_CUDA;
-  int v = 0;
+  int v = 0, w = 0;
   if (rmsi::take_device_status(&v) != cudaSuccess) return RMS_ERR_CUDA;
-  return v ? RMS_ERR_TIMEOUT : RMS_OK;
+  if (rmsi::take_ln_device_status(&w) != cudaSuccess) return RMS_ERR_CUDA;
+  return (v || w) ? RMS_ERR_TIMEOUT : RMS_OK;
+}
+
+size_t ln_bwd_workspace_size(int64_t M, int64_t N) {
+  if (M <= 0 || N <= 0) return 0;
+  DeviceInfo d;
+  if (!current_device(&d)) return 0;
+  return 2 * workspace_need(M, N, d);
+}
+
+rms_status ln_fwd_ex(const void* x, const void* w, const void* b, void* y, float* mean,
+                     float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype, rms_path path,
+                     void* stream) {
+  if (!valid_common(M, N, dtype, 0)) return RMS_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.f) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_SCALAR || path == RMS_PATH_STAGED)
+    return path == RMS_PATH_STAGED ? RMS_ERR_UNSUPPORTED : RMS_ERR_INVALID_ARG;
+  if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
+  if (M == 0) return RMS_OK;
+  if (!x || !w || !y || !mean || !rstd) return RMS_ERR_INVALID_ARG;
+  const int bsz = elem_bytes(dtype);
+  const size_t xb = matrix_bytes(M, N, bsz);
+  if (xb == 0) return RMS_ERR_INVALID_ARG;
+  const size_t wb = (size_t)N * rmsi::weight_bytes(dtype), rb = (size_t)M * sizeof(float);
+  const void* reads[3] = {x, w, b};
+  const size_t read_n[3] = {xb, wb, wb};
+  const void* writes[3] = {y, mean, rstd};
+  const size_t write_n[3] = {xb, rb, rb};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(writes[i], write_n[i], reads[j], read_n[j])) return RMS_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(writes[i], write_n[i], writes[j], write_n[j])) return RMS_ERR_INVALID_ARG;
+  }
+  DeviceInfo d;
+  if (!current_device(&d)) return RMS_ERR_CUDA;
+  const bool aligned = (N * bsz) % 16 == 0 && aligned16(x) && aligned16(w) && aligned16(y) &&
+                       (!b || aligned16(b));
+  Mapping m;
+  if (path == RMS_PATH_REGISTERS && !aligned) return RMS_ERR_ALIGNMENT;
+  if (!rmsi::ln_plan((int)N, dtype, false, path, aligned, d, &m)) return RMS_ERR_UNSUPPORTED;
+  if (m.path == rmsi::kScalar && M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
+  if (m.path == rmsi::kRegisters && (M + m.rows_per_cta - 1) / m.rows_per_cta > INT32_MAX)
+    return RMS_ERR_UNSUPPORTED;
+  rmsi::LnFwdArgs a{x, w, b, y, mean, rstd, M, (int)N, eps, (int)dtype};
+  if (rmsi::ln_launch_fwd(a, m, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return RMS_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return RMS_OK;
+}
+
+rms_status ln_fwd(const void* x, const void* w, const void* b, void* y, float* mean, float* rstd,
+                  int64_t M, int64_t N, float eps, rms_dtype dtype, void* stream) {
+  return ln_fwd_ex(x, w, b, y, mean, rstd, M, N, eps, dtype, RMS_PATH_AUTO, stream);
+}
+
+rms_status ln_bwd_ex(void* dy, const void* x, const void* w, const float* mean,
+                     const float* rstd, void* dx, float* dw, float* db, void* workspace,
+                     size_t workspace_bytes, int64_t M, int64_t N, rms_dtype dtype, int inplace_dx,
+                     rms_path path, void* stream) {
+  if (!valid_common(M, N, dtype, 0)) return RMS_ERR_INVALID_ARG;
+  if (inplace_dx != 0 && inplace_dx != 1) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_SCALAR) return RMS_ERR_INVALID_ARG;
+  if (path == RMS_PATH_REGISTERS) return RMS_ERR_UNSUPPORTED;
+  if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
+  if (inplace_dx) {
+    if (dx && dx != dy) return RMS_ERR_INVALID_ARG;
+    dx = dy;
+  }
+  if (!dw) return RMS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    if (cudaMemsetAsync(dw, 0, (size_t)N * sizeof(float), s) != cudaSuccess) return RMS_ERR_CUDA;
+    if (db && cudaMemsetAsync(db, 0, (size_t)N * sizeof(float), s) != cudaSuccess)
+      return RMS_ERR_CUDA;
+    return RMS_OK;
+  }
+  if (!dx || !dy || !x || !w || !mean || !rstd) return RMS_ERR_INVALID_ARG;
+  if (!workspace) return RMS_ERR_WORKSPACE;
+  const int bsz = elem_bytes(dtype);
+  const size_t xb = matrix_bytes(M, N, bsz);
+  if (xb == 0) return RMS_ERR_INVALID_ARG;
+  DeviceInfo d;
+  if (!current_device(&d)) return RMS_ERR_CUDA;
+  const size_t half = workspace_need(M, N, d);
+  if (workspace_bytes < 2 * half || ((uintptr_t)workspace & 255u) != 0) return RMS_ERR_WORKSPACE;
+  const size_t wb = (size_t)N * rmsi::weight_bytes(dtype), rb = (size_t)M * sizeof(float),
+               vb = (size_t)N * sizeof(float);
+  const void* reads[5] = {dy, x, w, mean, rstd};
+  const size_t read_n[5] = {xb, xb, wb, rb, rb};
+  const void* writes[4] = {dx, dw, db, workspace};
+  const size_t write_n[4] = {xb, vb, vb, 2 * half};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 5; ++j) {
+      if (i == 0 && j == 0 && dx == dy) continue;  // the sanctioned in-place alias
+      if (overlap(writes[i], write_n[i], reads[j], read_n[j])) return RMS_ERR_INVALID_ARG;
+    }
+    for (int j = i + 1; j < 4; ++j)
+      if (overlap(writes[i], write_n[i], writes[j], write_n[j])) return RMS_ERR_INVALID_ARG;
+  }
+  const bool aligned = (N * bsz) % 16 == 0 && aligned16(dy) && aligned16(x) && aligned16(w) &&
+                       aligned16(dx);
+  if (path == RMS_PATH_STAGED && !aligned) return RMS_ERR_ALIGNMENT;
+  Mapping m;
+  if (!rmsi::ln_plan((int)N, dtype, true, path, aligned, d, &m)) return RMS_ERR_UNSUPPORTED;
+  float* wsw = static_cast<float*>(workspace);
+  float* wsb = reinterpret_cast<float*>(static_cast<char*>(workspace) + half);
+  rmsi::LnBwdArgs a{dy, x, w, mean, rstd, dx, wsw, wsb, M, (int)N, (int)dtype};
+  if (rmsi::ln_size_bwd(a, d, &m) != cudaSuccess) return RMS_ERR_CUDA;
+  if ((size_t)m.partials * (size_t)N * sizeof(float) > half) return RMS_ERR_WORKSPACE;  // unreachable
+  if (rmsi::ln_launch_bwd(a, m, g_wait_limit.load(), s) != cudaSuccess) return RMS_ERR_CUDA;
+  if (rmsi::launch_colreduce(wsw, dw, m.partials, (int)N, s) != cudaSuccess) return RMS_ERR_CUDA;
+  int launches = 2;
+  if (db) {
+    if (rmsi::launch_colreduce(wsb, db, m.partials, (int)N, s) != cudaSuccess) return RMS_ERR_CUDA;
+    ++launches;
+  }
+  g_launches.fetch_add(launches);
+  return RMS_OK;
+}
+
+rms_status ln_bwd(void* dy, const void* x, const void* w, const float* mean, const float* rstd,
+                  void* dx, float* dw, float* db, void* workspace, int64_t M, int64_t N,
+                  rms_dtype dtype, int inplace_dx, void* stream) {
+  return ln_bwd_ex(dy, x, w, mean, rstd, dx, dw, db, workspace, SIZE_MAX, M, N, dtype, inplace_dx,
+                   RMS_PATH_AUTO, stream);
 }
 
 }  // extern "C"

@@ -54,6 +54,7 @@ struct Mapping {
   int stages = 0;        // shared-memory pipeline depth (staged path)
   int cluster = 1;       // CTAs per cluster sharing one row (staged path)
   int sv = 0;            // 16-byte vectors per CTA's column slice (staged path)
+  int smem_acc = 0;      // LayerNorm scalar backward: partials in shared memory
   size_t smem = 0;       // dynamic shared memory bytes
 };
 
@@ -85,6 +86,43 @@ cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m);
 cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s);
 // dgamma[j] = sum_{p < P} ws[p][j], p in increasing order.
 cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, cudaStream_t s);
+
+// ---- LayerNorm (layernorm.cu) ----
+struct LnFwdArgs {
+  const void* x;
+  const void* w;
+  const void* b;  // may be null: no bias
+  void* y;
+  float* mean;
+  float* rstd;
+  int64_t M;
+  int N;
+  float eps;
+  int dtype;
+};
+
+struct LnBwdArgs {
+  const void* dy;
+  const void* x;
+  const void* w;
+  const float* mean;
+  const float* rstd;
+  void* dx;   // == dy for in-place dx
+  float* wsw;  // [P][N] dw partials
+  float* wsb;  // [P][N] db partials
+  int64_t M;
+  int N;
+  int dtype;
+};
+
+// Chooses the LayerNorm mapping for a call (path as rms_path); false when
+// the requested path cannot take the shape.
+bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInfo& d, Mapping* m);
+cudaError_t ln_launch_fwd(const LnFwdArgs& a, const Mapping& m, cudaStream_t s);
+cudaError_t ln_size_bwd(const LnBwdArgs& a, const DeviceInfo& d, Mapping* m);
+cudaError_t ln_launch_bwd(const LnBwdArgs& a, const Mapping& m, long long wait_limit,
+                          cudaStream_t s);
+cudaError_t take_ln_device_status(int* status);
 
 // ---- staged path (staged.cu) ----
 bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m);

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for RMSNorm row workloads.
+"""Seeded synthetic inputs for RMSNorm and LayerNorm row workloads.
 
 Every tensor is drawn in float64 from numpy's SFC64 bit generator, seeded by
 ``SeedSequence([seed, tensor_id])`` so that x, gamma, dy and the row scales
@@ -29,7 +29,7 @@ from typing import Optional, Tuple
 
 import numpy as np
 
-_TENSOR_IDS = {"x": 1, "gamma": 2, "dy": 3, "row_scale": 4}
+_TENSOR_IDS = {"x": 1, "gamma": 2, "dy": 3, "row_scale": 4, "beta": 5}
 _CHUNK_ELEMS = 1 << 22
 
 Dist = Tuple[str, float, float]
@@ -37,7 +37,9 @@ Dist = Tuple[str, float, float]
 
 @dataclass(frozen=True)
 class Workload:
-    """One synthetic RMSNorm workload: shapes, dtype, eps, flags and input laws."""
+    """One synthetic workload: the operation ("rms" or "ln"), shapes, dtype,
+    eps, flags and input laws.  For LayerNorm ``gamma`` is the weight w and
+    ``beta`` the bias law (None: no bias)."""
 
     name: str
     M: int
@@ -52,6 +54,8 @@ class Workload:
     inplace_dx: int = 0
     seed: int = 0
     weight_dtype: str = ""  # "" (the activations' dtype) or "f32"
+    op: str = "rms"  # "rms" or "ln"
+    beta: Optional[Dist] = None  # LayerNorm bias law
     note: str = field(default="", compare=False)
 
     @property
@@ -107,8 +111,22 @@ WORKLOADS = {
                  note="the Llama-7B shape with a float32 weight (mixed precision)"),
         Workload("timing_f32_128x257", 128, 257, "f32", 1e-6,
                  note="the tutorial's timing shape, ragged N"),
-        Workload("layernorm_test_bf16_1151x8192", 1151, 8192, "bf16", 1e-5,
-                 note="the LayerNorm chapter's unit-test shape"),
+        Workload("rms_bf16_1151x8192", 1151, 8192, "bf16", 1e-5,
+                 note="RMSNorm at the LayerNorm chapter's unit-test shape"),
+        # LayerNorm: the chapter's unit test (1151 x 8192 fp16, x = -2.3 + 0.5 N(0,1),
+        # w, b ~ U(0,1), dy = 0.1 N(0,1), eps 1e-5) and its backward benchmark
+        # (M = 4096 fp16, N = 512 k for k = 2..31), plus the large-hidden shape.
+        Workload("ln_test_f16_1151x8192", 1151, 8192, "f16", 1e-5, op="ln",
+                 x=("normal", -2.3, 0.5), gamma=("uniform", 0.0, 1.0), beta=("uniform", 0.0, 1.0),
+                 dy=("normal", 0.0, 0.1), note="the LayerNorm chapter's unit test"),
+        *[Workload(f"ln_bench_f16_4096x{n}", 4096, n, "f16", 1e-5, op="ln",
+                   x=("normal", -2.3, 0.5), gamma=("uniform", 0.0, 1.0),
+                   beta=("uniform", 0.0, 1.0), dy=("normal", 0.0, 0.1),
+                   note="the LayerNorm chapter's backward benchmark")
+          for n in (1024, 4096, 8192, 15872)],
+        Workload("ln_wide_bf16_16384x8192", 16384, 8192, "bf16", 1e-5, op="ln",
+                 x=("normal", -2.3, 0.5), gamma=("uniform", 0.0, 1.0), beta=("uniform", 0.0, 1.0),
+                 dy=("normal", 0.0, 0.1), note="LayerNorm at the large-hidden shape"),
     ]
 }
 
@@ -189,8 +207,8 @@ def make_inputs(w: Workload) -> dict:
 
     Returns a dict with keys ``x``, ``gamma``, ``dy`` (float32 arrays for f32
     workloads, float16 arrays for f16 ones, uint16 bf16 bit patterns for bf16
-    ones) and ``row_scale``
-    (float64, or None).
+    ones), ``beta`` (the LayerNorm bias in the weight dtype, or None) and
+    ``row_scale`` (float64, or None).
     """
     scale = None
     if w.row_scale is not None:
@@ -198,9 +216,15 @@ def make_inputs(w: Workload) -> dict:
         _draw(_generator(w.seed, "row_scale"), w.row_scale, scale)
     gvals = np.empty(w.N, dtype=np.float64)
     _draw(_generator(w.seed, "gamma"), w.gamma, gvals)
+    beta = None
+    if w.beta is not None:
+        bvals = np.empty(w.N, dtype=np.float64)
+        _draw(_generator(w.seed, "beta"), w.beta, bvals)
+        beta = _store(bvals, w.wdtype)
     return {
         "x": _matrix(w, "x", w.x, scale),
         "gamma": _store(gvals, w.wdtype),
+        "beta": beta,
         "dy": _matrix(w, "dy", w.dy, None),
         "row_scale": scale,
     }

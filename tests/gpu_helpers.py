@@ -9,6 +9,7 @@ import torch
 
 import row_wise_normalization_rms_gb300 as rms
 from oracle import compare
+from oracle import layernorm_oracle as lno
 from oracle import rmsnorm_oracle as orc
 from synthetic import make_inputs, storage_to_float64
 
@@ -141,3 +142,98 @@ def assert_parity(w, inp, res: GpuResult, rows=None):
 
 def inputs_for(w):
     return make_inputs(w)
+
+
+# ---------------------------------------------------------------- LayerNorm
+
+
+@dataclass
+class LnResult:
+    y: torch.Tensor
+    mean: torch.Tensor
+    rstd: torch.Tensor
+    dx: torch.Tensor
+    dw: torch.Tensor
+    db: "torch.Tensor | None"
+    guards_ok: bool
+
+
+def run_ln(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None, with_db=True,
+           bias=True) -> LnResult:
+    """LayerNorm forward then backward through the C ABI on device copies of ``inp``."""
+    dt = tdtype(w.dtype)
+    M, N = w.M, w.N
+    inplace = w.inplace_dx if inplace is None else inplace
+    x = to_device(inp["x"], w.dtype)
+    g = to_device(inp["gamma"], w.wdtype)
+    b = to_device(inp["beta"], w.wdtype) if (bias and inp["beta"] is not None) else None
+    dy = to_device(inp["dy"], w.dtype)
+    y = Guarded((M, N), dt, _SENTINEL[w.dtype])
+    mean = Guarded((M,), torch.float32, _SENTINEL["f32"])
+    rstd = Guarded((M,), torch.float32, _SENTINEL["f32"])
+    dw = Guarded((N,), torch.float32, _SENTINEL["f32"])
+    db = Guarded((N,), torch.float32, _SENTINEL["f32"])
+    dx = None if inplace else Guarded((M, N), dt, _SENTINEL[w.dtype])
+    ws = torch.empty(max(rms.ln_bwd_workspace_size(M, N), 256), dtype=torch.uint8, device="cuda")
+    rms.ln_fwd(x, g, b, y.t, mean.t, rstd.t, w.eps, path=fwd_path or path)
+    rms.ln_bwd(dy, x, g, mean.t, rstd.t, None if inplace else dx.t, dw.t,
+               db.t if with_db else None, ws, inplace, path=bwd_path or path)
+    torch.cuda.synchronize()
+    assert rms.rms_last_device_status() == rms.RMS_OK
+    guards = all(t.guards_intact() for t in (y, mean, rstd, dw, db)) and (
+        inplace or dx.guards_intact())
+    if not with_db:  # db must be untouched
+        guards = guards and bool((db.t.view(torch.int32) == _SENTINEL["f32"]).all())
+    return LnResult(y.t, mean.t, rstd.t, dy if inplace else dx.t, dw.t,
+                    db.t if with_db else None, guards)
+
+
+def ln_oracle_rows(w, inp, rows, bias=True):
+    x = storage_to_float64(inp["x"][rows], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.wdtype)
+    b = storage_to_float64(inp["beta"], w.wdtype) if (bias and inp["beta"] is not None) else None
+    dy = storage_to_float64(inp["dy"][rows], w.dtype)
+    y, mean, rstd, ys, am = lno.ln_forward(x, g, b, w.eps, with_scales=True)
+    dx, _, _, dxs, _, _ = lno.ln_backward(x, g, dy, w.eps, with_scales=True)
+    return y, mean, rstd, ys, am, dx, dxs
+
+
+def ln_oracle_wsums(w, inp, block_rows: int = 1024):
+    """Oracle dw and db (and their scales) over all M rows, summed over row
+    blocks to bound host memory (each block is the oracle's column sum)."""
+    N = w.N
+    g = storage_to_float64(inp["gamma"], w.wdtype)
+    acc = [np.zeros(N) for _ in range(4)]
+    for r0 in range(0, w.M, block_rows):
+        r1 = min(w.M, r0 + block_rows)
+        x = storage_to_float64(inp["x"][r0:r1], w.dtype)
+        dy = storage_to_float64(inp["dy"][r0:r1], w.dtype)
+        _, dw, db, _, dws, dbs = lno.ln_backward(x, g, dy, w.eps, with_scales=True)
+        for a, v in zip(acc, (dw, db, dws, dbs)):
+            a += v
+    return tuple(acc)
+
+
+def ln_checks(w, inp, res: LnResult, rows=None, bias=True):
+    rows = np.arange(w.M) if rows is None else rows
+    y, mean, rstd, ys, am, dx, dxs = ln_oracle_rows(w, inp, rows, bias)
+    dw, db, dws, dbs = ln_oracle_wsums(w, inp)
+    idx = torch.as_tensor(rows, device=res.y.device)
+    checks = [
+        compare.check_ln_y(to_host64(res.y.index_select(0, idx)), y, ys, w.dtype),
+        compare.check_ln_mean(to_host64(res.mean.index_select(0, idx)), mean, am),
+        compare.check_ln_rstd(to_host64(res.rstd.index_select(0, idx)), rstd),
+        compare.check_ln_dx(to_host64(res.dx.index_select(0, idx)), dx, dxs, w.dtype),
+        compare.check_ln_wsum("dw", to_host64(res.dw), dw, dws, w.dtype),
+    ]
+    if res.db is not None:
+        checks.append(compare.check_ln_wsum("db", to_host64(res.db), db, dbs, w.dtype))
+    return checks
+
+
+def assert_ln_parity(w, inp, res: LnResult, rows=None, bias=True):
+    assert res.guards_ok, "a kernel wrote outside its output buffer"
+    checks = ln_checks(w, inp, res, rows, bias)
+    bad = [str(c) for c in checks if not c.ok]
+    assert not bad, f"{w.name}: " + "; ".join(bad)
+    return checks

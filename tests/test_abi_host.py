@@ -31,7 +31,7 @@ def lib():
 def declared_functions():
     text = HEADER.read_text()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(rms_\w+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b((?:rms|ln)_\w+)\s*\(", text)))
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -124,3 +124,52 @@ def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="no fallback"):
         _lib.load()
+
+
+def ln_f(lib, x=A, w=2 * A, b=3 * A, y=4 * A, mu=5 * A, r=6 * A, M=4, N=8, eps=1e-5, dtype=1,
+         path=0):
+    return lib.ln_fwd_ex(x, w, b, y, mu, r, M, N, eps, dtype, path, None)
+
+
+def test_ln_fwd_rejects_bad_arguments(lib):
+    assert ln_f(lib, dtype=5) == INVALID
+    assert ln_f(lib, M=-1) == INVALID
+    assert ln_f(lib, N=0) == INVALID
+    assert ln_f(lib, eps=float("nan")) == INVALID
+    assert ln_f(lib, eps=-1.0) == INVALID
+    assert ln_f(lib, path=9) == INVALID
+    assert ln_f(lib, path=2) == UNSUPPORTED  # no staged forward mapping
+    for k in ("x", "w", "y", "mu", "r"):
+        assert ln_f(lib, **{k: None}) == INVALID, k
+    assert ln_f(lib, N=1 << 40) == UNSUPPORTED
+
+
+def test_ln_fwd_rejects_overlap(lib):
+    assert ln_f(lib, y=A + 16) == INVALID        # y inside x
+    assert ln_f(lib, y=3 * A - 16) == INVALID    # y's tail runs into b
+    assert ln_f(lib, mu=4 * A + 4) == INVALID    # mean inside y
+    assert ln_f(lib, r=5 * A + 8) == INVALID     # rstd overlaps mean
+    assert ln_f(lib, mu=2 * A) == INVALID        # mean on w
+
+
+def test_ln_fwd_empty_batch_is_a_noop(lib):
+    assert ln_f(lib, M=0, x=None, w=None, b=None, y=None, mu=None, r=None) == OK
+
+
+def ln_b(lib, dy=A, x=2 * A, w=3 * A, mu=4 * A, r=5 * A, dx=6 * A, dw=7 * A, db=8 * A, ws=9 * A,
+         wsb=1 << 30, M=4, N=8, dtype=1, inplace=0, path=0):
+    return lib.ln_bwd_ex(dy, x, w, mu, r, dx, dw, db, ws, wsb, M, N, dtype, inplace, path, None)
+
+
+def test_ln_bwd_rejects_bad_arguments(lib):
+    assert ln_b(lib, dtype=7) == INVALID
+    assert ln_b(lib, inplace=3) == INVALID
+    assert ln_b(lib, M=-2) == INVALID
+    assert ln_b(lib, N=0) == INVALID
+    assert ln_b(lib, path=4) == INVALID
+    assert ln_b(lib, path=1) == UNSUPPORTED  # no register backward mapping
+    assert ln_b(lib, dw=None) == INVALID
+    for k in ("dy", "x", "w", "mu", "r", "dx"):
+        assert ln_b(lib, **{k: None}) == INVALID, k
+    assert ln_b(lib, inplace=1, dx=10 * A) == INVALID
+    assert ln_b(lib, ws=None) == WORKSPACE

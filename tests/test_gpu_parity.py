@@ -70,7 +70,7 @@ def test_gemma_and_inplace(M, N, dtype, gemma, inplace):
     H.assert_parity(w, inp, H.run_gpu(w, inp))
 
 
-FULL = [n for n in WORKLOADS] if torch.cuda.is_available() else []
+FULL = [n for n, w in WORKLOADS.items() if w.op == "rms"] if torch.cuda.is_available() else []
 
 
 @pytest.mark.parametrize("name", FULL)
