@@ -45,6 +45,14 @@ def step_bytes(M: int, N: int, b: int):
     return fwd, bwd
 
 
+def ln_step_bytes(M: int, N: int, b: int, wb: int, bias: bool):
+    """LayerNorm algorithmic bytes: fwd reads x, w (and b), writes y, mean and
+    rstd; bwd reads dy, x, w, mean and rstd, writes dx, dw and db."""
+    fwd = 2 * M * N * b + 8 * M + (2 if bias else 1) * N * wb
+    bwd = 3 * M * N * b + 8 * M + N * wb + 8 * N
+    return fwd, bwd
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -490,24 +498,44 @@ def run_sweep(args):
         set_bytes = 4 * M * N * b
         k = int(min(64, max(1, -(-3 * L2_BYTES // set_bytes))))
         x0, dy0, g = dev_t(inp["x"]), dev_t(inp["dy"]), dev_t(inp["gamma"], w.wdtype)
+        ln = w.op == "ln"
+        beta = dev_t(inp["beta"], w.wdtype) if ln and inp["beta"] is not None else None
         sets = []
         for i in range(k):
             sets.append((x0 if i == 0 else x0.clone(), dy0 if i == 0 else dy0.clone(),
                          torch.empty_like(x0), torch.empty_like(x0),
-                         torch.empty(M, device=dev)))
+                         torch.empty(M, device=dev), torch.empty(M, device=dev)))
         dg = torch.empty(N, device=dev)
-        ws = torch.empty(max(256, rms.rms_bwd_workspace_size(M, N)), dtype=torch.uint8, device=dev)
-        fwd_b, bwd_b = step_bytes(M, N, b)
+        db = torch.empty(N, device=dev)
+        ws_need = rms.ln_bwd_workspace_size(M, N) if ln else rms.rms_bwd_workspace_size(M, N)
+        ws = torch.empty(max(256, ws_need), dtype=torch.uint8, device=dev)
+        if ln:
+            wb = 4 if w.wdtype == "f32" else b
+            fwd_b, bwd_b = ln_step_bytes(M, N, b, wb, beta is not None)
+        else:
+            fwd_b, bwd_b = step_bytes(M, N, b)
         calls = max(args.steps, 2 * k)
         for path in paths:
-            def fwd_call(i):
-                x, dy, y, dx, r = sets[i % k]
-                rms.rms_fwd(x, g, y, r, w.eps, w.gemma, path=path)
+            if ln:
+                fpath, bpath = {"vector": ("registers", "staged")}.get(path, (path, path))
 
-            def bwd_call(i):
-                x, dy, y, dx, r = sets[i % k]
-                rms.rms_bwd(dy, x, g, r, None if w.inplace_dx else dx, dg, ws, w.gemma,
-                            w.inplace_dx, path=path)
+                def fwd_call(i):
+                    x, dy, y, dx, r, mu = sets[i % k]
+                    rms.ln_fwd(x, g, beta, y, mu, r, w.eps, path=fpath)
+
+                def bwd_call(i):
+                    x, dy, y, dx, r, mu = sets[i % k]
+                    rms.ln_bwd(dy, x, g, mu, r, None if w.inplace_dx else dx, dg, db, ws,
+                               w.inplace_dx, path=bpath)
+            else:
+                def fwd_call(i):
+                    x, dy, y, dx, r, _ = sets[i % k]
+                    rms.rms_fwd(x, g, y, r, w.eps, w.gemma, path=path)
+
+                def bwd_call(i):
+                    x, dy, y, dx, r, _ = sets[i % k]
+                    rms.rms_bwd(dy, x, g, r, None if w.inplace_dx else dx, dg, ws, w.gemma,
+                                w.inplace_dx, path=path)
 
             def timed(fn, n):
                 for i in range(max(3, args.warmup)):
@@ -531,7 +559,8 @@ def run_sweep(args):
             fg = fwd_b / (f_ms * 1e-3) / 1e9
             bg = bwd_b / (b_ms * 1e-3) / 1e9
             print(json.dumps({
-                "workload": name, "M": M, "N": N, "dtype": w.dtype, "weight_dtype": w.wdtype,
+                "workload": name, "op": w.op, "M": M, "N": N, "dtype": w.dtype,
+                "weight_dtype": w.wdtype,
                 "gemma": w.gemma,
                 "inplace_dx": w.inplace_dx, "path": path, "calls": calls, "buffer_sets": k,
                 "l2": ("rotating sets exceed 3x L2" if k * set_bytes >= 3 * L2_BYTES

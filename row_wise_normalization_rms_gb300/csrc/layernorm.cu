@@ -561,7 +561,23 @@ cudaError_t ln_size_bwd(const LnBwdArgs& a, const DeviceInfo& d, Mapping* m) {
       k = reinterpret_cast<const void*>(&rmsk::ln_bwd_scalar_kernel<T, W>);
     }
     int occ = 0;
-    cudaError_t e = ln_occupancy(k, d, m->threads, m->smem, &occ);
+    cudaError_t e;
+    if (m->path == kStaged) {
+      // CTAs per SM as registers allow (with the smallest ring), then the
+      // deepest ring that many CTAs can share.
+      const int64_t stage = (int64_t)m->smem - rmsk::kLnHeaderBytes;
+      const int64_t one = stage / m->stages;
+      e = ln_occupancy(k, d, m->threads, rmsk::kLnHeaderBytes + 3 * one, &occ);
+      if (e != cudaSuccess) return e;
+      if (occ < 1) return cudaErrorInvalidConfiguration;
+      const int cps = std::min<int>(occ, m->blocks);
+      const int64_t per = std::min<int64_t>(224 * 1024 / cps,
+                                            (int64_t)d.smem_optin - rmsk::kLnHeaderBytes);
+      m->stages = (int)std::max<int64_t>(3, std::min<int64_t>(8, per / one));
+      m->smem = rmsk::kLnHeaderBytes + (size_t)m->stages * one;
+      m->blocks = cps;
+    }
+    e = ln_occupancy(k, d, m->threads, m->smem, &occ);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t per_sm = m->path == kStaged ? std::min<int64_t>(occ, m->blocks) : occ;
