@@ -51,18 +51,22 @@ ln_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ w, const 
   pdl_trigger();
   pdl_wait();
 
-  uint4 xv[KV];
+  // The row is widened to float pairs once; the same registers then hold
+  // the centred values x - mean.
+  f32x2 xf[KV][NP];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * G;
-    xv[k] = (active && v < NV) ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 q = (active && v < NV) ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int i = 0; i < NP; ++i) xf[k][i] = P::get(q, i);
   }
   // mean
   f32x2 s2 = 0ull;
 #pragma unroll
   for (int k = 0; k < KV; ++k)
 #pragma unroll
-    for (int i = 0; i < NP; ++i) s2 = add2(s2, P::get(xv[k], i));
+    for (int i = 0; i < NP; ++i) s2 = add2(s2, xf[k][i]);
   const float mean = group_sum(lo2(s2) + hi2(s2), G, grp * (G >> 5), red_a) / (float)N;
   // variance of the centred values (padding lanes and columns excluded)
   const f32x2 nm = splat2(-mean);
@@ -73,8 +77,8 @@ ln_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ w, const 
     if (active && v < NV) {
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
-        const f32x2 d = add2(P::get(xv[k], i), nm);
-        q2 = fma2(d, d, q2);
+        xf[k][i] = add2(xf[k][i], nm);
+        q2 = fma2(xf[k][i], xf[k][i], q2);
       }
     }
   }
@@ -96,7 +100,7 @@ ln_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ w, const 
       uint32_t o[4];
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
-        const f32x2 xh = mul2(add2(P::get(xv[k], i), nm), rr);
+        const f32x2 xh = mul2(xf[k][i], rr);
         const f32x2 yy = fma2(xh, wv.pair(i), bv.pair(i));  // + 0 without a bias
         if constexpr (sizeof(T) == 2) {
           o[i] = Half2Ops<T>::narrow(yy);
@@ -168,7 +172,7 @@ constexpr int kLnHeaderBytes = 1024;
 // barrier, second pass (dx); a stage is refilled one barrier after its
 // second pass.  Two row sums travel together (c1 and c2).
 template <typename T, typename W, int KV>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(512, 1)
 ln_bwd_staged_kernel(const LnStagedParams p) {
   using P = Pairs<T>;
   using GV = GammaVec<T, W>;
@@ -219,12 +223,15 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
     for (; issued < pre; ++issued) issue(issued);
   }
 
-  GV wv[KV];
+  // With four vectors per thread the weight is re-read through L1 at each
+  // use (the partials already take 64 registers); otherwise it is held.
+  constexpr bool kHoldW = KV < 4;
+  GV wv[kHoldW ? KV : 1];
   f32x2 accw[KV][NP], accb[KV][NP];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * p.G;
-    wv[k] = v < NV ? GV::load(p.w, v) : GV::zero();
+    if (kHoldW) wv[k] = v < NV ? GV::load(p.w, v) : GV::zero();
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
       accw[k][i] = 0ull;
@@ -232,6 +239,18 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
     }
   }
 
+  // The row statistics are fetched one tile ahead, off the critical path.
+  auto stats = [&](int64_t t, float& m, float& r) {
+    const int64_t rw = (blockIdx.x + t * gridDim.x) * p.R + q;
+    m = 0.f;
+    r = 0.f;
+    if (t < my_tiles && rw < p.M) {
+      m = p.mean[rw];
+      r = p.rstd[rw];
+    }
+  };
+  float mu_next, rs_next;
+  stats(0, mu_next, rs_next);
   int64_t i = 0;
   bool aborted = false;
   for (; i < my_tiles; ++i) {
@@ -239,8 +258,8 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
     const int buf = (int)(i & 1);
     const int64_t row = (blockIdx.x + i * gridDim.x) * p.R + q;
     const bool active = row < p.M;
-    const float mu = active ? p.mean[row] : 0.f;
-    const float rs = active ? p.rstd[row] : 0.f;
+    const float mu = mu_next, rs = rs_next;
+    stats(i + 1, mu_next, rs_next);
     if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) abort_flag[buf] = 1;
 
     const uint32_t xs = smem_u32(stages + (size_t)s * p.stage_bytes) + row_off;
@@ -253,11 +272,12 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
         const int v = lig + k * p.G;
         if (v < NV) {
           const uint4 xq = lds128(xs + 16u * v), dq = lds128(ds + 16u * v);
+          const GV wk = kHoldW ? wv[k] : GV::load(p.w, v);
 #pragma unroll
           for (int e = 0; e < NP; ++e) {
             const f32x2 xh = mul2(add2(P::get(xq, e), nm), rr);
             const f32x2 d = P::get(dq, e);
-            const f32x2 g = mul2(d, wv[k].pair(e));
+            const f32x2 g = mul2(d, wk.pair(e));
             s1 = fma2(xh, g, s1);
             s2 = add2(s2, g);
             accw[k][e] = fma2(d, xh, accw[k][e]);
@@ -289,11 +309,12 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
         const int v = lig + k * p.G;
         if (v < NV) {
           const uint4 xq = lds128(xs + 16u * v), dq = lds128(ds + 16u * v);
+          const GV wk = kHoldW ? wv[k] : GV::load(p.w, v);
           uint32_t o[4];
 #pragma unroll
           for (int e = 0; e < NP; ++e) {
             const f32x2 xh = mul2(add2(P::get(xq, e), nm), rr);
-            const f32x2 g = mul2(P::get(dq, e), wv[k].pair(e));
+            const f32x2 g = mul2(P::get(dq, e), wk.pair(e));
             // (g - (xhat*c1 + c2)) * rstd
             const f32x2 dxe = mul2(add2(fma2(xh, c1, g), c2), rr);
             if constexpr (sizeof(T) == 2) {
@@ -482,13 +503,16 @@ bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInf
     }
   }
   if (bwd && (path == kAuto || path == kStaged) && vec_ok) {
-    // At most two vectors per thread: dw and db partials both live in registers.
-    int kv = NV <= 32 ? 1 : 2;
-    int G = ((NV + kv - 1) / kv + 31) / 32 * 32;
+    // At most four vectors per thread: the dw and db partials of a thread's
+    // columns live in registers (at most 128 a thread).  CTAs of up to 256
+    // threads (two per SM) where the row allows, else one row of up to 512
+    // threads (32 KiB rows) and one CTA per SM.
+    const int kv = NV <= 32 ? 1 : NV <= 64 ? 2 : 4;
+    const int G = ((NV + kv - 1) / kv + 31) / 32 * 32;
     if (G <= 512) {
       int R = (int)(16384 / row_bytes);
       R = std::max(1, std::min(R, 16));
-      while (R > 1 && G * R > 512) --R;
+      while (R > 1 && G * R > 256) --R;
       const int64_t stage = 2 * (int64_t)R * row_bytes;
       const int64_t budget = 224 * 1024, cap = (int64_t)d.smem_optin - rmsk::kLnHeaderBytes;
       int cps = 0, S = 0;
@@ -555,8 +579,9 @@ cudaError_t ln_size_bwd(const LnBwdArgs& a, const DeviceInfo& d, Mapping* m) {
     using W = std::remove_pointer_t<decltype(wp)>;
     const void* k;
     if (m->path == kStaged) {
-      k = m->kv == 1 ? reinterpret_cast<const void*>(&rmsk::ln_bwd_staged_kernel<T, W, 1>)
-                     : reinterpret_cast<const void*>(&rmsk::ln_bwd_staged_kernel<T, W, 2>);
+      k = m->kv == 1   ? reinterpret_cast<const void*>(&rmsk::ln_bwd_staged_kernel<T, W, 1>)
+          : m->kv == 2 ? reinterpret_cast<const void*>(&rmsk::ln_bwd_staged_kernel<T, W, 2>)
+                       : reinterpret_cast<const void*>(&rmsk::ln_bwd_staged_kernel<T, W, 4>);
     } else {
       k = reinterpret_cast<const void*>(&rmsk::ln_bwd_scalar_kernel<T, W>);
     }
@@ -619,7 +644,9 @@ cudaError_t ln_launch_bwd(const LnBwdArgs& a, const Mapping& m, long long wait_l
       const dim3 grid((unsigned)m.blocks), block(m.threads);
       if (m.kv == 1)
         return rmsk::launch_pdl(rmsk::ln_bwd_staged_kernel<T, W, 1>, grid, block, m.smem, s, p);
-      return rmsk::launch_pdl(rmsk::ln_bwd_staged_kernel<T, W, 2>, grid, block, m.smem, s, p);
+      if (m.kv == 2)
+        return rmsk::launch_pdl(rmsk::ln_bwd_staged_kernel<T, W, 2>, grid, block, m.smem, s, p);
+      return rmsk::launch_pdl(rmsk::ln_bwd_staged_kernel<T, W, 4>, grid, block, m.smem, s, p);
     }
     return rmsk::launch_pdl(rmsk::ln_bwd_scalar_kernel<T, W>, dim3((unsigned)m.blocks), dim3(256),
                             m.smem, s, static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
