@@ -30,13 +30,28 @@ namespace rmsk {
 // Nonzero once a bounded wait in a LayerNorm kernel gave up.
 __device__ int g_ln_device_status = 0;
 
+// Sum over a group of G threads (G a multiple of 32; warps [first_warp,
+// first_warp + G/32) of the CTA), every thread of the CTA calling: warp
+// butterflies, one barrier, then each warp reduces the per-warp sums with a
+// second butterfly, so all threads of the group get identical bits.  `red`
+// holds one float per warp of the CTA.
+__device__ __forceinline__ float ln_group_sum(float v, int G, int first_warp, float* red) {
+  v = warp_sum(v);
+  if (G == 32) return v;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return warp_sum(lane < (G >> 5) ? red[first_warp + lane] : 0.f);
+}
+
 // ---------------------------------------------------------------- forward
 
 template <typename T, typename W, int KV>
 __global__ void __launch_bounds__(1024)
 ln_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ w, const W* __restrict__ b,
                         T* __restrict__ y, float* __restrict__ mean_out,
-                        float* __restrict__ rstd_out, int64_t M, int N, float eps, int G) {
+                        float* __restrict__ rstd_out, int64_t M, int N, float inv_n, float eps,
+                        int G) {
   using P = Pairs<T>;
   using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
@@ -67,7 +82,7 @@ ln_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ w, const 
   for (int k = 0; k < KV; ++k)
 #pragma unroll
     for (int i = 0; i < NP; ++i) s2 = add2(s2, xf[k][i]);
-  const float mean = group_sum(lo2(s2) + hi2(s2), G, grp * (G >> 5), red_a) / (float)N;
+  const float mean = ln_group_sum(lo2(s2) + hi2(s2), G, grp * (G >> 5), red_a) * inv_n;
   // variance of the centred values (padding lanes and columns excluded)
   const f32x2 nm = splat2(-mean);
   f32x2 q2 = 0ull;
@@ -82,7 +97,7 @@ ln_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ w, const 
       }
     }
   }
-  const float var = group_sum(lo2(q2) + hi2(q2), G, grp * (G >> 5), red_b) / (float)N;
+  const float var = ln_group_sum(lo2(q2) + hi2(q2), G, grp * (G >> 5), red_b) * inv_n;
   const float rstd = 1.0f / sqrtf(var + eps);
   if (!active) return;  // no barrier follows
   if (lig == 0) {
@@ -118,7 +133,7 @@ template <typename T, typename W>
 __global__ void __launch_bounds__(256)
 ln_fwd_scalar_kernel(const T* __restrict__ x, const W* __restrict__ w, const W* __restrict__ b,
                      T* __restrict__ y, float* __restrict__ mean_out, float* __restrict__ rstd_out,
-                     int64_t M, int N, float eps) {
+                     int64_t M, int N, float inv_n, float eps) {
   using E = Elem<T>;
   __shared__ float red_a[8], red_b[8];
   const int64_t row = blockIdx.x;
@@ -127,13 +142,13 @@ ln_fwd_scalar_kernel(const T* __restrict__ x, const W* __restrict__ w, const W* 
   pdl_wait();
   float s = 0.f;
   for (int j = threadIdx.x; j < N; j += 256) s += E::to_f(xr[j]);
-  const float mean = group_sum(s, 256, 0, red_a) / (float)N;
+  const float mean = group_sum(s, 256, 0, red_a) * inv_n;
   float q = 0.f;
   for (int j = threadIdx.x; j < N; j += 256) {
     const float d = E::to_f(xr[j]) - mean;
     q = fmaf(d, d, q);
   }
-  const float rstd = 1.0f / sqrtf(group_sum(q, 256, 0, red_b) / (float)N + eps);
+  const float rstd = 1.0f / sqrtf(group_sum(q, 256, 0, red_b) * inv_n + eps);
   if (threadIdx.x == 0) {
     mean_out[row] = mean;
     rstd_out[row] = rstd;
@@ -159,6 +174,7 @@ struct LnStagedParams {
   float* wsb;  // [grid][N] db partials
   int64_t M;
   int N;
+  float inv_n;  // 1/N rounded to float
   int G, R, S;
   int64_t ntiles;
   uint32_t tile_bytes, stage_bytes;
@@ -205,11 +221,13 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
 
   uint64_t pol = 0;
   int64_t issued = 0;  // thread 0 only
+  int issue_stage = 0;  // issued % S, thread 0 only
   auto issue = [&](int64_t i) {
     const int64_t row0 = (blockIdx.x + i * gridDim.x) * p.R;
     const int64_t rows = min((int64_t)p.R, p.M - row0);
     const uint32_t bytes = (uint32_t)(rows * row_bytes);
-    const int s = (int)(i % p.S);
+    const int s = issue_stage;
+    issue_stage = issue_stage + 1 == p.S ? 0 : issue_stage + 1;
     const uint32_t bar = smem_u32(&full[s]);
     const uint32_t dst = smem_u32(stages + (size_t)s * p.stage_bytes);
     mbar_arrive_expect_tx(bar, 2 * bytes);
@@ -240,8 +258,10 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
   }
 
   // The row statistics are fetched one tile ahead, off the critical path.
-  auto stats = [&](int64_t t, float& m, float& r) {
-    const int64_t rw = (blockIdx.x + t * gridDim.x) * p.R + q;
+  // Rows advance by a fixed step; the stage and its parity are counters.
+  const int64_t row_step = (int64_t)gridDim.x * p.R;
+  int64_t row = (int64_t)blockIdx.x * p.R + q;
+  auto stats = [&](int64_t t, int64_t rw, float& m, float& r) {
     m = 0.f;
     r = 0.f;
     if (t < my_tiles && rw < p.M) {
@@ -250,17 +270,17 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
     }
   };
   float mu_next, rs_next;
-  stats(0, mu_next, rs_next);
+  stats(0, row, mu_next, rs_next);
+  int s = 0;
+  uint32_t parity = 0;
   int64_t i = 0;
   bool aborted = false;
-  for (; i < my_tiles; ++i) {
-    const int s = (int)(i % p.S);
+  for (; i < my_tiles; ++i, row += row_step, s = (s + 1 == p.S) ? 0 : s + 1, parity ^= (s == 0)) {
     const int buf = (int)(i & 1);
-    const int64_t row = (blockIdx.x + i * gridDim.x) * p.R + q;
     const bool active = row < p.M;
     const float mu = mu_next, rs = rs_next;
-    stats(i + 1, mu_next, rs_next);
-    if (!mbar_wait(smem_u32(&full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) abort_flag[buf] = 1;
+    stats(i + 1, row + row_step, mu_next, rs_next);
+    if (!mbar_wait(smem_u32(&full[s]), parity, p.wait_limit)) abort_flag[buf] = 1;
 
     const uint32_t xs = smem_u32(stages + (size_t)s * p.stage_bytes) + row_off;
     const uint32_t ds = xs + p.tile_bytes;
@@ -295,13 +315,14 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
       break;
     }
     if (threadIdx.x == 0 && i >= 1 && issued < my_tiles) issue(issued++);
-    float t1 = 0.f, t2 = 0.f;
-    for (int ww = 0; ww < nw; ++ww) {
-      const float2 v = red[buf * 32 + first_warp + ww];
-      t1 += v.x;
-      t2 += v.y;
+    float t1, t2;
+    {
+      const int lane = threadIdx.x & 31;
+      const float2 v = lane < nw ? red[buf * 32 + first_warp + lane] : make_float2(0.f, 0.f);
+      t1 = warp_sum(v.x);
+      t2 = warp_sum(v.y);
     }
-    const f32x2 c1 = splat2(-t1 / (float)p.N), c2 = splat2(-t2 / (float)p.N);
+    const f32x2 c1 = splat2(-t1 * p.inv_n), c2 = splat2(-t2 * p.inv_n);
     if (active) {
       uint4* out = reinterpret_cast<uint4*>(p.dx) + row * (int64_t)NV;
 #pragma unroll
@@ -394,7 +415,7 @@ __global__ void __launch_bounds__(256)
 ln_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__ w,
                      const float* __restrict__ mean, const float* __restrict__ rstd, T* dx,
                      float* __restrict__ wsw, float* __restrict__ wsb, int64_t M, int N,
-                     int acc_in_smem) {
+                     float inv_n, int acc_in_smem) {
   using E = Elem<T>;
   __shared__ float red[2][2][8];
   // dw and db partials of this CTA, column j owned by thread j % 256: in
@@ -422,8 +443,8 @@ ln_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__
       accw[j] = fmaf(d, xh, accw[j]);
       accb[j] += d;
     }
-    const float c1 = group_sum(s1, 256, 0, red[it & 1][0]) / (float)N;
-    const float c2 = group_sum(s2, 256, 0, red[it & 1][1]) / (float)N;
+    const float c1 = group_sum(s1, 256, 0, red[it & 1][0]) * inv_n;
+    const float c2 = group_sum(s2, 256, 0, red[it & 1][1]) * inv_n;
     T* out = dx + row * N;
     for (int j = threadIdx.x; j < N; j += 256) {
       const float xh = (E::to_f(xr[j]) - mu) * rs;
@@ -560,16 +581,17 @@ cudaError_t ln_launch_fwd(const LnFwdArgs& a, const Mapping& m, cudaStream_t s) 
     const W* w = static_cast<const W*>(a.w);
     const W* b = static_cast<const W*>(a.b);
     T* y = static_cast<T*>(a.y);
+    const float inv_n = (float)(1.0 / a.N);
     if (m.path == kRegisters) {
       const dim3 grid((unsigned)((a.M + m.rows_per_cta - 1) / m.rows_per_cta)), block(m.threads);
       switch (m.kv) {
-        case 1: return rmsk::launch_pdl(rmsk::ln_fwd_registers_kernel<T, W, 1>, grid, block, 0, s, x, w, b, y, a.mean, a.rstd, a.M, a.N, a.eps, m.G);
-        case 2: return rmsk::launch_pdl(rmsk::ln_fwd_registers_kernel<T, W, 2>, grid, block, 0, s, x, w, b, y, a.mean, a.rstd, a.M, a.N, a.eps, m.G);
-        default: return rmsk::launch_pdl(rmsk::ln_fwd_registers_kernel<T, W, 4>, grid, block, 0, s, x, w, b, y, a.mean, a.rstd, a.M, a.N, a.eps, m.G);
+        case 1: return rmsk::launch_pdl(rmsk::ln_fwd_registers_kernel<T, W, 1>, grid, block, 0, s, x, w, b, y, a.mean, a.rstd, a.M, a.N, inv_n, a.eps, m.G);
+        case 2: return rmsk::launch_pdl(rmsk::ln_fwd_registers_kernel<T, W, 2>, grid, block, 0, s, x, w, b, y, a.mean, a.rstd, a.M, a.N, inv_n, a.eps, m.G);
+        default: return rmsk::launch_pdl(rmsk::ln_fwd_registers_kernel<T, W, 4>, grid, block, 0, s, x, w, b, y, a.mean, a.rstd, a.M, a.N, inv_n, a.eps, m.G);
       }
     }
     return rmsk::launch_pdl(rmsk::ln_fwd_scalar_kernel<T, W>, dim3((unsigned)a.M), dim3(256), 0, s,
-                            x, w, b, y, a.mean, a.rstd, a.M, a.N, a.eps);
+                            x, w, b, y, a.mean, a.rstd, a.M, a.N, inv_n, a.eps);
   });
 }
 
@@ -634,6 +656,7 @@ cudaError_t ln_launch_bwd(const LnBwdArgs& a, const Mapping& m, long long wait_l
       p.wsb = a.wsb;
       p.M = a.M;
       p.N = a.N;
+      p.inv_n = (float)(1.0 / a.N);
       p.G = m.G;
       p.R = m.rows_per_cta;
       p.S = m.stages;
@@ -651,7 +674,7 @@ cudaError_t ln_launch_bwd(const LnBwdArgs& a, const Mapping& m, long long wait_l
     return rmsk::launch_pdl(rmsk::ln_bwd_scalar_kernel<T, W>, dim3((unsigned)m.blocks), dim3(256),
                             m.smem, s, static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
                             static_cast<const W*>(a.w), a.mean, a.rstd, static_cast<T*>(a.dx),
-                            a.wsw, a.wsb, a.M, a.N, m.smem_acc);
+                            a.wsw, a.wsb, a.M, a.N, (float)(1.0 / a.N), m.smem_acc);
   });
 }
 

@@ -218,12 +218,13 @@ rms_fwd_staged_kernel(const StagedParams p) {
 
   int64_t i = 0;
   bool aborted = false;
-  for (; i < my_tiles; ++i) {
-    const int s = (int)(i % p.S);
+  int s = 0;               // i % S, kept as a counter (no 64-bit division per tile)
+  uint32_t parity = 0;     // (i / S) & 1
+  for (; i < my_tiles; ++i, s = (s + 1 == p.S) ? 0 : s + 1, parity ^= (s == 0)) {
     const int buf = (int)(i & 1);
     const int64_t row = (sl.unit + i * sl.units) * p.R + q;
     const bool active = row < p.M;
-    if (!mbar_wait(smem_u32(&h.full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) h.abort[buf] = 1;
+    if (!mbar_wait(smem_u32(&h.full[s]), parity, p.wait_limit)) h.abort[buf] = 1;
 
     const uint32_t xs = smem_u32(h.stages + (size_t)s * p.stage_bytes) + row_off;
     f32x2 ss2 = 0ull;
@@ -301,13 +302,14 @@ rms_bwd_staged_kernel(const StagedParams p) {
 
   int64_t i = 0;
   bool aborted = false;
-  for (; i < my_tiles; ++i) {
-    const int s = (int)(i % p.S);
+  int s = 0;               // i % S, kept as a counter (no 64-bit division per tile)
+  uint32_t parity = 0;     // (i / S) & 1
+  for (; i < my_tiles; ++i, s = (s + 1 == p.S) ? 0 : s + 1, parity ^= (s == 0)) {
     const int buf = (int)(i & 1);
     const int64_t row = (sl.unit + i * sl.units) * p.R + q;
     const bool active = row < p.M;
     const float r = active ? p.rstd_in[row] : 0.f;
-    if (!mbar_wait(smem_u32(&h.full[s]), (uint32_t)((i / p.S) & 1), p.wait_limit)) h.abort[buf] = 1;
+    if (!mbar_wait(smem_u32(&h.full[s]), parity, p.wait_limit)) h.abort[buf] = 1;
 
     const uint32_t xs = smem_u32(h.stages + (size_t)s * p.stage_bytes) + row_off;
     const uint32_t ds = xs + p.tile_bytes;
