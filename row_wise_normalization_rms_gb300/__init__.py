@@ -19,11 +19,11 @@ from __future__ import annotations
 from . import _lib
 
 RMS_F32, RMS_BF16, RMS_F16, RMS_BF16_W32, RMS_F16_W32 = 0, 1, 2, 3, 4
-RMS_PATH_AUTO, RMS_PATH_REGISTERS, RMS_PATH_STAGED, RMS_PATH_SCALAR = 0, 1, 2, 3
+RMS_PATH_AUTO, RMS_PATH_REGISTERS, RMS_PATH_STAGED, RMS_PATH_SCALAR, RMS_PATH_CHUNKED = 0, 1, 2, 3, 4
 (RMS_OK, RMS_ERR_INVALID_ARG, RMS_ERR_UNSUPPORTED, RMS_ERR_ALIGNMENT, RMS_ERR_WORKSPACE,
  RMS_ERR_CUDA, RMS_ERR_TIMEOUT) = range(7)
 PATHS = {"auto": RMS_PATH_AUTO, "registers": RMS_PATH_REGISTERS, "staged": RMS_PATH_STAGED,
-         "scalar": RMS_PATH_SCALAR}
+         "scalar": RMS_PATH_SCALAR, "chunked": RMS_PATH_CHUNKED}
 
 __all__ = [
     "RmsError", "lib", "rms_fwd", "rms_bwd", "rms_bwd_noalloc", "rms_bwd_workspace_size",

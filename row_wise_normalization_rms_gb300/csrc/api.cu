@@ -93,6 +93,8 @@ size_t workspace_need(int64_t M, int64_t N, const DeviceInfo& d) {
 // copy pipeline as soon as rows exceed 1 KiB.
 constexpr int64_t kAutoStagedRowBytesFwd = 16384;
 constexpr int64_t kAutoStagedRowBytesBwd = 1024;
+constexpr int kAutoChunkedClusterFwd = 4;
+constexpr int kAutoChunkedClusterBwd = 8;
 
 bool prefer_staged(int N, int dtype, bool bwd) {
   const int64_t row = (int64_t)N * elem_bytes(dtype);
@@ -105,10 +107,18 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
                   Mapping* m) {
   switch (path) {
     case RMS_PATH_AUTO:
-      if (aligned && prefer_staged(N, dtype, bwd) && rmsi::plan_staged(N, dtype, bwd, d, m))
+      if (aligned && prefer_staged(N, dtype, bwd) && rmsi::plan_staged(N, dtype, bwd, d, m)) {
+        // A row split over many CTAs of a cluster serialises on the per-row
+        // exchange; from 4 (fwd) / 8 (bwd) CTAs the chunked mapping's extra
+        // pass over the row costs less (GB300, N = 65536 .. 131072 bf16).
+        if (m->cluster >= (bwd ? kAutoChunkedClusterBwd : kAutoChunkedClusterFwd) &&
+            rmsi::plan_chunked(N, dtype, m))
+          return RMS_OK;
         return RMS_OK;
+      }
       if (aligned && rmsi::plan_registers(N, dtype, bwd, m)) return RMS_OK;
       if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m)) return RMS_OK;
+      if (aligned && rmsi::plan_chunked(N, dtype, m)) return RMS_OK;
       if (rmsi::plan_scalar(N, dtype, bwd, d, m)) return RMS_OK;
       return RMS_ERR_UNSUPPORTED;
     case RMS_PATH_REGISTERS:
@@ -119,6 +129,9 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
       return rmsi::plan_staged(N, dtype, bwd, d, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     case RMS_PATH_SCALAR:
       return rmsi::plan_scalar(N, dtype, bwd, d, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
+    case RMS_PATH_CHUNKED:
+      if (!aligned) return RMS_ERR_ALIGNMENT;
+      return rmsi::plan_chunked(N, dtype, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     default:
       return RMS_ERR_INVALID_ARG;
   }
@@ -179,7 +192,7 @@ rms_status rms_fwd_ex(const void* x, const void* gamma, void* y, float* rstd, in
                       void* stream) {
   if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.f) return RMS_ERR_INVALID_ARG;
-  if (path < RMS_PATH_AUTO || path > RMS_PATH_SCALAR) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
   if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
   if (M == 0) return RMS_OK;
   if (!x || !gamma || !y || !rstd) return RMS_ERR_INVALID_ARG;
@@ -209,6 +222,10 @@ rms_status rms_fwd_ex(const void* x, const void* gamma, void* y, float* rstd, in
     case rmsi::kStaged:
       e = rmsi::launch_fwd_staged(a, m, d, g_wait_limit.load(), s);
       break;
+    case rmsi::kChunked:
+      e = rmsi::launch_fwd_chunked(a, m, d, s);
+      if (e == cudaSuccess) g_launches.fetch_add(1);  // two kernels
+      break;
     default:
       if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
       e = rmsi::launch_fwd_scalar(a, m, s);
@@ -230,7 +247,7 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
                       void* stream) {
   if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
   if (inplace_dx != 0 && inplace_dx != 1) return RMS_ERR_INVALID_ARG;
-  if (path < RMS_PATH_AUTO || path > RMS_PATH_SCALAR) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
   if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
   if (inplace_dx) {
     if (dx && dx != dy) return RMS_ERR_INVALID_ARG;
@@ -289,6 +306,13 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
       e = rmsi::size_bwd_staged(a, d, &m);
       if (e == cudaSuccess) e = rmsi::launch_bwd_staged(a, m, d, g_wait_limit.load(), s);
       break;
+    case rmsi::kChunked: {
+      float* kbuf = nullptr;
+      if (!rmsi::size_bwd_chunked(a, d, &m, &kbuf)) return RMS_ERR_UNSUPPORTED;
+      e = rmsi::launch_bwd_chunked(a, m, kbuf, d, s);
+      if (e == cudaSuccess) g_launches.fetch_add(1);  // three kernels
+      break;
+    }
     default:
       e = rmsi::size_bwd_scalar(a, d, &m);
       if (e == cudaSuccess) e = rmsi::launch_bwd_scalar(a, m, s);
@@ -329,8 +353,8 @@ rms_status ln_fwd_ex(const void* x, const void* w, const void* b, void* y, float
                      void* stream) {
   if (!valid_common(M, N, dtype, 0)) return RMS_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.f) return RMS_ERR_INVALID_ARG;
-  if (path < RMS_PATH_AUTO || path > RMS_PATH_SCALAR || path == RMS_PATH_STAGED)
-    return path == RMS_PATH_STAGED ? RMS_ERR_UNSUPPORTED : RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
+  if (path == RMS_PATH_STAGED || path == RMS_PATH_CHUNKED) return RMS_ERR_UNSUPPORTED;
   if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
   if (M == 0) return RMS_OK;
   if (!x || !w || !y || !mean || !rstd) return RMS_ERR_INVALID_ARG;
@@ -376,8 +400,8 @@ rms_status ln_bwd_ex(void* dy, const void* x, const void* w, const float* mean,
                      rms_path path, void* stream) {
   if (!valid_common(M, N, dtype, 0)) return RMS_ERR_INVALID_ARG;
   if (inplace_dx != 0 && inplace_dx != 1) return RMS_ERR_INVALID_ARG;
-  if (path < RMS_PATH_AUTO || path > RMS_PATH_SCALAR) return RMS_ERR_INVALID_ARG;
-  if (path == RMS_PATH_REGISTERS) return RMS_ERR_UNSUPPORTED;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
+  if (path == RMS_PATH_REGISTERS || path == RMS_PATH_CHUNKED) return RMS_ERR_UNSUPPORTED;
   if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
   if (inplace_dx) {
     if (dx && dx != dy) return RMS_ERR_INVALID_ARG;

@@ -128,6 +128,36 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
   return d;
 }
 __device__ __forceinline__ f32x2 splat2(float v) { return pk2(v, v); }
+// Exact negation of both halves (sign bits flipped).
+__device__ __forceinline__ f32x2 neg2(f32x2 v) { return v ^ 0x8000000080000000ull; }
+
+// Compensated (Kahan) running sums, for row reductions whose per-thread
+// chains grow with N: the error stays a few units in the last place of the
+// sum of magnitudes however many terms are added.  Every step is an
+// explicitly rounded add, so nothing is reassociated or contracted.
+struct Kahan2 {
+  f32x2 s = 0ull, c = 0ull;  // sum, and the negated part lost so far
+  __device__ __forceinline__ void add(f32x2 v) {
+    const f32x2 y = add2(v, neg2(c));
+    const f32x2 t = add2(s, y);
+    c = add2(add2(t, neg2(s)), neg2(y));
+    s = t;
+  }
+  __device__ __forceinline__ float total() const {
+    const f32x2 r = add2(s, neg2(c));
+    return __fadd_rn(lo2(r), hi2(r));
+  }
+};
+struct Kahan1 {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float v) {
+    const float y = __fsub_rn(v, c);
+    const float t = __fadd_rn(s, y);
+    c = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
+  }
+  __device__ __forceinline__ float total() const { return __fsub_rn(s, c); }
+};
 
 // Two bf16 (one 32-bit word, low half first) widened exactly to a pair.
 __device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
@@ -322,6 +352,24 @@ struct RowMath {
       sux = fma2(mul2(d, weight(g, i)), xn, sux);
       acc[i] = fma2(d, xn, acc[i]);
     }
+  }
+
+  // The two halves of backward_sums, for mappings that take them in
+  // separate passes: sux += u*xn, and acc += dy*xn.
+  __device__ static __forceinline__ void backward_dot(const uint4& x, const uint4& dy, const G& g,
+                                                      float r, f32x2& sux) {
+    const f32x2 rr = splat2(r);
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) {
+      const f32x2 xn = mul2(P::get(x, i), rr);
+      sux = fma2(mul2(P::get(dy, i), weight(g, i)), xn, sux);
+    }
+  }
+  __device__ static __forceinline__ void backward_acc(const uint4& x, const uint4& dy, float r,
+                                                      f32x2* acc) {
+    const f32x2 rr = splat2(r);
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) acc[i] = fma2(P::get(dy, i), mul2(P::get(x, i), rr), acc[i]);
   }
 
   // dx for one vector: r*u - x*r^3*c = r*(u - xn*k) with k = r*c.

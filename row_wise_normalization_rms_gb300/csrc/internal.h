@@ -14,7 +14,7 @@ enum Dtype { kF32 = 0, kBF16 = 1, kF16 = 2, kBF16W32 = 3, kF16W32 = 4 };
 // Bytes of one activation element / one weight element.
 inline int dtype_bytes(int dtype) { return dtype == kF32 ? 4 : 2; }
 inline int weight_bytes(int dtype) { return (dtype == kBF16 || dtype == kF16) ? 2 : 4; }
-enum Path { kAuto = 0, kRegisters = 1, kStaged = 2, kScalar = 3 };
+enum Path { kAuto = 0, kRegisters = 1, kStaged = 2, kScalar = 3, kChunked = 4 };
 
 struct FwdArgs {
   const void* x;
@@ -54,7 +54,8 @@ struct Mapping {
   int stages = 0;        // shared-memory pipeline depth (staged path)
   int cluster = 1;       // CTAs per cluster sharing one row (staged path)
   int sv = 0;            // 16-byte vectors per CTA's column slice (staged path)
-  int smem_acc = 0;      // LayerNorm scalar backward: partials in shared memory
+  int smem_acc = 0;      // scalar backward: partials in shared memory (else in the workspace)
+  int chunks = 0;        // chunked path: chunks per row
   size_t smem = 0;       // dynamic shared memory bytes
 };
 
@@ -86,6 +87,16 @@ cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m);
 cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s);
 // dgamma[j] = sum_{p < P} ws[p][j], p in increasing order.
 cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, cudaStream_t s);
+
+// ---- chunked path: rows of any width (chunked.cu) ----
+bool plan_chunked(int N, int dtype, Mapping* m);
+cudaError_t launch_fwd_chunked(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
+                               cudaStream_t s);
+// Fill m.blocks and m.partials and choose where the per-row k values live;
+// false when the shape leaves no room for them in the workspace.
+bool size_bwd_chunked(const BwdArgs& a, const DeviceInfo& d, Mapping* m, float** kbuf);
+cudaError_t launch_bwd_chunked(const BwdArgs& a, const Mapping& m, float* kbuf,
+                               const DeviceInfo& d, cudaStream_t s);
 
 // ---- LayerNorm (layernorm.cu) ----
 struct LnFwdArgs {

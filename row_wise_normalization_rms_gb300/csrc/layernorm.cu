@@ -140,15 +140,16 @@ ln_fwd_scalar_kernel(const T* __restrict__ x, const W* __restrict__ w, const W* 
   const T* xr = x + row * N;
   pdl_trigger();
   pdl_wait();
-  float s = 0.f;
-  for (int j = threadIdx.x; j < N; j += 256) s += E::to_f(xr[j]);
-  const float mean = group_sum(s, 256, 0, red_a) * inv_n;
-  float q = 0.f;
+  // Compensated sums: a thread adds N / 256 terms in sequence.
+  Kahan1 s;
+  for (int j = threadIdx.x; j < N; j += 256) s.add(E::to_f(xr[j]));
+  const float mean = group_sum(s.total(), 256, 0, red_a) * inv_n;
+  Kahan1 q;
   for (int j = threadIdx.x; j < N; j += 256) {
     const float d = E::to_f(xr[j]) - mean;
-    q = fmaf(d, d, q);
+    q.add(__fmul_rn(d, d));
   }
-  const float rstd = 1.0f / sqrtf(group_sum(q, 256, 0, red_b) * inv_n + eps);
+  const float rstd = 1.0f / sqrtf(group_sum(q.total(), 256, 0, red_b) * inv_n + eps);
   if (threadIdx.x == 0) {
     mean_out[row] = mean;
     rstd_out[row] = rstd;
@@ -433,18 +434,18 @@ ln_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__
     const T* xr = x + row * N;
     const T* dr = dy + row * N;
     const float mu = mean[row], rs = rstd[row];
-    float s1 = 0.f, s2 = 0.f;
+    Kahan1 s1, s2;
     for (int j = threadIdx.x; j < N; j += 256) {
       const float xh = (E::to_f(xr[j]) - mu) * rs;
       const float d = E::to_f(dr[j]);
       const float g = d * Elem<W>::to_f(w[j]);
-      s1 = fmaf(xh, g, s1);
-      s2 += g;
+      s1.add(__fmul_rn(xh, g));
+      s2.add(g);
       accw[j] = fmaf(d, xh, accw[j]);
       accb[j] += d;
     }
-    const float c1 = group_sum(s1, 256, 0, red[it & 1][0]) * inv_n;
-    const float c2 = group_sum(s2, 256, 0, red[it & 1][1]) * inv_n;
+    const float c1 = group_sum(s1.total(), 256, 0, red[it & 1][0]) * inv_n;
+    const float c2 = group_sum(s2.total(), 256, 0, red[it & 1][1]) * inv_n;
     T* out = dx + row * N;
     for (int j = threadIdx.x; j < N; j += 256) {
       const float xh = (E::to_f(xr[j]) - mu) * rs;

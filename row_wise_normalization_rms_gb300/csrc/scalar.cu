@@ -30,12 +30,12 @@ rms_fwd_scalar_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T* _
   const T* xr = x + row * N;
   pdl_trigger();
   pdl_wait();
-  float ss = 0.f;
+  Kahan1 acc;  // a thread adds N / kScalarThreads squares in sequence
   for (int j = threadIdx.x; j < N; j += kScalarThreads) {
     const float f = E::to_f(xr[j]);
-    ss = fmaf(f, f, ss);
+    acc.add(__fmul_rn(f, f));
   }
-  ss = group_sum(ss, kScalarThreads, 0, red);
+  const float ss = group_sum(acc.total(), kScalarThreads, 0, red);
   const float r = 1.0f / sqrtf(ss / (float)N + eps);
   if (threadIdx.x == 0) rstd[row] = r;
   T* yr = y + row * N;
@@ -51,12 +51,15 @@ template <typename T, typename W>
 __global__ void __launch_bounds__(kScalarThreads)
 rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__ gamma,
                       const float* __restrict__ rstd, T* dx, float* __restrict__ ws, int64_t M,
-                      int N, int gemma) {
+                      int N, int gemma, int acc_in_smem) {
   using E = Elem<T>;
   __shared__ float red[2][kScalarThreads / 32];
-  extern __shared__ float acc[];  // [N]: column j belongs to thread j % kScalarThreads
-  for (int j = threadIdx.x; j < N; j += kScalarThreads) acc[j] = 0.f;
+  // dgamma partials of this CTA, column j owned by thread j % kScalarThreads:
+  // in shared memory when N floats fit, else in the CTA's workspace row.
+  extern __shared__ float acc_s[];
+  float* acc = acc_in_smem ? acc_s : ws + (int64_t)blockIdx.x * N;
   pdl_wait();
+  for (int j = threadIdx.x; j < N; j += kScalarThreads) acc[j] = 0.f;
 
   int it = 0;
   for (int64_t row = blockIdx.x; row < M; row += gridDim.x, ++it) {
@@ -64,13 +67,13 @@ rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict_
     const T* dr = dy + row * N;
     const float r = rstd[row];
     // xn = x*r, u = dy*w:  k = mean(u*xn) = r*c,  dx = r*(u - xn*k).
-    float s = 0.f;
+    Kahan1 dot;
     for (int j = threadIdx.x; j < N; j += kScalarThreads) {
       const float g = Elem<W>::to_f(gamma[j]);
       const float w = gemma ? 1.0f + g : g;
-      s = fmaf(E::to_f(dr[j]) * w, E::to_f(xr[j]) * r, s);
+      dot.add(__fmul_rn(E::to_f(dr[j]) * w, E::to_f(xr[j]) * r));
     }
-    s = group_sum(s, kScalarThreads, 0, red[it & 1]);
+    const float s = group_sum(dot.total(), kScalarThreads, 0, red[it & 1]);
     const float k = s / (float)N;
     T* out = dx + row * N;
     for (int j = threadIdx.x; j < N; j += kScalarThreads) {
@@ -82,8 +85,10 @@ rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict_
       out[j] = E::from_f(fmaf(-xn, k, d * w) * r);
     }
   }
-  float* wp = ws + (int64_t)blockIdx.x * N;
-  for (int j = threadIdx.x; j < N; j += kScalarThreads) wp[j] = acc[j];
+  if (acc_in_smem) {
+    float* wp = ws + (int64_t)blockIdx.x * N;
+    for (int j = threadIdx.x; j < N; j += kScalarThreads) wp[j] = acc[j];
+  }
 }
 
 // dgamma[j] = sum over p = 0..P-1 of ws[p][j].  A CTA covers 32 columns with
@@ -165,7 +170,11 @@ bool plan_scalar(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
   m->threads = rmsk::kScalarThreads;
   m->rows_per_cta = 1;
   m->smem = bwd ? (size_t)N * sizeof(float) : 0;
-  if (m->smem + 1024 > d.smem_optin) return false;  // room for the static reduction slots
+  m->smem_acc = 1;
+  if (m->smem + 1024 > d.smem_optin) {  // room for the static reduction slots
+    m->smem = 0;                         // too wide: partials in the workspace rows
+    m->smem_acc = 0;
+  }
   return true;
 }
 
@@ -222,7 +231,7 @@ static cudaError_t launch_bwd_scalar_t(const BwdArgs& a, const Mapping& m, cudaS
   return rmsk::launch_pdl(rmsk::rms_bwd_scalar_kernel<T, W>, grid, block, m.smem, s,
                           static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
                           static_cast<const W*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.ws,
-                          a.M, a.N, a.gemma);
+                          a.M, a.N, a.gemma, m.smem_acc);
 }
 
 cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s) {

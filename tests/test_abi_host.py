@@ -67,6 +67,7 @@ def test_fwd_rejects_bad_arguments(lib):
     assert fwd(lib, eps=inf) == INVALID
     assert fwd(lib, eps=-1e-6) == INVALID
     assert fwd(lib, path=7) == INVALID
+    assert fwd(lib, path=5) == INVALID
     assert fwd(lib, x=None) == INVALID
     assert fwd(lib, g=None) == INVALID
     assert fwd(lib, y=None) == INVALID
@@ -99,6 +100,7 @@ def test_bwd_rejects_bad_arguments(lib):
     assert bwd(lib, M=-3) == INVALID
     assert bwd(lib, N=0) == INVALID
     assert bwd(lib, path=-1) == INVALID
+    assert bwd(lib, path=5) == INVALID
     assert bwd(lib, dg=None) == INVALID
     assert bwd(lib, dx=None) == INVALID
     assert bwd(lib, x=None) == INVALID
@@ -139,6 +141,7 @@ def test_ln_fwd_rejects_bad_arguments(lib):
     assert ln_f(lib, eps=-1.0) == INVALID
     assert ln_f(lib, path=9) == INVALID
     assert ln_f(lib, path=2) == UNSUPPORTED  # no staged forward mapping
+    assert ln_f(lib, path=4) == UNSUPPORTED  # no chunked LayerNorm mapping
     for k in ("x", "w", "y", "mu", "r"):
         assert ln_f(lib, **{k: None}) == INVALID, k
     assert ln_f(lib, N=1 << 40) == UNSUPPORTED
@@ -166,8 +169,9 @@ def test_ln_bwd_rejects_bad_arguments(lib):
     assert ln_b(lib, inplace=3) == INVALID
     assert ln_b(lib, M=-2) == INVALID
     assert ln_b(lib, N=0) == INVALID
-    assert ln_b(lib, path=4) == INVALID
+    assert ln_b(lib, path=5) == INVALID
     assert ln_b(lib, path=1) == UNSUPPORTED  # no register backward mapping
+    assert ln_b(lib, path=4) == UNSUPPORTED  # no chunked LayerNorm mapping
     assert ln_b(lib, dw=None) == INVALID
     for k in ("dy", "x", "w", "mu", "r", "dx"):
         assert ln_b(lib, **{k: None}) == INVALID, k

@@ -43,12 +43,12 @@ SMALL_SHAPES = [
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "bf16w32", "f16w32"])
 @pytest.mark.parametrize("M,N", SMALL_SHAPES, ids=[f"{m}x{n}" for m, n in SMALL_SHAPES])
-@pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar"])
+@pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar", "chunked"])
 def test_small_shapes_full_parity(M, N, dtype, path):
     w = _w(M, N, dtype, seed=M + N)
     b = 4 if w.dtype == "f32" else 2
     inp = H.inputs_for(w)
-    if path in ("registers", "staged") and (N * b) % 16 != 0:
+    if path in ("registers", "staged", "chunked") and (N * b) % 16 != 0:
         with pytest.raises(rms.RmsError) as ei:
             H.run_gpu(w, inp, path=path)
         assert ei.value.status == rms.RMS_ERR_ALIGNMENT
@@ -103,7 +103,7 @@ def test_dgamma_bitwise_reproducible():
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
-@pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar"])
+@pytest.mark.parametrize("path", ["auto", "registers", "staged", "scalar", "chunked"])
 def test_inplace_matches_out_of_place_bitwise(dtype, path):
     w = _w(1500, 2048, dtype, seed=3)
     inp = H.inputs_for(w)
@@ -395,36 +395,62 @@ def test_more_than_2_31_elements():
     assert np.all(np.abs(full - parts) <= 2e-5 * (np.abs(full) + np.sqrt(M))), np.abs(full - parts).max()
 
 
-@pytest.mark.parametrize("N,fwd_ok,bwd_ok", [(32768, True, True), (65536, True, True),
-                                             (131072, True, True), (262144, True, False)])
-def test_widest_rows_and_unsupported(N, fwd_ok, bwd_ok):
-    """The widest rows each direction accepts (bf16), and a clear
-    RMS_ERR_UNSUPPORTED beyond them (nothing is launched)."""
-    M = 64
-    w = _w(M, N, "bf16", seed=N)
+@pytest.mark.parametrize("N", [32768, 65536, 131072, 262144])
+def test_widest_rows(N):
+    """Wide bf16 rows in the automatic mapping: cluster split up to 128K
+    (backward) / 256K (forward), the chunked mapping beyond."""
+    w = _w(64, N, "bf16", seed=N)
     inp = H.inputs_for(w)
-    x = H.to_device(inp["x"], "bf16")
-    g = H.to_device(inp["gamma"], "bf16")
-    y = torch.empty_like(x)
-    r = torch.empty(M, device="cuda")
-    rms.rms_fwd(x, g, y, r, w.eps)
-    dy = H.to_device(inp["dy"], "bf16")
-    dx = torch.empty_like(x)
-    dg = torch.empty(N, device="cuda")
-    ws = torch.empty(rms.rms_bwd_workspace_size(M, N), dtype=torch.uint8, device="cuda")
-    if bwd_ok:
-        rms.rms_bwd(dy, x, g, r, dx, dg, ws)
-        torch.cuda.synchronize()
-        H.assert_parity(w, inp, H.GpuResult(y, r, dx, dg, True))
-    else:
-        with pytest.raises(rms.RmsError) as ei:
-            rms.rms_bwd(dy, x, g, r, dx, dg, ws)
-        assert ei.value.status == rms.RMS_ERR_UNSUPPORTED
-        torch.cuda.synchronize()
-        from oracle import compare
+    H.assert_parity(w, inp, H.run_gpu(w, inp))
 
-        xf = storage_to_float64(inp["x"], "bf16")
-        gf = storage_to_float64(inp["gamma"], "bf16")
-        y_ref, r_ref = orc.rms_forward(xf, gf, w.eps)
-        assert compare.check_y(H.to_host64(y), y_ref, "bf16").ok
-        assert compare.check_rstd(H.to_host64(r), r_ref).ok
+
+def test_chunked_unsupported_corner():
+    """Forced chunked backward on many 16-byte rows: the per-row values do not
+    fit beside the partial rows of the workspace, so the call is refused
+    before any launch (the automatic mapping never picks it there)."""
+    M, N = 5000, 8
+    w = _w(M, N, "bf16", seed=1)
+    inp = H.inputs_for(w)
+    with pytest.raises(rms.RmsError) as ei:
+        H.run_gpu(w, inp, fwd_path="chunked", bwd_path="chunked")
+    assert ei.value.status == rms.RMS_ERR_UNSUPPORTED
+    H.assert_parity(w, inp, H.run_gpu(w, inp, fwd_path="chunked", bwd_path="auto"))
+
+
+@pytest.mark.parametrize("gemma,inplace", [(0, 0), (1, 1)])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "bf16w32"])
+@pytest.mark.parametrize("M,N", [(257, 3072), (1000, 512), (3, 65536), (700, 8192)])
+def test_chunked_mapping(M, N, dtype, gemma, inplace):
+    """The any-width mapping forced on ordinary shapes, M > N (per-row values
+    in the workspace) and M <= N (in dgamma), Gemma and in-place dx."""
+    w = _w(M, N, dtype, gemma=gemma, inplace=inplace, seed=M * 7 + N)
+    inp = H.inputs_for(w)
+    H.assert_parity(w, inp, H.run_gpu(w, inp, path="chunked"))
+
+
+def test_chunked_dgamma_bitwise_reproducible():
+    w = _w(3000, 4096, "bf16", seed=5)
+    inp = H.inputs_for(w)
+    a = H.run_gpu(w, inp, path="chunked")
+    b = H.run_gpu(w, inp, path="chunked")
+    assert torch.equal(a.dgamma.view(torch.int32), b.dgamma.view(torch.int32))
+    assert torch.equal(a.dx.view(torch.int16), b.dx.view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype,N,M", [("bf16", 262144, 48), ("f32", 200000, 12),
+                                       ("bf16", 1 << 20, 6), ("f16", 393216, 9)])
+def test_rows_beyond_the_cluster_split(dtype, N, M):
+    """Rows wider than a cluster of CTAs holds take the chunked mapping
+    automatically, forward and backward."""
+    w = _w(M, N, dtype, seed=N % 1000 + M)
+    inp = H.inputs_for(w)
+    H.assert_parity(w, inp, H.run_gpu(w, inp))
+
+
+@pytest.mark.parametrize("dtype,N", [("f32", 70001), ("bf16", 120003)])
+def test_misaligned_wide_rows_scalar_workspace_partials(dtype, N):
+    """Rows whose dgamma partials do not fit in shared memory, on the scalar
+    mapping (N*b not a multiple of 16): the partials live in the workspace."""
+    w = _w(9, N, dtype, seed=N % 977)
+    inp = H.inputs_for(w)
+    H.assert_parity(w, inp, H.run_gpu(w, inp))
