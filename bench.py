@@ -53,6 +53,14 @@ def ln_step_bytes(M: int, N: int, b: int, wb: int, bias: bool):
     return fwd, bwd
 
 
+def add_step_bytes(M: int, N: int, b: int, wb: int):
+    """Residual add fused into RMSNorm: fwd reads x and the residual, writes h,
+    y and rstd; bwd reads dy, h, rstd and dh, writes dx and dgamma."""
+    fwd = 4 * M * N * b + 4 * M + N * wb
+    bwd = 4 * M * N * b + 4 * M + N * wb + 4 * N
+    return fwd, bwd
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -499,19 +507,29 @@ def run_sweep(args):
         k = int(min(64, max(1, -(-3 * L2_BYTES // set_bytes))))
         x0, dy0, g = dev_t(inp["x"]), dev_t(inp["dy"]), dev_t(inp["gamma"], w.wdtype)
         ln = w.op == "ln"
+        fused = w.op == "rms_add"
         beta = dev_t(inp["beta"], w.wdtype) if ln and inp["beta"] is not None else None
+        if fused:  # residual, h and dh add three matrices per set
+            set_bytes = 7 * M * N * b
+            k = int(min(64, max(1, -(-3 * L2_BYTES // set_bytes))))
         sets = []
         for i in range(k):
             sets.append((x0 if i == 0 else x0.clone(), dy0 if i == 0 else dy0.clone(),
                          torch.empty_like(x0), torch.empty_like(x0),
                          torch.empty(M, device=dev), torch.empty(M, device=dev)))
+        if fused:
+            r0, dh0 = dev_t(inp["residual"]), dev_t(inp["dh"])
+            extra = [(r0 if i == 0 else r0.clone(), torch.empty_like(x0),
+                      dh0 if i == 0 else dh0.clone()) for i in range(k)]
         dg = torch.empty(N, device=dev)
         db = torch.empty(N, device=dev)
         ws_need = rms.ln_bwd_workspace_size(M, N) if ln else rms.rms_bwd_workspace_size(M, N)
         ws = torch.empty(max(256, ws_need), dtype=torch.uint8, device=dev)
+        wb = 4 if w.wdtype == "f32" else b
         if ln:
-            wb = 4 if w.wdtype == "f32" else b
             fwd_b, bwd_b = ln_step_bytes(M, N, b, wb, beta is not None)
+        elif fused:
+            fwd_b, bwd_b = add_step_bytes(M, N, b, wb)
         else:
             fwd_b, bwd_b = step_bytes(M, N, b)
         calls = max(args.steps, 2 * k)
@@ -527,6 +545,16 @@ def run_sweep(args):
                     x, dy, y, dx, r, mu = sets[i % k]
                     rms.ln_bwd(dy, x, g, mu, r, None if w.inplace_dx else dx, dg, db, ws,
                                w.inplace_dx, path=bpath)
+            elif fused:
+                def fwd_call(i):
+                    x, dy, y, dx, r, _ = sets[i % k]
+                    rr, hh, dh = extra[i % k]
+                    rms.rms_fwd_add(x, rr, g, y, hh, r, w.eps, w.gemma, path=path)
+
+                def bwd_call(i):
+                    x, dy, y, dx, r, _ = sets[i % k]
+                    rr, hh, dh = extra[i % k]
+                    rms.rms_bwd_add(dy, hh, g, r, dh, dx, dg, ws, w.gemma, 0, path=path)
             else:
                 def fwd_call(i):
                     x, dy, y, dx, r, _ = sets[i % k]

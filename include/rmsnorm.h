@@ -178,6 +178,53 @@ rms_status rms_bwd_noalloc(void* dy, const void* x, const void* gamma, const flo
                            int gemma, int inplace_dx, void* stream);
 
 /*
+ * rms_fwd_add — residual add fused into the forward: one read of x and of
+ * the residual, one write of h and of y, instead of an add kernel whose
+ * output is read back by rms_fwd.
+ *   h = round(x + residual)   (float32 sum, one rounding to dtype: the
+ *                              residual stream keeps the activation type)
+ *   y, rstd = rms_fwd(h)      (exactly as rms_fwd on the stored h)
+ *   x, residual [M*N] dtype, read; h [M*N] dtype, written (h may be the
+ *   residual buffer itself, updating the stream in place; it must not
+ *   overlap x, gamma, y or rstd); other arguments as rms_fwd.
+ * Source: "02 · 手写 Triton kernel:RMSNorm / RoPE / SwiGLU", sections 1-2
+ * (neighbouring elementwise work kept in registers, each tensor read and
+ * written once, results written back over an input); the add itself is the
+ * residual connection around the normalisation.
+ * Errors: as rms_fwd; RMS_ERR_INVALID_ARG when residual or h is NULL.
+ */
+rms_status rms_fwd_add(const void* x, const void* residual, const void* gamma, void* y, void* h,
+                       float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype, int gemma,
+                       void* stream);
+
+/* rms_fwd_add with an explicit row mapping. */
+rms_status rms_fwd_add_ex(const void* x, const void* residual, const void* gamma, void* y,
+                          void* h, float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype,
+                          int gemma, rms_path path, void* stream);
+
+/*
+ * rms_bwd_add — the backward of rms_fwd_add: the gradient reaching h
+ * through the residual path is added to the normalisation's input
+ * gradient before the one rounding of dx.
+ *   dx = round(dRMS(dy; h, gamma, rstd) + dh)   (dRMS as rms_bwd, in float32)
+ *   dgamma as rms_bwd (on h).
+ *   h [M*N] dtype: the forward's h; dh [M*N] dtype, read; dx [M*N] written,
+ *   may be dh itself (accumulating in place) or dy with inplace_dx = 1;
+ *   dh must not overlap dy.  Other arguments as rms_bwd.
+ * Source: as rms_fwd_add; dRMS as rms_bwd.
+ * Errors: as rms_bwd; RMS_ERR_INVALID_ARG when dh is NULL.
+ */
+rms_status rms_bwd_add(void* dy, const void* h, const void* gamma, const float* rstd,
+                       const void* dh, void* dx, float* dgamma, void* workspace, int64_t M,
+                       int64_t N, rms_dtype dtype, int gemma, int inplace_dx, void* stream);
+
+/* rms_bwd_add with the workspace size stated and an explicit row mapping. */
+rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const float* rstd,
+                          const void* dh, void* dx, float* dgamma, void* workspace,
+                          size_t workspace_bytes, int64_t M, int64_t N, rms_dtype dtype,
+                          int gemma, int inplace_dx, rms_path path, void* stream);
+
+/*
  * ln_fwd — forward LayerNorm over M rows of N, on the same engine.
  *   mean_i = (1/N) sum_j x_ij,  var_i = (1/N) sum_j (x_ij - mean_i)^2,
  *   rstd_i = 1/sqrt(var_i + eps),  y_ij = (x_ij - mean_i) * rstd_i * w_j + b_j

@@ -26,9 +26,17 @@ Sources (web pages on row-wise RMS normalisation):
   - § 2 item 3 and § 3: normed is cast to the weight dtype, then multiplied
     by the weight (the order ``emulate_forward_lowp`` reproduces).
 
-Every function here is pinned by ``tests/test_oracle_pins.py`` against values
-the pages print, closed forms, invariants, finite differences and
-``torch.nn.functional.rms_norm`` in float64; none is "parity unpinned".
+* Fused residual add ([UNS] §§ 1-2: neighbouring elementwise work is kept
+  in registers, each tensor read and written once): ``residual_add``,
+  ``rms_forward_add`` and ``rms_backward_add`` compose the definitions above
+  with h = x + residual as the residual stream stores it (the float32 sum
+  rounded once to the I/O dtype) and dx = dRMS + dh.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` (and, for the
+fused residual add, ``tests/test_fused_add_oracle.py``) against values the
+pages print, closed forms, invariants, finite differences, torch's own
+dtype arithmetic and ``torch.nn.functional.rms_norm`` with autograd in
+float64; none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -205,3 +213,32 @@ def emulate_forward_lowp(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf1
         normed = rnd_w(xr)
         y = rnd(_round_f32(normed.astype(np.float64) * gf[None, :]))
     return y.astype(np.float64)
+
+
+# ---- fused residual add ------------------------------------------------------
+
+def residual_add(x, residual, dtype: str = "f32") -> np.ndarray:
+    """h = x + residual as stored in ``dtype``: the IEEE float32 sum of the two
+    (dtype-exact) inputs, rounded once more to ``dtype`` (nothing more for
+    float32).  Returns the float64 values of h."""
+    s = _round_f32(x) + _round_f32(residual)  # numpy float32 arithmetic: one rounding
+    rnd = {"bf16": _round_bf16, "f16": _round_f16}.get(dtype, _round_f32)
+    return rnd(s).astype(np.float64)
+
+
+def rms_forward_add(x, residual, gamma, eps: float, gemma: int = 0, dtype: str = "f32"):
+    """(y, r, h): h = residual_add(x, residual), then the RMSNorm of h."""
+    h = residual_add(x, residual, dtype)
+    y, r = rms_forward(h, gamma, eps, gemma)
+    return y, r, h
+
+
+def rms_backward_add(h, gamma, dy, dh, eps: float, gemma: int = 0, with_scales: bool = False):
+    """dx = dRMS(dy; h) + dh (the gradient reaching h through the residual
+    path) and dgamma of the RMSNorm of h.  With ``with_scales`` the dx scale
+    is rms_backward's plus |dh|."""
+    out = rms_backward(h, gamma, dy, eps, gemma, with_scales=with_scales)
+    dx = out[0] + _f64(dh)
+    if not with_scales:
+        return dx, out[1]
+    return dx, out[1], out[2] + np.abs(_f64(dh)), out[3]

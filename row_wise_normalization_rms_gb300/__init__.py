@@ -115,6 +115,31 @@ def rms_bwd_noalloc(dy, x, gamma, rstd, dx, dgamma, gemma: int = 0, inplace_dx: 
         raise RmsError(st, "rms_bwd_noalloc")
 
 
+def rms_fwd_add(x, residual, gamma, y, h, rstd, eps: float = 1e-6, gemma: int = 0, stream=None,
+                path="auto"):
+    """Fused residual add + RMSNorm: h = x + residual (rounded to x's dtype;
+    h may be residual itself) and y, rstd = RMSNorm(h)."""
+    M, N = x.shape
+    st = lib().rms_fwd_add_ex(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(y), _ptr(h), _ptr(rstd),
+                              M, N, float(eps), dtype_code(x, gamma), int(gemma), _path(path),
+                              _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "rms_fwd_add")
+
+
+def rms_bwd_add(dy, h, gamma, rstd, dh, dx, dgamma, workspace, gemma: int = 0, inplace_dx: int = 0,
+                stream=None, path="auto"):
+    """Backward of rms_fwd_add: dx = dRMS + dh (dx may be dh itself, or dy
+    with inplace_dx=1 and dx=None); dgamma as rms_bwd."""
+    M, N = h.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().rms_bwd_add_ex(_ptr(dy), _ptr(h), _ptr(gamma), _ptr(rstd), _ptr(dh), _ptr(dx),
+                              _ptr(dgamma), _ptr(workspace), ws_bytes, M, N, dtype_code(h, gamma),
+                              int(gemma), int(inplace_dx), _path(path), _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "rms_bwd_add")
+
+
 def ln_fwd(x, w, b, y, mean, rstd, eps: float = 1e-5, stream=None, path="auto"):
     """LayerNorm forward: y (M,N), mean and rstd (M,) float32 from x (M,N),
     w (N,) and b (N,) or None (no bias)."""

@@ -103,11 +103,17 @@ bool prefer_staged(int N, int dtype, bool bwd) {
 
 // Picks the row mapping for a call.  A forced path that cannot take the
 // shape is an error, never a silent switch.
+// With a fused residual the register forward holds twice the vectors and is
+// built for at most 512 threads per CTA.
+bool plan_registers_for(int N, int dtype, bool bwd, bool res, Mapping* m) {
+  return rmsi::plan_registers(N, dtype, bwd, m) && !(res && !bwd && m->threads > 512);
+}
+
 rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const DeviceInfo& d,
-                  Mapping* m) {
+                  Mapping* m, bool res = false) {
   switch (path) {
     case RMS_PATH_AUTO:
-      if (aligned && prefer_staged(N, dtype, bwd) && rmsi::plan_staged(N, dtype, bwd, d, m)) {
+      if (aligned && prefer_staged(N, dtype, bwd) && rmsi::plan_staged(N, dtype, bwd, d, m, res)) {
         // A row split over many CTAs of a cluster serialises on the per-row
         // exchange; from 4 (fwd) / 8 (bwd) CTAs the chunked mapping's extra
         // pass over the row costs less (GB300, N = 65536 .. 131072 bf16).
@@ -116,17 +122,17 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
           return RMS_OK;
         return RMS_OK;
       }
-      if (aligned && rmsi::plan_registers(N, dtype, bwd, m)) return RMS_OK;
-      if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m)) return RMS_OK;
+      if (aligned && plan_registers_for(N, dtype, bwd, res, m)) return RMS_OK;
+      if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m, res)) return RMS_OK;
       if (aligned && rmsi::plan_chunked(N, dtype, m)) return RMS_OK;
       if (rmsi::plan_scalar(N, dtype, bwd, d, m)) return RMS_OK;
       return RMS_ERR_UNSUPPORTED;
     case RMS_PATH_REGISTERS:
       if (!aligned) return RMS_ERR_ALIGNMENT;
-      return rmsi::plan_registers(N, dtype, bwd, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
+      return plan_registers_for(N, dtype, bwd, res, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     case RMS_PATH_STAGED:
       if (!aligned) return RMS_ERR_ALIGNMENT;
-      return rmsi::plan_staged(N, dtype, bwd, d, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
+      return rmsi::plan_staged(N, dtype, bwd, d, m, res) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     case RMS_PATH_SCALAR:
       return rmsi::plan_scalar(N, dtype, bwd, d, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     case RMS_PATH_CHUNKED:
@@ -187,31 +193,46 @@ size_t rms_bwd_workspace_size(int64_t M, int64_t N) {
   return workspace_need(M, N, d);
 }
 
-rms_status rms_fwd_ex(const void* x, const void* gamma, void* y, float* rstd, int64_t M,
-                      int64_t N, float eps, rms_dtype dtype, int gemma, rms_path path,
-                      void* stream) {
+// The forward, with or without a fused residual add (res and h both given,
+// or both NULL).
+static rms_status fwd_impl(const void* x, const void* res, const void* gamma, void* y, void* h,
+                           float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype, int gemma,
+                    rms_path path, void* stream) {
   if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.f) return RMS_ERR_INVALID_ARG;
   if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
   if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
   if (M == 0) return RMS_OK;
   if (!x || !gamma || !y || !rstd) return RMS_ERR_INVALID_ARG;
+  const bool fused = res != nullptr || h != nullptr;
+  if (fused && (!res || !h)) return RMS_ERR_INVALID_ARG;
   const int b = elem_bytes(dtype);
   const size_t xb = matrix_bytes(M, N, b);
   if (xb == 0) return RMS_ERR_INVALID_ARG;
   const size_t gb = (size_t)N * rmsi::weight_bytes(dtype), rb = (size_t)M * sizeof(float);
-  if (overlap(y, xb, x, xb) || overlap(y, xb, gamma, gb) || overlap(y, xb, rstd, rb) ||
-      overlap(rstd, rb, x, xb) || overlap(rstd, rb, gamma, gb))
-    return RMS_ERR_INVALID_ARG;
+  // Written: y, rstd and (fused) h; h == res is the one sanctioned alias.
+  const void* reads[3] = {x, gamma, res};
+  const size_t read_n[3] = {xb, gb, xb};
+  const void* writes[3] = {y, rstd, h};
+  const size_t write_n[3] = {xb, rb, xb};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j) {
+      if (i == 2 && j == 2 && h == res) continue;
+      if (overlap(writes[i], write_n[i], reads[j], read_n[j])) return RMS_ERR_INVALID_ARG;
+    }
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(writes[i], write_n[i], writes[j], write_n[j])) return RMS_ERR_INVALID_ARG;
+  }
 
   DeviceInfo d;
   if (!current_device(&d)) return RMS_ERR_CUDA;
-  const bool aligned = (N * b) % 16 == 0 && aligned16(x) && aligned16(gamma) && aligned16(y);
+  const bool aligned = (N * b) % 16 == 0 && aligned16(x) && aligned16(gamma) && aligned16(y) &&
+                       (!fused || (aligned16(res) && aligned16(h)));
   Mapping m;
-  const rms_status st = choose(path, (int)N, dtype, false, aligned, d, &m);
+  const rms_status st = choose(path, (int)N, dtype, false, aligned, d, &m, fused);
   if (st != RMS_OK) return st;
 
-  FwdArgs a{x, gamma, y, rstd, M, (int)N, eps, (int)dtype, gemma};
+  FwdArgs a{x, gamma, y, rstd, M, (int)N, eps, (int)dtype, gemma, res, h};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (m.path) {
@@ -236,15 +257,37 @@ rms_status rms_fwd_ex(const void* x, const void* gamma, void* y, float* rstd, in
   return RMS_OK;
 }
 
-rms_status rms_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t M, int64_t N,
-                   float eps, rms_dtype dtype, int gemma, void* stream) {
-  return rms_fwd_ex(x, gamma, y, rstd, M, N, eps, dtype, gemma, RMS_PATH_AUTO, stream);
+rms_status rms_fwd_ex(const void* x, const void* gamma, void* y, float* rstd, int64_t M,
+                      int64_t N, float eps, rms_dtype dtype, int gemma, rms_path path,
+                      void* stream) {
+  return fwd_impl(x, nullptr, gamma, y, nullptr, rstd, M, N, eps, dtype, gemma, path, stream);
 }
 
-rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* rstd, void* dx,
-                      float* dgamma, void* workspace, size_t workspace_bytes, int64_t M,
-                      int64_t N, rms_dtype dtype, int gemma, int inplace_dx, rms_path path,
-                      void* stream) {
+rms_status rms_fwd(const void* x, const void* gamma, void* y, float* rstd, int64_t M, int64_t N,
+                   float eps, rms_dtype dtype, int gemma, void* stream) {
+  return fwd_impl(x, nullptr, gamma, y, nullptr, rstd, M, N, eps, dtype, gemma, RMS_PATH_AUTO,
+                  stream);
+}
+
+rms_status rms_fwd_add_ex(const void* x, const void* residual, const void* gamma, void* y,
+                          void* h, float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype,
+                          int gemma, rms_path path, void* stream) {
+  if (M > 0 && (!residual || !h)) return RMS_ERR_INVALID_ARG;
+  return fwd_impl(x, residual, gamma, y, h, rstd, M, N, eps, dtype, gemma, path, stream);
+}
+
+rms_status rms_fwd_add(const void* x, const void* residual, const void* gamma, void* y, void* h,
+                       float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype, int gemma,
+                       void* stream) {
+  return rms_fwd_add_ex(x, residual, gamma, y, h, rstd, M, N, eps, dtype, gemma, RMS_PATH_AUTO,
+                        stream);
+}
+
+// The backward, with or without a fused residual gradient dh (NULL: none).
+static rms_status bwd_impl(void* dy, const void* x, const void* gamma, const float* rstd,
+                           const void* dh, void* dx, float* dgamma, void* workspace,
+                           size_t workspace_bytes, int64_t M, int64_t N, rms_dtype dtype,
+                           int gemma, int inplace_dx, rms_path path, void* stream) {
   if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
   if (inplace_dx != 0 && inplace_dx != 1) return RMS_ERR_INVALID_ARG;
   if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
@@ -274,28 +317,29 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
   if (workspace_bytes < need || ((uintptr_t)workspace & 255u) != 0) return RMS_ERR_WORKSPACE;
 
   // Written ranges (dx, dgamma, workspace) must not overlap anything else;
-  // dx == dy is the one sanctioned alias.
-  const void* reads[3] = {x, gamma, rstd};
-  const size_t read_n[3] = {xb, gb, rb};
+  // dx == dy (inplace_dx) and dx == dh are the sanctioned aliases.
+  const void* reads[5] = {x, gamma, rstd, dy, dh};
+  const size_t read_n[5] = {xb, gb, rb, xb, xb};
+  const void* writes[3] = {dx, dgamma, workspace};
+  const size_t write_n[3] = {xb, db, need};
   for (int i = 0; i < 3; ++i) {
-    if (overlap(dx, xb, reads[i], read_n[i]) || overlap(dgamma, db, reads[i], read_n[i]) ||
-        overlap(workspace, need, reads[i], read_n[i]))
-      return RMS_ERR_INVALID_ARG;
+    for (int j = 0; j < 5; ++j) {
+      if (i == 0 && reads[j] == dx && (j == 3 || j == 4)) continue;
+      if (overlap(writes[i], write_n[i], reads[j], read_n[j])) return RMS_ERR_INVALID_ARG;
+    }
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(writes[i], write_n[i], writes[j], write_n[j])) return RMS_ERR_INVALID_ARG;
   }
-  if (dx != dy && overlap(dx, xb, dy, xb)) return RMS_ERR_INVALID_ARG;
-  if (overlap(dgamma, db, dy, xb) || overlap(workspace, need, dy, xb) ||
-      overlap(dgamma, db, dx, xb) || overlap(workspace, need, dx, xb) ||
-      overlap(workspace, need, dgamma, db))
-    return RMS_ERR_INVALID_ARG;
+  if (dh && overlap(dh, xb, dy, xb)) return RMS_ERR_INVALID_ARG;
 
-  const bool aligned =
-      (N * b) % 16 == 0 && aligned16(dy) && aligned16(x) && aligned16(gamma) && aligned16(dx);
+  const bool aligned = (N * b) % 16 == 0 && aligned16(dy) && aligned16(x) && aligned16(gamma) &&
+                       aligned16(dx) && (!dh || aligned16(dh));
   Mapping m;
-  const rms_status st = choose(path, (int)N, dtype, true, aligned, d, &m);
+  const rms_status st = choose(path, (int)N, dtype, true, aligned, d, &m, dh != nullptr);
   if (st != RMS_OK) return st;
 
   BwdArgs a{dy, x, gamma, rstd, dx, dgamma, static_cast<float*>(workspace), M, (int)N,
-            (int)dtype, gemma};
+            (int)dtype, gemma, dh};
   cudaError_t e;
   switch (m.path) {
     case rmsi::kRegisters:
@@ -326,11 +370,35 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
   return RMS_OK;
 }
 
+rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* rstd, void* dx,
+                      float* dgamma, void* workspace, size_t workspace_bytes, int64_t M,
+                      int64_t N, rms_dtype dtype, int gemma, int inplace_dx, rms_path path,
+                      void* stream) {
+  return bwd_impl(dy, x, gamma, rstd, nullptr, dx, dgamma, workspace, workspace_bytes, M, N,
+                  dtype, gemma, inplace_dx, path, stream);
+}
+
 rms_status rms_bwd(void* dy, const void* x, const void* gamma, const float* rstd, void* dx,
                    float* dgamma, void* workspace, int64_t M, int64_t N, rms_dtype dtype, int gemma,
                    int inplace_dx, void* stream) {
-  return rms_bwd_ex(dy, x, gamma, rstd, dx, dgamma, workspace, SIZE_MAX, M, N, dtype, gemma,
-                    inplace_dx, RMS_PATH_AUTO, stream);
+  return bwd_impl(dy, x, gamma, rstd, nullptr, dx, dgamma, workspace, SIZE_MAX, M, N, dtype,
+                  gemma, inplace_dx, RMS_PATH_AUTO, stream);
+}
+
+rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const float* rstd,
+                          const void* dh, void* dx, float* dgamma, void* workspace,
+                          size_t workspace_bytes, int64_t M, int64_t N, rms_dtype dtype,
+                          int gemma, int inplace_dx, rms_path path, void* stream) {
+  if (M > 0 && !dh) return RMS_ERR_INVALID_ARG;
+  return bwd_impl(dy, h, gamma, rstd, dh, dx, dgamma, workspace, workspace_bytes, M, N, dtype,
+                  gemma, inplace_dx, path, stream);
+}
+
+rms_status rms_bwd_add(void* dy, const void* h, const void* gamma, const float* rstd,
+                       const void* dh, void* dx, float* dgamma, void* workspace, int64_t M,
+                       int64_t N, rms_dtype dtype, int gemma, int inplace_dx, void* stream) {
+  return rms_bwd_add_ex(dy, h, gamma, rstd, dh, dx, dgamma, workspace, SIZE_MAX, M, N, dtype,
+                        gemma, inplace_dx, RMS_PATH_AUTO, stream);
 }
 
 rms_status rms_last_device_status(void* stream) {

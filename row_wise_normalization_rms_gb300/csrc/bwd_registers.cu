@@ -26,11 +26,13 @@
 
 namespace rmsk {
 
-template <typename T, typename W, int KV, bool GEMMA>
+// With RES, dh (the gradient reaching the same input through a residual
+// path; it may be the dx buffer itself) is added to dx before its rounding.
+template <typename T, typename W, int KV, bool GEMMA, bool RES>
 __global__ void __launch_bounds__(512)
 rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__ gamma,
                          const float* __restrict__ rstd, T* dx, float* __restrict__ ws, int64_t M,
-                         int N, int G) {
+                         int N, int G, const T* dh) {
   using Math = RowMath<T, W, GEMMA>;
   using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
@@ -80,6 +82,15 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const W* __restri
     f32x2 sux2 = 0ull;
 #pragma unroll
     for (int k = 0; k < KV; ++k) Math::backward_sums(xv[k], dv[k], gw[k], r, sux2, acc[k]);
+    uint4 hv[RES ? KV : 1];  // fetched while the row sum is reduced
+    if (RES) {
+#pragma unroll
+      for (int k = 0; k < KV; ++k) {
+        const int v = lig + k * G;
+        hv[k] = (active && v < NV) ? ld_stream(reinterpret_cast<const uint4*>(dh) + base + v)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     const float sux = group_sum(lo2(sux2) + hi2(sux2), G, grp * (G >> 5), red[it & 1]);
     const float kc = sux / (float)N;  // r * mean(u*x)
 
@@ -88,7 +99,9 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const W* __restri
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * G;
-        if (v < NV) st_stream(out + v, Math::backward_dx(xv[k], dv[k], gw[k], r, kc));
+        if (v < NV)
+          st_stream(out + v, Math::template backward_dx<RES>(xv[k], dv[k], gw[k], r, kc,
+                                                               hv[RES ? k : 0]));
       }
     }
   }
@@ -128,40 +141,42 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const W* __restri
   }
 }
 
-template <typename T, typename W, int KV>
+template <typename T, typename W, int KV, bool RES>
 static const void* kernel_ptr(bool gemma) {
-  return gemma ? reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, W, KV, true>)
-               : reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, W, KV, false>);
+  return gemma ? reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, W, KV, true, RES>)
+               : reinterpret_cast<const void*>(&rms_bwd_registers_kernel<T, W, KV, false, RES>);
 }
 
 template <typename T, typename W>
-static const void* pick(int kv, bool gemma) {
+static const void* pick(int kv, bool gemma, bool res) {
   switch (kv) {
-    case 1: return kernel_ptr<T, W, 1>(gemma);
-    case 2: return kernel_ptr<T, W, 2>(gemma);
-    case 4: return kernel_ptr<T, W, 4>(gemma);
+    case 1: return res ? kernel_ptr<T, W, 1, true>(gemma) : kernel_ptr<T, W, 1, false>(gemma);
+    case 2: return res ? kernel_ptr<T, W, 2, true>(gemma) : kernel_ptr<T, W, 2, false>(gemma);
+    case 4: return res ? kernel_ptr<T, W, 4, true>(gemma) : kernel_ptr<T, W, 4, false>(gemma);
     default: return nullptr;
   }
 }
 
-template <typename T, typename W, bool GEMMA>
+template <typename T, typename W, bool GEMMA, bool RES>
 static cudaError_t launch_g(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)m.blocks), block(m.threads);
   const T* dy = static_cast<const T*>(a.dy);
   const T* x = static_cast<const T*>(a.x);
   const W* g = static_cast<const W*>(a.gamma);
   T* dx = static_cast<T*>(a.dx);
+  const T* dh = static_cast<const T*>(a.dh);
   switch (m.kv) {
-    case 1: return launch_pdl(rms_bwd_registers_kernel<T, W, 1, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G);
-    case 2: return launch_pdl(rms_bwd_registers_kernel<T, W, 2, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G);
-    case 4: return launch_pdl(rms_bwd_registers_kernel<T, W, 4, GEMMA>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G);
+    case 1: return launch_pdl(rms_bwd_registers_kernel<T, W, 1, GEMMA, RES>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G, dh);
+    case 2: return launch_pdl(rms_bwd_registers_kernel<T, W, 2, GEMMA, RES>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G, dh);
+    case 4: return launch_pdl(rms_bwd_registers_kernel<T, W, 4, GEMMA, RES>, grid, block, m.smem, s, dy, x, g, a.rstd, dx, a.ws, a.M, a.N, m.G, dh);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T, typename W>
 static cudaError_t launch_t(const rmsi::BwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
-  return a.gemma ? launch_g<T, W, true>(a, m, s) : launch_g<T, W, false>(a, m, s);
+  if (a.dh) return a.gemma ? launch_g<T, W, true, true>(a, m, s) : launch_g<T, W, false, true>(a, m, s);
+  return a.gemma ? launch_g<T, W, true, false>(a, m, s) : launch_g<T, W, false, false>(a, m, s);
 }
 
 }  // namespace rmsk
@@ -172,11 +187,11 @@ cudaError_t size_bwd_registers(const BwdArgs& a, const DeviceInfo& d, Mapping* m
   m->smem = m->rows_per_cta > 1 ? (size_t)m->rows_per_cta * a.N * sizeof(float) : 0;
   const void* k;
   switch (a.dtype) {
-    case kBF16: k = rmsk::pick<__nv_bfloat16, __nv_bfloat16>(m->kv, a.gemma); break;
-    case kF16: k = rmsk::pick<__half, __half>(m->kv, a.gemma); break;
-    case kBF16W32: k = rmsk::pick<__nv_bfloat16, float>(m->kv, a.gemma); break;
-    case kF16W32: k = rmsk::pick<__half, float>(m->kv, a.gemma); break;
-    default: k = rmsk::pick<float, float>(m->kv, a.gemma); break;
+    case kBF16: k = rmsk::pick<__nv_bfloat16, __nv_bfloat16>(m->kv, a.gemma, a.dh != nullptr); break;
+    case kF16: k = rmsk::pick<__half, __half>(m->kv, a.gemma, a.dh != nullptr); break;
+    case kBF16W32: k = rmsk::pick<__nv_bfloat16, float>(m->kv, a.gemma, a.dh != nullptr); break;
+    case kF16W32: k = rmsk::pick<__half, float>(m->kv, a.gemma, a.dh != nullptr); break;
+    default: k = rmsk::pick<float, float>(m->kv, a.gemma, a.dh != nullptr); break;
   }
   if (!k) return cudaErrorInvalidValue;
   int occ = 0;

@@ -33,12 +33,13 @@ __device__ __forceinline__ float cta_sum(float v, float* red, int buf) {
 }
 
 // One CTA per row at a time (grid-stride over rows).  Forward: out = r =
-// 1/sqrt(sum(x^2)/N + eps).  Backward: out = k = sum(u * x * r)/N.
-template <typename T, typename W, bool GEMMA, bool BWD>
+// 1/sqrt(sum(x^2)/N + eps); with RES the row is h = x + res, stored to h for
+// the normalise pass.  Backward: out = k = sum(u * x * r)/N.
+template <typename T, typename W, bool GEMMA, bool BWD, bool RES>
 __global__ void __launch_bounds__(kChunkThreads)
 rms_rowstat_kernel(const T* __restrict__ x, const T* __restrict__ dy, const W* __restrict__ gamma,
                    const float* __restrict__ rstd_in, float* __restrict__ out, int64_t M, int N,
-                   float eps) {
+                   float eps, const T* res, T* h) {
   using Math = RowMath<T, W, GEMMA>;
   using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
@@ -57,7 +58,18 @@ rms_rowstat_kernel(const T* __restrict__ x, const T* __restrict__ dy, const W* _
       for (int u = 0; u < kChunkVecs; ++u) {
         const int v = v0 + u * kChunkThreads;
         xv[u] = v < NV ? ld_keep(xr + v) : make_uint4(0u, 0u, 0u, 0u);
-        if (BWD) dv[u] = v < NV ? ld_keep(dr + v) : make_uint4(0u, 0u, 0u, 0u);
+        if (BWD || RES) {
+          const uint4* src = BWD ? dr : reinterpret_cast<const uint4*>(res) + row * (int64_t)NV;
+          dv[u] = v < NV ? ld_stream(src + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (RES) {
+#pragma unroll
+        for (int u = 0; u < kChunkVecs; ++u) {
+          const int v = v0 + u * kChunkThreads;
+          xv[u] = Math::add_round(xv[u], dv[u]);
+          if (v < NV) __stcg(reinterpret_cast<uint4*>(h) + row * (int64_t)NV + v, xv[u]);
+        }
       }
       f32x2 part = 0ull;
 #pragma unroll
@@ -113,11 +125,12 @@ rms_fwd_chunk_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T* __
 // dx over (row group, chunk) units: unit = (rg, c) takes rows rg, rg + RG,
 // ... in increasing order, and writes its dgamma partial for chunk c's
 // columns into workspace row rg.
-template <typename T, typename W, bool GEMMA>
+template <typename T, typename W, bool GEMMA, bool RES>
 __global__ void __launch_bounds__(kChunkThreads)
 rms_bwd_chunk_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__ gamma,
                      const float* __restrict__ rstd, const float* __restrict__ kbuf, T* dx,
-                     float* __restrict__ ws, int64_t M, int N, int nchunks, int64_t RG) {
+                     float* __restrict__ ws, int64_t M, int N, int nchunks, int64_t RG,
+                     const T* dh) {
   using Math = RowMath<T, W, GEMMA>;
   using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
@@ -155,7 +168,9 @@ rms_bwd_chunk_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__
       const int v = v0 + u * kChunkThreads;
       if (v < NV) {
         Math::backward_acc(xv[u], dv[u], r, acc[u]);
-        st_stream(out + v, Math::backward_dx(xv[u], dv[u], gv[u], r, k));
+        const uint4 hv = RES ? ld_stream(reinterpret_cast<const uint4*>(dh) + row * (int64_t)NV + v)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        st_stream(out + v, Math::template backward_dx<RES>(xv[u], dv[u], gv[u], r, k, hv));
       }
     }
   }
@@ -174,9 +189,12 @@ rms_bwd_chunk_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__
 }
 
 template <typename F>
-cudaError_t with_types(int dtype, int gemma, F&& f) {
+cudaError_t with_types(int dtype, int gemma, bool res, F&& f) {
   auto g = [&](auto* tp, auto* wp) -> cudaError_t {
-    return gemma ? f(tp, wp, std::true_type{}) : f(tp, wp, std::false_type{});
+    if (res) return gemma ? f(tp, wp, std::true_type{}, std::true_type{})
+                          : f(tp, wp, std::false_type{}, std::true_type{});
+    return gemma ? f(tp, wp, std::true_type{}, std::false_type{})
+                 : f(tp, wp, std::false_type{}, std::false_type{});
   };
   switch (dtype) {
     case rmsi::kBF16: return g((__nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr);
@@ -208,22 +226,26 @@ bool plan_chunked(int N, int dtype, Mapping* m) {
 
 cudaError_t launch_fwd_chunked(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
                                cudaStream_t s) {
-  return rmsk::with_types(a.dtype, a.gemma, [&](auto* tp, auto* wp, auto gm) -> cudaError_t {
+  return rmsk::with_types(a.dtype, a.gemma, a.res != nullptr,
+                         [&](auto* tp, auto* wp, auto gm, auto rs) -> cudaError_t {
     using T = std::remove_pointer_t<decltype(tp)>;
     using W = std::remove_pointer_t<decltype(wp)>;
     constexpr bool GEMMA = decltype(gm)::value;
+    constexpr bool RES = decltype(rs)::value;
     const T* x = static_cast<const T*>(a.x);
     const W* g = static_cast<const W*>(a.gamma);
     const int64_t rows_grid = std::min<int64_t>(a.M, (int64_t)d.sms * 4);
-    cudaError_t e = rmsk::launch_pdl(rmsk::rms_rowstat_kernel<T, W, GEMMA, false>,
+    cudaError_t e = rmsk::launch_pdl(rmsk::rms_rowstat_kernel<T, W, GEMMA, false, RES>,
                                dim3((unsigned)rows_grid), dim3(rmsk::kChunkThreads), 0, s, x,
                                (const T*)nullptr, g, (const float*)nullptr, a.rstd, a.M, a.N,
-                               a.eps);
+                               a.eps, static_cast<const T*>(a.res), static_cast<T*>(a.h));
     if (e != cudaSuccess) return e;
     const int64_t units = a.M * (int64_t)m.chunks;
     const int64_t grid = std::min<int64_t>(units, (int64_t)d.sms * 16);
+    // With a residual the normalise pass reads h, which the row pass wrote.
+    const T* src = RES ? static_cast<const T*>(a.h) : x;
     return rmsk::launch_pdl(rmsk::rms_fwd_chunk_kernel<T, W, GEMMA>, dim3((unsigned)grid),
-                      dim3(rmsk::kChunkThreads), 0, s, x, g, static_cast<T*>(a.y),
+                      dim3(rmsk::kChunkThreads), 0, s, src, g, static_cast<T*>(a.y),
                       (const float*)a.rstd, a.M, a.N, m.chunks);
   });
 }
@@ -251,21 +273,24 @@ bool size_bwd_chunked(const BwdArgs& a, const DeviceInfo& d, Mapping* m, float**
 
 cudaError_t launch_bwd_chunked(const BwdArgs& a, const Mapping& m, float* kbuf,
                                const DeviceInfo& d, cudaStream_t s) {
-  return rmsk::with_types(a.dtype, a.gemma, [&](auto* tp, auto* wp, auto gm) -> cudaError_t {
+  return rmsk::with_types(a.dtype, a.gemma, a.dh != nullptr,
+                         [&](auto* tp, auto* wp, auto gm, auto rs) -> cudaError_t {
     using T = std::remove_pointer_t<decltype(tp)>;
     using W = std::remove_pointer_t<decltype(wp)>;
     constexpr bool GEMMA = decltype(gm)::value;
+    constexpr bool RES = decltype(rs)::value;
     const T* x = static_cast<const T*>(a.x);
     const T* dy = static_cast<const T*>(a.dy);
     const W* g = static_cast<const W*>(a.gamma);
     const int64_t rows_grid = std::min<int64_t>(a.M, (int64_t)d.sms * 4);
-    cudaError_t e = rmsk::launch_pdl(rmsk::rms_rowstat_kernel<T, W, GEMMA, true>,
+    cudaError_t e = rmsk::launch_pdl(rmsk::rms_rowstat_kernel<T, W, GEMMA, true, false>,
                                dim3((unsigned)rows_grid), dim3(rmsk::kChunkThreads), 0, s, x, dy,
-                               g, a.rstd, kbuf, a.M, a.N, 0.f);
+                               g, a.rstd, kbuf, a.M, a.N, 0.f, (const T*)nullptr, (T*)nullptr);
     if (e != cudaSuccess) return e;
-    return rmsk::launch_pdl(rmsk::rms_bwd_chunk_kernel<T, W, GEMMA>, dim3((unsigned)m.blocks),
+    return rmsk::launch_pdl(rmsk::rms_bwd_chunk_kernel<T, W, GEMMA, RES>, dim3((unsigned)m.blocks),
                       dim3(rmsk::kChunkThreads), 0, s, dy, x, g, a.rstd, (const float*)kbuf,
-                      static_cast<T*>(a.dx), a.ws, a.M, a.N, m.chunks, m.partials);
+                      static_cast<T*>(a.dx), a.ws, a.M, a.N, m.chunks, m.partials,
+                      static_cast<const T*>(a.dh));
   });
 }
 

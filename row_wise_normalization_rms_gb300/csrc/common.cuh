@@ -372,9 +372,13 @@ struct RowMath {
     for (int i = 0; i < kPairs; ++i) acc[i] = fma2(P::get(dy, i), mul2(P::get(x, i), rr), acc[i]);
   }
 
-  // dx for one vector: r*u - x*r^3*c = r*(u - xn*k) with k = r*c.
+  // dx for one vector: r*u - x*r^3*c = r*(u - xn*k) with k = r*c.  With
+  // ADD, the gradient dh reaching the same input through a residual path is
+  // added in float32 before the one rounding to the output type.
+  template <bool ADD = false>
   __device__ static __forceinline__ uint4 backward_dx(const uint4& x, const uint4& dy, const G& g,
-                                                      float r, float k) {
+                                                      float r, float k,
+                                                      const uint4& dh = uint4{}) {
     const f32x2 rr = splat2(r);
     const f32x2 nk = splat2(-k);
     uint32_t o[4];
@@ -382,12 +386,30 @@ struct RowMath {
     for (int i = 0; i < kPairs; ++i) {
       const f32x2 xn = mul2(P::get(x, i), rr);
       const f32x2 u = mul2(P::get(dy, i), weight(g, i));
-      const f32x2 dx = mul2(fma2(xn, nk, u), rr);
+      f32x2 dx = mul2(fma2(xn, nk, u), rr);
+      if (ADD) dx = add2(dx, P::get(dh, i));
       if constexpr (sizeof(T) == 2) {
         o[i] = Half2Ops<T>::narrow(dx);
       } else {
         o[2 * i] = __float_as_uint(lo2(dx));
         o[2 * i + 1] = __float_as_uint(hi2(dx));
+      }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+
+  // h = x + residual for one vector: float32 sum, one rounding to the
+  // activation type (the residual stream keeps that type).
+  __device__ static __forceinline__ uint4 add_round(const uint4& a, const uint4& b) {
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) {
+      const f32x2 h = add2(P::get(a, i), P::get(b, i));
+      if constexpr (sizeof(T) == 2) {
+        o[i] = Half2Ops<T>::narrow(h);
+      } else {
+        o[2 * i] = __float_as_uint(lo2(h));
+        o[2 * i + 1] = __float_as_uint(hi2(h));
       }
     }
     return make_uint4(o[0], o[1], o[2], o[3]);

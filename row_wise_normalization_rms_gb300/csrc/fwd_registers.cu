@@ -16,10 +16,14 @@
 
 namespace rmsk {
 
-template <typename T, typename W, int KV, bool GEMMA>
-__global__ void __launch_bounds__(1024)
+// With RES the row normalised is h = x + residual (rounded to T), which is
+// also stored to h (h may be the residual buffer itself: each thread reads
+// its residual vectors before it overwrites them).
+template <typename T, typename W, int KV, bool GEMMA, bool RES>
+__global__ void __launch_bounds__(RES ? 512 : 1024)
 rms_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T* __restrict__ y,
-                         float* __restrict__ rstd, int64_t M, int N, float eps, int G) {
+                         float* __restrict__ rstd, int64_t M, int N, float eps, int G,
+                         const T* res, T* h) {
   using Math = RowMath<T, W, GEMMA>;
   using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
@@ -29,15 +33,27 @@ rms_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T
   const int lig = threadIdx.x - grp * G;
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / G) + grp;
   const bool active = row < M;
-  const uint4* xr = reinterpret_cast<const uint4*>(x) + (active ? row : 0) * (int64_t)NV;
+  const int64_t base = (active ? row : 0) * (int64_t)NV;
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + base;
   pdl_trigger();
   pdl_wait();
 
-  uint4 xv[KV];
+  uint4 xv[KV], rv[RES ? KV : 1];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * G;
-    xv[k] = (active && v < NV) ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    const bool in = active && v < NV;
+    xv[k] = in ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    if (RES) rv[k] = in ? ld_stream(reinterpret_cast<const uint4*>(res) + base + v)
+                        : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (RES) {
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = lig + k * G;
+      xv[k] = Math::add_round(xv[k], rv[k]);  // zero vectors stay zero
+      if (active && v < NV) st_stream(reinterpret_cast<uint4*>(h) + base + v, xv[k]);
+    }
   }
   f32x2 ss2 = 0ull;
 #pragma unroll
@@ -55,23 +71,26 @@ rms_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T
   }
 }
 
-template <typename T, typename W, bool GEMMA>
+template <typename T, typename W, bool GEMMA, bool RES>
 static cudaError_t launch_g(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
   const dim3 grid((unsigned)m.blocks), block(m.threads);
   const T* x = static_cast<const T*>(a.x);
   const W* g = static_cast<const W*>(a.gamma);
   T* y = static_cast<T*>(a.y);
+  const T* r = static_cast<const T*>(a.res);
+  T* h = static_cast<T*>(a.h);
   switch (m.kv) {
-    case 1: return launch_pdl(rms_fwd_registers_kernel<T, W, 1, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G);
-    case 2: return launch_pdl(rms_fwd_registers_kernel<T, W, 2, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G);
-    case 4: return launch_pdl(rms_fwd_registers_kernel<T, W, 4, GEMMA>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G);
+    case 1: return launch_pdl(rms_fwd_registers_kernel<T, W, 1, GEMMA, RES>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G, r, h);
+    case 2: return launch_pdl(rms_fwd_registers_kernel<T, W, 2, GEMMA, RES>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G, r, h);
+    case 4: return launch_pdl(rms_fwd_registers_kernel<T, W, 4, GEMMA, RES>, grid, block, 0, s, x, g, y, a.rstd, a.M, a.N, a.eps, m.G, r, h);
     default: return cudaErrorInvalidValue;
   }
 }
 
 template <typename T, typename W>
 static cudaError_t launch_t(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cudaStream_t s) {
-  return a.gemma ? launch_g<T, W, true>(a, m, s) : launch_g<T, W, false>(a, m, s);
+  if (a.res) return a.gemma ? launch_g<T, W, true, true>(a, m, s) : launch_g<T, W, false, true>(a, m, s);
+  return a.gemma ? launch_g<T, W, true, false>(a, m, s) : launch_g<T, W, false, false>(a, m, s);
 }
 
 }  // namespace rmsk

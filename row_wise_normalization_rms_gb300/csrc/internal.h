@@ -26,6 +26,8 @@ struct FwdArgs {
   float eps;
   int dtype;
   int gemma;
+  const void* res = nullptr;  // fused residual add: the row is h = x + res ...
+  void* h = nullptr;          // ... stored here (may equal res)
 };
 
 struct BwdArgs {
@@ -40,6 +42,7 @@ struct BwdArgs {
   int N;
   int dtype;
   int gemma;
+  const void* dh = nullptr;  // fused residual add: dx += dh (may equal dx)
 };
 
 // How one launch maps rows onto the GPU.
@@ -136,7 +139,8 @@ cudaError_t ln_launch_bwd(const LnBwdArgs& a, const Mapping& m, long long wait_l
 cudaError_t take_ln_device_status(int* status);
 
 // ---- staged path (staged.cu) ----
-bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m);
+// res: the fused residual add stages one more tensor (the residual, or dh).
+bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m, bool res = false);
 cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
                               long long wait_limit, cudaStream_t s);
 cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m);

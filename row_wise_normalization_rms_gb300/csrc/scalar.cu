@@ -23,7 +23,8 @@ constexpr int kScalarThreads = 256;
 template <typename T, typename W>
 __global__ void __launch_bounds__(kScalarThreads)
 rms_fwd_scalar_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T* __restrict__ y,
-                      float* __restrict__ rstd, int64_t M, int N, float eps, int gemma) {
+                      float* __restrict__ rstd, int64_t M, int N, float eps, int gemma,
+                      const T* res, T* h) {
   using E = Elem<T>;
   __shared__ float red[kScalarThreads / 32];
   const int64_t row = blockIdx.x;
@@ -32,9 +33,15 @@ rms_fwd_scalar_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T* _
   pdl_wait();
   Kahan1 acc;  // a thread adds N / kScalarThreads squares in sequence
   for (int j = threadIdx.x; j < N; j += kScalarThreads) {
-    const float f = E::to_f(xr[j]);
+    float f = E::to_f(xr[j]);
+    if (res) {  // fused residual add: h = x + res, rounded to T, stored and normalised
+      const T hv = E::from_f(f + E::to_f(res[row * N + j]));
+      h[row * N + j] = hv;
+      f = E::to_f(hv);
+    }
     acc.add(__fmul_rn(f, f));
   }
+  if (res) xr = h + row * N;  // the second pass reads h back (this thread's own elements)
   const float ss = group_sum(acc.total(), kScalarThreads, 0, red);
   const float r = 1.0f / sqrtf(ss / (float)N + eps);
   if (threadIdx.x == 0) rstd[row] = r;
@@ -51,7 +58,7 @@ template <typename T, typename W>
 __global__ void __launch_bounds__(kScalarThreads)
 rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__ gamma,
                       const float* __restrict__ rstd, T* dx, float* __restrict__ ws, int64_t M,
-                      int N, int gemma, int acc_in_smem) {
+                      int N, int gemma, int acc_in_smem, const T* dh) {
   using E = Elem<T>;
   __shared__ float red[2][kScalarThreads / 32];
   // dgamma partials of this CTA, column j owned by thread j % kScalarThreads:
@@ -82,7 +89,8 @@ rms_bwd_scalar_kernel(const T* dy, const T* __restrict__ x, const W* __restrict_
       const float g = Elem<W>::to_f(gamma[j]);
       const float w = gemma ? 1.0f + g : g;
       acc[j] = fmaf(d, xn, acc[j]);
-      out[j] = E::from_f(fmaf(-xn, k, d * w) * r);
+      const float o = fmaf(-xn, k, d * w) * r;
+      out[j] = E::from_f(dh ? o + E::to_f(dh[row * N + j]) : o);  // fused residual gradient
     }
   }
   if (acc_in_smem) {
@@ -182,7 +190,8 @@ template <typename T, typename W>
 static cudaError_t launch_fwd_scalar_t(const FwdArgs& a, dim3 grid, dim3 block, cudaStream_t s) {
   return rmsk::launch_pdl(rmsk::rms_fwd_scalar_kernel<T, W>, grid, block, 0, s,
                           static_cast<const T*>(a.x), static_cast<const W*>(a.gamma),
-                          static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps, a.gemma);
+                          static_cast<T*>(a.y), a.rstd, a.M, a.N, a.eps, a.gemma,
+                          static_cast<const T*>(a.res), static_cast<T*>(a.h));
 }
 
 cudaError_t launch_fwd_scalar(const FwdArgs& a, const Mapping& m, cudaStream_t s) {
@@ -231,7 +240,7 @@ static cudaError_t launch_bwd_scalar_t(const BwdArgs& a, const Mapping& m, cudaS
   return rmsk::launch_pdl(rmsk::rms_bwd_scalar_kernel<T, W>, grid, block, m.smem, s,
                           static_cast<const T*>(a.dy), static_cast<const T*>(a.x),
                           static_cast<const W*>(a.gamma), a.rstd, static_cast<T*>(a.dx), a.ws,
-                          a.M, a.N, a.gemma, m.smem_acc);
+                          a.M, a.N, a.gemma, m.smem_acc, static_cast<const T*>(a.dh));
 }
 
 cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s) {

@@ -45,6 +45,9 @@ struct StagedParams {
   const void* dy;        // backward input
   void* dx;              // backward output (may equal dy)
   float* ws;             // backward: [units][N] column partials
+  const void* res;       // forward with a fused residual add: h = x + res ...
+  void* h;               // ... is stored here (may equal res) and normalised
+  const void* dh;        // backward with a fused residual add: dx += dh
   int64_t M;
   int N;
   float eps;
@@ -56,7 +59,7 @@ struct StagedParams {
   int SV;  // 16-byte vectors per CTA's column slice (the whole row when C == 1)
   int64_t ntiles;
   uint32_t tile_bytes;   // R * SV * 16
-  uint32_t stage_bytes;  // tile_bytes (forward) or 2 * tile_bytes (backward)
+  uint32_t stage_bytes;  // tile_bytes times the tensors staged (x; dy; residual or dh)
   long long wait_limit;
 };
 
@@ -100,8 +103,10 @@ __device__ __forceinline__ Slice my_slice(const StagedParams& p, int NV) {
 }
 
 // Thread 0: start the copy of local tile i (rows of tile unit + i*units,
-// this CTA's slice) into stage i % S: x, and for the backward dy after it.
-template <typename T, bool BWD>
+// this CTA's slice) into stage i % S: NT tensors one after the other, x
+// first, then t1 (dy for the backward, the residual for a fused forward)
+// and t2 (dh for a fused backward).
+template <typename T, int NT, bool BWD>
 __device__ __forceinline__ void issue_tile(const StagedParams& p, const StageHeader& h,
                                            const Slice& sl, int64_t i, uint64_t pol) {
   const int64_t t = sl.unit + i * sl.units;
@@ -114,9 +119,13 @@ __device__ __forceinline__ void issue_tile(const StagedParams& p, const StageHea
   const int s = (int)(i % p.S);
   const uint32_t bar = smem_u32(&h.full[s]);
   const uint32_t dst = smem_u32(h.stages + (size_t)s * p.stage_bytes);
-  mbar_arrive_expect_tx(bar, BWD ? 2 * bytes : bytes);
+  mbar_arrive_expect_tx(bar, NT * bytes);
   tma_load_1d(dst, static_cast<const char*>(p.x) + src, bytes, bar, pol);
-  if (BWD) tma_load_1d(dst + p.tile_bytes, static_cast<const char*>(p.dy) + src, bytes, bar, pol);
+  if (NT > 1)
+    tma_load_1d(dst + p.tile_bytes, static_cast<const char*>(BWD ? p.dy : p.res) + src, bytes, bar,
+                pol);
+  if (NT > 2)
+    tma_load_1d(dst + 2 * p.tile_bytes, static_cast<const char*>(p.dh) + src, bytes, bar, pol);
 }
 
 // After an abort at local tile i: wait (bounded) for the copies this CTA
@@ -181,8 +190,11 @@ __device__ __forceinline__ float row_total(const StagedParams& p, const StageHea
 // the exchange of row partials, and a last one before exit keeps every CTA's
 // shared memory alive while its peers may still read it.
 
-template <typename T, typename W, int KV, bool GEMMA>
-__global__ void __launch_bounds__(1024)
+// With RES the residual is staged beside x; the first pass forms h = x +
+// res, stores it and reduces it, the second forms it again from the stage
+// (at most 512 threads: twice the vectors per thread are live).
+template <typename T, typename W, int KV, bool GEMMA, bool RES>
+__global__ void __launch_bounds__(RES ? 512 : 1024)
 rms_fwd_staged_kernel(const StagedParams p) {
   using Math = RowMath<T, W, GEMMA>;
   using GV = GammaVec<T, W>;
@@ -206,7 +218,7 @@ rms_fwd_staged_kernel(const StagedParams p) {
   if (threadIdx.x == 0) {
     pol = l2_evict_first_policy();
     const int64_t pre = min((int64_t)p.S, my_tiles);
-    for (; issued < pre; ++issued) issue_tile<T, false>(p, h, sl, issued, pol);
+    for (; issued < pre; ++issued) issue_tile<T, RES ? 2 : 1, false>(p, h, sl, issued, pol);
   }
 
   GV gw[KV];
@@ -232,14 +244,23 @@ rms_fwd_staged_kernel(const StagedParams p) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < sl.nvs) Math::sumsq(lds128(xs + 16u * v), ss2);
+        if (v < sl.nvs) {
+          if (RES) {
+            const uint4 hv = Math::add_round(lds128(xs + 16u * v),
+                                             lds128(xs + p.tile_bytes + 16u * v));
+            st_stream(reinterpret_cast<uint4*>(p.h) + row * (int64_t)NV + sl.v0 + v, hv);
+            Math::sumsq(hv, ss2);
+          } else {
+            Math::sumsq(lds128(xs + 16u * v), ss2);
+          }
+        }
       }
     }
     const float ss = warp_sum(lo2(ss2) + hi2(ss2));
     if ((threadIdx.x & 31) == 0) h.red[buf * 32 + warp] = ss;
     __syncthreads();  // partial sums visible; tile i-1 fully consumed
     if (threadIdx.x == 0 && i >= 1 && issued < my_tiles && !h.abort[buf])
-      issue_tile<T, false>(p, h, sl, issued++, pol);
+      issue_tile<T, RES ? 2 : 1, false>(p, h, sl, issued++, pol);
     bool abort;
     const float tot = row_total(p, h, buf, first_warp, nw, &abort);
     if (abort) {
@@ -253,7 +274,15 @@ rms_fwd_staged_kernel(const StagedParams p) {
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < sl.nvs) st_stream(yr + v, Math::forward(lds128(xs + 16u * v), gw[k], r));
+        if (v < sl.nvs) {
+          if (RES) {
+            st_stream(yr + v, Math::forward(Math::add_round(lds128(xs + 16u * v),
+                                                            lds128(xs + p.tile_bytes + 16u * v)),
+                                            gw[k], r));
+          } else {
+            st_stream(yr + v, Math::forward(lds128(xs + 16u * v), gw[k], r));
+          }
+        }
       }
     }
   }
@@ -261,7 +290,8 @@ rms_fwd_staged_kernel(const StagedParams p) {
   if (p.C > 1) cluster_sync();
 }
 
-template <typename T, typename W, int KV, bool GEMMA>
+// With RES, dh is staged after dy and added to dx before its rounding.
+template <typename T, typename W, int KV, bool GEMMA, bool RES>
 __global__ void __launch_bounds__(512)
 rms_bwd_staged_kernel(const StagedParams p) {
   using Math = RowMath<T, W, GEMMA>;
@@ -287,7 +317,7 @@ rms_bwd_staged_kernel(const StagedParams p) {
   if (threadIdx.x == 0) {
     pol = l2_evict_first_policy();
     const int64_t pre = min((int64_t)p.S, my_tiles);
-    for (; issued < pre; ++issued) issue_tile<T, true>(p, h, sl, issued, pol);
+    for (; issued < pre; ++issued) issue_tile<T, RES ? 3 : 2, true>(p, h, sl, issued, pol);
   }
 
   GV gw[KV];
@@ -327,7 +357,7 @@ rms_bwd_staged_kernel(const StagedParams p) {
     if ((threadIdx.x & 31) == 0) h.red[buf * 32 + warp] = sux;
     __syncthreads();  // partial sums visible; tile i-1 fully consumed
     if (threadIdx.x == 0 && i >= 1 && issued < my_tiles && !h.abort[buf])
-      issue_tile<T, true>(p, h, sl, issued++, pol);
+      issue_tile<T, RES ? 3 : 2, true>(p, h, sl, issued++, pol);
     bool abort;
     const float tot = row_total(p, h, buf, first_warp, nw, &abort);
     if (abort) {
@@ -337,12 +367,17 @@ rms_bwd_staged_kernel(const StagedParams p) {
     const float kc = tot / (float)p.N;  // r * mean(u*x)
     // Second pass: dx = r*(u - x*r*kc).
     if (active) {
-      uint4* out = reinterpret_cast<uint4*>(p.dx) + row * (int64_t)NV + sl.v0;
+      const int64_t vrow = row * (int64_t)NV + sl.v0;
+      uint4* out = reinterpret_cast<uint4*>(p.dx) + vrow;
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < sl.nvs)
-          st_stream(out + v, Math::backward_dx(lds128(xs + 16u * v), lds128(ds + 16u * v), gw[k], r, kc));
+        if (v < sl.nvs) {
+          const uint4 hv = RES ? lds128(ds + p.tile_bytes + 16u * v) : make_uint4(0u, 0u, 0u, 0u);
+          st_stream(out + v, Math::template backward_dx<RES>(lds128(xs + 16u * v),
+                                                             lds128(ds + 16u * v), gw[k], r, kc,
+                                                             hv));
+        }
       }
     }
   }
@@ -392,27 +427,28 @@ rms_bwd_staged_kernel(const StagedParams p) {
   if (p.C > 1) cluster_sync();
 }
 
-template <typename T, typename W, bool BWD, bool GEMMA>
+template <typename T, typename W, bool BWD, bool GEMMA, bool RES>
 static const void* staged_ptr_g(int kv) {
   if (BWD) {
     switch (kv) {
-      case 1: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 1, GEMMA>);
-      case 2: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 2, GEMMA>);
-      case 4: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 4, GEMMA>);
+      case 1: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 1, GEMMA, RES>);
+      case 2: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 2, GEMMA, RES>);
+      case 4: return reinterpret_cast<const void*>(&rms_bwd_staged_kernel<T, W, 4, GEMMA, RES>);
     }
   } else {
     switch (kv) {
-      case 1: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 1, GEMMA>);
-      case 2: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 2, GEMMA>);
-      case 4: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 4, GEMMA>);
+      case 1: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 1, GEMMA, RES>);
+      case 2: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 2, GEMMA, RES>);
+      case 4: return reinterpret_cast<const void*>(&rms_fwd_staged_kernel<T, W, 4, GEMMA, RES>);
     }
   }
   return nullptr;
 }
 
 template <typename T, typename W, bool BWD>
-static const void* staged_ptr(int kv, bool gemma) {
-  return gemma ? staged_ptr_g<T, W, BWD, true>(kv) : staged_ptr_g<T, W, BWD, false>(kv);
+static const void* staged_ptr(int kv, bool gemma, bool res) {
+  if (res) return gemma ? staged_ptr_g<T, W, BWD, true, true>(kv) : staged_ptr_g<T, W, BWD, false, true>(kv);
+  return gemma ? staged_ptr_g<T, W, BWD, true, false>(kv) : staged_ptr_g<T, W, BWD, false, false>(kv);
 }
 
 }  // namespace rmsk
@@ -442,23 +478,23 @@ namespace {
 #define RMS_STAGED_MIN_CPS 1
 #endif
 
-const void* staged_kernel(int dtype, bool bwd, int kv, bool gemma) {
+const void* staged_kernel(int dtype, bool bwd, int kv, bool gemma, bool res) {
   switch (dtype) {
     case kBF16:
-      return bwd ? rmsk::staged_ptr<__nv_bfloat16, __nv_bfloat16, true>(kv, gemma)
-                 : rmsk::staged_ptr<__nv_bfloat16, __nv_bfloat16, false>(kv, gemma);
+      return bwd ? rmsk::staged_ptr<__nv_bfloat16, __nv_bfloat16, true>(kv, gemma, res)
+                 : rmsk::staged_ptr<__nv_bfloat16, __nv_bfloat16, false>(kv, gemma, res);
     case kF16:
-      return bwd ? rmsk::staged_ptr<__half, __half, true>(kv, gemma)
-                 : rmsk::staged_ptr<__half, __half, false>(kv, gemma);
+      return bwd ? rmsk::staged_ptr<__half, __half, true>(kv, gemma, res)
+                 : rmsk::staged_ptr<__half, __half, false>(kv, gemma, res);
     case kBF16W32:
-      return bwd ? rmsk::staged_ptr<__nv_bfloat16, float, true>(kv, gemma)
-                 : rmsk::staged_ptr<__nv_bfloat16, float, false>(kv, gemma);
+      return bwd ? rmsk::staged_ptr<__nv_bfloat16, float, true>(kv, gemma, res)
+                 : rmsk::staged_ptr<__nv_bfloat16, float, false>(kv, gemma, res);
     case kF16W32:
-      return bwd ? rmsk::staged_ptr<__half, float, true>(kv, gemma)
-                 : rmsk::staged_ptr<__half, float, false>(kv, gemma);
+      return bwd ? rmsk::staged_ptr<__half, float, true>(kv, gemma, res)
+                 : rmsk::staged_ptr<__half, float, false>(kv, gemma, res);
     default:
-      return bwd ? rmsk::staged_ptr<float, float, true>(kv, gemma)
-                 : rmsk::staged_ptr<float, float, false>(kv, gemma);
+      return bwd ? rmsk::staged_ptr<float, float, true>(kv, gemma, res)
+                 : rmsk::staged_ptr<float, float, false>(kv, gemma, res);
   }
 }
 
@@ -501,11 +537,11 @@ cudaError_t occupancy(const void* k, const DeviceInfo& d, int threads, size_t sm
 // in the per-SM shared-memory budget, at least three per CTA (one being
 // processed, one whose refill waits for the next barrier, one in flight):
 // the most CTAs per SM, up to the cap, whose three stages fit.
-static bool plan_for_cluster(int C, int NV, int64_t row_bytes, bool bwd, const DeviceInfo& d,
-                             Mapping* m) {
+static bool plan_for_cluster(int C, int NV, int64_t row_bytes, bool bwd, int tensors,
+                             const DeviceInfo& d, Mapping* m) {
   if (C > 1 && NV < 64 * C) return false;  // rows this short never need a cluster
   const int SV = (NV + C - 1) / C;
-  const int max_threads = bwd ? 512 : 1024;
+  const int max_threads = (bwd || tensors > 1) ? 512 : 1024;
   int kv, G;
   if (SV <= 32) {
     kv = 1; G = 32;
@@ -528,7 +564,7 @@ static bool plan_for_cluster(int C, int NV, int64_t row_bytes, bool bwd, const D
     while (R > 1 && G * R > max_threads) --R;
   }
   const int64_t tile = (int64_t)R * SV * 16;
-  const int64_t stage = bwd ? 2 * tile : tile;
+  const int64_t stage = tensors * tile;
   const int64_t budget = RMS_STAGED_SMEM_PER_SM;
   const int64_t cap = (int64_t)d.smem_optin - rmsk::kHeaderBytes;
   int cps = 0, S = 0;
@@ -558,16 +594,17 @@ static bool plan_for_cluster(int C, int NV, int64_t row_bytes, bool bwd, const D
 // The smallest cluster (1, 2, 4 or 8 CTAs) whose plan fits: rows up to
 // 16 KiB (backward) or 64 KiB (forward) per CTA, so clusters take rows of
 // up to 128 K bf16 elements in the backward and 256 K in the forward.
-bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m) {
+bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m, bool res) {
   const int b = dtype_bytes(dtype);
   if (N <= 0 || ((int64_t)N * b) % 16 != 0) return false;
   const int64_t row_bytes = (int64_t)N * b;
   const int NV = (int)(row_bytes / 16);
+  const int tensors = (bwd ? 2 : 1) + (res ? 1 : 0);  // x [, dy] [, residual or dh]
   for (int C = 1; C <= 8; C *= 2)
-    if (plan_for_cluster(C, NV, row_bytes, bwd, d, m) && m->blocks >= RMS_STAGED_MIN_CPS)
+    if (plan_for_cluster(C, NV, row_bytes, bwd, tensors, d, m) && m->blocks >= RMS_STAGED_MIN_CPS)
       return true;
   for (int C = 1; C <= 8; C *= 2)
-    if (plan_for_cluster(C, NV, row_bytes, bwd, d, m)) return true;
+    if (plan_for_cluster(C, NV, row_bytes, bwd, tensors, d, m)) return true;
   return false;
 }
 
@@ -619,7 +656,7 @@ static cudaError_t grid_for(const void* k, const Mapping& m, const DeviceInfo& d
   return cudaSuccess;
 }
 
-static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, bool bwd,
+static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, int tensors,
                                  long long wait_limit) {
   rmsk::StagedParams p{};
   p.M = M;
@@ -631,31 +668,31 @@ static rmsk::StagedParams params(const Mapping& m, int64_t M, int N, bool bwd,
   p.SV = m.sv;
   p.ntiles = (M + p.R - 1) / p.R;
   p.tile_bytes = (uint32_t)((int64_t)p.R * p.SV * 16);
-  p.stage_bytes = bwd ? 2 * p.tile_bytes : p.tile_bytes;
+  p.stage_bytes = tensors * p.tile_bytes;
   p.wait_limit = wait_limit;
   return p;
 }
 
-template <typename T, typename W, bool GEMMA>
+template <typename T, typename W, bool GEMMA, bool RES>
 static cudaError_t launch_fwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
   StagedLaunch L(m, grid, s);
   switch (m.kv) {
-    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 1, GEMMA>, p);
-    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 2, GEMMA>, p);
-    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 4, GEMMA>, p);
+    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 1, GEMMA, RES>, p);
+    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 2, GEMMA, RES>, p);
+    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_fwd_staged_kernel<T, W, 4, GEMMA, RES>, p);
     default: return cudaErrorInvalidValue;
   }
 }
 
-template <typename T, typename W, bool GEMMA>
+template <typename T, typename W, bool GEMMA, bool RES>
 static cudaError_t launch_bwd_g(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
   StagedLaunch L(m, grid, s);
   switch (m.kv) {
-    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 1, GEMMA>, p);
-    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 2, GEMMA>, p);
-    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 4, GEMMA>, p);
+    case 1: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 1, GEMMA, RES>, p);
+    case 2: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 2, GEMMA, RES>, p);
+    case 4: return cudaLaunchKernelEx(&L.cfg, rmsk::rms_bwd_staged_kernel<T, W, 4, GEMMA, RES>, p);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -663,26 +700,37 @@ static cudaError_t launch_bwd_g(const rmsk::StagedParams& p, const Mapping& m, i
 template <typename T, typename W>
 static cudaError_t launch_fwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
-  return p.gemma ? launch_fwd_g<T, W, true>(p, m, grid, s) : launch_fwd_g<T, W, false>(p, m, grid, s);
+  if (p.res)
+    return p.gemma ? launch_fwd_g<T, W, true, true>(p, m, grid, s)
+                   : launch_fwd_g<T, W, false, true>(p, m, grid, s);
+  return p.gemma ? launch_fwd_g<T, W, true, false>(p, m, grid, s)
+                 : launch_fwd_g<T, W, false, false>(p, m, grid, s);
 }
 
 template <typename T, typename W>
 static cudaError_t launch_bwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
                                 cudaStream_t s) {
-  return p.gemma ? launch_bwd_g<T, W, true>(p, m, grid, s) : launch_bwd_g<T, W, false>(p, m, grid, s);
+  if (p.dh)
+    return p.gemma ? launch_bwd_g<T, W, true, true>(p, m, grid, s)
+                   : launch_bwd_g<T, W, false, true>(p, m, grid, s);
+  return p.gemma ? launch_bwd_g<T, W, true, false>(p, m, grid, s)
+                 : launch_bwd_g<T, W, false, false>(p, m, grid, s);
 }
 
 cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
                               long long wait_limit, cudaStream_t s) {
-  rmsk::StagedParams p = params(m, a.M, a.N, false, wait_limit);
+  rmsk::StagedParams p = params(m, a.M, a.N, a.res ? 2 : 1, wait_limit);
   p.x = a.x;
   p.gamma = a.gamma;
   p.y = a.y;
   p.rstd_out = a.rstd;
   p.eps = a.eps;
   p.gemma = a.gemma;
+  p.res = a.res;
+  p.h = a.h;
   int64_t grid = 0;
-  cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv, a.gemma), m, d, p.ntiles, &grid);
+  cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv, a.gemma, a.res != nullptr), m, d,
+                           p.ntiles, &grid);
   if (e != cudaSuccess) return e;
   switch (a.dtype) {
     case kBF16: return launch_fwd_t<__nv_bfloat16, __nv_bfloat16>(p, m, grid, s);
@@ -696,7 +744,8 @@ cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceIn
 cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
   const int64_t ntiles = (a.M + m->rows_per_cta - 1) / m->rows_per_cta;
   int64_t grid = 0;
-  cudaError_t e = grid_for(staged_kernel(a.dtype, true, m->kv, a.gemma), *m, d, ntiles, &grid);
+  cudaError_t e = grid_for(staged_kernel(a.dtype, true, m->kv, a.gemma, a.dh != nullptr), *m, d,
+                           ntiles, &grid);
   if (e != cudaSuccess) return e;
   m->blocks = grid;
   m->partials = grid / m->cluster;  // one workspace row per unit
@@ -706,7 +755,7 @@ cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
 cudaError_t launch_bwd_staged(const BwdArgs& a, const Mapping& m, const DeviceInfo& d,
                               long long wait_limit, cudaStream_t s) {
   (void)d;
-  rmsk::StagedParams p = params(m, a.M, a.N, true, wait_limit);
+  rmsk::StagedParams p = params(m, a.M, a.N, a.dh ? 3 : 2, wait_limit);
   p.x = a.x;
   p.gamma = a.gamma;
   p.rstd_in = a.rstd;
@@ -714,6 +763,7 @@ cudaError_t launch_bwd_staged(const BwdArgs& a, const Mapping& m, const DeviceIn
   p.dx = a.dx;
   p.ws = a.ws;
   p.gemma = a.gemma;
+  p.dh = a.dh;
   switch (a.dtype) {
     case kBF16: return launch_bwd_t<__nv_bfloat16, __nv_bfloat16>(p, m, m.blocks, s);
     case kF16: return launch_bwd_t<__half, __half>(p, m, m.blocks, s);

@@ -29,7 +29,7 @@ from typing import Optional, Tuple
 
 import numpy as np
 
-_TENSOR_IDS = {"x": 1, "gamma": 2, "dy": 3, "row_scale": 4, "beta": 5}
+_TENSOR_IDS = {"x": 1, "gamma": 2, "dy": 3, "row_scale": 4, "beta": 5, "residual": 6, "dh": 7}
 _CHUNK_ELEMS = 1 << 22
 
 Dist = Tuple[str, float, float]
@@ -37,9 +37,12 @@ Dist = Tuple[str, float, float]
 
 @dataclass(frozen=True)
 class Workload:
-    """One synthetic workload: the operation ("rms" or "ln"), shapes, dtype,
-    eps, flags and input laws.  For LayerNorm ``gamma`` is the weight w and
-    ``beta`` the bias law (None: no bias)."""
+    """One synthetic workload: the operation ("rms", "ln" or "rms_add": the
+    residual add fused into RMSNorm), shapes, dtype, eps, flags and input
+    laws.  For LayerNorm ``gamma`` is the weight w and ``beta`` the bias law
+    (None: no bias); for "rms_add" ``residual`` is the law of the residual
+    stream added to x, and the gradient dh reaching h through the residual
+    path follows the dy law."""
 
     name: str
     M: int
@@ -54,8 +57,9 @@ class Workload:
     inplace_dx: int = 0
     seed: int = 0
     weight_dtype: str = ""  # "" (the activations' dtype) or "f32"
-    op: str = "rms"  # "rms" or "ln"
+    op: str = "rms"  # "rms", "ln" or "rms_add"
     beta: Optional[Dist] = None  # LayerNorm bias law
+    residual: Optional[Dist] = None  # fused residual add: law of the residual stream
     note: str = field(default="", compare=False)
 
     @property
@@ -124,6 +128,16 @@ WORKLOADS = {
                    beta=("uniform", 0.0, 1.0), dy=("normal", 0.0, 0.1),
                    note="the LayerNorm chapter's backward benchmark")
           for n in (1024, 4096, 8192, 15872)],
+        # The residual add fused into RMSNorm at the Llama-7B and large-hidden
+        # shapes (the residual stream as large as x).
+        Workload("resadd_llama7b_bf16_8192x4096", 8192, 4096, "bf16", 1e-6, op="rms_add",
+                 gamma=("normal", 1.0, 0.1), dy=("normal", 0.0, 1e-2),
+                 row_scale=("loguniform", 0.1, 10.0), residual=("normal", 0.0, 1.0),
+                 note="residual add + RMSNorm, Llama-7B shape"),
+        Workload("resadd_wide_bf16_16384x8192", 16384, 8192, "bf16", 1e-5, op="rms_add",
+                 gamma=("normal", 1.0, 0.2), dy=("normal", 0.0, 1.0),
+                 row_scale=("loguniform", 0.01, 100.0), residual=("normal", 0.0, 1.0),
+                 note="residual add + RMSNorm, large-hidden shape"),
         Workload("ln_wide_bf16_16384x8192", 16384, 8192, "bf16", 1e-5, op="ln",
                  x=("normal", -2.3, 0.5), gamma=("uniform", 0.0, 1.0), beta=("uniform", 0.0, 1.0),
                  dy=("normal", 0.0, 0.1), note="LayerNorm at the large-hidden shape"),
@@ -207,8 +221,9 @@ def make_inputs(w: Workload) -> dict:
 
     Returns a dict with keys ``x``, ``gamma``, ``dy`` (float32 arrays for f32
     workloads, float16 arrays for f16 ones, uint16 bf16 bit patterns for bf16
-    ones), ``beta`` (the LayerNorm bias in the weight dtype, or None) and
-    ``row_scale`` (float64, or None).
+    ones), ``beta`` (the LayerNorm bias in the weight dtype, or None),
+    ``row_scale`` (float64, or None) and, for workloads with a residual law,
+    ``residual`` and ``dh`` (activation dtype).
     """
     scale = None
     if w.row_scale is not None:
@@ -221,7 +236,12 @@ def make_inputs(w: Workload) -> dict:
         bvals = np.empty(w.N, dtype=np.float64)
         _draw(_generator(w.seed, "beta"), w.beta, bvals)
         beta = _store(bvals, w.wdtype)
+    fused = {}
+    if w.residual is not None:
+        fused["residual"] = _matrix(w, "residual", w.residual, None)
+        fused["dh"] = _matrix(w, "dh", w.dy, None)
     return {
+        **fused,
         "x": _matrix(w, "x", w.x, scale),
         "gamma": _store(gvals, w.wdtype),
         "beta": beta,

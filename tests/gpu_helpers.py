@@ -237,3 +237,94 @@ def assert_ln_parity(w, inp, res: LnResult, rows=None, bias=True):
     bad = [str(c) for c in checks if not c.ok]
     assert not bad, f"{w.name}: " + "; ".join(bad)
     return checks
+
+
+# ------------------------------------------------------- fused residual add
+
+
+@dataclass
+class AddResult:
+    y: torch.Tensor
+    rstd: torch.Tensor
+    h: torch.Tensor
+    dx: torch.Tensor
+    dgamma: torch.Tensor
+    guards_ok: bool
+
+
+def run_fused(w, inp, path="auto", fwd_path=None, bwd_path=None, h_alias=False, dx_alias="none",
+              inplace=None) -> AddResult:
+    """rms_fwd_add then rms_bwd_add through the C ABI.  ``h_alias``: h is
+    written over the residual buffer; ``dx_alias``: "dh" (dx accumulated
+    into dh), "dy" (in place into dy) or "none"."""
+    dt = tdtype(w.dtype)
+    M, N = w.M, w.N
+    x = to_device(inp["x"], w.dtype)
+    g = to_device(inp["gamma"], w.wdtype)
+    dy = to_device(inp["dy"], w.dtype)
+    res = to_device(inp["residual"], w.dtype)
+    dh = to_device(inp["dh"], w.dtype)
+    y = Guarded((M, N), dt, _SENTINEL[w.dtype])
+    rstd = Guarded((M,), torch.float32, _SENTINEL["f32"])
+    dg = Guarded((N,), torch.float32, _SENTINEL["f32"])
+    hbuf = None if h_alias else Guarded((M, N), dt, _SENTINEL[w.dtype])
+    h = res if h_alias else hbuf.t
+    dxbuf = Guarded((M, N), dt, _SENTINEL[w.dtype]) if dx_alias == "none" else None
+    ws = torch.empty(max(rms.rms_bwd_workspace_size(M, N), 256), dtype=torch.uint8, device="cuda")
+    rms.rms_fwd_add(x, res, g, y.t, h, rstd.t, w.eps, w.gemma, path=fwd_path or path)
+    if dx_alias == "dy":
+        rms.rms_bwd_add(dy, h, g, rstd.t, dh, None, dg.t, ws, w.gemma, 1, path=bwd_path or path)
+        dx = dy
+    elif dx_alias == "dh":
+        rms.rms_bwd_add(dy, h, g, rstd.t, dh, dh, dg.t, ws, w.gemma, 0, path=bwd_path or path)
+        dx = dh
+    else:
+        rms.rms_bwd_add(dy, h, g, rstd.t, dh, dxbuf.t, dg.t, ws, w.gemma, 0, path=bwd_path or path)
+        dx = dxbuf.t
+    torch.cuda.synchronize()
+    assert rms.rms_last_device_status() == rms.RMS_OK
+    guards = y.guards_intact() and rstd.guards_intact() and dg.guards_intact() and (
+        h_alias or hbuf.guards_intact()) and (dx_alias != "none" or dxbuf.guards_intact())
+    return AddResult(y.t, rstd.t, h, dx, dg.t, guards)
+
+
+def fused_checks(w, inp, res: AddResult, rows=None):
+    """h bit-for-bit against the oracle's stored sum; y, rstd, dx, dgamma
+    within the bars, with the oracle evaluated on that h."""
+    rows = np.arange(w.M) if rows is None else rows
+    idx = torch.as_tensor(rows, device=res.y.device)
+    x = storage_to_float64(inp["x"][rows], w.dtype)
+    r_in = storage_to_float64(inp["residual"][rows], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.wdtype)
+    dy = storage_to_float64(inp["dy"][rows], w.dtype)
+    dh = storage_to_float64(inp["dh"][rows], w.dtype)
+    y_ref, r_ref, h_ref = orc.rms_forward_add(x, r_in, g, w.eps, w.gemma, w.dtype)
+    dx_ref, _, dxs, _ = orc.rms_backward_add(h_ref, g, dy, dh, w.eps, w.gemma, with_scales=True)
+    h_got = to_host64(res.h.index_select(0, idx))
+    h_bad = int(np.sum(h_got != h_ref))
+    checks = [
+        compare.check_y(to_host64(res.y.index_select(0, idx)), y_ref, w.dtype),
+        compare.check_rstd(to_host64(res.rstd.index_select(0, idx)), r_ref),
+        compare.check_dx(to_host64(res.dx.index_select(0, idx)), dx_ref, dxs, w.dtype),
+    ]
+    # dgamma over all rows, on the oracle's h
+    total = np.zeros(w.N)
+    scale = np.zeros(w.N)
+    for r0 in range(0, w.M, 1024):
+        r1 = min(w.M, r0 + 1024)
+        hh = orc.residual_add(storage_to_float64(inp["x"][r0:r1], w.dtype),
+                              storage_to_float64(inp["residual"][r0:r1], w.dtype), w.dtype)
+        d, sc = orc.rms_dgamma(hh, storage_to_float64(inp["dy"][r0:r1], w.dtype), w.eps,
+                               with_scales=True)
+        total += d
+        scale += sc
+    checks.append(compare.check_dgamma(to_host64(res.dgamma), total, scale, w.dtype))
+    return h_bad, checks
+
+
+def assert_fused_parity(w, inp, res: AddResult, rows=None):
+    assert res.guards_ok, "a kernel wrote outside its output buffer"
+    h_bad, checks = fused_checks(w, inp, res, rows)
+    assert h_bad == 0, f"{w.name}: {h_bad} elements of h differ from the stored sum"
+    bad = [str(c) for c in checks if not c.ok]
+    assert not bad, f"{w.name}: " + "; ".join(bad)

@@ -177,3 +177,23 @@ def test_ln_bwd_rejects_bad_arguments(lib):
         assert ln_b(lib, **{k: None}) == INVALID, k
     assert ln_b(lib, inplace=1, dx=10 * A) == INVALID
     assert ln_b(lib, ws=None) == WORKSPACE
+
+
+def test_fused_add_rejects_bad_arguments(lib):
+    # rms_fwd_add_ex(x, residual, gamma, y, h, rstd, M, N, eps, dtype, gemma, path, stream)
+    f = lambda **k: lib.rms_fwd_add_ex(k.get("x", A), k.get("res", 2 * A), k.get("g", 3 * A),
+                                       k.get("y", 4 * A), k.get("h", 5 * A), k.get("r", 6 * A),
+                                       k.get("M", 4), k.get("N", 8), 1e-6, 1, 0,
+                                       k.get("path", 0), None)
+    assert f(res=None) == INVALID
+    assert f(h=None) == INVALID
+    assert f(h=A) == INVALID           # h over x
+    assert f(h=4 * A) == INVALID       # h over y
+    assert f(path=5) == INVALID
+    assert f(M=0, x=None, res=None, g=None, y=None, h=None, r=None) == OK
+    # rms_bwd_add_ex(dy, h, gamma, rstd, dh, dx, dgamma, ws, wsb, M, N, dtype, gemma, inplace, path, s)
+    b = lambda **k: lib.rms_bwd_add_ex(A, 2 * A, 3 * A, 4 * A, k.get("dh", 5 * A),
+                                       k.get("dx", 6 * A), 7 * A, 8 * A, 1 << 30, 4, 8, 1, 0,
+                                       k.get("inplace", 0), 0, None)
+    assert b(dh=None) == INVALID
+    assert b(inplace=1, dx=5 * A) == INVALID  # in place means dx is dy
