@@ -533,6 +533,7 @@ def run_sweep(args):
         else:
             fwd_b, bwd_b = step_bytes(M, N, b)
         calls = max(args.steps, 2 * k)
+        first = True
         for path in paths:
             if ln:
                 fpath, bpath = {"vector": ("registers", "staged")}.get(path, (path, path))
@@ -579,6 +580,10 @@ def run_sweep(args):
             try:
                 for i in range(k):
                     fwd_call(i)  # every set gets its rstd before the backward loop
+                if first:  # the first mapping timed also pays for touching fresh buffers
+                    timed(fwd_call, calls)
+                    timed(bwd_call, calls)
+                    first = False
                 f_ms = timed(fwd_call, calls)
                 b_ms = timed(bwd_call, calls)
             except rms.RmsError as e:

@@ -100,8 +100,8 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const W* __restri
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * G;
         if (v < NV)
-          st_stream(out + v, Math::template backward_dx<RES>(xv[k], dv[k], gw[k], r, kc,
-                                                               hv[RES ? k : 0]));
+          st_stream(out + v, RES ? Math::backward_dx_add(xv[k], dv[k], gw[k], r, kc, hv[RES ? k : 0])
+                                 : Math::backward_dx(xv[k], dv[k], gw[k], r, kc));
       }
     }
   }

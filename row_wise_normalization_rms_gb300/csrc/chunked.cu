@@ -170,7 +170,8 @@ rms_bwd_chunk_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__
         Math::backward_acc(xv[u], dv[u], r, acc[u]);
         const uint4 hv = RES ? ld_stream(reinterpret_cast<const uint4*>(dh) + row * (int64_t)NV + v)
                              : make_uint4(0u, 0u, 0u, 0u);
-        st_stream(out + v, Math::template backward_dx<RES>(xv[u], dv[u], gv[u], r, k, hv));
+        st_stream(out + v, RES ? Math::backward_dx_add(xv[u], dv[u], gv[u], r, k, hv)
+                               : Math::backward_dx(xv[u], dv[u], gv[u], r, k));
       }
     }
   }

@@ -372,13 +372,9 @@ struct RowMath {
     for (int i = 0; i < kPairs; ++i) acc[i] = fma2(P::get(dy, i), mul2(P::get(x, i), rr), acc[i]);
   }
 
-  // dx for one vector: r*u - x*r^3*c = r*(u - xn*k) with k = r*c.  With
-  // ADD, the gradient dh reaching the same input through a residual path is
-  // added in float32 before the one rounding to the output type.
-  template <bool ADD = false>
+  // dx for one vector: r*u - x*r^3*c = r*(u - xn*k) with k = r*c.
   __device__ static __forceinline__ uint4 backward_dx(const uint4& x, const uint4& dy, const G& g,
-                                                      float r, float k,
-                                                      const uint4& dh = uint4{}) {
+                                                      float r, float k) {
     const f32x2 rr = splat2(r);
     const f32x2 nk = splat2(-k);
     uint32_t o[4];
@@ -386,8 +382,30 @@ struct RowMath {
     for (int i = 0; i < kPairs; ++i) {
       const f32x2 xn = mul2(P::get(x, i), rr);
       const f32x2 u = mul2(P::get(dy, i), weight(g, i));
-      f32x2 dx = mul2(fma2(xn, nk, u), rr);
-      if (ADD) dx = add2(dx, P::get(dh, i));
+      const f32x2 dx = mul2(fma2(xn, nk, u), rr);
+      if constexpr (sizeof(T) == 2) {
+        o[i] = Half2Ops<T>::narrow(dx);
+      } else {
+        o[2 * i] = __float_as_uint(lo2(dx));
+        o[2 * i + 1] = __float_as_uint(hi2(dx));
+      }
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+  }
+
+  // The same dx with the gradient dh reaching the same input through a
+  // residual path added in float32 before the one rounding.
+  __device__ static __forceinline__ uint4 backward_dx_add(const uint4& x, const uint4& dy,
+                                                          const G& g, float r, float k,
+                                                          const uint4& dh) {
+    const f32x2 rr = splat2(r);
+    const f32x2 nk = splat2(-k);
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < kPairs; ++i) {
+      const f32x2 xn = mul2(P::get(x, i), rr);
+      const f32x2 u = mul2(P::get(dy, i), weight(g, i));
+      const f32x2 dx = add2(mul2(fma2(xn, nk, u), rr), P::get(dh, i));
       if constexpr (sizeof(T) == 2) {
         o[i] = Half2Ops<T>::narrow(dx);
       } else {

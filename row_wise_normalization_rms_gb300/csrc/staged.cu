@@ -36,32 +36,32 @@ __device__ int g_rms_device_status = 0;
 
 constexpr int kHeaderBytes = 1024;  // barriers, reduction slots, abort flags
 
+// Kernel arguments, kept within 128 bytes: at 152 bytes (three more
+// pointers) the backward measured 2-7 % slower on GB300 at several shapes
+// with no other change, so the roles of the two directions share fields.
 struct StagedParams {
   const void* x;
   const void* gamma;
-  const float* rstd_in;  // backward: saved r
-  float* rstd_out;       // forward: r
-  void* y;               // forward output
-  const void* dy;        // backward input
-  void* dx;              // backward output (may equal dy)
-  float* ws;             // backward: [units][N] column partials
-  const void* res;       // forward with a fused residual add: h = x + res ...
-  void* h;               // ... is stored here (may equal res) and normalised
-  const void* dh;        // backward with a fused residual add: dx += dh
+  const void* in2;  // backward: dy; fused forward: the residual (staged beside x)
+  const void* in3;  // fused backward: dh (staged after dy)
+  void* out;        // forward: y; backward: dx (may equal dy, or dh)
+  void* h;          // fused forward: h = x + residual (may equal the residual)
+  float* rstd;      // forward: written; backward: read
+  float* ws;        // backward: [units][N] column partials
   int64_t M;
   int N;
   float eps;
-  int gemma;
   int G;   // threads per row slice
   int R;   // rows per tile (1 when C > 1)
   int S;   // stages
   int C;   // CTAs per cluster sharing one row (1: no cluster)
   int SV;  // 16-byte vectors per CTA's column slice (the whole row when C == 1)
-  int64_t ntiles;
   uint32_t tile_bytes;   // R * SV * 16
   uint32_t stage_bytes;  // tile_bytes times the tensors staged (x; dy; residual or dh)
   long long wait_limit;
+  int64_t ntiles;
 };
+static_assert(sizeof(StagedParams) <= 128, "staged kernel arguments grew past 128 bytes");
 
 struct StageHeader {
   uint64_t* full;
@@ -122,10 +122,10 @@ __device__ __forceinline__ void issue_tile(const StagedParams& p, const StageHea
   mbar_arrive_expect_tx(bar, NT * bytes);
   tma_load_1d(dst, static_cast<const char*>(p.x) + src, bytes, bar, pol);
   if (NT > 1)
-    tma_load_1d(dst + p.tile_bytes, static_cast<const char*>(BWD ? p.dy : p.res) + src, bytes, bar,
+    tma_load_1d(dst + p.tile_bytes, static_cast<const char*>(p.in2) + src, bytes, bar,
                 pol);
   if (NT > 2)
-    tma_load_1d(dst + 2 * p.tile_bytes, static_cast<const char*>(p.dh) + src, bytes, bar, pol);
+    tma_load_1d(dst + 2 * p.tile_bytes, static_cast<const char*>(p.in3) + src, bytes, bar, pol);
 }
 
 // After an abort at local tile i: wait (bounded) for the copies this CTA
@@ -269,8 +269,8 @@ rms_fwd_staged_kernel(const StagedParams p) {
     }
     const float r = 1.0f / sqrtf(tot / (float)p.N + p.eps);
     if (active) {
-      if (lig == 0 && sl.rank == 0) p.rstd_out[row] = r;
-      uint4* yr = reinterpret_cast<uint4*>(p.y) + row * (int64_t)NV + sl.v0;
+      if (lig == 0 && sl.rank == 0) p.rstd[row] = r;
+      uint4* yr = reinterpret_cast<uint4*>(p.out) + row * (int64_t)NV + sl.v0;
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
@@ -338,7 +338,7 @@ rms_bwd_staged_kernel(const StagedParams p) {
     const int buf = (int)(i & 1);
     const int64_t row = (sl.unit + i * sl.units) * p.R + q;
     const bool active = row < p.M;
-    const float r = active ? p.rstd_in[row] : 0.f;
+    const float r = active ? p.rstd[row] : 0.f;
     if (!mbar_wait(smem_u32(&h.full[s]), parity, p.wait_limit)) h.abort[buf] = 1;
 
     const uint32_t xs = smem_u32(h.stages + (size_t)s * p.stage_bytes) + row_off;
@@ -367,16 +367,18 @@ rms_bwd_staged_kernel(const StagedParams p) {
     const float kc = tot / (float)p.N;  // r * mean(u*x)
     // Second pass: dx = r*(u - x*r*kc).
     if (active) {
-      const int64_t vrow = row * (int64_t)NV + sl.v0;
-      uint4* out = reinterpret_cast<uint4*>(p.dx) + vrow;
+      uint4* out = reinterpret_cast<uint4*>(p.out) + row * (int64_t)NV + sl.v0;
 #pragma unroll
       for (int k = 0; k < KV; ++k) {
         const int v = lig + k * p.G;
-        if (v < sl.nvs) {
-          const uint4 hv = RES ? lds128(ds + p.tile_bytes + 16u * v) : make_uint4(0u, 0u, 0u, 0u);
-          st_stream(out + v, Math::template backward_dx<RES>(lds128(xs + 16u * v),
-                                                             lds128(ds + 16u * v), gw[k], r, kc,
-                                                             hv));
+        if constexpr (RES) {
+          if (v < sl.nvs)
+            st_stream(out + v, Math::backward_dx_add(lds128(xs + 16u * v), lds128(ds + 16u * v),
+                                                     gw[k], r, kc,
+                                                     lds128(ds + p.tile_bytes + 16u * v)));
+        } else {
+          if (v < sl.nvs)
+            st_stream(out + v, Math::backward_dx(lds128(xs + 16u * v), lds128(ds + 16u * v), gw[k], r, kc));
         }
       }
     }
@@ -699,45 +701,46 @@ static cudaError_t launch_bwd_g(const rmsk::StagedParams& p, const Mapping& m, i
 
 template <typename T, typename W>
 static cudaError_t launch_fwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
-                                cudaStream_t s) {
-  if (p.res)
-    return p.gemma ? launch_fwd_g<T, W, true, true>(p, m, grid, s)
-                   : launch_fwd_g<T, W, false, true>(p, m, grid, s);
-  return p.gemma ? launch_fwd_g<T, W, true, false>(p, m, grid, s)
-                 : launch_fwd_g<T, W, false, false>(p, m, grid, s);
+                                bool gemma, bool res, cudaStream_t s) {
+  if (res)
+    return gemma ? launch_fwd_g<T, W, true, true>(p, m, grid, s)
+                 : launch_fwd_g<T, W, false, true>(p, m, grid, s);
+  return gemma ? launch_fwd_g<T, W, true, false>(p, m, grid, s)
+               : launch_fwd_g<T, W, false, false>(p, m, grid, s);
 }
 
 template <typename T, typename W>
 static cudaError_t launch_bwd_t(const rmsk::StagedParams& p, const Mapping& m, int64_t grid,
-                                cudaStream_t s) {
-  if (p.dh)
-    return p.gemma ? launch_bwd_g<T, W, true, true>(p, m, grid, s)
-                   : launch_bwd_g<T, W, false, true>(p, m, grid, s);
-  return p.gemma ? launch_bwd_g<T, W, true, false>(p, m, grid, s)
-                 : launch_bwd_g<T, W, false, false>(p, m, grid, s);
+                                bool gemma, bool res, cudaStream_t s) {
+  if (res)
+    return gemma ? launch_bwd_g<T, W, true, true>(p, m, grid, s)
+                 : launch_bwd_g<T, W, false, true>(p, m, grid, s);
+  return gemma ? launch_bwd_g<T, W, true, false>(p, m, grid, s)
+               : launch_bwd_g<T, W, false, false>(p, m, grid, s);
 }
 
 cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
                               long long wait_limit, cudaStream_t s) {
-  rmsk::StagedParams p = params(m, a.M, a.N, a.res ? 2 : 1, wait_limit);
+  const bool res = a.res != nullptr;
+  rmsk::StagedParams p = params(m, a.M, a.N, res ? 2 : 1, wait_limit);
   p.x = a.x;
   p.gamma = a.gamma;
-  p.y = a.y;
-  p.rstd_out = a.rstd;
+  p.out = a.y;
+  p.rstd = a.rstd;
   p.eps = a.eps;
-  p.gemma = a.gemma;
-  p.res = a.res;
+  p.in2 = a.res;
   p.h = a.h;
   int64_t grid = 0;
-  cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv, a.gemma, a.res != nullptr), m, d,
-                           p.ntiles, &grid);
+  cudaError_t e = grid_for(staged_kernel(a.dtype, false, m.kv, a.gemma, res), m, d, p.ntiles,
+                           &grid);
   if (e != cudaSuccess) return e;
+  const bool g = a.gemma != 0;
   switch (a.dtype) {
-    case kBF16: return launch_fwd_t<__nv_bfloat16, __nv_bfloat16>(p, m, grid, s);
-    case kF16: return launch_fwd_t<__half, __half>(p, m, grid, s);
-    case kBF16W32: return launch_fwd_t<__nv_bfloat16, float>(p, m, grid, s);
-    case kF16W32: return launch_fwd_t<__half, float>(p, m, grid, s);
-    default: return launch_fwd_t<float, float>(p, m, grid, s);
+    case kBF16: return launch_fwd_t<__nv_bfloat16, __nv_bfloat16>(p, m, grid, g, res, s);
+    case kF16: return launch_fwd_t<__half, __half>(p, m, grid, g, res, s);
+    case kBF16W32: return launch_fwd_t<__nv_bfloat16, float>(p, m, grid, g, res, s);
+    case kF16W32: return launch_fwd_t<__half, float>(p, m, grid, g, res, s);
+    default: return launch_fwd_t<float, float>(p, m, grid, g, res, s);
   }
 }
 
@@ -755,21 +758,22 @@ cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m) {
 cudaError_t launch_bwd_staged(const BwdArgs& a, const Mapping& m, const DeviceInfo& d,
                               long long wait_limit, cudaStream_t s) {
   (void)d;
-  rmsk::StagedParams p = params(m, a.M, a.N, a.dh ? 3 : 2, wait_limit);
+  const bool res = a.dh != nullptr;
+  rmsk::StagedParams p = params(m, a.M, a.N, res ? 3 : 2, wait_limit);
   p.x = a.x;
   p.gamma = a.gamma;
-  p.rstd_in = a.rstd;
-  p.dy = a.dy;
-  p.dx = a.dx;
+  p.rstd = const_cast<float*>(a.rstd);  // read only in the backward
+  p.in2 = a.dy;
+  p.in3 = a.dh;
+  p.out = a.dx;
   p.ws = a.ws;
-  p.gemma = a.gemma;
-  p.dh = a.dh;
+  const bool g = a.gemma != 0;
   switch (a.dtype) {
-    case kBF16: return launch_bwd_t<__nv_bfloat16, __nv_bfloat16>(p, m, m.blocks, s);
-    case kF16: return launch_bwd_t<__half, __half>(p, m, m.blocks, s);
-    case kBF16W32: return launch_bwd_t<__nv_bfloat16, float>(p, m, m.blocks, s);
-    case kF16W32: return launch_bwd_t<__half, float>(p, m, m.blocks, s);
-    default: return launch_bwd_t<float, float>(p, m, m.blocks, s);
+    case kBF16: return launch_bwd_t<__nv_bfloat16, __nv_bfloat16>(p, m, m.blocks, g, res, s);
+    case kF16: return launch_bwd_t<__half, __half>(p, m, m.blocks, g, res, s);
+    case kBF16W32: return launch_bwd_t<__nv_bfloat16, float>(p, m, m.blocks, g, res, s);
+    case kF16W32: return launch_bwd_t<__half, float>(p, m, m.blocks, g, res, s);
+    default: return launch_bwd_t<float, float>(p, m, m.blocks, g, res, s);
   }
 }
 
