@@ -91,7 +91,9 @@ rms_bwd_registers_kernel(const T* dy, const T* __restrict__ x, const W* __restri
                                    : make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    const float sux = group_sum(lo2(sux2) + hi2(sux2), G, grp * (G >> 5), red[it & 1]);
+    const float sux = (KV == 1 && G < 32)
+                          ? lane_group_sum(lo2(sux2) + hi2(sux2), G)
+                          : group_sum(lo2(sux2) + hi2(sux2), G, grp * (G >> 5), red[it & 1]);
     const float kc = sux / (float)N;  // r * mean(u*x)
 
     if (active) {

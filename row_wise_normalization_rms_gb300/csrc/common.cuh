@@ -482,6 +482,13 @@ __device__ __forceinline__ float group_sum(float v, int G, int first_warp, float
   return s;
 }
 
+// Sum over an aligned group of G lanes of one warp (G a power of two up to
+// 32), butterfly order: every lane of the group gets the same bits.
+__device__ __forceinline__ float lane_group_sum(float v, int G) {
+  for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // Host side: launch `kernel` with programmatic stream serialisation allowed.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,

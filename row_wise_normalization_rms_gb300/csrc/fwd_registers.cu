@@ -58,7 +58,9 @@ rms_fwd_registers_kernel(const T* __restrict__ x, const W* __restrict__ gamma, T
   f32x2 ss2 = 0ull;
 #pragma unroll
   for (int k = 0; k < KV; ++k) Math::sumsq(xv[k], ss2);
-  const float ss = group_sum(lo2(ss2) + hi2(ss2), G, grp * (G >> 5), red);
+  // Rows of at most 16 vectors (KV = 1) may give each row a sub-warp group.
+  const float ss = (KV == 1 && G < 32) ? lane_group_sum(lo2(ss2) + hi2(ss2), G)
+                                       : group_sum(lo2(ss2) + hi2(ss2), G, grp * (G >> 5), red);
   const float r = 1.0f / sqrtf(ss / (float)N + eps);
   if (!active) return;  // no barrier follows
   if (lig == 0) rstd[row] = r;
@@ -98,8 +100,9 @@ static cudaError_t launch_t(const rmsi::FwdArgs& a, const rmsi::Mapping& m, cuda
 namespace rmsi {
 
 // Threads per row and vectors per thread for a row of N elements held in
-// registers.  Rows of up to 128 vectors (2 KiB) get one warp each, several
-// rows per CTA; wider rows get ceil(vectors / 4) threads rounded up to a
+// registers.  Rows of up to 16 vectors get a power-of-two group of lanes
+// (several rows per warp); rows of up to 128 vectors (2 KiB) one warp each,
+// several rows per CTA; wider rows ceil(vectors / 4) threads rounded up to a
 // warp multiple, up to 1024 threads (wider rows use the staged mapping).
 bool plan_registers(int N, int dtype, bool bwd, Mapping* m) {
   const int b = dtype_bytes(dtype);
@@ -107,7 +110,13 @@ bool plan_registers(int N, int dtype, bool bwd, Mapping* m) {
   const int NV = (int)(((int64_t)N * b) / 16);
   const int max_threads = bwd ? 512 : 1024;
   int kv, G;
-  if (NV <= 32) {
+  if (NV <= 16) {
+    // Narrow rows: a power-of-two group of lanes per row, several rows per
+    // warp, so no lane idles beyond the rounding of NV up to a power of two.
+    kv = 1;
+    G = 1;
+    while (G < NV) G *= 2;
+  } else if (NV <= 32) {
     kv = 1; G = 32;
   } else if (NV <= 64) {
     kv = 2; G = 32;

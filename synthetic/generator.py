@@ -105,6 +105,9 @@ WORKLOADS = {
         *[Workload(f"widerows_bf16_N{n}", (1 << 27) // n, n, "bf16", 1e-6,
                    note="rows wider than one CTA's shared memory (cluster split)")
           for n in (32768, 65536, 131072)],
+        *[Workload(f"widerows_bf16_N{n}", (1 << 27) // n, n, "bf16", 1e-6,
+                   note="rows wider than a cluster holds (chunked mapping)")
+          for n in (262144, 1048576)],
         Workload("wide_f16_16384x8192", 16384, 8192, "f16", 1e-5,
                  gamma=("normal", 1.0, 0.2), dy=("normal", 0.0, 1.0),
                  row_scale=("loguniform", 0.01, 100.0),
