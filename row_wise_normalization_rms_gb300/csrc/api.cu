@@ -110,10 +110,10 @@ bool plan_registers_for(int N, int dtype, bool bwd, bool res, Mapping* m) {
 }
 
 rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const DeviceInfo& d,
-                  Mapping* m, bool res = false) {
+                  Mapping* m, bool res = false, int64_t M = 0) {
   switch (path) {
     case RMS_PATH_AUTO:
-      if (aligned && prefer_staged(N, dtype, bwd) && rmsi::plan_staged(N, dtype, bwd, d, m, res)) {
+      if (aligned && prefer_staged(N, dtype, bwd) && rmsi::plan_staged(N, dtype, bwd, d, m, res, M)) {
         // A row split over many CTAs of a cluster serialises on the per-row
         // exchange; from 4 (fwd) / 8 (bwd) CTAs the chunked mapping's extra
         // pass over the row costs less (GB300, N = 65536 .. 131072 bf16).
@@ -123,7 +123,7 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
         return RMS_OK;
       }
       if (aligned && plan_registers_for(N, dtype, bwd, res, m)) return RMS_OK;
-      if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m, res)) return RMS_OK;
+      if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m, res, M)) return RMS_OK;
       if (aligned && rmsi::plan_chunked(N, dtype, m)) return RMS_OK;
       if (rmsi::plan_scalar(N, dtype, bwd, d, m)) return RMS_OK;
       return RMS_ERR_UNSUPPORTED;
@@ -132,7 +132,7 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
       return plan_registers_for(N, dtype, bwd, res, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     case RMS_PATH_STAGED:
       if (!aligned) return RMS_ERR_ALIGNMENT;
-      return rmsi::plan_staged(N, dtype, bwd, d, m, res) ? RMS_OK : RMS_ERR_UNSUPPORTED;
+      return rmsi::plan_staged(N, dtype, bwd, d, m, res, M) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     case RMS_PATH_SCALAR:
       return rmsi::plan_scalar(N, dtype, bwd, d, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     case RMS_PATH_CHUNKED:
@@ -229,7 +229,7 @@ static rms_status fwd_impl(const void* x, const void* res, const void* gamma, vo
   const bool aligned = (N * b) % 16 == 0 && aligned16(x) && aligned16(gamma) && aligned16(y) &&
                        (!fused || (aligned16(res) && aligned16(h)));
   Mapping m;
-  const rms_status st = choose(path, (int)N, dtype, false, aligned, d, &m, fused);
+  const rms_status st = choose(path, (int)N, dtype, false, aligned, d, &m, fused, M);
   if (st != RMS_OK) return st;
 
   FwdArgs a{x, gamma, y, rstd, M, (int)N, eps, (int)dtype, gemma, res, h};
@@ -335,7 +335,7 @@ static rms_status bwd_impl(void* dy, const void* x, const void* gamma, const flo
   const bool aligned = (N * b) % 16 == 0 && aligned16(dy) && aligned16(x) && aligned16(gamma) &&
                        aligned16(dx) && (!dh || aligned16(dh));
   Mapping m;
-  const rms_status st = choose(path, (int)N, dtype, true, aligned, d, &m, dh != nullptr);
+  const rms_status st = choose(path, (int)N, dtype, true, aligned, d, &m, dh != nullptr, M);
   if (st != RMS_OK) return st;
 
   BwdArgs a{dy, x, gamma, rstd, dx, dgamma, static_cast<float*>(workspace), M, (int)N,

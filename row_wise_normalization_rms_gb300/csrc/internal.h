@@ -140,7 +140,10 @@ cudaError_t take_ln_device_status(int* status);
 
 // ---- staged path (staged.cu) ----
 // res: the fused residual add stages one more tensor (the residual, or dh).
-bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m, bool res = false);
+// M (0: unknown) lets the plan shorten tiles when few rows would leave the
+// persistent CTAs' last wave ragged.
+bool plan_staged(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m, bool res = false,
+                 int64_t M = 0);
 cudaError_t launch_fwd_staged(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
                               long long wait_limit, cudaStream_t s);
 cudaError_t size_bwd_staged(const BwdArgs& a, const DeviceInfo& d, Mapping* m);
