@@ -61,6 +61,12 @@ def add_step_bytes(M: int, N: int, b: int, wb: int):
     return fwd, bwd
 
 
+def quant_fwd_bytes(M: int, N: int, b: int, wb: int):
+    """Forward with an E4M3 output: reads x, writes one byte per element, the
+    per-row scale and rstd."""
+    return M * N * b + M * N + 8 * M + N * wb
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -508,6 +514,7 @@ def run_sweep(args):
         x0, dy0, g = dev_t(inp["x"]), dev_t(inp["dy"]), dev_t(inp["gamma"], w.wdtype)
         ln = w.op == "ln"
         fused = w.op == "rms_add"
+        quant = w.op == "rms_quant"
         beta = dev_t(inp["beta"], w.wdtype) if ln and inp["beta"] is not None else None
         if fused:  # residual, h and dh add three matrices per set
             set_bytes = 7 * M * N * b
@@ -530,6 +537,10 @@ def run_sweep(args):
             fwd_b, bwd_b = ln_step_bytes(M, N, b, wb, beta is not None)
         elif fused:
             fwd_b, bwd_b = add_step_bytes(M, N, b, wb)
+        elif quant:
+            fwd_b, bwd_b = quant_fwd_bytes(M, N, b, wb), 0
+            qsets = [(torch.empty(M, N, dtype=torch.uint8, device=dev),
+                      torch.empty(M, device=dev)) for _ in range(k)]
         else:
             fwd_b, bwd_b = step_bytes(M, N, b)
         calls = max(args.steps, 2 * k)
@@ -546,6 +557,13 @@ def run_sweep(args):
                     x, dy, y, dx, r, mu = sets[i % k]
                     rms.ln_bwd(dy, x, g, mu, r, None if w.inplace_dx else dx, dg, db, ws,
                                w.inplace_dx, path=bpath)
+            elif quant:
+                def fwd_call(i):
+                    x, dy, y, dx, r, _ = sets[i % k]
+                    qq, ss = qsets[i % k]
+                    rms.rms_fwd_quant(x, g, qq, ss, r, w.eps, w.gemma, path=path)
+
+                bwd_call = None
             elif fused:
                 def fwd_call(i):
                     x, dy, y, dx, r, _ = sets[i % k]
@@ -582,15 +600,16 @@ def run_sweep(args):
                     fwd_call(i)  # every set gets its rstd before the backward loop
                 if first:  # the first mapping timed also pays for touching fresh buffers
                     timed(fwd_call, calls)
-                    timed(bwd_call, calls)
+                    if bwd_call:
+                        timed(bwd_call, calls)
                     first = False
                 f_ms = timed(fwd_call, calls)
-                b_ms = timed(bwd_call, calls)
+                b_ms = timed(bwd_call, calls) if bwd_call else None
             except rms.RmsError as e:
                 print(json.dumps({"workload": name, "path": path, "error": str(e)}), flush=True)
                 continue
             fg = fwd_b / (f_ms * 1e-3) / 1e9
-            bg = bwd_b / (b_ms * 1e-3) / 1e9
+            bg = bwd_b / (b_ms * 1e-3) / 1e9 if b_ms else None
             print(json.dumps({
                 "workload": name, "op": w.op, "M": M, "N": N, "dtype": w.dtype,
                 "weight_dtype": w.wdtype,
@@ -600,8 +619,9 @@ def run_sweep(args):
                        else "sets fit in L2: launch-bound shape"),
                 "fwd_us": round(f_ms * 1e3, 2), "fwd_gbs": round(fg, 1),
                 "fwd_frac": round(fg / peak, 4),
-                "bwd_us": round(b_ms * 1e3, 2), "bwd_gbs": round(bg, 1),
-                "bwd_frac": round(bg / peak, 4),
+                "bwd_us": round(b_ms * 1e3, 2) if b_ms else None,
+                "bwd_gbs": round(bg, 1) if bg else None,
+                "bwd_frac": round(bg / peak, 4) if bg else None,
                 "peak_gbs": peak, "peak_source": peak_kind}), flush=True)
         del sets, x0, dy0
         torch.cuda.empty_cache()

@@ -225,6 +225,32 @@ rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const floa
                           int gemma, int inplace_dx, rms_path path, void* stream);
 
 /*
+ * rms_fwd_quant — the forward with its output quantised to FP8 E4M3 in the
+ * same pass, for a GEMM that consumes it: y is computed exactly as rms_fwd
+ * stores it (same cast order and roundings) but never written; instead
+ *   amax_i = max_j |y_ij|,  scale_i = amax_i / 448  (1 for an all-zero row)
+ *   q_ij   = e4m3(y_ij * (448 / amax_i))   (float32 multiply, then round to
+ *            nearest even, saturating at +-448; y_ij ~ e4m3 value * scale_i)
+ *   x [M*N] dtype, gamma [N] read; q [M*N] bytes (E4M3: sign, 4 exponent
+ *   bits with bias 7, 3 mantissa bits, no infinities), scale [M] and
+ *   rstd [M] float32 written; no output may overlap another argument.
+ *   Mappings: RMS_PATH_REGISTERS (16-byte aligned rows and pointers, rows
+ *   up to 32 KiB) or RMS_PATH_SCALAR (any); AUTO picks the first that fits.
+ * Source: y as rms_fwd; the fusion of the consumer's cast as "02 · 手写
+ * Triton kernel:RMSNorm / RoPE / SwiGLU", sections 1-2 (neighbouring
+ * elementwise work kept in registers, each tensor read or written once).
+ * Errors: as rms_fwd; RMS_ERR_UNSUPPORTED for RMS_PATH_STAGED / CHUNKED.
+ */
+rms_status rms_fwd_quant(const void* x, const void* gamma, uint8_t* q, float* scale, float* rstd,
+                         int64_t M, int64_t N, float eps, rms_dtype dtype, int gemma,
+                         void* stream);
+
+/* rms_fwd_quant with an explicit row mapping. */
+rms_status rms_fwd_quant_ex(const void* x, const void* gamma, uint8_t* q, float* scale,
+                            float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype,
+                            int gemma, rms_path path, void* stream);
+
+/*
  * ln_fwd — forward LayerNorm over M rows of N, on the same engine.
  *   mean_i = (1/N) sum_j x_ij,  var_i = (1/N) sum_j (x_ij - mean_i)^2,
  *   rstd_i = 1/sqrt(var_i + eps),  y_ij = (x_ij - mean_i) * rstd_i * w_j + b_j

@@ -32,8 +32,15 @@ Sources (web pages on row-wise RMS normalisation):
   with h = x + residual as the residual stream stores it (the float32 sum
   rounded once to the I/O dtype) and dx = dRMS + dh.
 
+* Output quantised to FP8 E4M3 for the next GEMM (the same fusion principle):
+  ``round_e4m3`` / ``e4m3_code`` (the format: sign, 4 exponent bits with
+  bias 7, 3 mantissa bits, subnormals, no infinities, largest 448; round to
+  nearest even, saturating) and ``quantize_rows_e4m3`` / ``rms_forward_quant``
+  (per-row scale amax/448, codes of y·(448/amax) in float32).
+
 Every function here is pinned by ``tests/test_oracle_pins.py`` (and, for the
-fused residual add, ``tests/test_fused_add_oracle.py``) against values the
+fused residual add and the E4M3 output, ``tests/test_fused_add_oracle.py``
+and ``tests/test_quant_oracle.py``) against values the
 pages print, closed forms, invariants, finite differences, torch's own
 dtype arithmetic and ``torch.nn.functional.rms_norm`` with autograd in
 float64; none is "parity unpinned".
@@ -242,3 +249,55 @@ def rms_backward_add(h, gamma, dy, dh, eps: float, gemma: int = 0, with_scales: 
     if not with_scales:
         return dx, out[1]
     return dx, out[1], out[2] + np.abs(_f64(dh)), out[3]
+
+
+# ---- FP8 E4M3 output ---------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def round_e4m3(v) -> np.ndarray:
+    """Nearest E4M3 value (ties to even), saturating at ±448: spacing 2^(e-3)
+    for |v| in [2^e, 2^(e+1)), e >= -6, and 2^-9 below 2^-6 (subnormals)."""
+    v = _f64(v)
+    a = np.abs(v)
+    _, ex = np.frexp(np.maximum(a, 2.0 ** -6))  # a = m * 2^ex, m in [0.5, 1)
+    spacing = np.ldexp(1.0, ex - 1 - 3)
+    q = np.minimum(np.round(a / spacing) * spacing, E4M3_MAX)  # np.round: half to even
+    return np.copysign(q, v)
+
+
+def e4m3_code(q) -> np.ndarray:
+    """The byte of E4M3 values (as round_e4m3 returns them)."""
+    q = _f64(q)
+    a = np.abs(q)
+    sign = (np.signbit(q)).astype(np.uint8) << 7
+    sub = a < 2.0 ** -6
+    _, ex = np.frexp(np.where(sub, 1.0, a))
+    e = ex - 1
+    expf = np.where(sub, 0, e + 7)
+    mant = np.where(sub, np.round(a / 2.0 ** -9), np.round((a / np.ldexp(1.0, e) - 1.0) * 8))
+    return (sign | (expf.astype(np.uint8) << 3) | mant.astype(np.uint8)).astype(np.uint8)
+
+
+def quantize_rows_e4m3(y):
+    """Codes and per-row scales of y (values exact in float32): amax = max|y|,
+    scale = amax/448 (1 for a zero row), codes of y·(448/amax), the reciprocal
+    and the product each rounded once in float32.  Returns (q values, scale)."""
+    y32 = _round_f32(y)
+    amax = np.max(np.abs(y32), axis=-1)
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1))
+    inv = np.where(nz, np.float32(E4M3_MAX) / safe, np.float32(1)).astype(np.float32)
+    scale = np.where(nz, safe / np.float32(E4M3_MAX), np.float32(1)).astype(np.float32)
+    v = (y32 * inv[:, None]).astype(np.float32)
+    return round_e4m3(v.astype(np.float64)), scale.astype(np.float64)
+
+
+def rms_forward_quant(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf16",
+                      weight_dtype: str = ""):
+    """(q values, scale, r): y as the forward stores it (the cast-order
+    emulation, in ``dtype``), then quantize_rows_e4m3."""
+    y = emulate_forward_lowp(x, gamma, eps, gemma, dtype, weight_dtype)
+    q, scale = quantize_rows_e4m3(y)
+    return q, scale, rms_rstd(x, eps)

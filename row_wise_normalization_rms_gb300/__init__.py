@@ -140,6 +140,18 @@ def rms_bwd_add(dy, h, gamma, rstd, dh, dx, dgamma, workspace, gemma: int = 0, i
         raise RmsError(st, "rms_bwd_add")
 
 
+def rms_fwd_quant(x, gamma, q, scale, rstd, eps: float = 1e-6, gemma: int = 0, stream=None,
+                  path="auto"):
+    """RMSNorm forward quantised to FP8 E4M3: q (M,N) uint8 codes (or a
+    torch.float8_e4m3fn tensor), scale and rstd (M,) float32."""
+    M, N = x.shape
+    st = lib().rms_fwd_quant_ex(_ptr(x), _ptr(gamma), _ptr(q), _ptr(scale), _ptr(rstd), M, N,
+                                float(eps), dtype_code(x, gamma), int(gemma), _path(path),
+                                _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "rms_fwd_quant")
+
+
 def ln_fwd(x, w, b, y, mean, rstd, eps: float = 1e-5, stream=None, path="auto"):
     """LayerNorm forward: y (M,N), mean and rstd (M,) float32 from x (M,N),
     w (N,) and b (N,) or None (no bias)."""

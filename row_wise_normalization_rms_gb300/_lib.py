@@ -30,6 +30,10 @@ SIGNATURES = {
                             c_vp]),
     "rms_fwd_add_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_float, c_int,
                                c_int, c_int, c_vp]),
+    "rms_fwd_quant": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_float, c_int, c_int,
+                              c_vp]),
+    "rms_fwd_quant_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_float, c_int,
+                                 c_int, c_int, c_vp]),
     "rms_bwd_add": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_int,
                             c_int, c_int, c_vp]),
     "rms_bwd_add_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_i64,

@@ -19,7 +19,7 @@ INCLUDE = ROOT / "include"
 BUILD_DIR = ROOT / "_build"
 LIB_PATH = PKG / "librmsnorm.so"
 SOURCES = ["api.cu", "fwd_registers.cu", "bwd_registers.cu", "scalar.cu", "staged.cu", "noalloc.cu",
-           "layernorm.cu", "chunked.cu"]
+           "layernorm.cu", "chunked.cu", "quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
           f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -385,6 +385,59 @@ rms_status rms_bwd(void* dy, const void* x, const void* gamma, const float* rstd
                   gemma, inplace_dx, RMS_PATH_AUTO, stream);
 }
 
+rms_status rms_fwd_quant_ex(const void* x, const void* gamma, uint8_t* q, float* scale,
+                            float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype,
+                            int gemma, rms_path path, void* stream) {
+  if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
+  if (!isfinite(eps) || eps < 0.f) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
+  if (path == RMS_PATH_STAGED || path == RMS_PATH_CHUNKED) return RMS_ERR_UNSUPPORTED;
+  if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
+  if (M == 0) return RMS_OK;
+  if (!x || !gamma || !q || !scale || !rstd) return RMS_ERR_INVALID_ARG;
+  const int b = elem_bytes(dtype);
+  const size_t xb = matrix_bytes(M, N, b);
+  const size_t qb = matrix_bytes(M, N, 1);
+  if (xb == 0 || qb == 0) return RMS_ERR_INVALID_ARG;
+  const size_t gb = (size_t)N * rmsi::weight_bytes(dtype), rb = (size_t)M * sizeof(float);
+  const void* reads[2] = {x, gamma};
+  const size_t read_n[2] = {xb, gb};
+  const void* writes[3] = {q, scale, rstd};
+  const size_t write_n[3] = {qb, rb, rb};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 2; ++j)
+      if (overlap(writes[i], write_n[i], reads[j], read_n[j])) return RMS_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(writes[i], write_n[i], writes[j], write_n[j])) return RMS_ERR_INVALID_ARG;
+  }
+  DeviceInfo d;
+  if (!current_device(&d)) return RMS_ERR_CUDA;
+  const bool aligned =
+      (N * b) % 16 == 0 && aligned16(x) && aligned16(gamma) && aligned16(q);
+  Mapping m;
+  if (path == RMS_PATH_REGISTERS && !aligned) return RMS_ERR_ALIGNMENT;
+  const bool regs = aligned && rmsi::plan_registers((int)N, dtype, false, &m) && m.threads <= 512;
+  if (path == RMS_PATH_REGISTERS && !regs) return RMS_ERR_UNSUPPORTED;
+  if (path == RMS_PATH_SCALAR || !regs) {
+    if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
+    m.path = rmsi::kScalar;
+  } else if ((M + m.rows_per_cta - 1) / m.rows_per_cta > INT32_MAX) {
+    return RMS_ERR_UNSUPPORTED;
+  }
+  rmsi::QuantArgs a{x, gamma, q, scale, rstd, M, (int)N, eps, (int)dtype, gemma};
+  if (rmsi::launch_fwd_quant(a, m, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return RMS_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return RMS_OK;
+}
+
+rms_status rms_fwd_quant(const void* x, const void* gamma, uint8_t* q, float* scale, float* rstd,
+                         int64_t M, int64_t N, float eps, rms_dtype dtype, int gemma,
+                         void* stream) {
+  return rms_fwd_quant_ex(x, gamma, q, scale, rstd, M, N, eps, dtype, gemma, RMS_PATH_AUTO,
+                          stream);
+}
+
 rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const float* rstd,
                           const void* dh, void* dx, float* dgamma, void* workspace,
                           size_t workspace_bytes, int64_t M, int64_t N, rms_dtype dtype,
@@ -510,7 +563,7 @@ rms_status ln_bwd_ex(void* dy, const void* x, const void* w, const float* mean,
                        aligned16(dx);
   if (path == RMS_PATH_STAGED && !aligned) return RMS_ERR_ALIGNMENT;
   Mapping m;
-  if (!rmsi::ln_plan((int)N, dtype, true, path, aligned, d, &m)) return RMS_ERR_UNSUPPORTED;
+  if (!rmsi::ln_plan((int)N, dtype, true, path, aligned, d, &m, M)) return RMS_ERR_UNSUPPORTED;
   float* wsw = static_cast<float*>(workspace);
   float* wsb = reinterpret_cast<float*>(static_cast<char*>(workspace) + half);
   rmsi::LnBwdArgs a{dy, x, w, mean, rstd, dx, wsw, wsb, M, (int)N, (int)dtype};

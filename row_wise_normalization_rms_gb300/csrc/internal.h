@@ -101,6 +101,22 @@ bool size_bwd_chunked(const BwdArgs& a, const DeviceInfo& d, Mapping* m, float**
 cudaError_t launch_bwd_chunked(const BwdArgs& a, const Mapping& m, float* kbuf,
                                const DeviceInfo& d, cudaStream_t s);
 
+// ---- forward with the output quantised to FP8 E4M3 (quant.cu) ----
+struct QuantArgs {
+  const void* x;
+  const void* gamma;
+  uint8_t* q;     // [M][N] E4M3 codes
+  float* scale;   // [M] per-row scale: y ~ code * scale
+  float* rstd;    // [M]
+  int64_t M;
+  int N;
+  float eps;
+  int dtype;
+  int gemma;
+};
+// m.path kRegisters (plan_registers) or kScalar.
+cudaError_t launch_fwd_quant(const QuantArgs& a, const Mapping& m, cudaStream_t s);
+
 // ---- LayerNorm (layernorm.cu) ----
 struct LnFwdArgs {
   const void* x;
@@ -131,7 +147,8 @@ struct LnBwdArgs {
 
 // Chooses the LayerNorm mapping for a call (path as rms_path); false when
 // the requested path cannot take the shape.
-bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInfo& d, Mapping* m);
+bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInfo& d, Mapping* m,
+             int64_t M = 0);
 cudaError_t ln_launch_fwd(const LnFwdArgs& a, const Mapping& m, cudaStream_t s);
 cudaError_t ln_size_bwd(const LnBwdArgs& a, const DeviceInfo& d, Mapping* m);
 cudaError_t ln_launch_bwd(const LnBwdArgs& a, const Mapping& m, long long wait_limit,

@@ -506,7 +506,8 @@ cudaError_t ln_occupancy(const void* k, const DeviceInfo& d, int threads, size_t
 
 }  // namespace
 
-bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInfo& d, Mapping* m) {
+bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInfo& d, Mapping* m,
+             int64_t M) {
   const int b = dtype_bytes(dtype);
   const int64_t row_bytes = (int64_t)N * b;
   const int NV = (int)(row_bytes / 16);
@@ -535,6 +536,13 @@ bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInf
       int R = (int)(16384 / row_bytes);
       R = std::max(1, std::min(R, 16));
       while (R > 1 && G * R > 256) --R;
+      // Halve the tile while the persistent CTAs (two per SM at 256 threads,
+      // by registers) would get fewer than 20 tiles each (a ragged last
+      // wave), down to 8 KiB a tensor (smaller tiles cost more per row than
+      // the tail they save).
+      const int64_t ctas = (int64_t)(G * R <= 256 ? 2 : 1) * d.sms;
+      while (R > 1 && (R / 2) * row_bytes >= 8192 && M > 0 && (M + R - 1) / R < 20 * ctas)
+        R /= 2;
       const int64_t stage = 2 * (int64_t)R * row_bytes;
       const int64_t budget = 224 * 1024, cap = (int64_t)d.smem_optin - rmsk::kLnHeaderBytes;
       int cps = 0, S = 0;

@@ -1,0 +1,248 @@
+// RMSNorm forward with the output quantised to FP8 (E4M3) for the GEMM that
+// consumes it, in the same kernel: y never reaches memory in the activation
+// type, only its 1-byte codes and one float32 scale per row.
+//
+//   y    = the forward's y, with the forward's roundings (the stored value)
+//   amax = max_j |y_j|,  s = amax / 448,  q_j = e4m3(y_j * (448 / amax))
+//   (round to nearest even, saturating at +-448; a zero row gets s = 1)
+//
+// Source for y: "Hướng dẫn Triton RMSNorm: kernel, backward…", section "Vấn
+// đề và công thức tham chiếu", and the cast order of "02 · 手写 Triton
+// kernel:RMSNorm / RoPE / SwiGLU", section 3.  The fusion (an elementwise
+// neighbour kept in registers, each tensor read or written once) is that
+// page's sections 1-2; the E4M3 format and the per-row absolute-maximum
+// scale are the plain reading of "quantise y for the next GEMM".
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace rmsk {
+
+// Two float32 values to two E4M3 codes (round to nearest even, saturating
+// to the largest finite value), low element in the low byte.
+__device__ __forceinline__ uint32_t f2_to_e4m3x2(float lo, float hi) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Max over a group of G threads (as group_sum; max is order-free).
+__device__ __forceinline__ float group_max(float v, int G, int first_warp, float* red) {
+  if (G < 32) {
+    for (int o = G >> 1; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+  }
+  v = warp_max(v);
+  if (G == 32) return v;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  return warp_max(lane < (G >> 5) ? red[first_warp + lane] : 0.f);
+}
+
+// The stored y of one vector widened back to float32 pairs.
+template <typename T>
+__device__ __forceinline__ f32x2 stored_pair(const uint4& yv, int i) {
+  return Pairs<T>::get(yv, i);
+}
+
+// max |y| over one stored vector, folded into a running maximum.  For the
+// 16-bit types the magnitudes are compared packed (sign bits cleared, one
+// two-lane max per word); the float32 value of the result is exact.
+template <typename T>
+struct AbsMax;
+template <>
+struct AbsMax<float> {
+  float m = 0.f;
+  __device__ __forceinline__ void add(const uint4& v) {
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(__uint_as_float(v.x)), fabsf(__uint_as_float(v.y))),
+                       fmaxf(fabsf(__uint_as_float(v.z)), fabsf(__uint_as_float(v.w)))));
+  }
+  __device__ __forceinline__ float value() const { return m; }
+};
+template <>
+struct AbsMax<__nv_bfloat16> {
+  __nv_bfloat162 m = __floats2bfloat162_rn(0.f, 0.f);
+  __device__ __forceinline__ void add(const uint4& v) {
+    const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
+                           v.w & 0x7fff7fffu};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = __hmax2(m, *reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+  }
+  __device__ __forceinline__ float value() const {
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+};
+template <>
+struct AbsMax<__half> {
+  __half2 m = __floats2half2_rn(0.f, 0.f);
+  __device__ __forceinline__ void add(const uint4& v) {
+    const uint32_t w[4] = {v.x & 0x7fff7fffu, v.y & 0x7fff7fffu, v.z & 0x7fff7fffu,
+                           v.w & 0x7fff7fffu};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) m = __hmax2(m, *reinterpret_cast<const __half2*>(&w[i]));
+  }
+  __device__ __forceinline__ float value() const {
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+};
+
+// Row in registers (the register forward's mapping, at most 512 threads a
+// CTA, two CTAs an SM at least): r, y, amax, codes.
+template <typename T, typename W, int KV, bool GEMMA>
+__global__ void __launch_bounds__(512, 2)
+rms_fwd_quant_registers_kernel(const T* __restrict__ x, const W* __restrict__ gamma,
+                               uint8_t* __restrict__ q, float* __restrict__ scale,
+                               float* __restrict__ rstd, int64_t M, int N, float eps, int G) {
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
+  using P = Pairs<T>;
+  constexpr int VN = Elem<T>::kPerVec;
+  constexpr int NP = P::n;
+  __shared__ float red_s[32], red_m[32];
+  const int NV = N / VN;
+  const int grp = threadIdx.x / G;
+  const int lig = threadIdx.x - grp * G;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / G) + grp;
+  const bool active = row < M;
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + (active ? row : 0) * (int64_t)NV;
+  pdl_trigger();
+  pdl_wait();
+
+  uint4 v[KV];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int j = lig + k * G;
+    v[k] = (active && j < NV) ? ld_stream(xr + j) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  f32x2 ss2 = 0ull;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) Math::sumsq(v[k], ss2);
+  const float ss = (KV == 1 && G < 32) ? lane_group_sum(lo2(ss2) + hi2(ss2), G)
+                                       : group_sum(lo2(ss2) + hi2(ss2), G, grp * (G >> 5), red_s);
+  const float r = 1.0f / sqrtf(ss / (float)N + eps);
+  // y as the forward stores it, in place of x; its absolute maximum
+  AbsMax<T> am;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int j = lig + k * G;
+    if (active && j < NV) {
+      v[k] = Math::forward(v[k], GV::load(gamma, j), r);
+      am.add(v[k]);
+    }
+  }
+  const float amax = group_max(am.value(), G, grp * (G >> 5), red_m);
+  if (!active) return;  // no barrier follows
+  const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+  if (lig == 0) {
+    rstd[row] = r;
+    scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  }
+  uint8_t* qr = q + row * (int64_t)N;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int j = lig + k * G;
+    if (j < NV) {
+      uint32_t c[NP];
+      const f32x2 iv = splat2(inv);
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        const f32x2 p = mul2(stored_pair<T>(v[k], i), iv);
+        c[i] = f2_to_e4m3x2(lo2(p), hi2(p));
+      }
+      if constexpr (NP == 4) {  // 8 codes
+        *reinterpret_cast<uint2*>(qr + (int64_t)j * VN) =
+            make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+      } else {  // 4 codes
+        *reinterpret_cast<uint32_t*>(qr + (int64_t)j * VN) = c[0] | (c[1] << 16);
+      }
+    }
+  }
+}
+
+// Any alignment and width: one CTA per row, the row read three times (sum
+// of squares, absolute maximum of y, codes); element for element the same
+// roundings as the scalar forward.
+template <typename T, typename W>
+__global__ void __launch_bounds__(256)
+rms_fwd_quant_scalar_kernel(const T* __restrict__ x, const W* __restrict__ gamma,
+                            uint8_t* __restrict__ q, float* __restrict__ scale,
+                            float* __restrict__ rstd, int64_t M, int N, float eps, int gemma) {
+  using E = Elem<T>;
+  __shared__ float red_s[8], red_m[8];
+  const int64_t row = blockIdx.x;
+  const T* xr = x + row * N;
+  pdl_trigger();
+  pdl_wait();
+  Kahan1 acc;
+  for (int j = threadIdx.x; j < N; j += 256) {
+    const float f = E::to_f(xr[j]);
+    acc.add(__fmul_rn(f, f));
+  }
+  const float ss = group_sum(acc.total(), 256, 0, red_s);
+  const float r = 1.0f / sqrtf(ss / (float)N + eps);
+  auto y_at = [&](int j) {
+    const float f = E::to_f(xr[j]);
+    const float g = Elem<W>::to_f(gamma[j]);
+    const float o = gemma ? (f * r) * (1.0f + g) : Elem<W>::round(f * r) * g;
+    return E::to_f(E::from_f(o));  // the stored value
+  };
+  float am = 0.f;
+  for (int j = threadIdx.x; j < N; j += 256) am = fmaxf(am, fabsf(y_at(j)));
+  const float amax = group_max(am, 256, 0, red_m);
+  const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+  if (threadIdx.x == 0) {
+    rstd[row] = r;
+    scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  }
+  uint8_t* qr = q + row * (int64_t)N;
+  for (int j = threadIdx.x; j < N; j += 256)
+    qr[j] = (uint8_t)(f2_to_e4m3x2(__fmul_rn(y_at(j), inv), 0.f) & 0xffu);
+}
+
+template <typename F>
+cudaError_t quant_types(int dtype, int gemma, F&& f) {
+  auto g = [&](auto* tp, auto* wp) -> cudaError_t {
+    return gemma ? f(tp, wp, std::true_type{}) : f(tp, wp, std::false_type{});
+  };
+  switch (dtype) {
+    case rmsi::kBF16: return g((__nv_bfloat16*)nullptr, (__nv_bfloat16*)nullptr);
+    case rmsi::kF16: return g((__half*)nullptr, (__half*)nullptr);
+    case rmsi::kBF16W32: return g((__nv_bfloat16*)nullptr, (float*)nullptr);
+    case rmsi::kF16W32: return g((__half*)nullptr, (float*)nullptr);
+    default: return g((float*)nullptr, (float*)nullptr);
+  }
+}
+
+}  // namespace rmsk
+
+namespace rmsi {
+
+cudaError_t launch_fwd_quant(const QuantArgs& a, const Mapping& m, cudaStream_t s) {
+  return rmsk::quant_types(a.dtype, a.gemma, [&](auto* tp, auto* wp, auto gm) -> cudaError_t {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    using W = std::remove_pointer_t<decltype(wp)>;
+    constexpr bool GEMMA = decltype(gm)::value;
+    const T* x = static_cast<const T*>(a.x);
+    const W* g = static_cast<const W*>(a.gamma);
+    if (m.path == kRegisters) {
+      const dim3 grid((unsigned)((a.M + m.rows_per_cta - 1) / m.rows_per_cta)), block(m.threads);
+      switch (m.kv) {
+        case 1: return rmsk::launch_pdl(rmsk::rms_fwd_quant_registers_kernel<T, W, 1, GEMMA>, grid, block, 0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, m.G);
+        case 2: return rmsk::launch_pdl(rmsk::rms_fwd_quant_registers_kernel<T, W, 2, GEMMA>, grid, block, 0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, m.G);
+        default: return rmsk::launch_pdl(rmsk::rms_fwd_quant_registers_kernel<T, W, 4, GEMMA>, grid, block, 0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, m.G);
+      }
+    }
+    return rmsk::launch_pdl(rmsk::rms_fwd_quant_scalar_kernel<T, W>, dim3((unsigned)a.M), dim3(256),
+                            0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, a.gemma);
+  });
+}
+
+}  // namespace rmsi

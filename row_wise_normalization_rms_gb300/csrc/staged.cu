@@ -564,6 +564,7 @@ static bool plan_for_cluster(int C, int NV, int64_t row_bytes, bool bwd, int ten
   // fewer than kMinTilesPerCta tiles (coarse tiles leave the last wave
   // ragged: Llama-7B-shaped 8192 x 4096 backward 38.9 -> 36.7 us on GB300).
   constexpr int64_t kMinTilesPerCta = 20;
+  constexpr int64_t kMinTileBytes = 8192;  // per tensor: smaller tiles cost more than they save
   int R = 1;
   if (C == 1) {
     R = (int)((bwd ? 2 : 1) * RMS_STAGED_TILE_BYTES / tensors / row_bytes);
@@ -587,7 +588,7 @@ static bool plan_for_cluster(int C, int NV, int64_t row_bytes, bool bwd, int ten
         break;
       }
     }
-    if (cps == 0 || R == 1 || M <= 0) break;
+    if (cps == 0 || R == 1 || M <= 0 || (R / 2) * row_bytes < kMinTileBytes) break;
     const int64_t tiles = (M + R - 1) / R;
     if (tiles >= kMinTilesPerCta * cps * d.sms) break;
     R /= 2;

@@ -37,9 +37,9 @@ Dist = Tuple[str, float, float]
 
 @dataclass(frozen=True)
 class Workload:
-    """One synthetic workload: the operation ("rms", "ln" or "rms_add": the
-    residual add fused into RMSNorm), shapes, dtype, eps, flags and input
-    laws.  For LayerNorm ``gamma`` is the weight w and ``beta`` the bias law
+    """One synthetic workload: the operation ("rms", "ln", "rms_add": the
+    residual add fused into RMSNorm, or "rms_quant": the forward with an FP8
+    E4M3 output), shapes, dtype, eps, flags and input laws.  For LayerNorm ``gamma`` is the weight w and ``beta`` the bias law
     (None: no bias); for "rms_add" ``residual`` is the law of the residual
     stream added to x, and the gradient dh reaching h through the residual
     path follows the dy law."""
@@ -57,7 +57,7 @@ class Workload:
     inplace_dx: int = 0
     seed: int = 0
     weight_dtype: str = ""  # "" (the activations' dtype) or "f32"
-    op: str = "rms"  # "rms", "ln" or "rms_add"
+    op: str = "rms"  # "rms", "ln", "rms_add" or "rms_quant"
     beta: Optional[Dist] = None  # LayerNorm bias law
     residual: Optional[Dist] = None  # fused residual add: law of the residual stream
     note: str = field(default="", compare=False)
@@ -141,6 +141,14 @@ WORKLOADS = {
                  gamma=("normal", 1.0, 0.2), dy=("normal", 0.0, 1.0),
                  row_scale=("loguniform", 0.01, 100.0), residual=("normal", 0.0, 1.0),
                  note="residual add + RMSNorm, large-hidden shape"),
+        # The forward with its output quantised to FP8 E4M3 (one byte per
+        # element and a scale per row) at the same two shapes.
+        Workload("quant_llama7b_bf16_8192x4096", 8192, 4096, "bf16", 1e-6, op="rms_quant",
+                 gamma=("normal", 1.0, 0.1), row_scale=("loguniform", 0.1, 10.0),
+                 note="RMSNorm + E4M3 output, Llama-7B shape"),
+        Workload("quant_wide_bf16_16384x8192", 16384, 8192, "bf16", 1e-5, op="rms_quant",
+                 gamma=("normal", 1.0, 0.2), row_scale=("loguniform", 0.01, 100.0),
+                 note="RMSNorm + E4M3 output, large-hidden shape"),
         Workload("ln_wide_bf16_16384x8192", 16384, 8192, "bf16", 1e-5, op="ln",
                  x=("normal", -2.3, 0.5), gamma=("uniform", 0.0, 1.0), beta=("uniform", 0.0, 1.0),
                  dy=("normal", 0.0, 0.1), note="LayerNorm at the large-hidden shape"),

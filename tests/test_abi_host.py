@@ -197,3 +197,19 @@ def test_fused_add_rejects_bad_arguments(lib):
                                        k.get("inplace", 0), 0, None)
     assert b(dh=None) == INVALID
     assert b(inplace=1, dx=5 * A) == INVALID  # in place means dx is dy
+
+
+def test_quant_rejects_bad_arguments(lib):
+    f = lambda **k: lib.rms_fwd_quant_ex(k.get("x", A), k.get("g", 2 * A), k.get("q", 3 * A),
+                                         k.get("s", 4 * A), k.get("r", 5 * A), k.get("M", 4),
+                                         k.get("N", 8), 1e-6, k.get("dtype", 1), 0,
+                                         k.get("path", 0), None)
+    assert f(dtype=5) == INVALID
+    assert f(q=None) == INVALID
+    assert f(s=None) == INVALID
+    assert f(path=2) == UNSUPPORTED
+    assert f(path=4) == UNSUPPORTED
+    assert f(path=5) == INVALID
+    assert f(q=A + 4) == INVALID          # codes over x
+    assert f(s=3 * A + 8) == INVALID      # scale over the codes
+    assert f(M=0, x=None, g=None, q=None, s=None, r=None) == OK
