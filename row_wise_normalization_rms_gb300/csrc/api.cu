@@ -364,7 +364,7 @@ static rms_status bwd_impl(void* dy, const void* x, const void* gamma, const flo
   }
   if (e != cudaSuccess) return RMS_ERR_CUDA;
   if ((size_t)m.partials * (size_t)N * sizeof(float) > need) return RMS_ERR_WORKSPACE;  // unreachable
-  e = rmsi::launch_colreduce(a.ws, dgamma, m.partials, (int)N, s);
+  e = rmsi::launch_colreduce(a.ws, dgamma, m.partials, (int)N, d.sms, s);
   if (e != cudaSuccess) return RMS_ERR_CUDA;
   g_launches.fetch_add(2);
   return RMS_OK;
@@ -570,13 +570,12 @@ rms_status ln_bwd_ex(void* dy, const void* x, const void* w, const float* mean,
   if (rmsi::ln_size_bwd(a, d, &m) != cudaSuccess) return RMS_ERR_CUDA;
   if ((size_t)m.partials * (size_t)N * sizeof(float) > half) return RMS_ERR_WORKSPACE;  // unreachable
   if (rmsi::ln_launch_bwd(a, m, g_wait_limit.load(), s) != cudaSuccess) return RMS_ERR_CUDA;
-  if (rmsi::launch_colreduce(wsw, dw, m.partials, (int)N, s) != cudaSuccess) return RMS_ERR_CUDA;
-  int launches = 2;
-  if (db) {
-    if (rmsi::launch_colreduce(wsb, db, m.partials, (int)N, s) != cudaSuccess) return RMS_ERR_CUDA;
-    ++launches;
-  }
-  g_launches.fetch_add(launches);
+  // dw and db: one launch when both are vectorisable, else one each
+  if (rmsi::launch_colreduce2(wsw, dw, db ? wsb : nullptr, db, m.partials, (int)N, d.sms, s) !=
+      cudaSuccess)
+    return RMS_ERR_CUDA;
+  const bool vec = N % 4 == 0 && aligned16(dw) && (!db || aligned16(db));
+  g_launches.fetch_add(db && !vec ? 3 : 2);
   return RMS_OK;
 }
 

@@ -88,8 +88,14 @@ bool plan_scalar(int N, int dtype, bool bwd, const DeviceInfo& d, Mapping* m);
 cudaError_t launch_fwd_scalar(const FwdArgs& a, const Mapping& m, cudaStream_t s);
 cudaError_t size_bwd_scalar(const BwdArgs& a, const DeviceInfo& d, Mapping* m);
 cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s);
-// dgamma[j] = sum_{p < P} ws[p][j], p in increasing order.
-cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, cudaStream_t s);
+// dgamma[j] = sum_{p < P} ws[p][j] in a fixed order that depends on P and N
+// only (bitwise reproducible); sms sizes the grid.
+cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, int sms,
+                             cudaStream_t s);
+// Two such sums (out0 from ws0, out1 from ws1) in one launch; ws1 == NULL
+// makes it the single sum.
+cudaError_t launch_colreduce2(const float* ws0, float* out0, const float* ws1, float* out1,
+                              int64_t P, int N, int sms, cudaStream_t s);
 
 // ---- chunked path: rows of any width (chunked.cu) ----
 bool plan_chunked(int N, int dtype, Mapping* m);

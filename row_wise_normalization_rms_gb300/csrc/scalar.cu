@@ -124,44 +124,64 @@ rms_dgamma_colreduce_kernel(const float* __restrict__ ws, float* __restrict__ dg
   }
 }
 
-// The same sum for N % 4 == 0 with 16-byte loads: a CTA covers 32 columns
-// (8 float4 lanes) with 32 row strands; strand t sums rows t, t+32, ... in
-// increasing order with four independent float4 loads in flight, then the 32
-// strand sums are added in strand order.
-__global__ void __launch_bounds__(256)
-rms_dgamma_colreduce4_kernel(const float4* __restrict__ ws, float4* __restrict__ dgamma,
-                             int64_t P, int N4) {
-  __shared__ float4 part[32][9];
-  const int cx = threadIdx.x & 7;
-  const int strand = threadIdx.x >> 3;
-  const int64_t col4 = (int64_t)blockIdx.x * 8 + cx;
+// The same sum for N % 4 == 0 with 16-byte loads.  A CTA of 512 threads
+// covers L float4 columns with S = 512 / L row strands (L a power of two,
+// chosen on the host from P and N).  Strand t sums rows t, t+S, t+2S, ... in
+// increasing order, eight rows loaded before any is added so that a strand's
+// loads are in flight together; the S strand sums are then combined by a
+// fixed radix-8 tree (strand t adds t+h, t+2h, ... in order at each level).
+// blockIdx.y picks one of two (ws, out) pairs so that two column sums
+// (LayerNorm's dw and db) share one launch.  The order depends only on P and
+// N, so the sums are reproducible bit for bit.
+__global__ void __launch_bounds__(512)
+rms_colreduce4_kernel(const float4* __restrict__ ws0, float4* __restrict__ out0,
+                      const float4* __restrict__ ws1, float4* __restrict__ out1, int64_t P,
+                      int N4, int log2L) {
+  __shared__ float4 part[512];
+  const int L = 1 << log2L;
+  const int S = 512 >> log2L;
+  const int cx = threadIdx.x & (L - 1);
+  const int strand = threadIdx.x >> log2L;
+  const float4* ws = blockIdx.y ? ws1 : ws0;
+  float4* out = blockIdx.y ? out1 : out0;
+  const int64_t col4 = (int64_t)blockIdx.x * L + cx;
   pdl_wait();
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col4 < N4) {
     const float4* src = ws + col4;
-    int64_t p = strand;
-    for (; p + 96 < P; p += 128) {
-      const float4 a = src[p * N4], b = src[(p + 32) * N4], c = src[(p + 64) * N4],
-                   d = src[(p + 96) * N4];
-      s.x += a.x; s.y += a.y; s.z += a.z; s.w += a.w;
-      s.x += b.x; s.y += b.y; s.z += b.z; s.w += b.w;
-      s.x += c.x; s.y += c.y; s.z += c.z; s.w += c.w;
-      s.x += d.x; s.y += d.y; s.z += d.z; s.w += d.w;
-    }
-    for (; p < P; p += 32) {
-      const float4 a = src[p * N4];
-      s.x += a.x; s.y += a.y; s.z += a.z; s.w += a.w;
+    for (int64_t p0 = strand; p0 < P; p0 += 8 * (int64_t)S) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int64_t p = p0 + (int64_t)u * S;
+        if (p < P) v[u] = src[p * N4];
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (p0 + (int64_t)u * S < P) {
+          s.x += v[u].x; s.y += v[u].y; s.z += v[u].z; s.w += v[u].w;
+        }
+      }
     }
   }
-  part[strand][cx] = s;
-  __syncthreads();
-  if (strand == 0 && col4 < N4) {
-    float4 t = part[0][cx];
-    for (int q = 1; q < 32; ++q) {
-      const float4 u = part[q][cx];
-      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+  part[threadIdx.x] = s;
+  for (int h = S; h > 1;) {
+    const int g = h >= 8 ? 8 : h;
+    const int hn = h / g;
+    __syncthreads();
+    if (strand < hn) {
+      float4 t = part[threadIdx.x];
+      for (int q = 1; q < g; ++q) {
+        const float4 u = part[((strand + q * hn) << log2L) + cx];
+        t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+      }
+      part[threadIdx.x] = t;
     }
-    dgamma[col4] = t;
+    h = hn;
+  }
+  if (strand == 0 && col4 < N4) {
+    if (S > 1) s = part[cx];
+    out[col4] = s;
   }
 }
 
@@ -253,14 +273,43 @@ cudaError_t launch_bwd_scalar(const BwdArgs& a, const Mapping& m, cudaStream_t s
   }
 }
 
-cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, cudaStream_t s) {
-  if (N % 4 != 0 || ((uintptr_t)ws & 15u) || ((uintptr_t)dgamma & 15u))
+// Lanes per CTA for the vectorised column sum: at most eight rows per strand,
+// then narrower slabs (more CTAs) until the grid has a CTA per SM.  (A grid
+// past one resident wave, or a dependent launch triggered early, measured
+// slower on GB300: the column sum sits between two row kernels.)
+static int colreduce_log2_lanes(int64_t P, int N4, int sms) {
+  int log2S = 0;
+  while (log2S < 8 && ((int64_t)8 << log2S) < P) ++log2S;
+  while (log2S < 8 && ((int64_t)N4 >> (9 - log2S)) < (int64_t)sms) ++log2S;
+  return 9 - log2S;
+}
+
+cudaError_t launch_colreduce2(const float* ws0, float* out0, const float* ws1, float* out1,
+                              int64_t P, int N, int sms, cudaStream_t s) {
+  const bool two = ws1 != nullptr;
+  const bool vec = N % 4 == 0 && !((uintptr_t)ws0 & 15u) && !((uintptr_t)out0 & 15u) &&
+                   (!two || (!((uintptr_t)ws1 & 15u) && !((uintptr_t)out1 & 15u)));
+  if (!vec) {
+    cudaError_t e = rmsk::launch_pdl(rmsk::rms_dgamma_colreduce_kernel,
+                                     dim3((unsigned)((N + 31) / 32)), dim3(256), 0, s, ws0, out0,
+                                     P, N);
+    if (e != cudaSuccess || !two) return e;
     return rmsk::launch_pdl(rmsk::rms_dgamma_colreduce_kernel, dim3((unsigned)((N + 31) / 32)),
-                            dim3(256), 0, s, ws, dgamma, P, N);
+                            dim3(256), 0, s, ws1, out1, P, N);
+  }
   const int N4 = N / 4;
-  return rmsk::launch_pdl(rmsk::rms_dgamma_colreduce4_kernel, dim3((unsigned)((N4 + 7) / 8)),
-                          dim3(256), 0, s, reinterpret_cast<const float4*>(ws),
-                          reinterpret_cast<float4*>(dgamma), P, N4);
+  const int log2L = colreduce_log2_lanes(P, N4, sms);
+  const int L = 1 << log2L;
+  return rmsk::launch_pdl(rmsk::rms_colreduce4_kernel,
+                          dim3((unsigned)((N4 + L - 1) / L), two ? 2u : 1u), dim3(512), 0, s,
+                          reinterpret_cast<const float4*>(ws0), reinterpret_cast<float4*>(out0),
+                          reinterpret_cast<const float4*>(two ? ws1 : ws0),
+                          reinterpret_cast<float4*>(two ? out1 : out0), P, N4, log2L);
+}
+
+cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, int sms,
+                             cudaStream_t s) {
+  return launch_colreduce2(ws, dgamma, nullptr, nullptr, P, N, sms, s);
 }
 
 }  // namespace rmsi
