@@ -93,8 +93,8 @@ size_t workspace_need(int64_t M, int64_t N, const DeviceInfo& d) {
 // copy pipeline as soon as rows exceed 1 KiB.
 constexpr int64_t kAutoStagedRowBytesFwd = 16384;
 constexpr int64_t kAutoStagedRowBytesBwd = 1024;
-constexpr int kAutoChunkedClusterFwd = 4;
-constexpr int kAutoChunkedClusterBwd = 8;
+constexpr int kAutoChunkedClusterFwd = 2;
+constexpr int64_t kAutoChunkedRowBytesBwd = 65536;
 
 bool prefer_staged(int N, int dtype, bool bwd) {
   const int64_t row = (int64_t)N * elem_bytes(dtype);
@@ -114,17 +114,22 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
   switch (path) {
     case RMS_PATH_AUTO:
       if (aligned && prefer_staged(N, dtype, bwd) && rmsi::plan_staged(N, dtype, bwd, d, m, res, M)) {
-        // A row split over many CTAs of a cluster serialises on the per-row
-        // exchange; from 4 (fwd) / 8 (bwd) CTAs the chunked mapping's extra
-        // pass over the row costs less (GB300, N = 65536 .. 131072 bf16).
-        if (m->cluster >= (bwd ? kAutoChunkedClusterBwd : kAutoChunkedClusterFwd) &&
-            rmsi::plan_chunked(N, dtype, m))
-          return RMS_OK;
+        // A row the staged mapping splits over a cluster waits on a cluster
+        // barrier per row; the chunked mapping's one-pass cluster kernels
+        // overlap that exchange with the next row's loads.  They take
+        // forward rows the staged mapping splits at all and backward rows of
+        // 64 KiB and more (GB300 bf16: N = 65536 fwd 86 % of HBM against
+        // 68 %, N = 32768 bwd 86 % against 62 %; the 2-CTA staged backward
+        // at N = 11008 .. 16384 runs at 85-96 % against 75-86 %).
+        const bool wide = bwd ? (m->cluster > 1 && (int64_t)N * elem_bytes(dtype) >=
+                                                       kAutoChunkedRowBytesBwd)
+                              : m->cluster >= kAutoChunkedClusterFwd;
+        if (wide && rmsi::plan_chunked(N, dtype, bwd, res, m)) return RMS_OK;
         return RMS_OK;
       }
       if (aligned && plan_registers_for(N, dtype, bwd, res, m)) return RMS_OK;
       if (aligned && rmsi::plan_staged(N, dtype, bwd, d, m, res, M)) return RMS_OK;
-      if (aligned && rmsi::plan_chunked(N, dtype, m)) return RMS_OK;
+      if (aligned && rmsi::plan_chunked(N, dtype, bwd, res, m)) return RMS_OK;
       if (rmsi::plan_scalar(N, dtype, bwd, d, m)) return RMS_OK;
       return RMS_ERR_UNSUPPORTED;
     case RMS_PATH_REGISTERS:
@@ -137,7 +142,7 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
       return rmsi::plan_scalar(N, dtype, bwd, d, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     case RMS_PATH_CHUNKED:
       if (!aligned) return RMS_ERR_ALIGNMENT;
-      return rmsi::plan_chunked(N, dtype, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
+      return rmsi::plan_chunked(N, dtype, bwd, res, m) ? RMS_OK : RMS_ERR_UNSUPPORTED;
     default:
       return RMS_ERR_INVALID_ARG;
   }
@@ -244,8 +249,8 @@ static rms_status fwd_impl(const void* x, const void* res, const void* gamma, vo
       e = rmsi::launch_fwd_staged(a, m, d, g_wait_limit.load(), s);
       break;
     case rmsi::kChunked:
-      e = rmsi::launch_fwd_chunked(a, m, d, s);
-      if (e == cudaSuccess) g_launches.fetch_add(1);  // two kernels
+      e = rmsi::launch_fwd_chunked(a, m, d, g_wait_limit.load(), s);
+      if (e == cudaSuccess && !m.wide) g_launches.fetch_add(1);  // three-pass: two kernels
       break;
     default:
       if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
@@ -353,8 +358,8 @@ static rms_status bwd_impl(void* dy, const void* x, const void* gamma, const flo
     case rmsi::kChunked: {
       float* kbuf = nullptr;
       if (!rmsi::size_bwd_chunked(a, d, &m, &kbuf)) return RMS_ERR_UNSUPPORTED;
-      e = rmsi::launch_bwd_chunked(a, m, kbuf, d, s);
-      if (e == cudaSuccess) g_launches.fetch_add(1);  // three kernels
+      e = rmsi::launch_bwd_chunked(a, m, kbuf, d, g_wait_limit.load(), s);
+      if (e == cudaSuccess && !m.wide) g_launches.fetch_add(1);  // three-pass: three kernels
       break;
     }
     default:
@@ -456,10 +461,11 @@ rms_status rms_bwd_add(void* dy, const void* h, const void* gamma, const float* 
 
 rms_status rms_last_device_status(void* stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return RMS_ERR_CUDA;
-  int v = 0, w = 0;
+  int v = 0, w = 0, c = 0;
   if (rmsi::take_device_status(&v) != cudaSuccess) return RMS_ERR_CUDA;
   if (rmsi::take_ln_device_status(&w) != cudaSuccess) return RMS_ERR_CUDA;
-  return (v || w) ? RMS_ERR_TIMEOUT : RMS_OK;
+  if (rmsi::take_wide_device_status(&c) != cudaSuccess) return RMS_ERR_CUDA;
+  return (v || w || c) ? RMS_ERR_TIMEOUT : RMS_OK;
 }
 
 size_t ln_bwd_workspace_size(int64_t M, int64_t N) {

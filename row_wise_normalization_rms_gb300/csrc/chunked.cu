@@ -1,20 +1,32 @@
-// RMSNorm for rows of any width: the row is never held on chip, so every
-// pass streams it from memory.  Forward: a row pass computes r (into rstd),
-// then a normalise pass over (row, chunk) units writes y.  Backward: a row
-// pass computes k = r * mean(u * x) per row, then (row group, chunk) units
-// write dx and keep dgamma partials for their chunk's columns in registers
-// across the group's rows; the fixed-order column reduction finishes dgamma.
-// Three passes over x (and dy) instead of two, no shared-memory limit on N.
+// RMSNorm for rows wider than one CTA holds: the row is never held on chip
+// whole, so every pass streams it from memory.
+//
+// One-pass mapping (rows up to 16 slices): a thread-block cluster of C CTAs
+// takes each row, CTA rank c the column slice [c*SV, (c+1)*SV).  First pass:
+// the slice comes from HBM into registers and the CTA's partial sum goes to
+// its shared memory; a split cluster barrier publishes it, and while the
+// barrier completes the slice of the cluster's next row is already on its
+// way.  Second pass: every CTA adds the C partials in rank order (the same
+// total in each), reads its slice again -- from L2, where the first pass left
+// it a moment before -- and writes the outputs.  HBM sees every input once.
+// The backward keeps dgamma partials of its slice in registers across the
+// cluster's rows; the fixed-order column reduction finishes dgamma.
+//
+// Three-pass mapping (wider rows): a row pass computes r (forward) or
+// k = r * mean(u * x) (backward) per row, then (row, chunk) units write the
+// outputs, re-reading the row from memory; no width limit.
 //
 // Sources: "Hướng dẫn Triton RMSNorm: kernel, backward…", sections "Vấn đề
 // và công thức tham chiếu" (r, y) and "Backward đầu vào: giữ đúng N" (dx,
 // dgamma); the looped row reduction for rows wider than one block is the
 // LN chapter's ("第 07 章:LayerNorm——反向传播与原子锁", step 3).
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace rmsk {
 
@@ -189,6 +201,291 @@ rms_bwd_chunk_kernel(const T* dy, const T* __restrict__ x, const W* __restrict__
   }
 }
 
+
+// ---- one-pass mapping: a cluster of CTAs per row ------------------------------
+constexpr int kWideThreads = 512;
+constexpr int kWideWarps = kWideThreads / 32;
+constexpr int kWideMaxCluster = 16;            // non-portable cluster size
+constexpr int kWideGammaSmem = 128 * 1024;     // the CTA's weight slice in shared memory
+
+struct WideParams {
+  const void* x;
+  const void* gamma;
+  const void* in2;  // backward: dy; fused forward: the residual
+  const void* in3;  // fused backward: dh
+  void* out;        // forward: y; backward: dx (may equal dy, or dh)
+  void* h;          // fused forward: h = x + residual (may equal the residual)
+  float* rstd;      // forward: written; backward: read
+  float* ws;        // backward: [units][N] column partials
+  int64_t M;
+  int N;
+  float eps;
+  int C;   // CTAs per cluster
+  int SV;  // 16-byte vectors per CTA slice: KV * kWideThreads
+  long long wait_limit;  // polls of an exchange wait before the status word is raised
+};
+
+// Nonzero once an exchange wait of a one-pass kernel ran past the wait
+// limit; read and cleared by the host.
+__device__ int g_wide_device_status = 0;
+
+// Row-partial exchange of the one-pass kernels.  Slot [buf][c] of every CTA
+// of the cluster receives CTA c's partial of the row: from each peer by
+// st.async, which completes 4 transaction bytes on the receiver's barrier
+// bars[buf]; its own by a plain store followed by this CTA's one arrival on
+// bars[buf], which also expects the (C-1)*4 bytes of the peers.  No fence
+// and no cluster barrier per row.  Rows alternate between the two
+// slots/barriers (buf); a CTA pushes row i only after completing row i-1,
+// which needed the receiver's push of row i-1, made after the receiver had
+// finished with row i-2: so a push of row i never meets slot or barrier
+// state of row i-2.  With C == 1 no cluster instruction is used.
+struct WideExchange {
+  uint64_t bars[2];
+  float slots[2][kWideMaxCluster];
+};
+
+__device__ __forceinline__ void wide_init(WideExchange& x, int C) {
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&x.bars[0]), 1);
+    mbar_init(smem_u32(&x.bars[1]), 1);
+    fence_mbar_init();
+  }
+  if (C > 1) {
+    cluster_sync();  // every CTA's barriers exist before any push
+  } else {
+    __syncthreads();
+  }
+}
+
+// This CTA's sum of one float per thread (warps in order): thread c sends it
+// to slot [buf][rank] of CTA c (thread `rank` writes its own CTA's slot and
+// arrives).  `red` alternates with buf, so the one CTA barrier here suffices.
+__device__ __forceinline__ void wide_publish(float v, float (*red)[kWideWarps], WideExchange& x,
+                                             int buf, int rank, int C) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[buf][threadIdx.x >> 5] = v;
+  __syncthreads();
+  if ((int)threadIdx.x < C) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWideWarps; ++w) t += red[buf][w];
+    const uint32_t bar = smem_u32(&x.bars[buf]);
+    if ((int)threadIdx.x == rank) {
+      x.slots[buf][rank] = t;
+      // The arrival releases the slot store to the CTA's waiting threads.
+      if (C == 1) {
+        mbar_arrive(bar);
+      } else {
+        mbar_arrive_expect_tx(bar, 4u * (uint32_t)(C - 1));
+      }
+    } else {
+      const uint32_t slot = smem_u32(&x.slots[buf][rank]);
+      st_async_f32(map_to_rank(slot, threadIdx.x), t, map_to_rank(bar, threadIdx.x));
+    }
+  }
+}
+
+// The row total once all C partials of slot `buf` are in (barrier phase
+// parity `parity`): the slots in rank order.  A wait that runs past `limit`
+// polls raises the status word and then waits out the phase (bounded): the
+// exchange never skips a row, so every CTA keeps the same barrier phases.
+__device__ __forceinline__ float wide_total(WideExchange& x, int buf, uint32_t parity, int C,
+                                            long long limit) {
+  const uint32_t bar = smem_u32(&x.bars[buf]);
+  if (!mbar_wait(bar, parity, limit)) {
+    g_wide_device_status = 1;
+    mbar_wait(bar, parity, kDrainPolls);
+  }
+  float t = 0.f;
+  for (int c = 0; c < C; ++c) t += x.slots[buf][c];
+  return t;
+}
+
+// Forward.  Thread t owns vectors v0 + t + k*kWideThreads (k < KV) of every
+// row of its cluster; rows u, u + U, ... for cluster u of U.  The slice of
+// the next row is loaded while the current one is exchanged; the second
+// pass reads the current slice again, from L2 (holding it in registers
+// instead costs the second CTA per SM, and measured slower on GB300).  With
+// RES the first pass forms h = x + residual, stores it and reduces it.
+template <typename T, typename W, int KV, bool GEMMA, bool RES>
+__global__ void __launch_bounds__(kWideThreads, KV <= 4 ? 2 : 1)
+rms_fwd_wide_kernel(const WideParams p) {
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
+  constexpr int VN = Elem<T>::kPerVec;
+  extern __shared__ __align__(16) uint8_t wide_smem[];
+  GV* gs = reinterpret_cast<GV*>(wide_smem);  // this thread's weights at [t + k*kWideThreads]
+  __shared__ float red[2][kWideWarps];
+  __shared__ WideExchange xch;
+  const int NV = p.N / VN;
+  const int rank = p.C > 1 ? (int)cluster_rank() : 0;
+  const int64_t unit = blockIdx.x / p.C;
+  const int64_t units = gridDim.x / p.C;
+  const int tid = threadIdx.x;
+  const int v0 = rank * p.SV + tid;
+  wide_init(xch, p.C);
+  pdl_wait();
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = v0 + k * kWideThreads;
+    if (v < NV) gs[tid + k * kWideThreads] = GV::load(p.gamma, v);
+  }
+
+  uint4 a[KV], b[RES ? KV : 1];  // the slice of the next row, as loaded
+  auto fetch = [&](int64_t row) {
+    const uint4* xr = static_cast<const uint4*>(p.x) + row * (int64_t)NV;
+    const uint4* rr = static_cast<const uint4*>(p.in2) + row * (int64_t)NV;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = v0 + k * kWideThreads;
+      a[k] = v < NV ? __ldcg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+      if (RES) b[k] = v < NV ? __ldcg(rr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+
+  int64_t row = unit;
+  if (row < p.M) fetch(row);
+  for (int it = 0; row < p.M; ++it) {
+    const int buf = it & 1;
+    // First pass: the slice's sum of squares.
+    Kahan2 ss;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = v0 + k * kWideThreads;
+      uint4 hv = a[k];
+      if (v < NV) {
+        if (RES) {
+          hv = Math::add_round(a[k], b[k]);
+          __stcg(static_cast<uint4*>(p.h) + row * (int64_t)NV + v, hv);
+        }
+        f32x2 t = 0ull;
+        Math::sumsq(hv, t);
+        ss.add(t);
+      }
+    }
+    wide_publish(ss.total(), red, xch, buf, rank, p.C);
+    const int64_t next = row + units;
+    if (next < p.M) fetch(next);  // in flight across the exchange and the second pass
+    const float tot = wide_total(xch, buf, (uint32_t)(it >> 1) & 1u, p.C, p.wait_limit);
+    const float r = 1.0f / sqrtf(tot / (float)p.N + p.eps);
+    if (rank == 0 && tid == 0) p.rstd[row] = r;
+    // Second pass: the slice again, now from L2.
+    const uint4* src = static_cast<const uint4*>(RES ? p.h : p.x) + row * (int64_t)NV;
+    uint4* yr = static_cast<uint4*>(p.out) + row * (int64_t)NV;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = v0 + k * kWideThreads;
+      if (v < NV) {
+        st_stream(yr + v, Math::forward(__ldcs(src + v), gs[tid + k * kWideThreads], r));
+      }
+    }
+    row = next;
+  }
+  if (p.C > 1) cluster_sync();
+}
+
+// Backward (KV = 4, one CTA per SM): first pass r*sum(u*x) over the slice;
+// second pass dgamma terms and dx (+ dh with RES) from the held slice while
+// the next row's slice loads.  The cluster's dgamma partial for its slice
+// goes to workspace row u.
+template <typename T, typename W, bool GEMMA, bool RES>
+__global__ void __launch_bounds__(kWideThreads, 1)
+rms_bwd_wide_kernel(const WideParams p) {
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
+  constexpr int VN = Elem<T>::kPerVec;
+  constexpr int NP = Math::kPairs;
+  constexpr int KV = 4;
+  extern __shared__ __align__(16) uint8_t wide_smem[];
+  GV* gs = reinterpret_cast<GV*>(wide_smem);
+  __shared__ float red[2][kWideWarps];
+  __shared__ WideExchange xch;
+  const int NV = p.N / VN;
+  const int rank = p.C > 1 ? (int)cluster_rank() : 0;
+  const int64_t unit = blockIdx.x / p.C;
+  const int64_t units = gridDim.x / p.C;
+  const int tid = threadIdx.x;
+  const int v0 = rank * p.SV + tid;
+  wide_init(xch, p.C);
+  pdl_wait();
+  f32x2 acc[KV][NP];
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = v0 + k * kWideThreads;
+    if (v < NV) gs[tid + k * kWideThreads] = GV::load(p.gamma, v);
+#pragma unroll
+    for (int e = 0; e < NP; ++e) acc[k][e] = 0ull;
+  }
+
+  uint4 a[KV], d[KV];      // the next row's slice, as loaded
+  uint4 xc[KV], dc[KV];    // the current row's slice
+  float r_next = 0.f;
+  auto fetch = [&](int64_t row) {
+    const uint4* xr = static_cast<const uint4*>(p.x) + row * (int64_t)NV;
+    const uint4* dr = static_cast<const uint4*>(p.in2) + row * (int64_t)NV;
+    r_next = p.rstd[row];
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = v0 + k * kWideThreads;
+      a[k] = v < NV ? __ldcg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+      d[k] = v < NV ? __ldcg(dr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+
+  int64_t row = unit;
+  if (row < p.M) fetch(row);
+  for (int it = 0; row < p.M; ++it) {
+    const int buf = it & 1;
+    const float r = r_next;
+    Kahan2 sux;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = v0 + k * kWideThreads;
+      xc[k] = a[k];
+      dc[k] = d[k];
+      if (v < NV) {
+        f32x2 t = 0ull;
+        Math::backward_dot(xc[k], dc[k], gs[tid + k * kWideThreads], r, t);
+        sux.add(t);
+      }
+    }
+    wide_publish(sux.total(), red, xch, buf, rank, p.C);
+    const int64_t next = row + units;
+    if (next < p.M) fetch(next);
+    const float tot = wide_total(xch, buf, (uint32_t)(it >> 1) & 1u, p.C, p.wait_limit);
+    const float kc = tot / (float)p.N;  // r * mean(u*x)
+    uint4* out = static_cast<uint4*>(p.out) + row * (int64_t)NV;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = v0 + k * kWideThreads;
+      if (v < NV) {
+        const GV g = gs[tid + k * kWideThreads];
+        Math::backward_acc(xc[k], dc[k], r, acc[k]);
+        if constexpr (RES) {
+          const uint4 hv = __ldcs(static_cast<const uint4*>(p.in3) + row * (int64_t)NV + v);
+          st_stream(out + v, Math::backward_dx_add(xc[k], dc[k], g, r, kc, hv));
+        } else {
+          st_stream(out + v, Math::backward_dx(xc[k], dc[k], g, r, kc));
+        }
+      }
+    }
+    row = next;
+  }
+  float* wp = p.ws + unit * (int64_t)p.N;
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = v0 + k * kWideThreads;
+    if (v < NV) {
+      float4* w4 = reinterpret_cast<float4*>(wp + (int64_t)v * VN);
+#pragma unroll
+      for (int q = 0; q < NP / 2; ++q)
+        w4[q] = make_float4(lo2(acc[k][2 * q]), hi2(acc[k][2 * q]), lo2(acc[k][2 * q + 1]),
+                            hi2(acc[k][2 * q + 1]));
+    }
+  }
+  if (p.C > 1) cluster_sync();
+}
+
 template <typename F>
 cudaError_t with_types(int dtype, int gemma, bool res, F&& f) {
   auto g = [&](auto* tp, auto* wp) -> cudaError_t {
@@ -210,23 +507,188 @@ cudaError_t with_types(int dtype, int gemma, bool res, F&& f) {
 
 namespace rmsi {
 
-bool plan_chunked(int N, int dtype, Mapping* m) {
+// Vectors per thread of the one-pass mapping (the slice of a CTA is KV *
+// 512 vectors), or 0 when its slices would need more than kWideMaxCluster
+// CTAs.  Backward: 4 (one CTA per SM; the dgamma partials share the
+// registers).  Forward: 4 (two CTAs per SM) while that takes at most 16
+// CTAs, else 16 (8 with a residual or float32 weights).  Measured on GB300
+// (bf16, 256 MiB of rows): the backward with 4 vectors ran at 86 % of HBM at
+// N = 32768 and 84 % at 65536 against 81 % and 78 % with 2 (twice the
+// slices, two CTAs per SM); the forward at N = 131072 at 85 % with 8 slices
+// of 4 against 62 % with 2 of 16.
+static int64_t slices(int64_t NV, int kv) {
+  return (NV + (int64_t)kv * rmsk::kWideThreads - 1) / ((int64_t)kv * rmsk::kWideThreads);
+}
+static int wide_kv(int64_t NV, int dtype, bool bwd, bool res) {
+  const int gv_bytes = (dtype == kBF16W32 || dtype == kF16W32) ? 32 : 16;
+  if (slices(NV, 4) <= rmsk::kWideMaxCluster) return 4;
+  if (bwd) return 0;
+  const int kv = (res || gv_bytes == 32) ? 8 : 16;
+  if (slices(NV, kv) <= rmsk::kWideMaxCluster &&
+      (int64_t)kv * rmsk::kWideThreads * gv_bytes <= rmsk::kWideGammaSmem)
+    return kv;
+  return 0;
+}
+
+bool plan_chunked(int N, int dtype, bool bwd, bool res, Mapping* m) {
   const int64_t row_bytes = (int64_t)N * dtype_bytes(dtype);
   if (N <= 0 || row_bytes % 16 != 0) return false;
   const int64_t NV = row_bytes / 16;
   m->path = kChunked;
+  m->rows_per_cta = 1;
+  const int kv = wide_kv(NV, dtype, bwd, res);
+  if (kv > 0) {
+    const int gv_bytes = (dtype == kBF16W32 || dtype == kF16W32) ? 32 : 16;
+    m->wide = 1;
+    m->kv = kv;
+    m->threads = rmsk::kWideThreads;
+    m->G = rmsk::kWideThreads;
+    m->sv = kv * rmsk::kWideThreads;
+    m->cluster = (int)((NV + m->sv - 1) / m->sv);
+    m->chunks = 0;
+    m->smem = (size_t)m->sv * gv_bytes;
+    return true;
+  }
+  m->wide = 0;
   m->cluster = 1;
   m->threads = rmsk::kChunkThreads;
   m->kv = rmsk::kChunkVecs;
   m->G = rmsk::kChunkThreads;
-  m->rows_per_cta = 1;
   m->chunks = (int)((NV + rmsk::kChunkSpan - 1) / rmsk::kChunkSpan);
   m->smem = 0;
   return true;
 }
 
+// Launch configuration of the one-pass kernels: programmatic serialisation
+// and, for C > 1, the cluster dimension.
+struct WideLaunch {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  WideLaunch(const Mapping& m, int64_t grid, cudaStream_t s) {
+    cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(rmsk::kWideThreads);
+    cfg.dynamicSmemBytes = m.smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+    if (m.cluster > 1) {
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = m.cluster;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
+      cfg.numAttrs = 2;
+    }
+    cfg.attrs = attr;
+  }
+};
+
+namespace {
+struct ClusterFit {
+  const void* k;
+  int dev, C;
+  size_t smem;
+  int n;
+};
+std::mutex g_fit_mu;
+ClusterFit g_fit[64];
+int g_fit_n = 0;
+}  // namespace
+
+// How many clusters of m.cluster CTAs of kernel k are resident at once
+// (cached per kernel, device, cluster size and shared memory).  The kernel
+// is opted in to the device's full shared memory and, above 8 CTAs, to
+// non-portable cluster sizes, once.
+static cudaError_t wide_units(const void* k, const Mapping& m, const DeviceInfo& d, int* units) {
+  std::lock_guard<std::mutex> lk(g_fit_mu);
+  for (int i = 0; i < g_fit_n; ++i) {
+    const ClusterFit& f = g_fit[i];
+    if (f.k == k && f.dev == d.device && f.C == m.cluster && f.smem == m.smem) {
+      *units = f.n;
+      return cudaSuccess;
+    }
+  }
+  cudaError_t e = opt_in_max_smem(k, d);
+  if (e != cudaSuccess) return e;
+  if (m.cluster > 8) {
+    e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  int n = 0;
+  if (m.cluster > 1) {
+    WideLaunch L(m, m.cluster, nullptr);
+    e = cudaOccupancyMaxActiveClusters(&n, k, &L.cfg);
+  } else {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, rmsk::kWideThreads, m.smem);
+    n *= d.sms;
+  }
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  if (g_fit_n < 64) g_fit[g_fit_n++] = ClusterFit{k, d.device, m.cluster, m.smem, n};
+  *units = n;
+  return cudaSuccess;
+}
+
+template <typename T, typename W, bool GEMMA, bool RES>
+static const void* wide_fwd_kernel(int kv) {
+  switch (kv) {
+    case 4: return reinterpret_cast<const void*>(&rmsk::rms_fwd_wide_kernel<T, W, 4, GEMMA, RES>);
+    case 8: return reinterpret_cast<const void*>(&rmsk::rms_fwd_wide_kernel<T, W, 8, GEMMA, RES>);
+    case 16:
+      if constexpr (!RES && sizeof(rmsk::GammaVec<T, W>) == 16)
+        return reinterpret_cast<const void*>(&rmsk::rms_fwd_wide_kernel<T, W, 16, GEMMA, RES>);
+      return nullptr;
+  }
+  return nullptr;
+}
+
+template <typename T, typename W, bool GEMMA, bool RES>
+static const void* wide_bwd_kernel() {
+  return reinterpret_cast<const void*>(&rmsk::rms_bwd_wide_kernel<T, W, GEMMA, RES>);
+}
+
+static rmsk::WideParams wide_params(const Mapping& m, int64_t M, int N) {
+  rmsk::WideParams p{};
+  p.M = M;
+  p.N = N;
+  p.C = m.cluster;
+  p.SV = m.sv;
+  return p;
+}
+
+static cudaError_t launch_fwd_wide(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
+                                   long long wait_limit, cudaStream_t s) {
+  return rmsk::with_types(a.dtype, a.gemma, a.res != nullptr,
+                         [&](auto* tp, auto* wp, auto gm, auto rs) -> cudaError_t {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    using W = std::remove_pointer_t<decltype(wp)>;
+    constexpr bool GEMMA = decltype(gm)::value;
+    constexpr bool RES = decltype(rs)::value;
+    const void* k = wide_fwd_kernel<T, W, GEMMA, RES>(m.kv);
+    if (!k) return cudaErrorInvalidValue;
+    int units = 0;
+    cudaError_t e = wide_units(k, m, d, &units);
+    if (e != cudaSuccess) return e;
+    const int64_t U = std::min<int64_t>(units, a.M);
+    rmsk::WideParams p = wide_params(m, a.M, a.N);
+    p.x = a.x;
+    p.gamma = a.gamma;
+    p.in2 = a.res;
+    p.out = a.y;
+    p.h = a.h;
+    p.rstd = a.rstd;
+    p.eps = a.eps;
+    p.wait_limit = wait_limit;
+    WideLaunch L(m, U * m.cluster, s);
+    void* args[] = {&p};
+    return cudaLaunchKernelExC(&L.cfg, k, args);
+  });
+}
+
 cudaError_t launch_fwd_chunked(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
-                               cudaStream_t s) {
+                               long long wait_limit, cudaStream_t s) {
+  if (m.wide) return launch_fwd_wide(a, m, d, wait_limit, s);
   return rmsk::with_types(a.dtype, a.gemma, a.res != nullptr,
                          [&](auto* tp, auto* wp, auto gm, auto rs) -> cudaError_t {
     using T = std::remove_pointer_t<decltype(tp)>;
@@ -254,8 +716,30 @@ cudaError_t launch_fwd_chunked(const FwdArgs& a, const Mapping& m, const DeviceI
 // Row groups and the home of the per-row k values: the dgamma buffer when
 // it holds M floats (it is written only by the final column reduction),
 // else the workspace rows after the partials.
+// The one-pass backward kernel of a call.
+static const void* wide_bwd_for(const BwdArgs& a) {
+  const void* k = nullptr;
+  rmsk::with_types(a.dtype, a.gemma, a.dh != nullptr,
+                   [&](auto* tp, auto* wp, auto gm, auto rs) -> cudaError_t {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    using W = std::remove_pointer_t<decltype(wp)>;
+    k = wide_bwd_kernel<T, W, decltype(gm)::value, decltype(rs)::value>();
+    return cudaSuccess;
+  });
+  return k;
+}
+
 bool size_bwd_chunked(const BwdArgs& a, const DeviceInfo& d, Mapping* m, float** kbuf) {
   const int64_t cap = std::min<int64_t>(a.M, max_partials(d.sms));  // workspace rows
+  if (m->wide) {  // one workspace row per cluster; no per-row values to keep
+    int units = 0;
+    if (wide_units(wide_bwd_for(a), *m, d, &units) != cudaSuccess) return false;
+    const int64_t U = std::max<int64_t>(1, std::min<int64_t>(units, cap));
+    m->partials = U;
+    m->blocks = U * m->cluster;
+    *kbuf = nullptr;
+    return true;
+  }
   int64_t RG = std::max<int64_t>(1, max_partials(d.sms) / m->chunks);
   if (a.M <= a.N) {
     *kbuf = a.dgamma;
@@ -273,7 +757,21 @@ bool size_bwd_chunked(const BwdArgs& a, const DeviceInfo& d, Mapping* m, float**
 }
 
 cudaError_t launch_bwd_chunked(const BwdArgs& a, const Mapping& m, float* kbuf,
-                               const DeviceInfo& d, cudaStream_t s) {
+                               const DeviceInfo& d, long long wait_limit, cudaStream_t s) {
+  if (m.wide) {
+    rmsk::WideParams p = wide_params(m, a.M, a.N);
+    p.x = a.x;
+    p.gamma = a.gamma;
+    p.in2 = a.dy;
+    p.in3 = a.dh;
+    p.out = a.dx;
+    p.rstd = const_cast<float*>(a.rstd);
+    p.ws = a.ws;
+    p.wait_limit = wait_limit;
+    WideLaunch L(m, m.blocks, s);
+    void* args[] = {&p};
+    return cudaLaunchKernelExC(&L.cfg, wide_bwd_for(a), args);
+  }
   return rmsk::with_types(a.dtype, a.gemma, a.dh != nullptr,
                          [&](auto* tp, auto* wp, auto gm, auto rs) -> cudaError_t {
     using T = std::remove_pointer_t<decltype(tp)>;
@@ -293,6 +791,19 @@ cudaError_t launch_bwd_chunked(const BwdArgs& a, const Mapping& m, float* kbuf,
                       static_cast<T*>(a.dx), a.ws, a.M, a.N, m.chunks, m.partials,
                       static_cast<const T*>(a.dh));
   });
+}
+
+cudaError_t take_wide_device_status(int* status) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, rmsk::g_wide_device_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(rmsk::g_wide_device_status, &zero, sizeof(int));
+    if (e != cudaSuccess) return e;
+  }
+  *status = v;
+  return cudaSuccess;
 }
 
 }  // namespace rmsi

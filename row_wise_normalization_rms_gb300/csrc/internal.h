@@ -59,6 +59,7 @@ struct Mapping {
   int sv = 0;            // 16-byte vectors per CTA's column slice (staged path)
   int smem_acc = 0;      // scalar backward: partials in shared memory (else in the workspace)
   int chunks = 0;        // chunked path: chunks per row
+  int wide = 0;          // chunked path: one pass over memory, a cluster of CTAs per row
   size_t smem = 0;       // dynamic shared memory bytes
 };
 
@@ -98,14 +99,17 @@ cudaError_t launch_colreduce2(const float* ws0, float* out0, const float* ws1, f
                               int64_t P, int N, int sms, cudaStream_t s);
 
 // ---- chunked path: rows of any width (chunked.cu) ----
-bool plan_chunked(int N, int dtype, Mapping* m);
+bool plan_chunked(int N, int dtype, bool bwd, bool res, Mapping* m);
 cudaError_t launch_fwd_chunked(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
-                               cudaStream_t s);
+                               long long wait_limit, cudaStream_t s);
 // Fill m.blocks and m.partials and choose where the per-row k values live;
 // false when the shape leaves no room for them in the workspace.
 bool size_bwd_chunked(const BwdArgs& a, const DeviceInfo& d, Mapping* m, float** kbuf);
 cudaError_t launch_bwd_chunked(const BwdArgs& a, const Mapping& m, float* kbuf,
-                               const DeviceInfo& d, cudaStream_t s);
+                               const DeviceInfo& d, long long wait_limit, cudaStream_t s);
+// Reads and clears the one-pass kernels' device status word (nonzero: an
+// exchange wait ran past the wait limit).
+cudaError_t take_wide_device_status(int* status);
 
 // ---- forward with the output quantised to FP8 E4M3 (quant.cu) ----
 struct QuantArgs {

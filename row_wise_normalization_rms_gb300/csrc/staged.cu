@@ -67,8 +67,8 @@ struct StageHeader {
   uint64_t* full;
   float* red;             // [2][32] warp partial sums
   volatile int* abort;    // [2] a wait of this CTA gave up
-  float* cta_sum;         // [2] this CTA's partial of the row (clusters)
-  int* cta_abort;         // [2] this CTA's abort flag, as read by its peers
+  float* sum_in;          // [2][16] row partials pushed by the cluster's CTAs, by rank
+  int* abort_in;          // [2][16] their abort flags
   uint8_t* stages;
 };
 
@@ -77,8 +77,8 @@ __device__ __forceinline__ StageHeader header(uint8_t* smem) {
   h.full = reinterpret_cast<uint64_t*>(smem);
   h.red = reinterpret_cast<float*>(smem + 64);
   h.abort = reinterpret_cast<volatile int*>(smem + 320);
-  h.cta_sum = reinterpret_cast<float*>(smem + 336);
-  h.cta_abort = reinterpret_cast<int*>(smem + 352);
+  h.sum_in = reinterpret_cast<float*>(smem + 384);
+  h.abort_in = reinterpret_cast<int*>(smem + 512);
   h.stages = smem + kHeaderBytes;
   return h;
 }
@@ -151,30 +151,33 @@ __device__ __forceinline__ void init_barriers(const StagedParams& p, const Stage
 
 // The row's total of a per-thread partial, after the stage barrier of
 // iteration i.  Without clusters: the group's warp partials in warp order.
-// With clusters: each CTA's sum (warps in order) exchanged through
-// distributed shared memory, added in rank order; the abort decision is made
-// the same way, so every CTA of a cluster leaves the loop together.  Returns
-// the total; *abort tells whether any CTA (of the cluster) gave up a wait.
+// With clusters (one row per tile, the CTA is one group): thread c pushes
+// this CTA's sum and abort flag into slot [buf][rank] of CTA c, one cluster
+// barrier later every CTA adds the C slots in rank order from its own shared
+// memory (the same total everywhere) and makes the same abort decision, so
+// all CTAs of a cluster leave the loop together.  A slot [buf] is written
+// again two tiles later, after the next barrier, which no CTA passes before
+// every CTA has read it.  Returns the total; *abort tells whether any CTA
+// (of the cluster) gave up a wait.
 __device__ __forceinline__ float row_total(const StagedParams& p, const StageHeader& h, int buf,
-                                           int first_warp, int nw, bool* abort) {
+                                           int first_warp, int nw, int rank, bool* abort) {
   float tot = 0.f;
   for (int w = 0; w < nw; ++w) tot += h.red[buf * 32 + first_warp + w];
   if (p.C == 1) {
     *abort = h.abort[buf] != 0;
     return tot;
   }
-  if (threadIdx.x == 0) {
-    h.cta_sum[buf] = tot;
-    h.cta_abort[buf] = h.abort[buf];
+  if ((int)threadIdx.x < p.C) {
+    const uint32_t c = threadIdx.x;
+    st_cluster_f32(map_to_rank(smem_u32(&h.sum_in[buf * 16 + rank]), c), tot);
+    st_cluster_s32(map_to_rank(smem_u32(&h.abort_in[buf * 16 + rank]), c), h.abort[buf]);
   }
   cluster_sync();
-  const uint32_t sa = smem_u32(&h.cta_sum[buf]);
-  const uint32_t aa = smem_u32(&h.cta_abort[buf]);
   float all = 0.f;
   int ab = 0;
   for (int c = 0; c < p.C; ++c) {
-    all += ld_cluster_f32(map_to_rank(sa, (uint32_t)c));
-    ab |= ld_cluster_s32(map_to_rank(aa, (uint32_t)c));
+    all += h.sum_in[buf * 16 + c];
+    ab |= h.abort_in[buf * 16 + c];
   }
   *abort = ab != 0;
   return all;
@@ -262,7 +265,7 @@ rms_fwd_staged_kernel(const StagedParams p) {
     if (threadIdx.x == 0 && i >= 1 && issued < my_tiles && !h.abort[buf])
       issue_tile<T, RES ? 2 : 1, false>(p, h, sl, issued++, pol);
     bool abort;
-    const float tot = row_total(p, h, buf, first_warp, nw, &abort);
+    const float tot = row_total(p, h, buf, first_warp, nw, sl.rank, &abort);
     if (abort) {
       aborted = true;
       break;
@@ -359,7 +362,7 @@ rms_bwd_staged_kernel(const StagedParams p) {
     if (threadIdx.x == 0 && i >= 1 && issued < my_tiles && !h.abort[buf])
       issue_tile<T, RES ? 3 : 2, true>(p, h, sl, issued++, pol);
     bool abort;
-    const float tot = row_total(p, h, buf, first_warp, nw, &abort);
+    const float tot = row_total(p, h, buf, first_warp, nw, sl.rank, &abort);
     if (abort) {
       aborted = true;
       break;

@@ -60,8 +60,11 @@ class GpuResult:
     guards_ok: bool
 
 
-def run_gpu(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None) -> GpuResult:
-    """Forward then backward through the C ABI on device copies of ``inp``."""
+def run_gpu(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None,
+            expect_status=None) -> GpuResult:
+    """Forward then backward through the C ABI on device copies of ``inp``;
+    the device status word read afterwards must be ``expect_status``
+    (RMS_OK unless given)."""
     dt = tdtype(w.dtype)
     M, N = w.M, w.N
     inplace = w.inplace_dx if inplace is None else inplace
@@ -78,7 +81,8 @@ def run_gpu(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None) -> 
     rms.rms_bwd(dy, x, g, rstd.t, None if inplace else dx.t, dg.t, ws, w.gemma, inplace,
                 path=bwd_path or path)
     torch.cuda.synchronize()
-    assert rms.rms_last_device_status() == rms.RMS_OK
+    st = rms.rms_last_device_status()
+    assert st == (rms.RMS_OK if expect_status is None else expect_status), st
     guards = y.guards_intact() and rstd.guards_intact() and dg.guards_intact() and (
         inplace or dx.guards_intact())
     return GpuResult(y.t, rstd.t, dy if inplace else dx.t, dg.t, guards)

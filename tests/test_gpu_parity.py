@@ -351,6 +351,23 @@ def test_staged_wait_timeout_reports_status(bwd, N):
     H.assert_parity(w, inp, H.run_gpu(w, inp, path="staged"))
 
 
+@pytest.mark.parametrize("N", [8192, 65536, 262144])
+def test_chunked_exchange_wait_limit_reports_status(N):
+    """One-pass chunked mapping with the poll limit at 0: every row-partial
+    wait runs past the limit, so the kernels raise the device status, yet
+    they wait the exchange out (bounded) instead of skipping a row: the
+    outputs still match and the host reads RMS_ERR_TIMEOUT once."""
+    w = _w(24, N, "bf16", seed=13)
+    inp = H.inputs_for(w)
+    prev = rms.rms_set_wait_limit(0)
+    try:
+        res = H.run_gpu(w, inp, path="chunked", expect_status=rms.RMS_ERR_TIMEOUT)
+        assert rms.rms_last_device_status() == rms.RMS_OK  # cleared by the read
+    finally:
+        rms.rms_set_wait_limit(prev)
+    H.assert_parity(w, inp, res)
+
+
 def test_more_than_2_31_elements():
     """2,097,157 x 1024 bf16 (2^31 + 5120 elements per matrix): 64-bit
     indexing in every kernel.  Inputs are drawn on the device with a seeded
@@ -404,25 +421,23 @@ def test_widest_rows(N):
     H.assert_parity(w, inp, H.run_gpu(w, inp))
 
 
-def test_chunked_unsupported_corner():
-    """Forced chunked backward on many 16-byte rows: the per-row values do not
-    fit beside the partial rows of the workspace, so the call is refused
-    before any launch (the automatic mapping never picks it there)."""
+def test_chunked_many_short_rows():
+    """Forced chunked mapping on many 16-byte rows (M > N): the one-pass
+    cluster mapping keeps no per-row values in the workspace, so the shape
+    the three-pass mapping had no room for runs."""
     M, N = 5000, 8
     w = _w(M, N, "bf16", seed=1)
     inp = H.inputs_for(w)
-    with pytest.raises(rms.RmsError) as ei:
-        H.run_gpu(w, inp, fwd_path="chunked", bwd_path="chunked")
-    assert ei.value.status == rms.RMS_ERR_UNSUPPORTED
-    H.assert_parity(w, inp, H.run_gpu(w, inp, fwd_path="chunked", bwd_path="auto"))
+    H.assert_parity(w, inp, H.run_gpu(w, inp, fwd_path="chunked", bwd_path="chunked"))
 
 
 @pytest.mark.parametrize("gemma,inplace", [(0, 0), (1, 1)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "bf16w32"])
-@pytest.mark.parametrize("M,N", [(257, 3072), (1000, 512), (3, 65536), (700, 8192)])
+@pytest.mark.parametrize("M,N", [(257, 3072), (1000, 512), (3, 65536), (700, 8192), (37, 40960),
+                                 (19, 131072)])
 def test_chunked_mapping(M, N, dtype, gemma, inplace):
-    """The any-width mapping forced on ordinary shapes, M > N (per-row values
-    in the workspace) and M <= N (in dgamma), Gemma and in-place dx."""
+    """The chunked mapping forced on ordinary shapes: one-pass clusters of 1,
+    2, 3, 4, 8 and 16 CTAs (N = 131072 f32), Gemma and in-place dx."""
     w = _w(M, N, dtype, gemma=gemma, inplace=inplace, seed=M * 7 + N)
     inp = H.inputs_for(w)
     H.assert_parity(w, inp, H.run_gpu(w, inp, path="chunked"))
@@ -438,10 +453,14 @@ def test_chunked_dgamma_bitwise_reproducible():
 
 
 @pytest.mark.parametrize("dtype,N,M", [("bf16", 262144, 48), ("f32", 200000, 12),
-                                       ("bf16", 1 << 20, 6), ("f16", 393216, 9)])
+                                       ("bf16", 1 << 20, 6), ("f16", 393216, 9),
+                                       ("f32", 600000, 3)])
 def test_rows_beyond_the_cluster_split(dtype, N, M):
-    """Rows wider than a cluster of CTAs holds take the chunked mapping
-    automatically, forward and backward."""
+    """Rows wider than the staged cluster split holds take the chunked
+    mapping automatically: one pass in a cluster of up to 16 CTAs (forward
+    rows up to 2 MiB, backward up to 512 KiB), three passes beyond (the
+    backward from 200000 f32 / 393216 f16 / 2^20 bf16 here, the forward at
+    600000 f32)."""
     w = _w(M, N, dtype, seed=N % 1000 + M)
     inp = H.inputs_for(w)
     H.assert_parity(w, inp, H.run_gpu(w, inp))
