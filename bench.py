@@ -495,9 +495,9 @@ def run_gpu(args):
 # They are reported only while the kernel sources hash to the value they were
 # captured with; after any kernel change the traffic reads null.
 TRAFFIC_CAPTURE = {
-    "src_sha256_16": "58a3af807e3bd5a6",
-    "bwd": 537089024 + 233786368 + 9976064 + 0,  # staged rows kernel + column reduction
-    "fwd": 268471552 + 215547648,                # register-mapping forward
+    "src_sha256_16": "d6ec83ea500f300e",
+    "bwd": 537004544 + 233614848 + 9970688 + 0,  # staged rows kernel + column reduction
+    "fwd": 268471552 + 215866880,                # register-mapping forward
 }
 
 
