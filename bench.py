@@ -460,7 +460,7 @@ def run_gpu(args):
             "unit": "GB/s",
             "frac": round(bwd_gbs / peak, 4),
             "traffic": captured_traffic("bwd"),
-            "kernel": "rms_bwd (rms_bwd_staged_kernel + rms_dgamma_colreduce_kernel)",
+            "kernel": "rms_bwd (rms_bwd_staged_kernel + rms_colreduce4_kernel)",
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind}, burst copy)",
         },
         "roofline_fwd": {
