@@ -44,35 +44,43 @@ __device__ __forceinline__ float cta_sum(float v, float* red, int buf) {
   return warp_sum(lane < kChunkThreads / 32 ? red[buf * 32 + lane] : 0.f);
 }
 
-// One CTA per row at a time (grid-stride over rows).  Forward: out = r =
-// 1/sqrt(sum(x^2)/N + eps); with RES the row is h = x + res, stored to h for
-// the normalise pass.  Backward: out = k = sum(u * x * r)/N.
+// Row pass of the three-pass mapping.  Forward: out = r = 1/sqrt(sum(x^2)/N
+// + eps); with RES the row is h = x + res, stored to h for the normalise
+// pass.  Backward: out = k = sum(u * x * r)/N.  C CTAs share a row (C > 1:
+// a thread-block cluster, CTA rank c taking vectors [c*SV, (c+1)*SV)), so a
+// few rows still fill the GPU; their sums meet in rank order through
+// distributed shared memory after one cluster barrier per row (slots
+// alternate, so one barrier suffices).  Rows are grid-strided by cluster.
 template <typename T, typename W, bool GEMMA, bool BWD, bool RES>
 __global__ void __launch_bounds__(kChunkThreads)
 rms_rowstat_kernel(const T* __restrict__ x, const T* __restrict__ dy, const W* __restrict__ gamma,
                    const float* __restrict__ rstd_in, float* __restrict__ out, int64_t M, int N,
-                   float eps, const T* res, T* h) {
+                   float eps, const T* res, T* h, int C, int SV) {
   using Math = RowMath<T, W, GEMMA>;
   using GV = GammaVec<T, W>;
   constexpr int VN = Elem<T>::kPerVec;
   __shared__ float red[2 * 32];
+  __shared__ float slot[2];
   const int NV = N / VN;
+  const int rank = C > 1 ? (int)cluster_rank() : 0;
+  const int vbeg = rank * SV;
+  const int vend = min(NV, vbeg + SV);
   pdl_wait();
   int buf = 0;
-  for (int64_t row = blockIdx.x; row < M; row += gridDim.x, buf ^= 1) {
+  for (int64_t row = blockIdx.x / C; row < M; row += gridDim.x / C, buf ^= 1) {
     const uint4* xr = reinterpret_cast<const uint4*>(x) + row * (int64_t)NV;
     const uint4* dr = reinterpret_cast<const uint4*>(dy) + row * (int64_t)NV;
     const float r = BWD ? rstd_in[row] : 0.f;
-    Kahan2 acc;  // a thread adds NV / kChunkSpan partial sums in sequence
-    for (int v0 = threadIdx.x; v0 < NV; v0 += kChunkSpan) {
+    Kahan2 acc;  // a thread adds (vend - vbeg) / kChunkSpan partial sums in sequence
+    for (int v0 = vbeg + (int)threadIdx.x; v0 < vend; v0 += kChunkSpan) {
       uint4 xv[kChunkVecs], dv[kChunkVecs];
 #pragma unroll
       for (int u = 0; u < kChunkVecs; ++u) {
         const int v = v0 + u * kChunkThreads;
-        xv[u] = v < NV ? ld_keep(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+        xv[u] = v < vend ? ld_keep(xr + v) : make_uint4(0u, 0u, 0u, 0u);
         if (BWD || RES) {
           const uint4* src = BWD ? dr : reinterpret_cast<const uint4*>(res) + row * (int64_t)NV;
-          dv[u] = v < NV ? ld_stream(src + v) : make_uint4(0u, 0u, 0u, 0u);
+          dv[u] = v < vend ? ld_stream(src + v) : make_uint4(0u, 0u, 0u, 0u);
         }
       }
       if (RES) {
@@ -80,14 +88,14 @@ rms_rowstat_kernel(const T* __restrict__ x, const T* __restrict__ dy, const W* _
         for (int u = 0; u < kChunkVecs; ++u) {
           const int v = v0 + u * kChunkThreads;
           xv[u] = Math::add_round(xv[u], dv[u]);
-          if (v < NV) __stcg(reinterpret_cast<uint4*>(h) + row * (int64_t)NV + v, xv[u]);
+          if (v < vend) __stcg(reinterpret_cast<uint4*>(h) + row * (int64_t)NV + v, xv[u]);
         }
       }
       f32x2 part = 0ull;
 #pragma unroll
       for (int u = 0; u < kChunkVecs; ++u) {
         const int v = v0 + u * kChunkThreads;
-        if (v < NV) {
+        if (v < vend) {
           if (BWD) {
             Math::backward_dot(xv[u], dv[u], GV::load(gamma, v), r, part);
           } else {
@@ -97,9 +105,20 @@ rms_rowstat_kernel(const T* __restrict__ x, const T* __restrict__ dy, const W* _
       }
       acc.add(part);
     }
-    const float tot = cta_sum(acc.total(), red, buf);
-    if (threadIdx.x == 0) out[row] = BWD ? tot / (float)N : 1.0f / sqrtf(tot / (float)N + eps);
+    float tot = cta_sum(acc.total(), red, buf);
+    if (C > 1) {
+      if (threadIdx.x == 0) slot[buf] = tot;
+      cluster_sync();
+      if (rank == 0 && threadIdx.x == 0) {
+        const uint32_t a = smem_u32(&slot[buf]);
+        tot = 0.f;
+        for (int c = 0; c < C; ++c) tot += ld_cluster_f32(map_to_rank(a, (uint32_t)c));
+      }
+    }
+    if (rank == 0 && threadIdx.x == 0)
+      out[row] = BWD ? tot / (float)N : 1.0f / sqrtf(tot / (float)N + eps);
   }
+  if (C > 1) cluster_sync();  // rank 0 may still be reading this CTA's slot
 }
 
 // y over (row, chunk) units, grid-stride.
@@ -686,6 +705,61 @@ static cudaError_t launch_fwd_wide(const FwdArgs& a, const Mapping& m, const Dev
   });
 }
 
+// The three-pass row pass: C CTAs per row (a cluster), C doubling from 1
+// while the rows alone give fewer than 4 CTAs per SM and each CTA keeps at
+// least two chunks of the row; one row per cluster at a time, grid-strided.
+namespace {
+std::mutex g_c16_mu;
+const void* g_c16[64];
+int g_c16_n = 0;
+}  // namespace
+
+static cudaError_t allow_cluster16(const void* k) {
+  std::lock_guard<std::mutex> lk(g_c16_mu);
+  for (int i = 0; i < g_c16_n; ++i)
+    if (g_c16[i] == k) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess && g_c16_n < 64) g_c16[g_c16_n++] = k;
+  return e;
+}
+
+template <typename T, typename W, bool GEMMA, bool BWD, bool RES>
+static cudaError_t launch_rowstat(const T* x, const T* dy, const W* g, const float* rstd_in,
+                                  float* out, int64_t M, int N, float eps, const T* res, T* h,
+                                  const DeviceInfo& d, cudaStream_t s) {
+  const int64_t NV = (int64_t)N * sizeof(T) / 16;
+  int C = 1;
+  while (C < rmsk::kWideMaxCluster && M * C < 4ll * d.sms &&
+         (int64_t)(2 * C) * 2 * rmsk::kChunkSpan <= NV)
+    C *= 2;
+  const int SV = (int)((NV + C - 1) / C);
+  auto* k = rmsk::rms_rowstat_kernel<T, W, GEMMA, BWD, RES>;
+  if (C == 1) {
+    const int64_t grid = std::min<int64_t>(M, (int64_t)d.sms * 4);
+    return rmsk::launch_pdl(k, dim3((unsigned)grid), dim3(rmsk::kChunkThreads), 0, s, x, dy, g,
+                            rstd_in, out, M, N, eps, res, h, 1, SV);
+  }
+  if (C > 8) {
+    const cudaError_t e = allow_cluster16(reinterpret_cast<const void*>(k));
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t clusters = std::min<int64_t>(M, 65536);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(clusters * C));
+  cfg.blockDim = dim3(rmsk::kChunkThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = C;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k, x, dy, g, rstd_in, out, M, N, eps, res, h, C, SV);
+}
+
 cudaError_t launch_fwd_chunked(const FwdArgs& a, const Mapping& m, const DeviceInfo& d,
                                long long wait_limit, cudaStream_t s) {
   if (m.wide) return launch_fwd_wide(a, m, d, wait_limit, s);
@@ -697,11 +771,9 @@ cudaError_t launch_fwd_chunked(const FwdArgs& a, const Mapping& m, const DeviceI
     constexpr bool RES = decltype(rs)::value;
     const T* x = static_cast<const T*>(a.x);
     const W* g = static_cast<const W*>(a.gamma);
-    const int64_t rows_grid = std::min<int64_t>(a.M, (int64_t)d.sms * 4);
-    cudaError_t e = rmsk::launch_pdl(rmsk::rms_rowstat_kernel<T, W, GEMMA, false, RES>,
-                               dim3((unsigned)rows_grid), dim3(rmsk::kChunkThreads), 0, s, x,
-                               (const T*)nullptr, g, (const float*)nullptr, a.rstd, a.M, a.N,
-                               a.eps, static_cast<const T*>(a.res), static_cast<T*>(a.h));
+    cudaError_t e = launch_rowstat<T, W, GEMMA, false, RES>(
+        x, (const T*)nullptr, g, (const float*)nullptr, a.rstd, a.M, a.N, a.eps,
+        static_cast<const T*>(a.res), static_cast<T*>(a.h), d, s);
     if (e != cudaSuccess) return e;
     const int64_t units = a.M * (int64_t)m.chunks;
     const int64_t grid = std::min<int64_t>(units, (int64_t)d.sms * 16);
@@ -781,10 +853,8 @@ cudaError_t launch_bwd_chunked(const BwdArgs& a, const Mapping& m, float* kbuf,
     const T* x = static_cast<const T*>(a.x);
     const T* dy = static_cast<const T*>(a.dy);
     const W* g = static_cast<const W*>(a.gamma);
-    const int64_t rows_grid = std::min<int64_t>(a.M, (int64_t)d.sms * 4);
-    cudaError_t e = rmsk::launch_pdl(rmsk::rms_rowstat_kernel<T, W, GEMMA, true, false>,
-                               dim3((unsigned)rows_grid), dim3(rmsk::kChunkThreads), 0, s, x, dy,
-                               g, a.rstd, kbuf, a.M, a.N, 0.f, (const T*)nullptr, (T*)nullptr);
+    cudaError_t e = launch_rowstat<T, W, GEMMA, true, false>(
+        x, dy, g, a.rstd, kbuf, a.M, a.N, 0.f, (const T*)nullptr, (T*)nullptr, d, s);
     if (e != cudaSuccess) return e;
     return rmsk::launch_pdl(rmsk::rms_bwd_chunk_kernel<T, W, GEMMA, RES>, dim3((unsigned)m.blocks),
                       dim3(rmsk::kChunkThreads), 0, s, dy, x, g, a.rstd, (const float*)kbuf,

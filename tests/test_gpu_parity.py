@@ -443,8 +443,11 @@ def test_chunked_mapping(M, N, dtype, gemma, inplace):
     H.assert_parity(w, inp, H.run_gpu(w, inp, path="chunked"))
 
 
-def test_chunked_dgamma_bitwise_reproducible():
-    w = _w(3000, 4096, "bf16", seed=5)
+@pytest.mark.parametrize("M,N", [(3000, 4096), (300, 65536), (40, 1 << 20)])
+def test_chunked_dgamma_bitwise_reproducible(M, N):
+    """Run to run: one CTA per row (N = 4096), a 4-CTA cluster (65536), the
+    three-pass backward (2^20)."""
+    w = _w(M, N, "bf16", seed=5)
     inp = H.inputs_for(w)
     a = H.run_gpu(w, inp, path="chunked")
     b = H.run_gpu(w, inp, path="chunked")
