@@ -67,6 +67,18 @@ def test_fused_add_aliases(h_alias, dx_alias, gemma, dtype, path):
                                                dx_alias=dx_alias))
 
 
+@pytest.mark.parametrize("h_alias,dx_alias", [(True, "dy"), (True, "dh"), (False, "none")])
+@pytest.mark.parametrize("gemma", [0, 1])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fused_add_aliases_cluster_rows(h_alias, dx_alias, gemma, dtype):
+    """The aliases on rows the chunked mapping splits over a cluster of CTAs
+    (65536 columns: 4 CTAs a row for bf16, 8 for f32)."""
+    w = _aw(6, 65536, dtype, gemma=gemma, seed=29)
+    inp = H.inputs_for(w)
+    H.assert_fused_parity(w, inp, H.run_fused(w, inp, path="chunked", h_alias=h_alias,
+                                               dx_alias=dx_alias))
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("path", ["registers", "staged", "scalar", "chunked"])
 def test_fused_matches_unfused_bitwise(dtype, path):
