@@ -80,9 +80,12 @@ typedef enum {
   RMS_PATH_REGISTERS = 1, /* a warp or a thread group per row, row held in registers */
   RMS_PATH_STAGED = 2,    /* persistent CTAs, rows staged in shared memory by cp.async.bulk */
   RMS_PATH_SCALAR = 3,    /* element-wise loads, any alignment */
-  RMS_PATH_CHUNKED = 4    /* any width: the row is streamed in chunks, one pass to reduce it
-                             and one (fwd) or two (bwd) more to produce the outputs; RMSNorm
-                             only, chosen by RMS_PATH_AUTO for rows wider than the others take */
+  RMS_PATH_CHUNKED = 4    /* any width, RMSNorm only: rows of up to 16 slices (forward
+                             16 x 128 KiB, backward 16 x 32 KiB) go through a cluster of
+                             CTAs in one pass over memory; wider rows take three passes (a
+                             row pass, then the outputs from a second read).  Chosen by
+                             RMS_PATH_AUTO for rows the others split over a cluster or
+                             cannot take */
 } rms_path;
 
 /*
@@ -142,9 +145,10 @@ rms_status rms_bwd(void* dy, const void* x, const void* gamma, const float* rstd
 
 /* rms_bwd with the workspace size stated (checked against the need:
  * RMS_ERR_WORKSPACE when too small) and an explicit row mapping.  With
- * RMS_PATH_CHUNKED the per-row values between its passes are kept in dgamma
- * when M <= N, else in the workspace's last rows; RMS_ERR_UNSUPPORTED when
- * M > N and they do not fit beside the partial rows. */
+ * RMS_PATH_CHUNKED on rows over 16 slices (the three-pass form) the per-row
+ * values between its passes are kept in dgamma when M <= N, else in the
+ * workspace's last rows; RMS_ERR_UNSUPPORTED when M > N and they do not fit
+ * beside the partial rows. */
 rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* rstd,
                       void* dx, float* dgamma, void* workspace, size_t workspace_bytes,
                       int64_t M, int64_t N, rms_dtype dtype, int gemma, int inplace_dx,
