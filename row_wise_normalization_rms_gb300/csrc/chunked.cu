@@ -4,13 +4,15 @@
 // One-pass mapping (rows up to 16 slices): a thread-block cluster of C CTAs
 // takes each row, CTA rank c the column slice [c*SV, (c+1)*SV).  First pass:
 // the slice comes from HBM into registers and the CTA's partial sum goes to
-// its shared memory; a split cluster barrier publishes it, and while the
-// barrier completes the slice of the cluster's next row is already on its
-// way.  Second pass: every CTA adds the C partials in rank order (the same
-// total in each), reads its slice again -- from L2, where the first pass left
-// it a moment before -- and writes the outputs.  HBM sees every input once.
-// The backward keeps dgamma partials of its slice in registers across the
-// cluster's rows; the fixed-order column reduction finishes dgamma.
+// every CTA of the cluster (st.async into a slot of its shared memory,
+// completing on its mbarrier); while those arrive, the slice of the
+// cluster's next row is already on its way.  Second pass: every CTA adds the
+// C partials in rank order (the same total in each) and writes the outputs
+// -- the backward from the slice it held in registers, the forward from the
+// slice read again from L2, where the first pass left it a moment before.
+// HBM sees every input once.  The backward keeps dgamma partials of its
+// slice in registers across the cluster's rows; the fixed-order column
+// reduction finishes dgamma.
 //
 // Three-pass mapping (wider rows): a row pass computes r (forward) or
 // k = r * mean(u * x) (backward) per row, then (row, chunk) units write the

@@ -99,18 +99,6 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// The two halves of cluster_sync, for work placed between them: arrive
-// (release) publishes this CTA's prior shared-memory writes; wait (acquire)
-// returns once every thread of every CTA of the cluster has arrived.  Every
-// thread calls them in the same order and equally often: arrive, wait,
-// arrive, wait, ...
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -134,20 +122,15 @@ __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-// Asynchronous 4-byte store into the shared memory of a CTA of the cluster
-// that completes 4 transaction bytes on that CTA's mbarrier `bar` (both
-// addresses from map_to_rank).  No fence: the receiver learns of the data
-// from its own barrier.
+// Asynchronous 4-byte store into the shared memory of another CTA of the
+// cluster that completes 4 transaction bytes on that CTA's mbarrier `bar`
+// (both addresses from map_to_rank).  No fence: the receiver learns of the
+// data from its own barrier.  Only for peers of a cluster launch: a CTA
+// writes its own shared memory with a plain store.
 __device__ __forceinline__ void st_async_f32(uint32_t addr, float v, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
                ::"r"(addr), "r"(__float_as_uint(v)), "r"(bar)
                : "memory");
-}
-
-__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
 }
 
 }  // namespace rmsk
