@@ -495,9 +495,9 @@ def run_gpu(args):
 # They are reported only while the kernel sources hash to the value they were
 # captured with; after any kernel change the traffic reads null.
 TRAFFIC_CAPTURE = {
-    "src_sha256_16": "d6ec83ea500f300e",
-    "bwd": 537004544 + 233614848 + 9970688 + 0,  # staged rows kernel + column reduction
-    "fwd": 268471552 + 215866880,                # register-mapping forward
+    "src_sha256_16": "2a7d945b6fa81be0",
+    "bwd": 537013504 + 233166592 + 9969920 + 0,  # staged rows kernel + column reduction
+    "fwd": 268470272 + 215491584,                # register-mapping forward
 }
 
 
