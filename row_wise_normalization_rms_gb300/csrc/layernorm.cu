@@ -506,6 +506,13 @@ cudaError_t ln_occupancy(const void* k, const DeviceInfo& d, int threads, size_t
 
 }  // namespace
 
+// Backward rows of up to this many 16-byte vectors take two vectors per
+// thread (twice the threads a row, weights held in registers) instead of
+// four: GB300, M = 4096 fp16, N = 1024 17.4 -> 14.4 us and N = 4096 34.1 ->
+// 33.4 us per call; from N = 8192 four are faster (52.4 against 54.6 us).
+#ifndef RMS_LN_BWD_KV2_MAX_NV
+#define RMS_LN_BWD_KV2_MAX_NV 512
+#endif
 bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInfo& d, Mapping* m,
              int64_t M) {
   const int b = dtype_bytes(dtype);
@@ -530,7 +537,7 @@ bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInf
     // columns live in registers (at most 128 a thread).  CTAs of up to 256
     // threads (two per SM) where the row allows, else one row of up to 512
     // threads (32 KiB rows) and one CTA per SM.
-    const int kv = NV <= 32 ? 1 : NV <= 64 ? 2 : 4;
+    const int kv = NV <= 32 ? 1 : NV <= RMS_LN_BWD_KV2_MAX_NV ? 2 : 4;
     const int G = ((NV + kv - 1) / kv + 31) / 32 * 32;
     if (G <= 512) {
       int R = (int)(16384 / row_bytes);
