@@ -530,8 +530,11 @@ def run_sweep(args):
     contract line): one JSON line per workload and mapping.  Calls of one
     kind run back to back over k rotating buffer sets, k chosen so the sets
     together exceed three times the L2 (at most 64 sets); CUDA events around
-    each loop, average per call.  (In-place workloads overwrite dy with dx in
-    every backward call; the timing does not depend on the values.)"""
+    each loop, average per call.  With --graph the same calls are also
+    captured in a CUDA graph and replayed, which leaves out the host's
+    per-call enqueue cost (what bounds the smallest shapes).  (In-place
+    workloads overwrite dy with dx in every backward call; the timing does
+    not depend on the values.)"""
     import numpy as np
     import torch
 
@@ -639,6 +642,30 @@ def run_sweep(args):
                 torch.cuda.synchronize()
                 return a.elapsed_time(z) / n
 
+            def graphed(fn, n, reps=3):
+                """The same n calls captured once in a CUDA graph and replayed:
+                per-call device time without the host's enqueue cost."""
+                side = torch.cuda.Stream()
+                side.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(side):
+                    for i in range(3):
+                        fn(i)
+                torch.cuda.current_stream().wait_stream(side)
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    for i in range(n):
+                        fn(i)
+                gr.replay()
+                torch.cuda.synchronize()
+                a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                for _ in range(reps):
+                    gr.replay()
+                z.record()
+                torch.cuda.synchronize()
+                return a.elapsed_time(z) / (reps * n)
+
+            fg_ms = bg_ms = None
             try:
                 for i in range(k):
                     fwd_call(i)  # every set gets its rstd before the backward loop
@@ -649,6 +676,10 @@ def run_sweep(args):
                     first = False
                 f_ms = timed(fwd_call, calls)
                 b_ms = timed(bwd_call, calls) if bwd_call else None
+                if args.graph:
+                    n_graph = min(calls, max(2 * k, 64))
+                    fg_ms = graphed(fwd_call, n_graph)
+                    bg_ms = graphed(bwd_call, n_graph) if bwd_call else None
             except rms.RmsError as e:
                 print(json.dumps({"workload": name, "path": path, "error": str(e)}), flush=True)
                 continue
@@ -666,6 +697,12 @@ def run_sweep(args):
                 "bwd_us": round(b_ms * 1e3, 2) if b_ms else None,
                 "bwd_gbs": round(bg, 1) if bg else None,
                 "bwd_frac": round(bg / peak, 4) if bg else None,
+                "graph_fwd_us": round(fg_ms * 1e3, 2) if fg_ms else None,
+                "graph_fwd_frac": (round(fwd_b / (fg_ms * 1e-3) / 1e9 / peak, 4) if fg_ms
+                                   else None),
+                "graph_bwd_us": round(bg_ms * 1e3, 2) if bg_ms else None,
+                "graph_bwd_frac": (round(bwd_b / (bg_ms * 1e-3) / 1e9 / peak, 4) if bg_ms
+                                   else None),
                 "peak_gbs": peak, "peak_source": peak_kind}), flush=True)
         del sets, x0, dy0
         torch.cuda.empty_cache()
@@ -683,6 +720,8 @@ def main(argv=None):
                     help="per-call timing of every workload instead of the benchmark line")
     ap.add_argument("--workloads", default="", help="comma-separated workload names (--sweep)")
     ap.add_argument("--paths", default="auto", help="comma-separated row mappings (--sweep)")
+    ap.add_argument("--graph", action="store_true",
+                    help="--sweep: also time the calls replayed from a CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -38,34 +38,71 @@ class RmsError(RuntimeError):
         super().__init__(f"{where}: {rms_status_string(status)} (status {status})")
 
 
+_LIB = None  # the loaded library, kept once found (calls skip the loader's lock)
+
+
 def lib():
     """The raw ctypes library (see _lib.SIGNATURES for the argument types)."""
-    return _lib.load()
+    global _LIB
+    if _LIB is None:
+        _LIB = _lib.load()
+    return _LIB
 
 
 def rms_status_string(status: int) -> str:
     return lib().rms_status_string(int(status)).decode()
 
 
+_DTYPES = None  # (activation dtype, weight dtype) -> rms_dtype code, built on first use
+
+
+def _dtype_table():
+    global _DTYPES
+    if _DTYPES is None:
+        import torch
+
+        f32, bf16, f16 = torch.float32, torch.bfloat16, torch.float16
+        _DTYPES = {(f32, f32): RMS_F32, (bf16, bf16): RMS_BF16, (f16, f16): RMS_F16,
+                   (bf16, f32): RMS_BF16_W32, (f16, f32): RMS_F16_W32}
+    return _DTYPES
+
+
 def dtype_code(t, gamma=None) -> int:
     """The rms_dtype code of activations ``t`` and weight ``gamma`` (default: same type)."""
-    import torch
-
-    act = {torch.float32: RMS_F32, torch.bfloat16: RMS_BF16, torch.float16: RMS_F16}.get(t.dtype)
-    if act is None:
+    code = _dtype_table().get((t.dtype, t.dtype if gamma is None else gamma.dtype))
+    if code is not None:
+        return code
+    if (t.dtype, t.dtype) not in _DTYPES:
         raise ValueError(f"unsupported dtype {t.dtype}: float32, bfloat16 or float16")
-    if gamma is None or gamma.dtype == t.dtype:
-        return act
-    if gamma.dtype == torch.float32 and act in (RMS_BF16, RMS_F16):
-        return RMS_BF16_W32 if act == RMS_BF16 else RMS_F16_W32
     raise ValueError(f"unsupported weight dtype {gamma.dtype} for {t.dtype} activations")
 
 
-def _stream_handle(stream):
+_RAW_STREAM = None  # () -> the current device's current cudaStream_t as an int
+
+
+def _current_stream_getter():
+    """torch's raw-stream query (one call, no Stream object), else the public
+    torch.cuda.current_stream(); both name the current device's current stream."""
     import torch
 
+    torch.cuda.init()
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    dev = getattr(torch._C, "_cuda_getDevice", None)
+    if raw is not None and dev is not None:
+        try:
+            if raw(dev()) == torch.cuda.current_stream().cuda_stream:
+                return lambda: raw(dev())
+        except (RuntimeError, TypeError):
+            pass
+    return lambda: torch.cuda.current_stream().cuda_stream
+
+
+def _stream_handle(stream):
+    global _RAW_STREAM
     if stream is None:
-        stream = torch.cuda.current_stream()
+        if _RAW_STREAM is None:
+            _RAW_STREAM = _current_stream_getter()
+        return _RAW_STREAM()
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
