@@ -285,7 +285,9 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
 
     const uint32_t xs = smem_u32(stages + (size_t)s * p.stage_bytes) + row_off;
     const uint32_t ds = xs + p.tile_bytes;
-    const f32x2 nm = splat2(-mu), rr = splat2(rs);
+    // xhat = x*rstd + (-mean*rstd): one fused multiply-add per element; its
+    // rounding is within float32 steps of (|x| + |mean|)*rstd, as (x - mean)*rstd
+    const f32x2 nmr = splat2(-mu * rs), rr = splat2(rs);
     f32x2 s1 = 0ull, s2 = 0ull;  // sum(xhat*g), sum(g)
     if (active) {
 #pragma unroll
@@ -296,7 +298,7 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
           const GV wk = kHoldW ? wv[k] : GV::load(p.w, v);
 #pragma unroll
           for (int e = 0; e < NP; ++e) {
-            const f32x2 xh = mul2(add2(P::get(xq, e), nm), rr);
+            const f32x2 xh = fma2(P::get(xq, e), rr, nmr);
             const f32x2 d = P::get(dq, e);
             const f32x2 g = mul2(d, wk.pair(e));
             s1 = fma2(xh, g, s1);
@@ -323,7 +325,9 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
       t1 = warp_sum(v.x);
       t2 = warp_sum(v.y);
     }
-    const f32x2 c1 = splat2(-t1 * p.inv_n), c2 = splat2(-t2 * p.inv_n);
+    // dx = (g - (xhat*c1 + c2))*rstd = g*rstd + (xhat*c1r + c2r) with the row
+    // constants c1r = -c1*rstd, c2r = -c2*rstd: two fused multiply-adds
+    const f32x2 c1r = splat2(-t1 * p.inv_n * rs), c2r = splat2(-t2 * p.inv_n * rs);
     if (active) {
       uint4* out = reinterpret_cast<uint4*>(p.dx) + row * (int64_t)NV;
 #pragma unroll
@@ -335,10 +339,9 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
           uint32_t o[4];
 #pragma unroll
           for (int e = 0; e < NP; ++e) {
-            const f32x2 xh = mul2(add2(P::get(xq, e), nm), rr);
+            const f32x2 xh = fma2(P::get(xq, e), rr, nmr);
             const f32x2 g = mul2(P::get(dq, e), wk.pair(e));
-            // (g - (xhat*c1 + c2)) * rstd
-            const f32x2 dxe = mul2(add2(fma2(xh, c1, g), c2), rr);
+            const f32x2 dxe = fma2(g, rr, fma2(xh, c1r, c2r));
             if constexpr (sizeof(T) == 2) {
               o[e] = Half2Ops<T>::narrow(dxe);
             } else {
