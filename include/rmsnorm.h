@@ -85,7 +85,7 @@ typedef enum {
                              CTAs in one pass over memory; wider rows take three passes (a
                              row pass, then the outputs from a second read).  Chosen by
                              RMS_PATH_AUTO for rows the others split over a cluster or
-                             cannot take */
+                             cannot take.  rms_fwd_quant: a CTA per row, three passes */
 } rms_path;
 
 /*
@@ -239,11 +239,14 @@ rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const floa
  *   bits with bias 7, 3 mantissa bits, no infinities), scale [M] and
  *   rstd [M] float32 written; no output may overlap another argument.
  *   Mappings: RMS_PATH_REGISTERS (16-byte aligned rows and pointers, rows
- *   up to 32 KiB) or RMS_PATH_SCALAR (any); AUTO picks the first that fits.
+ *   up to 32 KiB), RMS_PATH_CHUNKED (aligned rows of any width: a CTA per
+ *   row, three passes over the row, the second and third served by L2) or
+ *   RMS_PATH_SCALAR (any); AUTO picks the first that fits.
  * Source: y as rms_fwd; the fusion of the consumer's cast as "02 · 手写
  * Triton kernel:RMSNorm / RoPE / SwiGLU", sections 1-2 (neighbouring
  * elementwise work kept in registers, each tensor read or written once).
- * Errors: as rms_fwd; RMS_ERR_UNSUPPORTED for RMS_PATH_STAGED / CHUNKED.
+ * Errors: as rms_fwd; RMS_ERR_UNSUPPORTED for RMS_PATH_STAGED,
+ * RMS_ERR_ALIGNMENT for RMS_PATH_REGISTERS / CHUNKED on unaligned rows.
  */
 rms_status rms_fwd_quant(const void* x, const void* gamma, uint8_t* q, float* scale, float* rstd,
                          int64_t M, int64_t N, float eps, rms_dtype dtype, int gemma,

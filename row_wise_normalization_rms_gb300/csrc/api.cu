@@ -396,7 +396,7 @@ rms_status rms_fwd_quant_ex(const void* x, const void* gamma, uint8_t* q, float*
   if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
   if (!isfinite(eps) || eps < 0.f) return RMS_ERR_INVALID_ARG;
   if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
-  if (path == RMS_PATH_STAGED || path == RMS_PATH_CHUNKED) return RMS_ERR_UNSUPPORTED;
+  if (path == RMS_PATH_STAGED) return RMS_ERR_UNSUPPORTED;
   if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
   if (M == 0) return RMS_OK;
   if (!x || !gamma || !q || !scale || !rstd) return RMS_ERR_INVALID_ARG;
@@ -420,12 +420,17 @@ rms_status rms_fwd_quant_ex(const void* x, const void* gamma, uint8_t* q, float*
   const bool aligned =
       (N * b) % 16 == 0 && aligned16(x) && aligned16(gamma) && aligned16(q);
   Mapping m;
-  if (path == RMS_PATH_REGISTERS && !aligned) return RMS_ERR_ALIGNMENT;
+  if ((path == RMS_PATH_REGISTERS || path == RMS_PATH_CHUNKED) && !aligned)
+    return RMS_ERR_ALIGNMENT;
   const bool regs = aligned && rmsi::plan_registers((int)N, dtype, false, &m) && m.threads <= 512;
   if (path == RMS_PATH_REGISTERS && !regs) return RMS_ERR_UNSUPPORTED;
-  if (path == RMS_PATH_SCALAR || !regs) {
+  if (path == RMS_PATH_SCALAR || !aligned) {
     if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
     m.path = rmsi::kScalar;
+  } else if (path == RMS_PATH_CHUNKED || !regs) {
+    // aligned rows too wide for the registers: a CTA per row, three passes
+    if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
+    m.path = rmsi::kChunked;
   } else if ((M + m.rows_per_cta - 1) / m.rows_per_cta > INT32_MAX) {
     return RMS_ERR_UNSUPPORTED;
   }

@@ -207,6 +207,104 @@ rms_fwd_quant_scalar_kernel(const T* __restrict__ x, const W* __restrict__ gamma
     qr[j] = (uint8_t)(f2_to_e4m3x2(__fmul_rn(y_at(j), inv), 0.f) & 0xffu);
 }
 
+// Aligned rows too wide for registers (any width): one CTA of 1024 threads
+// per row walks the row in 16-byte vectors three times: the sum of squares;
+// y as the forward stores it and its absolute maximum; y again (the same
+// instructions, so the same values) and the codes.  The first pass brings
+// the row from HBM; the later passes find it in L2 (a CTA's row is at most
+// a few hundred KiB, and one or two rows per SM are in flight).  A thread
+// adds up to N/8192 vectors in sequence, so each vector's partial enters a
+// compensated sum.  kLoads vectors per thread are in flight per step.
+constexpr int kQuantLoopThreads = 1024;
+
+template <typename T, typename W, bool GEMMA>
+__global__ void __launch_bounds__(kQuantLoopThreads)
+rms_fwd_quant_looped_kernel(const T* __restrict__ x, const W* __restrict__ gamma,
+                            uint8_t* __restrict__ q, float* __restrict__ scale,
+                            float* __restrict__ rstd, int N, float eps) {
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
+  constexpr int VN = Elem<T>::kPerVec;
+  constexpr int NP = Pairs<T>::n;
+  constexpr int kLoads = 4;
+  constexpr int kStep = kLoads * kQuantLoopThreads;
+  __shared__ float red_s[32], red_m[32];
+  const int NV = N / VN;
+  const int64_t row = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + row * (int64_t)NV;
+  pdl_trigger();
+  pdl_wait();
+
+  Kahan1 acc;
+  for (int v0 = threadIdx.x; v0 < NV; v0 += kStep) {
+    uint4 t[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int v = v0 + u * kQuantLoopThreads;
+      t[u] = v < NV ? ld_keep(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      f32x2 ss2 = 0ull;
+      Math::sumsq(t[u], ss2);
+      acc.add(lo2(ss2) + hi2(ss2));
+    }
+  }
+  const float ss = group_sum(acc.total(), kQuantLoopThreads, 0, red_s);
+  const float r = 1.0f / sqrtf(ss / (float)N + eps);
+
+  AbsMax<T> am;
+  for (int v0 = threadIdx.x; v0 < NV; v0 += kStep) {
+    uint4 t[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int v = v0 + u * kQuantLoopThreads;
+      t[u] = v < NV ? ld_keep(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int v = v0 + u * kQuantLoopThreads;
+      if (v < NV) am.add(Math::forward(t[u], GV::load(gamma, v), r));
+    }
+  }
+  const float amax = group_max(am.value(), kQuantLoopThreads, 0, red_m);
+  const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+  if (threadIdx.x == 0) {
+    rstd[row] = r;
+    scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  }
+
+  uint8_t* qr = q + row * (int64_t)N;
+  const f32x2 iv = splat2(inv);
+  for (int v0 = threadIdx.x; v0 < NV; v0 += kStep) {
+    uint4 t[kLoads];
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int v = v0 + u * kQuantLoopThreads;
+      t[u] = v < NV ? ld_stream(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kLoads; ++u) {
+      const int v = v0 + u * kQuantLoopThreads;
+      if (v < NV) {
+        const uint4 yv = Math::forward(t[u], GV::load(gamma, v), r);
+        uint32_t c[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          const f32x2 p = mul2(stored_pair<T>(yv, i), iv);
+          c[i] = f2_to_e4m3x2(lo2(p), hi2(p));
+        }
+        if constexpr (NP == 4) {
+          *reinterpret_cast<uint2*>(qr + (int64_t)v * VN) =
+              make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+        } else {
+          *reinterpret_cast<uint32_t*>(qr + (int64_t)v * VN) = c[0] | (c[1] << 16);
+        }
+      }
+    }
+  }
+}
+
 template <typename F>
 cudaError_t quant_types(int dtype, int gemma, F&& f) {
   auto g = [&](auto* tp, auto* wp) -> cudaError_t {
@@ -240,6 +338,10 @@ cudaError_t launch_fwd_quant(const QuantArgs& a, const Mapping& m, cudaStream_t 
         default: return rmsk::launch_pdl(rmsk::rms_fwd_quant_registers_kernel<T, W, 4, GEMMA>, grid, block, 0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, m.G);
       }
     }
+    if (m.path == kChunked)
+      return rmsk::launch_pdl(rmsk::rms_fwd_quant_looped_kernel<T, W, GEMMA>, dim3((unsigned)a.M),
+                              dim3(rmsk::kQuantLoopThreads), 0, s, x, g, a.q, a.scale, a.rstd,
+                              a.N, a.eps);
     return rmsk::launch_pdl(rmsk::rms_fwd_quant_scalar_kernel<T, W>, dim3((unsigned)a.M), dim3(256),
                             0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, a.gemma);
   });

@@ -149,6 +149,8 @@ WORKLOADS = {
         Workload("quant_wide_bf16_16384x8192", 16384, 8192, "bf16", 1e-5, op="rms_quant",
                  gamma=("normal", 1.0, 0.2), row_scale=("loguniform", 0.01, 100.0),
                  note="RMSNorm + E4M3 output, large-hidden shape"),
+        Workload("quant_widerows_bf16_N65536", 2048, 65536, "bf16", 1e-6, op="rms_quant",
+                 note="RMSNorm + E4M3 output, rows of 128 KiB (x 256 MiB)"),
         Workload("ln_wide_bf16_16384x8192", 16384, 8192, "bf16", 1e-5, op="ln",
                  x=("normal", -2.3, 0.5), gamma=("uniform", 0.0, 1.0), beta=("uniform", 0.0, 1.0),
                  dy=("normal", 0.0, 0.1), note="LayerNorm at the large-hidden shape"),

@@ -208,7 +208,7 @@ def test_quant_rejects_bad_arguments(lib):
     assert f(q=None) == INVALID
     assert f(s=None) == INVALID
     assert f(path=2) == UNSUPPORTED
-    assert f(path=4) == UNSUPPORTED
+    assert f(path=4, q=A + 4) == INVALID  # the any-width mapping: still checked on the host
     assert f(path=5) == INVALID
     assert f(q=A + 4) == INVALID          # codes over x
     assert f(s=3 * A + 8) == INVALID      # scale over the codes

@@ -63,17 +63,19 @@ def assert_quant_parity(w, inp, q, s, r, rows=None):
 
 
 SHAPES = [(1, 8), (3, 64), (17, 128), (64, 1000), (33, 1024), (65, 4096), (9, 8192), (4, 16384),
-          (2, 5000), (31, 257)]
+          (2, 5000), (31, 257), (3, 32768), (2, 40008), (2, 70000)]
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "bf16w32"])
 @pytest.mark.parametrize("M,N", SHAPES, ids=[f"{m}x{n}" for m, n in SHAPES])
-@pytest.mark.parametrize("path", ["auto", "registers", "scalar"])
+@pytest.mark.parametrize("path", ["auto", "registers", "chunked", "scalar"])
 @pytest.mark.parametrize("gemma", [0, 1])
 def test_quant_parity(M, N, dtype, path, gemma):
     w = _qw(M, N, dtype, gemma=gemma, seed=M + N)
     inp = H.inputs_for(w)
-    if path == "registers" and ((N * w.elem_bytes) % 16 != 0 or N * w.elem_bytes > 32768):
+    aligned = (N * w.elem_bytes) % 16 == 0
+    if (path == "registers" and (not aligned or N * w.elem_bytes > 32768)) or (
+            path == "chunked" and not aligned):
         with pytest.raises(rms.RmsError) as ei:
             run_quant(w, inp, path)
         assert ei.value.status in (rms.RMS_ERR_ALIGNMENT, rms.RMS_ERR_UNSUPPORTED)
@@ -111,7 +113,7 @@ def test_quant_edge_rows():
     x[1] = 0
     x[1, 7] = np.uint16(0x3F80)  # one nonzero element: its code is the largest
     inp = dict(inp, x=x)
-    for path in ("registers", "scalar"):
+    for path in ("registers", "chunked", "scalar"):
         q, s, r = run_quant(w, inp, path)
         assert float(s[0]) == 1.0 and int(q[0].abs().sum()) == 0
         assert int(q[1, 7]) == 0x7E and int((q[1] != 0).sum()) == 1
@@ -135,3 +137,11 @@ def test_quant_full_size_headline_shape():
     inp = H.inputs_for(w)
     q, s, r = run_quant(w, inp)
     assert_quant_parity(w, inp, q, s, r, rows=H.sample_rows(w.M, 64, seed=3))
+
+
+def test_quant_full_size_wide_rows():
+    """Rows of 128 KiB (too wide for the register mapping) at 256 MiB of x."""
+    w = WORKLOADS["quant_widerows_bf16_N65536"]
+    inp = H.inputs_for(w)
+    q, s, r = run_quant(w, inp)
+    assert_quant_parity(w, inp, q, s, r, rows=H.sample_rows(w.M, 16, seed=5))
