@@ -493,9 +493,10 @@ def run_gpu(args):
 # (dram__bytes_read.sum + dram__bytes_write.sum of one timed step, summed
 # over the call's launches; profiles/rms_launch_list_wide_bf16_16384x8192.md).
 # They are reported only while the kernel sources hash to the value they were
-# captured with; after any kernel change the traffic reads null.
+# captured with; after any change to their code the traffic reads null.  The
+# hash skips comments and whitespace, which do not reach the compiled code.
 TRAFFIC_CAPTURE = {
-    "src_sha256_16": "85e757e56b1baa6f",
+    "src_sha256_16": "b928d924547d5b30",
     "bwd": 537010688 + 233349632 + 9970176 + 0,  # staged rows kernel + column reduction
     "fwd": 268471552 + 215364096,                # register-mapping forward
 }
@@ -507,6 +508,33 @@ MEASURED_KERNEL_SOURCES = ["api.cu", "common.cuh", "fwd_registers.cu", "internal
                            "staged.cu", "tma.cuh"]
 
 
+def code_tokens(text: str) -> str:
+    """C/C++/CUDA source without its comments, whitespace runs collapsed to one
+    space (string and character literals kept as written)."""
+    import re
+
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(c)
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
 def kernel_source_hash() -> str:
     import hashlib
 
@@ -514,8 +542,8 @@ def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in MEASURED_KERNEL_SOURCES:
         h.update(name.encode())
-        with open(os.path.join(csrc, name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+            h.update(code_tokens(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

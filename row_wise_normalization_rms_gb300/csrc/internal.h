@@ -124,7 +124,8 @@ struct QuantArgs {
   int dtype;
   int gemma;
 };
-// m.path kRegisters (plan_registers) or kScalar.
+// m.path kRegisters (plan_registers), kChunked (aligned rows of any width:
+// a CTA per row) or kScalar.
 cudaError_t launch_fwd_quant(const QuantArgs& a, const Mapping& m, cudaStream_t s);
 
 // ---- LayerNorm (layernorm.cu) ----

@@ -67,3 +67,15 @@ def test_warmup_floor():
     r = subprocess.run([sys.executable, "bench.py", "--warmup", "2"], cwd=ROOT,
                        capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    import bench
+
+    src = 'int f(int a) {\n  return a * 2;  // twice\n}\nconst char* s = "x // y";\n'
+    commented = ('/* header */\nint f(int a) {\n  /* multi\n line */ return a * 2;\n}\n'
+                 'const char* s = "x // y";  // trailing\n')
+    assert bench.code_tokens(src) == bench.code_tokens(commented)
+    assert bench.code_tokens(src) != bench.code_tokens(src.replace("2", "3"))
+    assert bench.code_tokens(src) != bench.code_tokens(src.replace("x // y", "x y"))
+    assert len(bench.kernel_source_hash()) == 16
