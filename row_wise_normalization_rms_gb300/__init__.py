@@ -114,15 +114,54 @@ def _ptr(t):
     return t.data_ptr()
 
 
+# The C ABI takes plain device pointers and cannot see buffer sizes; the
+# binding checks what it can from the tensors before handing their pointers
+# over: every tensor lives on x's CUDA device and holds at least the bytes
+# the call reads or writes there.  None is passed through (the library
+# decides whether that argument may be NULL).
+
+def _rows(x, name="x"):
+    """M, N and the CUDA device index of the 2-D row-major tensor x."""
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D (rows, N), got shape {tuple(x.shape)}")
+    dev = x.get_device()
+    if dev < 0:
+        raise ValueError(f"{name} must be a CUDA tensor, got one on {x.device}")
+    M, N = x.shape
+    return M, N, dev
+
+
+def _arg(t, nbytes, name, dev):
+    """The device pointer of ``t`` after checking its device and byte size."""
+    if t is None:
+        return None
+    if t.get_device() != dev:
+        raise ValueError(f"{name} is on {t.device}; every tensor must be on cuda:{dev}, as x")
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes; the call needs {nbytes}")
+    return _ptr(t)
+
+
+def _weight(t, N, name, dev):
+    """As _arg for a weight vector, which needs N elements of its own type."""
+    if t is not None and t.numel() < N:
+        raise ValueError(f"{name} has {t.numel()} elements; the call needs {N}")
+    return _arg(t, 0, name, dev)
+
+
 def _path(path) -> int:
     return PATHS[path] if isinstance(path, str) else int(path)
 
 
 def rms_fwd(x, gamma, y, rstd, eps: float = 1e-6, gemma: int = 0, stream=None, path="auto"):
     """y and rstd from x (M,N) and gamma (N,); writes into y (M,N) and rstd (M,) float32."""
-    M, N = x.shape
-    st = lib().rms_fwd_ex(_ptr(x), _ptr(gamma), _ptr(y), _ptr(rstd), M, N, float(eps),
-                          dtype_code(x, gamma), int(gemma), _path(path), _stream_handle(stream))
+    M, N, dev = _rows(x)
+    mn = M * N * x.element_size()
+    st = lib().rms_fwd_ex(_ptr(x), _weight(gamma, N, "gamma", dev),
+                          _arg(y, mn, "y", dev), _arg(rstd, 4 * M, "rstd", dev), M, N,
+                          float(eps), dtype_code(x, gamma), int(gemma), _path(path),
+                          _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_fwd")
 
@@ -130,11 +169,15 @@ def rms_fwd(x, gamma, y, rstd, eps: float = 1e-6, gemma: int = 0, stream=None, p
 def rms_bwd(dy, x, gamma, rstd, dx, dgamma, workspace, gemma: int = 0, inplace_dx: int = 0,
             stream=None, path="auto"):
     """dx (M,N) and dgamma (N,) float32; with inplace_dx=1 dx is written into dy (pass dx=None)."""
-    M, N = x.shape
+    M, N, dev = _rows(x)
+    mn = M * N * x.element_size()
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().rms_bwd_ex(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
-                          _ptr(workspace), ws_bytes, M, N, dtype_code(x, gamma), int(gemma),
-                          int(inplace_dx), _path(path), _stream_handle(stream))
+    st = lib().rms_bwd_ex(_arg(dy, mn, "dy", dev), _ptr(x),
+                          _weight(gamma, N, "gamma", dev),
+                          _arg(rstd, 4 * M, "rstd", dev), _arg(dx, mn, "dx", dev),
+                          _arg(dgamma, 4 * N, "dgamma", dev), _arg(workspace, 0, "workspace", dev),
+                          ws_bytes, M, N, dtype_code(x, gamma), int(gemma), int(inplace_dx),
+                          _path(path), _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_bwd")
 
@@ -144,10 +187,13 @@ def rms_bwd_noalloc(dy, x, gamma, rstd, dx, dgamma, gemma: int = 0, inplace_dx: 
     """rms_bwd with the library's built-in scratch instead of a workspace
     argument, for callers that cannot allocate device scratch themselves
     (see include/rmsnorm.h for the size limit and the sharing rules)."""
-    M, N = x.shape
-    st = lib().rms_bwd_noalloc(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(rstd), _ptr(dx), _ptr(dgamma),
-                               M, N, dtype_code(x, gamma), int(gemma), int(inplace_dx),
-                               _stream_handle(stream))
+    M, N, dev = _rows(x)
+    mn = M * N * x.element_size()
+    st = lib().rms_bwd_noalloc(_arg(dy, mn, "dy", dev), _ptr(x),
+                               _weight(gamma, N, "gamma", dev),
+                               _arg(rstd, 4 * M, "rstd", dev), _arg(dx, mn, "dx", dev),
+                               _arg(dgamma, 4 * N, "dgamma", dev), M, N, dtype_code(x, gamma),
+                               int(gemma), int(inplace_dx), _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_bwd_noalloc")
 
@@ -156,9 +202,13 @@ def rms_fwd_add(x, residual, gamma, y, h, rstd, eps: float = 1e-6, gemma: int = 
                 path="auto"):
     """Fused residual add + RMSNorm: h = x + residual (rounded to x's dtype;
     h may be residual itself) and y, rstd = RMSNorm(h)."""
-    M, N = x.shape
-    st = lib().rms_fwd_add_ex(_ptr(x), _ptr(residual), _ptr(gamma), _ptr(y), _ptr(h), _ptr(rstd),
-                              M, N, float(eps), dtype_code(x, gamma), int(gemma), _path(path),
+    M, N, dev = _rows(x)
+    mn = M * N * x.element_size()
+    st = lib().rms_fwd_add_ex(_ptr(x), _arg(residual, mn, "residual", dev),
+                              _weight(gamma, N, "gamma", dev),
+                              _arg(y, mn, "y", dev), _arg(h, mn, "h", dev),
+                              _arg(rstd, 4 * M, "rstd", dev), M, N, float(eps),
+                              dtype_code(x, gamma), int(gemma), _path(path),
                               _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_fwd_add")
@@ -168,11 +218,16 @@ def rms_bwd_add(dy, h, gamma, rstd, dh, dx, dgamma, workspace, gemma: int = 0, i
                 stream=None, path="auto"):
     """Backward of rms_fwd_add: dx = dRMS + dh (dx may be dh itself, or dy
     with inplace_dx=1 and dx=None); dgamma as rms_bwd."""
-    M, N = h.shape
+    M, N, dev = _rows(h, "h")
+    mn = M * N * h.element_size()
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().rms_bwd_add_ex(_ptr(dy), _ptr(h), _ptr(gamma), _ptr(rstd), _ptr(dh), _ptr(dx),
-                              _ptr(dgamma), _ptr(workspace), ws_bytes, M, N, dtype_code(h, gamma),
-                              int(gemma), int(inplace_dx), _path(path), _stream_handle(stream))
+    st = lib().rms_bwd_add_ex(_arg(dy, mn, "dy", dev), _ptr(h),
+                              _weight(gamma, N, "gamma", dev),
+                              _arg(rstd, 4 * M, "rstd", dev), _arg(dh, mn, "dh", dev),
+                              _arg(dx, mn, "dx", dev), _arg(dgamma, 4 * N, "dgamma", dev),
+                              _arg(workspace, 0, "workspace", dev), ws_bytes, M, N,
+                              dtype_code(h, gamma), int(gemma), int(inplace_dx), _path(path),
+                              _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_bwd_add")
 
@@ -181,9 +236,11 @@ def rms_fwd_quant(x, gamma, q, scale, rstd, eps: float = 1e-6, gemma: int = 0, s
                   path="auto"):
     """RMSNorm forward quantised to FP8 E4M3: q (M,N) uint8 codes (or a
     torch.float8_e4m3fn tensor), scale and rstd (M,) float32."""
-    M, N = x.shape
-    st = lib().rms_fwd_quant_ex(_ptr(x), _ptr(gamma), _ptr(q), _ptr(scale), _ptr(rstd), M, N,
-                                float(eps), dtype_code(x, gamma), int(gemma), _path(path),
+    M, N, dev = _rows(x)
+    st = lib().rms_fwd_quant_ex(_ptr(x), _weight(gamma, N, "gamma", dev),
+                                _arg(q, M * N, "q", dev), _arg(scale, 4 * M, "scale", dev),
+                                _arg(rstd, 4 * M, "rstd", dev), M, N, float(eps),
+                                dtype_code(x, gamma), int(gemma), _path(path),
                                 _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_fwd_quant")
@@ -192,10 +249,12 @@ def rms_fwd_quant(x, gamma, q, scale, rstd, eps: float = 1e-6, gemma: int = 0, s
 def ln_fwd(x, w, b, y, mean, rstd, eps: float = 1e-5, stream=None, path="auto"):
     """LayerNorm forward: y (M,N), mean and rstd (M,) float32 from x (M,N),
     w (N,) and b (N,) or None (no bias)."""
-    M, N = x.shape
+    M, N, dev = _rows(x)
     if b is not None and b.dtype != w.dtype:
         raise ValueError("w and b must share one dtype")
-    st = lib().ln_fwd_ex(_ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(mean), _ptr(rstd), M, N,
+    st = lib().ln_fwd_ex(_ptr(x), _weight(w, N, "w", dev), _weight(b, N, "b", dev),
+                         _arg(y, M * N * x.element_size(), "y", dev),
+                         _arg(mean, 4 * M, "mean", dev), _arg(rstd, 4 * M, "rstd", dev), M, N,
                          float(eps), dtype_code(x, w), _path(path), _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "ln_fwd")
@@ -205,11 +264,15 @@ def ln_bwd(dy, x, w, mean, rstd, dx, dw, db, workspace, inplace_dx: int = 0, str
            path="auto"):
     """LayerNorm backward: dx (M,N); dw and db (N,) float32 (db may be None);
     with inplace_dx=1 dx is written into dy (pass dx=None)."""
-    M, N = x.shape
+    M, N, dev = _rows(x)
+    mn = M * N * x.element_size()
     ws_bytes = workspace.numel() * workspace.element_size()
-    st = lib().ln_bwd_ex(_ptr(dy), _ptr(x), _ptr(w), _ptr(mean), _ptr(rstd), _ptr(dx), _ptr(dw),
-                         _ptr(db), _ptr(workspace), ws_bytes, M, N, dtype_code(x, w),
-                         int(inplace_dx), _path(path), _stream_handle(stream))
+    st = lib().ln_bwd_ex(_arg(dy, mn, "dy", dev), _ptr(x), _weight(w, N, "w", dev),
+                         _arg(mean, 4 * M, "mean", dev), _arg(rstd, 4 * M, "rstd", dev),
+                         _arg(dx, mn, "dx", dev), _arg(dw, 4 * N, "dw", dev),
+                         _arg(db, 4 * N, "db", dev), _arg(workspace, 0, "workspace", dev),
+                         ws_bytes, M, N, dtype_code(x, w), int(inplace_dx), _path(path),
+                         _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "ln_bwd")
 
