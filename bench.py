@@ -174,9 +174,11 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- CPU oracle
-def cpu_oracle_throughput(w, inp, seconds: float = 10.0, rows: int = 256):
-    """The fp64 oracle's fwd+bwd on a fixed row sample, repeated for about
-    ``seconds``; GB/s on the same algorithmic-byte formula as the GPU."""
+def cpu_oracle_throughput(w, inp, seconds: float = 10.0, rows: int = 256, runs: int = 3):
+    """The fp64 oracle on a fixed row sample: forward and backward timed
+    separately, each in ``runs`` runs that repeat it for about
+    seconds / (2 runs); medians per direction, GB/s on the same
+    algorithmic-byte formula as the GPU."""
     from oracle import rmsnorm_oracle as orc
     from synthetic import storage_to_float64
 
@@ -184,26 +186,38 @@ def cpu_oracle_throughput(w, inp, seconds: float = 10.0, rows: int = 256):
     x = storage_to_float64(inp["x"][:rows], w.dtype)
     dy = storage_to_float64(inp["dy"][:rows], w.dtype)
     g = storage_to_float64(inp["gamma"], w.wdtype)
-    reps = 0
-    t0 = time.perf_counter()
-    while True:
-        orc.rms_forward(x, g, w.eps, w.gemma)
-        orc.rms_backward(x, g, dy, w.eps, w.gemma)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
+    budget = seconds / (2 * runs)
+
+    def per_call(fn):
+        times, reps_total = [], 0
+        for _ in range(runs):
+            reps, t0 = 0, time.perf_counter()
+            while True:
+                fn()
+                reps += 1
+                el = time.perf_counter() - t0
+                if el >= budget:
+                    break
+            times.append(el / reps)
+            reps_total += reps
+        return statistics.median(times), reps_total
+
+    t_f, n_f = per_call(lambda: orc.rms_forward(x, g, w.eps, w.gemma))
+    t_b, n_b = per_call(lambda: orc.rms_backward(x, g, dy, w.eps, w.gemma))
     f, b = step_bytes(rows, w.N, w.elem_bytes)
-    per_rep = el / reps
     return {
-        "value": round((f + b) / per_rep / 1e9, 3),
+        "value": round((f + b) / (t_f + t_b) / 1e9, 3),
         "unit": "GB/s",
-        "rows_per_s": round(rows / per_rep, 1),
+        "fwd_gbs": round(f / t_f / 1e9, 3),
+        "bwd_gbs": round(b / t_b / 1e9, 3),
+        "rows_per_s": round(rows / (t_f + t_b), 1),
         "cores": 1,
         "kind": "oracle",
-        "sample": (f"fp64 numpy oracle fwd+bwd on the first {rows} rows of the {w.M}x{w.N} "
-                   f"{w.dtype} workload, repeated {reps} times in {el:.1f} s (one thread: "
-                   "numpy elementwise ops and reductions)"),
+        "sample": (f"fp64 numpy oracle on the first {rows} rows of the {w.M}x{w.N} {w.dtype} "
+                   f"workload: forward ({n_f} calls) and backward ({n_b} calls) timed apart, "
+                   f"median of {runs} runs each, about {seconds:.0f} s in all; value = fwd+bwd "
+                   "bytes over the sum of the two medians (one thread: numpy elementwise ops "
+                   "and reductions)"),
     }
 
 

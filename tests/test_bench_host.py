@@ -79,3 +79,16 @@ def test_source_hash_ignores_comments_but_not_code():
     assert bench.code_tokens(src) != bench.code_tokens(src.replace("2", "3"))
     assert bench.code_tokens(src) != bench.code_tokens(src.replace("x // y", "x y"))
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_cpu_baseline_times_each_direction():
+    import bench
+    from synthetic import make_inputs, workload
+
+    w = workload("tiny_f32_64x128")
+    cb = bench.cpu_oracle_throughput(w, make_inputs(w), seconds=0.3, rows=16)
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "GB/s"
+    assert cb["value"] > 0 and cb["fwd_gbs"] > 0 and cb["bwd_gbs"] > 0
+    # the combined rate lies between the two directions' rates
+    assert min(cb["fwd_gbs"], cb["bwd_gbs"]) * 0.99 <= cb["value"] <= max(cb["fwd_gbs"],
+                                                                        cb["bwd_gbs"]) * 1.01
