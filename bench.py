@@ -567,6 +567,43 @@ def captured_traffic(which: str):
     return TRAFFIC_CAPTURE[which]
 
 
+SPEC_KEYS = {"M": int, "N": int, "dtype": str, "eps": float, "gemma": int, "inplace": int,
+             "seed": int, "op": str, "weight": str}
+
+
+def workload_from_spec(spec: str, name: str = ""):
+    """A workload from ``key=value`` pairs (M, N required; dtype bf16|f16|f32,
+    eps, gemma 0|1, inplace 0|1, seed, op rms|ln|rms_add|rms_quant, weight
+    f32 for a float32 weight); input laws are those of the row-width sweep."""
+    from synthetic import Workload
+
+    kv = {}
+    for part in filter(None, (p.strip() for p in spec.split(","))):
+        key, sep, val = part.partition("=")
+        if not sep or key not in SPEC_KEYS:
+            raise ValueError(f"bad workload field {part!r}; fields: {', '.join(SPEC_KEYS)}")
+        kv[key] = SPEC_KEYS[key](val)
+    if "M" not in kv or "N" not in kv:
+        raise ValueError("a workload spec needs M and N")
+    if kv["M"] < 0 or kv["N"] < 1:
+        raise ValueError("M >= 0 and N >= 1")
+    if kv.get("dtype", "bf16") not in ("bf16", "f16", "f32"):
+        raise ValueError("dtype is bf16, f16 or f32")
+    if kv.get("op", "rms") not in ("rms", "ln", "rms_add", "rms_quant"):
+        raise ValueError("op is rms, ln, rms_add or rms_quant")
+    if kv.get("gemma", 0) not in (0, 1) or kv.get("inplace", 0) not in (0, 1):
+        raise ValueError("gemma and inplace are 0 or 1")
+    op = kv.get("op", "rms")
+    return Workload(
+        name=name or "custom_" + "_".join(f"{k}{v}" for k, v in kv.items()),
+        M=kv["M"], N=kv["N"], dtype=kv.get("dtype", "bf16"), eps=kv.get("eps", 1e-6),
+        gemma=kv.get("gemma", 0), inplace_dx=kv.get("inplace", 0), seed=kv.get("seed", 0),
+        weight_dtype=kv.get("weight", ""), op=op,
+        beta=("uniform", 0.0, 1.0) if op == "ln" else None,
+        residual=("normal", 0.0, 1.0) if op == "rms_add" else None,
+        note="custom shape from the command line")
+
+
 def run_sweep(args):
     """Per-call forward and backward timing of every workload (not the
     contract line): one JSON line per workload and mapping.  Calls of one
@@ -587,9 +624,14 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     peak, peak_kind = measured_peaks()
     names = args.workloads.split(",") if args.workloads else list(WORKLOADS)
+    custom = {}
+    if args.workload_spec:
+        cw = workload_from_spec(args.workload_spec)
+        custom[cw.name] = cw
+        names = [cw.name] if not args.workloads else names + [cw.name]
     paths = args.paths.split(",")
     for name in names:
-        w = WORKLOADS[name]
+        w = custom.get(name) or WORKLOADS[name]
         M, N, b = w.M, w.N, w.elem_bytes
         inp = make_inputs(w)
 
@@ -734,6 +776,9 @@ def run_sweep(args):
                 "inplace_dx": w.inplace_dx, "path": path, "calls": calls, "buffer_sets": k,
                 "l2": ("rotating sets exceed 3x L2" if k * set_bytes >= 3 * L2_BYTES
                        else "sets fit in L2: launch-bound shape"),
+                "fwd_bytes": fwd_b, "bwd_bytes": bwd_b or None,
+                "fwd_rows_per_s": round(M / (f_ms * 1e-3), 1),
+                "bwd_rows_per_s": round(M / (b_ms * 1e-3), 1) if b_ms else None,
                 "fwd_us": round(f_ms * 1e3, 2), "fwd_gbs": round(fg, 1),
                 "fwd_frac": round(fg / peak, 4),
                 "bwd_us": round(b_ms * 1e3, 2) if b_ms else None,
@@ -762,11 +807,21 @@ def main(argv=None):
                     help="per-call timing of every workload instead of the benchmark line")
     ap.add_argument("--workloads", default="", help="comma-separated workload names (--sweep)")
     ap.add_argument("--paths", default="auto", help="comma-separated row mappings (--sweep)")
+    ap.add_argument("--workload-spec", default="",
+                    help="--sweep: one more workload from key=value pairs, e.g. "
+                         "M=4096,N=2048,dtype=f16,eps=1e-5,gemma=0,inplace=0,seed=0,op=rms")
     ap.add_argument("--graph", action="store_true",
                     help="--sweep: also time the calls replayed from a CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.workload_spec:
+        if not args.sweep:
+            ap.error("--workload-spec goes with --sweep")
+        try:
+            workload_from_spec(args.workload_spec)
+        except ValueError as e:
+            ap.error(f"--workload-spec: {e}")
     if args.impl == "reference":
         return run_reference(args)
     if args.sweep:

@@ -92,3 +92,27 @@ def test_cpu_baseline_times_each_direction():
     # the combined rate lies between the two directions' rates
     assert min(cb["fwd_gbs"], cb["bwd_gbs"]) * 0.99 <= cb["value"] <= max(cb["fwd_gbs"],
                                                                         cb["bwd_gbs"]) * 1.01
+
+
+def test_workload_spec_from_the_command_line():
+    import pytest
+
+    import bench
+    from synthetic import make_inputs
+
+    w = bench.workload_from_spec("M=12,N=96,dtype=f16,eps=1e-5,gemma=1,inplace=1,seed=3")
+    assert (w.M, w.N, w.dtype, w.eps, w.gemma, w.inplace_dx, w.seed, w.op) == \
+        (12, 96, "f16", 1e-5, 1, 1, 3, "rms")
+    for op in ("rms", "ln", "rms_add", "rms_quant"):
+        wo = bench.workload_from_spec(f"M=5,N=64,op={op}")
+        inp = make_inputs(wo)
+        assert inp["x"].shape == (5, 64)
+        if op == "rms_add":
+            assert inp["residual"] is not None and inp["dh"] is not None
+        if op == "ln":
+            assert inp["beta"] is not None
+    assert bench.workload_from_spec("M=2,N=8,weight=f32").wdtype == "f32"
+    for bad in ("N=8", "M=2", "M=2,N=8,foo=1", "M=2,N=0", "M=2,N=8,dtype=f64", "M=2,N=8,gemma=2",
+                "M=2,N=8,op=swiglu", "M=2,N8"):
+        with pytest.raises(ValueError):
+            bench.workload_from_spec(bad)
