@@ -11,10 +11,16 @@ Prints ONE JSON line (rank 0):
   cpu_baseline  the fp64 oracle on a bounded row sample, on the host cores
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--shard rows|replicas]
 
-For N > 1 launch one process per GPU with torch.distributed.run; every rank
-runs the same workload on its own GPU (replicas: the rows of independent
-batches need no exchange), timing is max over ranks.
+For N > 1 launch one process per GPU with torch.distributed.run.  With
+--shard rows (the default) the job is one batch of N x 16384 rows split into
+contiguous blocks, one per rank: each rank normalises its own rows (the
+forward and dx need no exchange) and the per-rank dgamma vectors are
+all-gathered and added in rank order by the library's kernel, so every rank
+ends with the whole batch's dgamma.  --shard replicas runs the same block on
+every rank with no exchange.  Per-GPU work is fixed as N grows (weak
+scaling); timing is max over ranks.
 """
 from __future__ import annotations
 
@@ -174,36 +180,117 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------- CPU oracle
-def cpu_oracle_throughput(w, inp, seconds: float = 10.0, rows: int = 256, runs: int = 3):
-    """The fp64 oracle on a fixed row sample: forward and backward timed
-    separately, each in ``runs`` runs that repeat it for about
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(conn, wname, rows, workers, k):
+    """One host core's share of the oracle timing: the k-th block of ``rows``
+    rows of a seeded sample of the workload, run on command."""
+    from oracle import rmsnorm_oracle as orc
+    from synthetic import make_inputs, storage_to_float64, workload
+
+    w = workload(wname)
+    inp = make_inputs(w.with_shape(rows * workers))
+    sl = slice(k * rows, (k + 1) * rows)
+    x = storage_to_float64(inp["x"][sl], w.dtype)
+    dy = storage_to_float64(inp["dy"][sl], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.wdtype)
+    conn.send("ready")
+    while True:
+        msg = conn.recv()
+        if msg is None:
+            break
+        what, reps = msg
+        dg = None
+        for _ in range(reps):
+            if what in ("fwd", "step"):
+                orc.rms_forward(x, g, w.eps, w.gemma)
+            if what in ("bwd", "step"):
+                _, dg = orc.rms_backward(x, g, dy, w.eps, w.gemma)
+        conn.send(dg)
+    conn.close()
+
+
+class OraclePool:
+    """The fp64 oracle on every host core: one spawned process per core, each
+    holding its own block of rows (processes, not threads: numpy's
+    elementwise work would serialise on the interpreter lock).  ``run`` sends
+    one command to every worker and returns the wall time until the last
+    reply, and the workers' dgamma partials summed in worker order."""
+
+    def __init__(self, wname: str, rows_per_worker: int, workers: int):
+        import multiprocessing as mp
+
+        # one thread per worker process; spawned (not forked) workers never
+        # inherit a CUDA context
+        for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ.setdefault(var, "1")
+        ctx = mp.get_context("spawn")
+        self.rows, self.workers = rows_per_worker, workers
+        self.conns, self.procs = [], []
+        for k in range(workers):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(b, wname, rows_per_worker, workers, k),
+                            daemon=True)
+            p.start()
+            self.conns.append(a)
+            self.procs.append(p)
+        for c in self.conns:
+            if c.recv() != "ready":
+                raise RuntimeError("oracle worker failed to start")
+
+    def run(self, what: str, reps: int = 1):
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send((what, reps))
+        parts = [c.recv() for c in self.conns]
+        el = time.perf_counter() - t0
+        dg = None
+        if parts[0] is not None:
+            dg = parts[0].copy()
+            for p in parts[1:]:
+                dg += p
+        return el, dg
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except (BrokenPipeError, OSError):
+                pass
+        for p in self.procs:
+            p.join(timeout=10)
+            if p.is_alive():
+                p.kill()
+
+
+def cpu_oracle_throughput(w, seconds: float = 12.0, rows_per_worker: int = 64, runs: int = 3,
+                          workers: int = 0):
+    """The fp64 oracle on a bounded row sample split over every host core:
+    forward and backward timed separately, each in ``runs`` runs of about
     seconds / (2 runs); medians per direction, GB/s on the same
     algorithmic-byte formula as the GPU."""
-    from oracle import rmsnorm_oracle as orc
-    from synthetic import storage_to_float64
+    workers = workers or host_cores()
+    pool = OraclePool(w.name, rows_per_worker, workers)
+    try:
+        budget = seconds / (2 * runs)
 
-    rows = min(rows, w.M)
-    x = storage_to_float64(inp["x"][:rows], w.dtype)
-    dy = storage_to_float64(inp["dy"][:rows], w.dtype)
-    g = storage_to_float64(inp["gamma"], w.wdtype)
-    budget = seconds / (2 * runs)
+        def per_call(what):
+            el, _ = pool.run(what, 1)  # calibration: repetitions that fill the budget
+            reps = max(1, int(budget / max(el, 1e-6)))
+            times = sorted(pool.run(what, reps)[0] / reps for _ in range(runs))
+            return times[len(times) // 2], reps * runs
 
-    def per_call(fn):
-        times, reps_total = [], 0
-        for _ in range(runs):
-            reps, t0 = 0, time.perf_counter()
-            while True:
-                fn()
-                reps += 1
-                el = time.perf_counter() - t0
-                if el >= budget:
-                    break
-            times.append(el / reps)
-            reps_total += reps
-        return statistics.median(times), reps_total
-
-    t_f, n_f = per_call(lambda: orc.rms_forward(x, g, w.eps, w.gemma))
-    t_b, n_b = per_call(lambda: orc.rms_backward(x, g, dy, w.eps, w.gemma))
+        t_f, n_f = per_call("fwd")
+        t_b, n_b = per_call("bwd")
+    finally:
+        pool.close()
+    rows = rows_per_worker * workers
     f, b = step_bytes(rows, w.N, w.elem_bytes)
     return {
         "value": round((f + b) / (t_f + t_b) / 1e9, 3),
@@ -211,48 +298,42 @@ def cpu_oracle_throughput(w, inp, seconds: float = 10.0, rows: int = 256, runs: 
         "fwd_gbs": round(f / t_f / 1e9, 3),
         "bwd_gbs": round(b / t_b / 1e9, 3),
         "rows_per_s": round(rows / (t_f + t_b), 1),
-        "cores": 1,
+        "cores": workers,
         "kind": "oracle",
-        "sample": (f"fp64 numpy oracle on the first {rows} rows of the {w.M}x{w.N} {w.dtype} "
-                   f"workload: forward ({n_f} calls) and backward ({n_b} calls) timed apart, "
-                   f"median of {runs} runs each, about {seconds:.0f} s in all; value = fwd+bwd "
-                   "bytes over the sum of the two medians (one thread: numpy elementwise ops "
-                   "and reductions)"),
+        "sample": (f"fp64 numpy oracle on {rows} seeded rows of the {w.M}x{w.N} {w.dtype} "
+                   f"workload, {rows_per_worker} rows on each of {workers} host cores (one "
+                   f"process per core): forward ({n_f} passes) and backward ({n_b} passes) "
+                   f"timed apart, median of {runs} runs each, about {seconds:.0f} s in all; "
+                   "value = fwd+bwd bytes over the sum of the two medians"),
     }
 
 
 # ------------------------------------------------------------------ reference
 def run_reference(args):
-    """The reference arm: the fp64 oracle on the host cores, one bounded row
-    sample of the same workload per step, rank 0 only."""
+    """The reference arm: the fp64 oracle on every host core, one bounded row
+    sample of the same workload per step (each core its own rows), rank 0
+    only."""
     rank, _, world = dist_env()
     if rank != 0:
         return 0
-    from oracle import rmsnorm_oracle as orc
-    from synthetic import make_inputs, storage_to_float64, workload
+    from synthetic import workload
 
     w = workload(WORKLOAD)
-    rows = 32
-    sub = w.with_shape(rows)
-    inp = make_inputs(sub)
-    x = storage_to_float64(inp["x"], w.dtype)
-    dy = storage_to_float64(inp["dy"], w.dtype)
-    g = storage_to_float64(inp["gamma"], w.wdtype)
-
-    def step():
-        orc.rms_forward(x, g, w.eps, w.gemma)
-        orc.rms_backward(x, g, dy, w.eps, w.gemma)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    el = time.perf_counter() - t0
+    workers = host_cores()
+    rows_per_worker = 64
+    rows = rows_per_worker * workers
+    pool = OraclePool(w.name, rows_per_worker, workers)
+    try:
+        for _ in range(args.warmup):
+            pool.run("step")
+        el = sum(pool.run("step")[0] for _ in range(args.steps))
+    finally:
+        pool.close()
     f, b = step_bytes(rows, w.N, w.elem_bytes)
     value = (f + b) * args.steps / el / 1e9
     sample = (f"fp64 numpy oracle fwd+bwd on {rows} rows x {w.N} per step (seeded rows of the "
-              f"{w.M}x{w.N} {w.dtype} workload), one thread")
+              f"{w.M}x{w.N} {w.dtype} workload), {rows_per_worker} rows on each of {workers} "
+              "host cores, one process per core")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -260,8 +341,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_dict(w),
         "rows_per_s": round(rows * args.steps / el, 2),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": workers,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -269,14 +350,21 @@ def run_reference(args):
     return 0
 
 
-def config_dict(w):
-    return {
+def config_dict(w, world: int = 1, shard: str = "rows"):
+    d = {
         "workload": f"RMSNorm fwd+bwd, M={w.M} rows x N={w.N} hidden, {w.dtype} I/O, "
                     f"eps={w.eps}, large-hidden synthetic rows (x ~ N(0,1) x log-uniform "
                     "row scale [0.01, 100], gamma ~ N(1, 0.2), dy ~ N(0, 1), seed 0)",
         "M": w.M, "N": w.N, "eps": w.eps, "gemma": w.gemma, "inplace_dx": w.inplace_dx,
         "l2": "inputs larger than L2: x, dy, y, dx are 256 MiB each (L2 is 129 MB)",
     }
+    if world > 1:
+        d["sharding"] = (
+            f"rows: a batch of {world} x {w.M} rows, rank r holding rows [r*{w.M}, (r+1)*{w.M}) "
+            "(drawn with seed r); dgamma all-gathered and added in rank order every step"
+            if shard == "rows" else
+            f"replicas: every rank runs the same {w.M}-row block, no exchange")
+    return d
 
 
 # ------------------------------------------------------------------------ GPU
@@ -284,7 +372,10 @@ def run_gpu(args):
     import numpy as np
     import torch
 
+    from dataclasses import replace
+
     import row_wise_normalization_rms_gb300 as rms
+    from row_wise_normalization_rms_gb300 import sharded
     from synthetic import make_inputs, workload
 
     rank, local, world = dist_env()
@@ -294,8 +385,11 @@ def run_gpu(args):
     w = workload(WORKLOAD)
     M, N, b = w.M, w.N, w.elem_bytes
     fwd_b, bwd_b = step_bytes(M, N, b)
+    rows_mode = args.shard == "rows"
 
-    inp = make_inputs(w)
+    # Row shards: rank r holds rows [r M, (r+1) M) of a world x M batch, drawn
+    # with seed + r (rank 0's block is the single-GPU workload itself).
+    inp = make_inputs(replace(w, seed=w.seed + rank) if rows_mode and rank else w)
 
     def pinned(a):
         t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
@@ -311,10 +405,20 @@ def run_gpu(args):
     dg = torch.empty(N, device=dev)
     ws = torch.empty(rms.rms_bwd_workspace_size(M, N), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    exchange = rows_mode and world > 1
+    dg_local = torch.empty(N, device=dev) if exchange else dg
+
+    def backward(dy, x, g, r, dx, dg, dgl, ws, s):
+        """This rank's rows; with row shards over several ranks, dgamma of
+        the whole batch from the rank-ordered exchange."""
+        if exchange:
+            sharded.rms_bwd_sharded(dy, x, g, r, dx, dg, dgl, ws, w.gemma, w.inplace_dx, stream=s)
+        else:
+            rms.rms_bwd(dy, x, g, r, dx, dg, ws, w.gemma, w.inplace_dx, stream=s)
 
     def step():
         rms.rms_fwd(x, g, y, rstd, w.eps, w.gemma, stream=stream)
-        rms.rms_bwd(dy, x, g, rstd, dx, dg, ws, w.gemma, w.inplace_dx, stream=stream)
+        backward(dy, x, g, rstd, dx, dg, dg_local, ws, stream)
 
     clocks = ClockSampler(local) if rank == 0 else None
     for _ in range(args.warmup):
@@ -359,8 +463,7 @@ def run_gpu(args):
 
     k_call = max(10, args.steps // 2)
     fwd_avg = per_call(lambda: rms.rms_fwd(x, g, y, rstd, w.eps, w.gemma, stream=stream), k_call)
-    bwd_avg = per_call(lambda: rms.rms_bwd(dy, x, g, rstd, dx, dg, ws, w.gemma, w.inplace_dx,
-                                           stream=stream), k_call)
+    bwd_avg = per_call(lambda: backward(dy, x, g, rstd, dx, dg, dg_local, ws, stream), k_call)
 
     # End to end: every step copies its inputs (x, dy, gamma) from pinned host
     # memory and its results (y, rstd, dx, dgamma) back, through the same C
@@ -373,10 +476,12 @@ def run_gpu(args):
     hdx = torch.empty_like(hy).pin_memory()
     hr = torch.empty(M).pin_memory()
     hdg = torch.empty(N).pin_memory()
-    bufs = [dict(x=x, dy=dy, g=g, y=y, dx=dx, r=rstd, dg=dg, ws=ws)]
+    bufs = [dict(x=x, dy=dy, g=g, y=y, dx=dx, r=rstd, dg=dg, dgl=dg_local, ws=ws)]
+    dg2 = torch.empty_like(dg)
     bufs.append(dict(x=torch.empty_like(x), dy=torch.empty_like(dy), g=torch.empty_like(g),
                      y=torch.empty_like(y), dx=torch.empty_like(dx), r=torch.empty_like(rstd),
-                     dg=torch.empty_like(dg), ws=torch.empty_like(ws)))
+                     dg=dg2, dgl=torch.empty_like(dg) if exchange else dg2,
+                     ws=torch.empty_like(ws)))
     s_comp = torch.cuda.Stream(dev)
     s_in = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
     s_out = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
@@ -402,8 +507,8 @@ def run_gpu(args):
         s_comp.wait_stream(s_in[1])
         s_comp.wait_event(out_done[j])  # this set's previous outputs are out
         rms.rms_fwd(B["x"], B["g"], B["y"], B["r"], w.eps, w.gemma, stream=s_comp)
-        rms.rms_bwd(B["dy"], B["x"], B["g"], B["r"], B["dx"], B["dg"], B["ws"], w.gemma,
-                    w.inplace_dx, stream=s_comp)
+        with torch.cuda.stream(s_comp):  # the exchange's collective runs on s_comp too
+            backward(B["dy"], B["x"], B["g"], B["r"], B["dx"], B["dg"], B["dgl"], B["ws"], s_comp)
         comp_done[j].record(s_comp)
         for k, (dst, src) in enumerate(((hy, B["y"]), (hdx, B["dx"]))):
             s_out[k].wait_event(comp_done[j])
@@ -456,7 +561,7 @@ def run_gpu(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": config_dict(w),
+        "config": config_dict(w, world, args.shard),
         "rows_per_s": round(M * world / (ms_step * 1e-3), 1),
         "pct_of_hbm_peak": round(100.0 * value / (peak * world), 2),
         "per_call": {
@@ -496,7 +601,7 @@ def run_gpu(args):
         "clocks": clocks.summary() if clocks else None,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_throughput(w, inp)
+        line["cpu_baseline"] = cpu_oracle_throughput(w)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -505,7 +610,7 @@ def run_gpu(args):
 
 # DRAM bytes per call from one ncu capture of these kernels at this workload
 # (dram__bytes_read.sum + dram__bytes_write.sum of one timed step, summed
-# over the call's launches; profiles/rms_launch_list_wide_bf16_16384x8192.md).
+# over the call's launches, as the committed launch-list summary records).
 # They are reported only while the kernel sources hash to the value they were
 # captured with; after any change to their code the traffic reads null.  The
 # hash skips comments and whitespace, which do not reach the compiled code.
@@ -803,6 +908,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shard", default="rows", choices=["rows", "replicas"],
+                    help="N > 1: split one batch into row blocks (dgamma exchanged), or run "
+                         "replicas")
     ap.add_argument("--sweep", action="store_true",
                     help="per-call timing of every workload instead of the benchmark line")
     ap.add_argument("--workloads", default="", help="comma-separated workload names (--sweep)")

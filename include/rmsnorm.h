@@ -155,6 +155,50 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
                       rms_path path, void* stream);
 
 /*
+ * rms_bwd_reduction — how rms_bwd (residual = 0) or rms_bwd_add
+ * (residual = 1) sums dgamma for M rows of N on the current device, so that
+ * a caller can bound its float32 rounding error.  The mapping is the one
+ * the call would take with 16-byte aligned pointers, or the one `path`
+ * forces.
+ *   *partials          P: the float32 partial rows the backward writes to
+ *                      its workspace; the column sum adds these P values
+ *                      per column in a fixed order.
+ *   *rows_per_partial  the most rows whose terms dy*x*r any one partial row
+ *                      sums (in a fixed order).
+ * Any fixed order of float32 additions of n terms carries each term through
+ * at most n - 1 roundings, so with u = 2^-24 and D = rows_per_partial + P:
+ *   |dgamma_j - sum_i t_ij| <= (D u / (1 - D u)) sum_i |t_ij|,
+ * t_ij being each term as the kernel forms it (x*r rounded once, times dy).
+ * Both are 0 for M == 0.  Launches nothing.
+ * Source: "Hướng dẫn Triton RMSNorm", section "Reduce dgamma không có race
+ * khi ghi" (per-part partial sums, then a second pass over the partials).
+ * Errors: RMS_ERR_INVALID_ARG (null outputs, bad shape, dtype, flag or
+ * path), RMS_ERR_ALIGNMENT / RMS_ERR_UNSUPPORTED as the forced mapping
+ * would return them, RMS_ERR_CUDA (device query failed).
+ */
+rms_status rms_bwd_reduction(int64_t M, int64_t N, rms_dtype dtype, int gemma, int residual,
+                             rms_path path, int64_t* partials, int64_t* rows_per_partial);
+
+/*
+ * rms_dgamma_combine — the exchange step of a row-sharded backward: each of
+ * `ranks` processes ran rms_bwd on its own contiguous block of rows and
+ * gathered every rank's dgamma; the total is
+ *   dgamma_j = parts[0][j] + parts[1][j] + ... + parts[ranks-1][j]
+ * added in increasing rank order, one float32 rounding per addition, so
+ * every rank computes the same bits whatever order the gather used.
+ *   parts   [ranks][N] float32, read (row r: rank r's dgamma).
+ *   dgamma  [N] float32, written; must not overlap parts.
+ * Source: "Hướng dẫn Triton RMSNorm", section "Tổng không phải trung bình"
+ * (dgamma is a sum over all rows, so per-part sums add up to it) and
+ * "Reduce dgamma không có race khi ghi" (partial sums reduced in a fixed
+ * second pass, no atomics).
+ * Errors: RMS_ERR_INVALID_ARG (null pointer, ranks < 1, N < 1, overlap),
+ * RMS_ERR_CUDA.
+ */
+rms_status rms_dgamma_combine(const float* parts, int64_t ranks, int64_t N, float* dgamma,
+                              void* stream);
+
+/*
  * rms_bwd_noalloc — rms_bwd without a caller-provided workspace.  The paper
  * has no counterpart: this entry point exists for callers, not for the
  * method.  It is for callers that cannot obtain device scratch memory
@@ -165,15 +209,24 @@ rms_status rms_bwd_ex(void* dy, const void* x, const void* gamma, const float* r
  * input and output, with the meanings, layouts and errors of rms_bwd.
  *   Scratch: a fixed array of RMS_NOALLOC_SCRATCH_BYTES (32 MiB) inside this
  *   library, held by every device that loads the library until the process
- *   exits.  Shapes whose workspace need, rms_bwd_workspace_size(M, N) =
- *   min(M, 4 * SMs) * N * 4 bytes rounded up to 256, exceeds it are
- *   rejected with RMS_ERR_WORKSPACE (on a 152-SM GB300: any M with
- *   N <= 13797, or M * N <= 8388608).
+ *   exits.  A shape fits when its workspace need, rms_bwd_workspace_size(M,
+ *   N) = min(M, 4 * SMs) * N * 4 bytes rounded up to 256, is at most that:
+ *   any M when N <= 32 MiB / (4 * SMs * 4 bytes) (on a 152-SM GB300, N <=
+ *   13797; on 148 SMs, N <= 14169), or M * N <= 8388608.  Ask
+ *   rms_bwd_workspace_size on the caller's own device; larger shapes are
+ *   rejected with RMS_ERR_WORKSPACE before anything else is checked.
+ *   M <= 0 or N <= 0 is answered exactly as rms_bwd answers it (M == 0
+ *   writes dgamma = 0) without touching the array; every other argument
+ *   error is rms_bwd's.
  *   The first call on each device looks up the array's device address with
- *   that device current; make that first call before any stream capture.
+ *   that device current and caches it; make that first call before any
+ *   stream capture.  A device reset (cudaDeviceReset) leaves the cached
+ *   address stale: do not use this entry point on a device after resetting
+ *   it in the same process.
  *   All calls on a device share the array and it keeps the last call's
- *   contents (nothing in it needs clearing): calls whose executions overlap
- *   on the GPU (other streams, other host threads) race and must be
+ *   contents (nothing in it needs clearing: every partial row the column
+ *   sum reads is written earlier in the same call): calls whose executions
+ *   overlap on the GPU (other streams, other host threads) race and must be
  *   serialised by the caller.
  */
 #define RMS_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -300,6 +353,14 @@ rms_status ln_bwd_ex(void* dy, const void* x, const void* w, const float* mean,
                      const float* rstd, void* dx, float* dw, float* db, void* workspace,
                      size_t workspace_bytes, int64_t M, int64_t N, rms_dtype dtype, int inplace_dx,
                      rms_path path, void* stream);
+
+/* ln_bwd_reduction — as rms_bwd_reduction, for ln_bwd's dw and db (each is
+ * summed through P partial rows of at most rows_per_partial rows; path
+ * RMS_PATH_AUTO, RMS_PATH_STAGED or RMS_PATH_SCALAR).
+ * Source: "第 07 章:LayerNorm——反向传播与原子锁", § 3.0 (row contributions
+ * summed over rows). */
+rms_status ln_bwd_reduction(int64_t M, int64_t N, rms_dtype dtype, rms_path path,
+                            int64_t* partials, int64_t* rows_per_partial);
 
 /* Bytes of workspace ln_bwd needs for M rows of N on the current device
  * (two rows of partials per CTA: dw and db; a multiple of 256). */

@@ -88,6 +88,20 @@ def ln_backward(x, w, dy, eps: float, with_scales: bool = False):
     return dx, dw, db, dx_scale, dw_scale, db_scale
 
 
+def ln_wsum_term_scales(x, dy, eps: float):
+    """Sizes of dw's row terms, for its error bound: ``(sum_i |dy·x̂|,
+    sum_i |dy|·(|x̂| + (|mean| + mean|x|)·rstd))`` per column, the second
+    being how far x̂ moves per unit relative error of the stored mean
+    (relative to |mean| + mean|x|) and rstd."""
+    x = _f64(x)
+    dy = _f64(dy)
+    mean, rstd = ln_stats(x, eps)
+    xhat = (x - mean[:, None]) * rstd[:, None]
+    stat = (np.abs(mean) + np.mean(np.abs(x), axis=-1)) * rstd
+    return (np.sum(np.abs(dy * xhat), axis=0),
+            np.sum(np.abs(dy) * (np.abs(xhat) + stat[:, None]), axis=0))
+
+
 def ln_loss(x, w, b, dy, eps: float) -> float:
     y, _, _ = ln_forward(x, w, b, eps)
     return float(np.sum(_f64(dy) * y))

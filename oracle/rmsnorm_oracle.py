@@ -137,43 +137,6 @@ def rms_backward_normed_form(x, gamma, dy, eps: float, gemma: int = 0):
     return (r / n)[:, None] * (n * dyw - normed * s[:, None])
 
 
-def loss(x, gamma, dy, eps: float, gemma: int = 0) -> float:
-    """Scalar L = Σ_ij dy_ij · y_ij(x, gamma), whose gradients rms_backward gives."""
-    y, _ = rms_forward(x, gamma, eps, gemma)
-    return float(np.sum(_f64(dy) * y))
-
-
-def fd_gradients(x, gamma, dy, eps: float, gemma: int = 0, h_rel: float = 1e-6):
-    """Central differences (L(a+h) − L(a−h)) / 2h of ``loss`` for every entry
-    of x and gamma ([TUT] § "Tham chiếu PyTorch: oracle số học", gradcheck).
-
-    h = h_rel · max(1, |a|).  Pure-Python loops: tiny inputs only.
-    """
-    x = _f64(x).copy()
-    g = _f64(gamma).copy()
-    dx = np.zeros_like(x)
-    dg = np.zeros_like(g)
-    for idx in np.ndindex(*x.shape):
-        a = x[idx]
-        h = h_rel * max(1.0, abs(a))
-        x[idx] = a + h
-        lp = loss(x, g, dy, eps, gemma)
-        x[idx] = a - h
-        lm = loss(x, g, dy, eps, gemma)
-        x[idx] = a
-        dx[idx] = (lp - lm) / (2.0 * h)
-    for j in range(g.shape[0]):
-        a = g[j]
-        h = h_rel * max(1.0, abs(a))
-        g[j] = a + h
-        lp = loss(x, g, dy, eps, gemma)
-        g[j] = a - h
-        lm = loss(x, g, dy, eps, gemma)
-        g[j] = a
-        dg[j] = (lp - lm) / (2.0 * h)
-    return dx, dg
-
-
 # --- low-precision cast-order emulation ------------------------------------
 
 def _round_f32(a) -> np.ndarray:

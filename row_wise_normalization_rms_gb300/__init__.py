@@ -27,6 +27,7 @@ PATHS = {"auto": RMS_PATH_AUTO, "registers": RMS_PATH_REGISTERS, "staged": RMS_P
 
 __all__ = [
     "RmsError", "lib", "rms_fwd", "rms_bwd", "rms_bwd_noalloc", "rms_bwd_workspace_size",
+    "rms_bwd_reduction", "ln_bwd_reduction", "rms_dgamma_combine",
     "rms_status_string",
     "rms_last_device_status", "rms_set_wait_limit", "rms_launch_count", "dtype_code",
 ]
@@ -198,6 +199,23 @@ def rms_bwd_noalloc(dy, x, gamma, rstd, dx, dgamma, gemma: int = 0, inplace_dx: 
         raise RmsError(st, "rms_bwd_noalloc")
 
 
+def rms_dgamma_combine(parts, dgamma, stream=None):
+    """dgamma (N,) = the rows of parts (ranks, N) float32 added in increasing
+    row order: the exchange step of a row-sharded backward."""
+    if parts.dim() != 2:
+        raise ValueError(f"parts must be 2-D (ranks, N), got shape {tuple(parts.shape)}")
+    R, N = parts.shape
+    dev = parts.get_device()
+    if dev < 0:
+        raise ValueError(f"parts must be a CUDA tensor, got one on {parts.device}")
+    if parts.dtype != dgamma.dtype or parts.element_size() != 4:
+        raise ValueError("parts and dgamma must be float32")
+    st = lib().rms_dgamma_combine(_ptr(parts), R, N, _arg(dgamma, 4 * N, "dgamma", dev),
+                                  _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "rms_dgamma_combine")
+
+
 def rms_fwd_add(x, residual, gamma, y, h, rstd, eps: float = 1e-6, gemma: int = 0, stream=None,
                 path="auto"):
     """Fused residual add + RMSNorm: h = x + residual (rounded to x's dtype;
@@ -283,6 +301,31 @@ def ln_bwd_workspace_size(M: int, N: int) -> int:
 
 def rms_bwd_workspace_size(M: int, N: int) -> int:
     return int(lib().rms_bwd_workspace_size(int(M), int(N)))
+
+
+def _reduction(fn, where, *args):
+    import ctypes
+
+    p = ctypes.c_int64(0)
+    n = ctypes.c_int64(0)
+    st = fn(*args, ctypes.byref(p), ctypes.byref(n))
+    if st != RMS_OK:
+        raise RmsError(st, where)
+    return int(p.value), int(n.value)
+
+
+def rms_bwd_reduction(M: int, N: int, dtype: int, gemma: int = 0, residual: int = 0,
+                      path="auto"):
+    """(P, rows_per_partial): the partial rows the backward's dgamma sum adds
+    and the most rows one partial row sums (``dtype`` an rms_dtype code)."""
+    return _reduction(lib().rms_bwd_reduction, "rms_bwd_reduction", int(M), int(N), int(dtype),
+                      int(gemma), int(residual), _path(path))
+
+
+def ln_bwd_reduction(M: int, N: int, dtype: int, path="auto"):
+    """(P, rows_per_partial) of ln_bwd's dw and db sums."""
+    return _reduction(lib().ln_bwd_reduction, "ln_bwd_reduction", int(M), int(N), int(dtype),
+                      _path(path))
 
 
 def rms_last_device_status(stream=None) -> int:

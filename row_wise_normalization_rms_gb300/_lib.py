@@ -24,6 +24,8 @@ SIGNATURES = {
                         c_vp]),
     "rms_bwd_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_i64, c_i64, c_int,
                            c_int, c_int, c_int, c_vp]),
+    "rms_bwd_reduction": (c_int, [c_i64, c_i64, c_int, c_int, c_int, c_int, c_vp, c_vp]),
+    "rms_dgamma_combine": (c_int, [c_vp, c_i64, c_i64, c_vp, c_vp]),
     "rms_bwd_noalloc": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_int, c_int,
                                 c_int, c_vp]),
     "rms_fwd_add": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_float, c_int, c_int,
@@ -45,6 +47,7 @@ SIGNATURES = {
                        c_int, c_vp]),
     "ln_bwd_ex": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_size, c_i64,
                           c_i64, c_int, c_int, c_int, c_vp]),
+    "ln_bwd_reduction": (c_int, [c_i64, c_i64, c_int, c_int, c_vp, c_vp]),
     "ln_bwd_workspace_size": (c_size, [c_i64, c_i64]),
     "rms_bwd_workspace_size": (c_size, [c_i64, c_i64]),
     "rms_status_string": (ctypes.c_char_p, [c_int]),

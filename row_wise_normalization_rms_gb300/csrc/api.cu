@@ -6,6 +6,8 @@
 
 #include <atomic>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "internal.h"
 #include "rmsnorm.h"
@@ -46,13 +48,9 @@ bool current_device(DeviceInfo* out) {
   return true;
 }
 
-struct OptIn {
-  const void* k;
-  int dev;
-};
+// (kernel, device) pairs whose dynamic shared memory limit is already raised.
 std::mutex g_optin_mu;
-OptIn g_optin[64];
-int g_optin_n = 0;
+std::set<std::pair<const void*, int>> g_optin;
 
 int elem_bytes(int dtype) { return rmsi::dtype_bytes(dtype); }
 
@@ -148,14 +146,41 @@ rms_status choose(rms_path path, int N, int dtype, bool bwd, bool aligned, const
   }
 }
 
+// The backward's mapping for a call, with its grid and partial rows sized
+// (m->partials workspace rows; *kbuf: where the three-pass chunked mapping
+// keeps its per-row values).  Launches nothing; a.ws and a.dgamma are only
+// used as addresses.
+rms_status plan_bwd(const BwdArgs& a, rms_path path, bool aligned, const DeviceInfo& d,
+                    Mapping* m, float** kbuf) {
+  const rms_status st = choose(path, a.N, a.dtype, true, aligned, d, m, a.dh != nullptr, a.M);
+  if (st != RMS_OK) return st;
+  cudaError_t e = cudaSuccess;
+  switch (m->path) {
+    case rmsi::kRegisters: e = rmsi::size_bwd_registers(a, d, m); break;
+    case rmsi::kStaged: e = rmsi::size_bwd_staged(a, d, m); break;
+    case rmsi::kChunked:
+      if (!rmsi::size_bwd_chunked(a, d, m, kbuf)) return RMS_ERR_UNSUPPORTED;
+      break;
+    default: e = rmsi::size_bwd_scalar(a, d, m); break;
+  }
+  return e == cudaSuccess ? RMS_OK : RMS_ERR_CUDA;
+}
+
+// Most rows whose terms one partial row sums: every mapping deals tiles of
+// m.rows_per_cta consecutive rows to its m.partials work units in turn.
+int64_t most_rows_per_partial(int64_t M, const Mapping& m) {
+  const int64_t R = m.rows_per_cta > 0 ? m.rows_per_cta : 1;
+  const int64_t tiles = (M + R - 1) / R;
+  return R * ((tiles + m.partials - 1) / m.partials);
+}
+
 }  // namespace
 
 namespace rmsi {
 
 cudaError_t opt_in_max_smem(const void* kernel, const DeviceInfo& d) {
   std::lock_guard<std::mutex> lk(g_optin_mu);
-  for (int i = 0; i < g_optin_n; ++i)
-    if (g_optin[i].k == kernel && g_optin[i].dev == d.device) return cudaSuccess;
+  if (g_optin.count({kernel, d.device})) return cudaSuccess;
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
   if (e != cudaSuccess) return e;
@@ -163,7 +188,7 @@ cudaError_t opt_in_max_smem(const void* kernel, const DeviceInfo& d) {
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)(d.smem_optin - fa.sharedSizeBytes));
   if (e != cudaSuccess) return e;
-  if (g_optin_n < 64) g_optin[g_optin_n++] = OptIn{kernel, d.device};
+  g_optin.insert({kernel, d.device});
   return cudaSuccess;
 }
 
@@ -339,36 +364,32 @@ static rms_status bwd_impl(void* dy, const void* x, const void* gamma, const flo
 
   const bool aligned = (N * b) % 16 == 0 && aligned16(dy) && aligned16(x) && aligned16(gamma) &&
                        aligned16(dx) && (!dh || aligned16(dh));
-  Mapping m;
-  const rms_status st = choose(path, (int)N, dtype, true, aligned, d, &m, dh != nullptr, M);
-  if (st != RMS_OK) return st;
-
   BwdArgs a{dy, x, gamma, rstd, dx, dgamma, static_cast<float*>(workspace), M, (int)N,
             (int)dtype, gemma, dh};
+  Mapping m;
+  float* kbuf = nullptr;
+  const rms_status st = plan_bwd(a, path, aligned, d, &m, &kbuf);
+  if (st != RMS_OK) return st;
+  // The partial rows must fit the workspace before any kernel writes them.
+  if ((size_t)m.partials * (size_t)N * sizeof(float) > need) return RMS_ERR_WORKSPACE;
+
   cudaError_t e;
   switch (m.path) {
     case rmsi::kRegisters:
-      e = rmsi::size_bwd_registers(a, d, &m);
-      if (e == cudaSuccess) e = rmsi::launch_bwd_registers(a, m, s);
+      e = rmsi::launch_bwd_registers(a, m, s);
       break;
     case rmsi::kStaged:
-      e = rmsi::size_bwd_staged(a, d, &m);
-      if (e == cudaSuccess) e = rmsi::launch_bwd_staged(a, m, d, g_wait_limit.load(), s);
+      e = rmsi::launch_bwd_staged(a, m, d, g_wait_limit.load(), s);
       break;
-    case rmsi::kChunked: {
-      float* kbuf = nullptr;
-      if (!rmsi::size_bwd_chunked(a, d, &m, &kbuf)) return RMS_ERR_UNSUPPORTED;
+    case rmsi::kChunked:
       e = rmsi::launch_bwd_chunked(a, m, kbuf, d, g_wait_limit.load(), s);
       if (e == cudaSuccess && !m.wide) g_launches.fetch_add(1);  // three-pass: three kernels
       break;
-    }
     default:
-      e = rmsi::size_bwd_scalar(a, d, &m);
-      if (e == cudaSuccess) e = rmsi::launch_bwd_scalar(a, m, s);
+      e = rmsi::launch_bwd_scalar(a, m, s);
       break;
   }
   if (e != cudaSuccess) return RMS_ERR_CUDA;
-  if ((size_t)m.partials * (size_t)N * sizeof(float) > need) return RMS_ERR_WORKSPACE;  // unreachable
   e = rmsi::launch_colreduce(a.ws, dgamma, m.partials, (int)N, d.sms, s);
   if (e != cudaSuccess) return RMS_ERR_CUDA;
   g_launches.fetch_add(2);
@@ -388,6 +409,47 @@ rms_status rms_bwd(void* dy, const void* x, const void* gamma, const float* rstd
                    int inplace_dx, void* stream) {
   return bwd_impl(dy, x, gamma, rstd, nullptr, dx, dgamma, workspace, SIZE_MAX, M, N, dtype,
                   gemma, inplace_dx, RMS_PATH_AUTO, stream);
+}
+
+rms_status rms_bwd_reduction(int64_t M, int64_t N, rms_dtype dtype, int gemma, int residual,
+                             rms_path path, int64_t* partials, int64_t* rows_per_partial) {
+  if (!partials || !rows_per_partial) return RMS_ERR_INVALID_ARG;
+  if (!valid_common(M, N, dtype, gemma)) return RMS_ERR_INVALID_ARG;
+  if (residual != 0 && residual != 1) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
+  if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
+  *partials = 0;
+  *rows_per_partial = 0;
+  if (M == 0) return RMS_OK;
+  DeviceInfo d;
+  if (!current_device(&d)) return RMS_ERR_CUDA;
+  // The plan reads only the shape, the types and whether a residual
+  // gradient is present (a non-null stand-in; nothing is dereferenced).
+  static const char kStandIn = 0;
+  BwdArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, M, (int)N, (int)dtype,
+            gemma, residual ? static_cast<const void*>(&kStandIn) : nullptr};
+  const bool aligned = (N * elem_bytes(dtype)) % 16 == 0;
+  Mapping m;
+  float* kbuf = nullptr;
+  const rms_status st = plan_bwd(a, path, aligned, d, &m, &kbuf);
+  if (st != RMS_OK) return st;
+  *partials = m.partials;
+  *rows_per_partial = most_rows_per_partial(M, m);
+  return RMS_OK;
+}
+
+rms_status rms_dgamma_combine(const float* parts, int64_t ranks, int64_t N, float* dgamma,
+                              void* stream) {
+  if (ranks < 1 || N < 1 || !parts || !dgamma) return RMS_ERR_INVALID_ARG;
+  if (ranks > INT64_MAX / N / (int64_t)sizeof(float)) return RMS_ERR_INVALID_ARG;
+  if ((N + 3) / 4 > (int64_t)INT32_MAX * 256) return RMS_ERR_UNSUPPORTED;
+  if (overlap(dgamma, (size_t)N * sizeof(float), parts, (size_t)(ranks * N) * sizeof(float)))
+    return RMS_ERR_INVALID_ARG;
+  if (rmsi::launch_rank_sum(parts, dgamma, ranks, N, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return RMS_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return RMS_OK;
 }
 
 rms_status rms_fwd_quant_ex(const void* x, const void* gamma, uint8_t* q, float* scale,
@@ -579,7 +641,8 @@ rms_status ln_bwd_ex(void* dy, const void* x, const void* w, const float* mean,
   float* wsb = reinterpret_cast<float*>(static_cast<char*>(workspace) + half);
   rmsi::LnBwdArgs a{dy, x, w, mean, rstd, dx, wsw, wsb, M, (int)N, (int)dtype};
   if (rmsi::ln_size_bwd(a, d, &m) != cudaSuccess) return RMS_ERR_CUDA;
-  if ((size_t)m.partials * (size_t)N * sizeof(float) > half) return RMS_ERR_WORKSPACE;  // unreachable
+  // The partial rows must fit the workspace before any kernel writes them.
+  if ((size_t)m.partials * (size_t)N * sizeof(float) > half) return RMS_ERR_WORKSPACE;
   if (rmsi::ln_launch_bwd(a, m, g_wait_limit.load(), s) != cudaSuccess) return RMS_ERR_CUDA;
   // dw and db: one launch when both are vectorisable, else one each
   if (rmsi::launch_colreduce2(wsw, dw, db ? wsb : nullptr, db, m.partials, (int)N, d.sms, s) !=
@@ -587,6 +650,30 @@ rms_status ln_bwd_ex(void* dy, const void* x, const void* w, const float* mean,
     return RMS_ERR_CUDA;
   const bool vec = N % 4 == 0 && aligned16(dw) && (!db || aligned16(db));
   g_launches.fetch_add(db && !vec ? 3 : 2);
+  return RMS_OK;
+}
+
+rms_status ln_bwd_reduction(int64_t M, int64_t N, rms_dtype dtype, rms_path path,
+                            int64_t* partials, int64_t* rows_per_partial) {
+  if (!partials || !rows_per_partial) return RMS_ERR_INVALID_ARG;
+  if (!valid_common(M, N, dtype, 0)) return RMS_ERR_INVALID_ARG;
+  if (path < RMS_PATH_AUTO || path > RMS_PATH_CHUNKED) return RMS_ERR_INVALID_ARG;
+  if (path == RMS_PATH_REGISTERS || path == RMS_PATH_CHUNKED) return RMS_ERR_UNSUPPORTED;
+  if (N > (int64_t)INT32_MAX) return RMS_ERR_UNSUPPORTED;
+  *partials = 0;
+  *rows_per_partial = 0;
+  if (M == 0) return RMS_OK;
+  DeviceInfo d;
+  if (!current_device(&d)) return RMS_ERR_CUDA;
+  const bool aligned = (N * elem_bytes(dtype)) % 16 == 0;
+  if (path == RMS_PATH_STAGED && !aligned) return RMS_ERR_ALIGNMENT;
+  Mapping m;
+  if (!rmsi::ln_plan((int)N, dtype, true, path, aligned, d, &m, M)) return RMS_ERR_UNSUPPORTED;
+  rmsi::LnBwdArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                    M, (int)N, (int)dtype};
+  if (rmsi::ln_size_bwd(a, d, &m) != cudaSuccess) return RMS_ERR_CUDA;
+  *partials = m.partials;
+  *rows_per_partial = most_rows_per_partial(M, m);
   return RMS_OK;
 }
 

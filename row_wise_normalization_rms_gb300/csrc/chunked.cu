@@ -821,7 +821,7 @@ bool size_bwd_chunked(const BwdArgs& a, const DeviceInfo& d, Mapping* m, float**
     const int64_t krows = (a.M + a.N - 1) / a.N;
     if (cap - krows < 1) return false;  // many short rows: not this mapping's shape
     RG = std::min<int64_t>(RG, cap - krows);
-    *kbuf = a.ws + (cap - krows) * (int64_t)a.N;
+    *kbuf = a.ws ? a.ws + (cap - krows) * (int64_t)a.N : nullptr;
   }
   RG = std::max<int64_t>(1, std::min<int64_t>(RG, cap));
   if (RG * m->chunks > INT32_MAX) return false;

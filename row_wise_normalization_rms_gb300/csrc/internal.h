@@ -97,6 +97,8 @@ cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, i
 // makes it the single sum.
 cudaError_t launch_colreduce2(const float* ws0, float* out0, const float* ws1, float* out1,
                               int64_t P, int N, int sms, cudaStream_t s);
+// out[j] = sum over r < R of parts[r][j], added in increasing r.
+cudaError_t launch_rank_sum(const float* parts, float* out, int64_t R, int64_t N, cudaStream_t s);
 
 // ---- chunked path: rows of any width (chunked.cu) ----
 bool plan_chunked(int N, int dtype, bool bwd, bool res, Mapping* m);

@@ -13,7 +13,9 @@
 // the host it is only a stand-in symbol), so the first call on each device
 // looks up its device address with cudaGetSymbolAddress, with that device
 // current, and caches it; that first call should therefore happen before
-// any stream capture.  All calls on a device share the one array: calls
+// any stream capture.  A device reset (cudaDeviceReset) unloads the module
+// and leaves the cached address stale: do not call this entry point on a
+// device after resetting it in the same process.  All calls on a device share the one array: calls
 // whose executions overlap on the GPU (different streams, or concurrent
 // host threads) race on it and must be serialised by the caller.  Nothing
 // in it needs clearing between calls: every partial row the column
@@ -50,10 +52,16 @@ extern "C" rms_status rms_bwd_noalloc(void* dy, const void* x, const void* gamma
                                       const float* rstd, void* dx, float* dgamma, int64_t M,
                                       int64_t N, rms_dtype dtype, int gemma, int inplace_dx,
                                       void* stream) {
+  // No rows (or a bad shape): rms_bwd answers without a workspace (M == 0
+  // zeroes dgamma), so the scratch array is not looked up at all.
+  if (M <= 0 || N <= 0)
+    return rms_bwd_ex(dy, x, gamma, rstd, dx, dgamma, nullptr, 0, M, N, dtype, gemma, inplace_dx,
+                      RMS_PATH_AUTO, stream);
+  const size_t need = rms_bwd_workspace_size(M, N);
+  if (need == 0) return RMS_ERR_CUDA;  // the current device could not be queried
+  if (need > (size_t)RMS_NOALLOC_SCRATCH_BYTES) return RMS_ERR_WORKSPACE;
   void* ws = scratch_on_current_device();
   if (!ws) return RMS_ERR_CUDA;
-  if (M > 0 && N > 0 && rms_bwd_workspace_size(M, N) > (size_t)RMS_NOALLOC_SCRATCH_BYTES)
-    return RMS_ERR_WORKSPACE;
   return rms_bwd_ex(dy, x, gamma, rstd, dx, dgamma, ws, (size_t)RMS_NOALLOC_SCRATCH_BYTES, M, N,
                     dtype, gemma, inplace_dx, RMS_PATH_AUTO, stream);
 }

@@ -185,6 +185,34 @@ rms_colreduce4_kernel(const float4* __restrict__ ws0, float4* __restrict__ out0,
   }
 }
 
+// out[j] = parts[0][j] + parts[1][j] + ... + parts[R-1][j], added one row
+// at a time in increasing row order (one float32 rounding per addition).
+// The rows are the per-rank dgamma vectors of a row-sharded backward, so the
+// total is the same on every rank and does not depend on how they were
+// exchanged.  A thread owns four columns (one float4 when aligned).
+__global__ void __launch_bounds__(256)
+rms_rank_sum_kernel(const float* __restrict__ parts, float* __restrict__ out, int64_t R, int64_t N,
+                    int vec) {
+  pdl_wait();
+  const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (j0 >= N) return;
+  if (vec) {  // N % 4 == 0 and both pointers 16-byte aligned
+    const float4* p4 = reinterpret_cast<const float4*>(parts) + j0 / 4;
+    float4 s = p4[0];
+    for (int64_t r = 1; r < R; ++r) {
+      const float4 v = p4[r * (N / 4)];
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    reinterpret_cast<float4*>(out)[j0 / 4] = s;
+    return;
+  }
+  for (int64_t j = j0; j < j0 + 4 && j < N; ++j) {
+    float s = parts[j];
+    for (int64_t r = 1; r < R; ++r) s += parts[r * N + j];
+    out[j] = s;
+  }
+}
+
 }  // namespace rmsk
 
 namespace rmsi {
@@ -310,6 +338,14 @@ cudaError_t launch_colreduce2(const float* ws0, float* out0, const float* ws1, f
 cudaError_t launch_colreduce(const float* ws, float* dgamma, int64_t P, int N, int sms,
                              cudaStream_t s) {
   return launch_colreduce2(ws, dgamma, nullptr, nullptr, P, N, sms, s);
+}
+
+cudaError_t launch_rank_sum(const float* parts, float* out, int64_t R, int64_t N,
+                            cudaStream_t s) {
+  const int vec = N % 4 == 0 && !((uintptr_t)parts & 15u) && !((uintptr_t)out & 15u);
+  const int64_t threads = (N + 3) / 4;
+  return rmsk::launch_pdl(rmsk::rms_rank_sum_kernel, dim3((unsigned)((threads + 255) / 256)),
+                          dim3(256), 0, s, parts, out, R, N, vec);
 }
 
 }  // namespace rmsi

@@ -58,6 +58,7 @@ class GpuResult:
     dx: torch.Tensor
     dgamma: torch.Tensor
     guards_ok: bool
+    reduction: tuple  # (partials, rows_per_partial) of the backward's dgamma sum
 
 
 def run_gpu(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None,
@@ -85,7 +86,8 @@ def run_gpu(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None,
     assert st == (rms.RMS_OK if expect_status is None else expect_status), st
     guards = y.guards_intact() and rstd.guards_intact() and dg.guards_intact() and (
         inplace or dx.guards_intact())
-    return GpuResult(y.t, rstd.t, dy if inplace else dx.t, dg.t, guards)
+    red = rms.rms_bwd_reduction(M, N, rms.dtype_code(x, g), w.gemma, 0, bwd_path or path)
+    return GpuResult(y.t, rstd.t, dy if inplace else dx.t, dg.t, guards, red)
 
 
 def oracle_rows(w, inp, rows):
@@ -121,18 +123,32 @@ def sample_rows(M: int, n: int = 48, seed: int = 0) -> np.ndarray:
     return np.array(sorted(rows), dtype=np.int64)
 
 
+def row_blocks(M: int, N: int, rows=None, elems: int = 1 << 22):
+    """The rows to compare (all when ``rows`` is None), in blocks of about
+    ``elems`` elements so that the fp64 oracle's arrays stay small."""
+    rows = np.arange(M, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
+    step = max(1, elems // max(1, N))
+    return [rows[i:i + step] for i in range(0, rows.size, step)]
+
+
+def _take(t: torch.Tensor, rows: np.ndarray) -> np.ndarray:
+    """Host float64 copy of the given rows of a device tensor."""
+    if rows.size and rows[-1] - rows[0] + 1 == rows.size:  # contiguous block: a plain slice
+        return to_host64(t[int(rows[0]):int(rows[-1]) + 1])
+    return to_host64(t.index_select(0, torch.as_tensor(rows, device=t.device)))
+
+
 def check_against_oracle(w, inp, res: GpuResult, rows=None):
-    """All tolerance checks; ``rows`` None compares every row."""
-    rows = np.arange(w.M) if rows is None else rows
-    y_ref, r_ref, dx_ref, dxs = oracle_rows(w, inp, rows)
+    """All tolerance checks; ``rows`` None compares every row (block by block)."""
+    parts = {"y": [], "rstd": [], "dx": []}
+    for blk in row_blocks(w.M, w.N, rows):
+        y_ref, r_ref, dx_ref, dxs = oracle_rows(w, inp, blk)
+        parts["y"].append(compare.check_y(_take(res.y, blk), y_ref, w.dtype))
+        parts["rstd"].append(compare.check_rstd(_take(res.rstd, blk), r_ref))
+        parts["dx"].append(compare.check_dx(_take(res.dx, blk), dx_ref, dxs, w.dtype))
     dg_ref, dgs = oracle_dgamma(w, inp)
-    idx = torch.as_tensor(rows, device=res.y.device)
-    checks = [
-        compare.check_y(to_host64(res.y.index_select(0, idx)), y_ref, w.dtype),
-        compare.check_rstd(to_host64(res.rstd.index_select(0, idx)), r_ref),
-        compare.check_dx(to_host64(res.dx.index_select(0, idx)), dx_ref, dxs, w.dtype),
-        compare.check_dgamma(to_host64(res.dgamma), dg_ref, dgs, w.dtype),
-    ]
+    checks = [compare.merge(parts[k]) for k in ("y", "rstd", "dx")]
+    checks += compare.dgamma_checks(to_host64(res.dgamma), dg_ref, dgs, w.dtype, res.reduction)
     return checks
 
 
@@ -160,6 +176,7 @@ class LnResult:
     dw: torch.Tensor
     db: "torch.Tensor | None"
     guards_ok: bool
+    reduction: tuple  # (partials, rows_per_partial) of the dw and db sums
 
 
 def run_ln(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None, with_db=True,
@@ -188,8 +205,9 @@ def run_ln(w, inp, path="auto", inplace=None, fwd_path=None, bwd_path=None, with
         inplace or dx.guards_intact())
     if not with_db:  # db must be untouched
         guards = guards and bool((db.t.view(torch.int32) == _SENTINEL["f32"]).all())
+    red = rms.ln_bwd_reduction(M, N, rms.dtype_code(x, g), bwd_path or path)
     return LnResult(y.t, mean.t, rstd.t, dy if inplace else dx.t, dw.t,
-                    db.t if with_db else None, guards)
+                    db.t if with_db else None, guards, red)
 
 
 def ln_oracle_rows(w, inp, rows, bias=True):
@@ -203,35 +221,36 @@ def ln_oracle_rows(w, inp, rows, bias=True):
 
 
 def ln_oracle_wsums(w, inp, block_rows: int = 1024):
-    """Oracle dw and db (and their scales) over all M rows, summed over row
-    blocks to bound host memory (each block is the oracle's column sum)."""
+    """Oracle dw and db with their tolerance scales (dw_scale, db_scale, and
+    the tight bar's dw_abs, dw_stat) over all M rows, summed over row blocks
+    to bound host memory (each block is the oracle's column sum)."""
     N = w.N
     g = storage_to_float64(inp["gamma"], w.wdtype)
-    acc = [np.zeros(N) for _ in range(4)]
+    acc = [np.zeros(N) for _ in range(6)]
     for r0 in range(0, w.M, block_rows):
         r1 = min(w.M, r0 + block_rows)
         x = storage_to_float64(inp["x"][r0:r1], w.dtype)
         dy = storage_to_float64(inp["dy"][r0:r1], w.dtype)
         _, dw, db, _, dws, dbs = lno.ln_backward(x, g, dy, w.eps, with_scales=True)
-        for a, v in zip(acc, (dw, db, dws, dbs)):
+        wa, wst = lno.ln_wsum_term_scales(x, dy, w.eps)
+        for a, v in zip(acc, (dw, db, dws, dbs, wa, wst)):
             a += v
     return tuple(acc)
 
 
 def ln_checks(w, inp, res: LnResult, rows=None, bias=True):
-    rows = np.arange(w.M) if rows is None else rows
-    y, mean, rstd, ys, am, dx, dxs = ln_oracle_rows(w, inp, rows, bias)
-    dw, db, dws, dbs = ln_oracle_wsums(w, inp)
-    idx = torch.as_tensor(rows, device=res.y.device)
-    checks = [
-        compare.check_ln_y(to_host64(res.y.index_select(0, idx)), y, ys, w.dtype),
-        compare.check_ln_mean(to_host64(res.mean.index_select(0, idx)), mean, am),
-        compare.check_ln_rstd(to_host64(res.rstd.index_select(0, idx)), rstd),
-        compare.check_ln_dx(to_host64(res.dx.index_select(0, idx)), dx, dxs, w.dtype),
-        compare.check_ln_wsum("dw", to_host64(res.dw), dw, dws, w.dtype),
-    ]
-    if res.db is not None:
-        checks.append(compare.check_ln_wsum("db", to_host64(res.db), db, dbs, w.dtype))
+    parts = {k: [] for k in ("y", "mean", "rstd", "dx")}
+    for blk in row_blocks(w.M, w.N, rows):
+        y, mean, rstd, ys, am, dx, dxs = ln_oracle_rows(w, inp, blk, bias)
+        parts["y"].append(compare.check_ln_y(_take(res.y, blk), y, ys, w.dtype))
+        parts["mean"].append(compare.check_ln_mean(_take(res.mean, blk), mean, am))
+        parts["rstd"].append(compare.check_ln_rstd(_take(res.rstd, blk), rstd))
+        parts["dx"].append(compare.check_ln_dx(_take(res.dx, blk), dx, dxs, w.dtype))
+    dw, db, dws, dbs, wa, wst = ln_oracle_wsums(w, inp)
+    checks = [compare.merge(parts[k]) for k in ("y", "mean", "rstd", "dx")]
+    checks += compare.ln_wsum_checks(
+        to_host64(res.dw), dw, dws, wa, wst,
+        to_host64(res.db) if res.db is not None else None, db, dbs, w.dtype, res.reduction)
     return checks
 
 
@@ -254,6 +273,7 @@ class AddResult:
     dx: torch.Tensor
     dgamma: torch.Tensor
     guards_ok: bool
+    reduction: tuple  # (partials, rows_per_partial) of the dgamma sum
 
 
 def run_fused(w, inp, path="auto", fwd_path=None, bwd_path=None, h_alias=False, dx_alias="none",
@@ -289,7 +309,8 @@ def run_fused(w, inp, path="auto", fwd_path=None, bwd_path=None, h_alias=False, 
     assert rms.rms_last_device_status() == rms.RMS_OK
     guards = y.guards_intact() and rstd.guards_intact() and dg.guards_intact() and (
         h_alias or hbuf.guards_intact()) and (dx_alias != "none" or dxbuf.guards_intact())
-    return AddResult(y.t, rstd.t, h, dx, dg.t, guards)
+    red = rms.rms_bwd_reduction(M, N, rms.dtype_code(x, g), w.gemma, 1, bwd_path or path)
+    return AddResult(y.t, rstd.t, h, dx, dg.t, guards, red)
 
 
 def fused_checks(w, inp, res: AddResult, rows=None):
@@ -322,7 +343,7 @@ def fused_checks(w, inp, res: AddResult, rows=None):
                                with_scales=True)
         total += d
         scale += sc
-    checks.append(compare.check_dgamma(to_host64(res.dgamma), total, scale, w.dtype))
+    checks += compare.dgamma_checks(to_host64(res.dgamma), total, scale, w.dtype, res.reduction)
     return h_bad, checks
 
 

@@ -213,3 +213,40 @@ def test_quant_rejects_bad_arguments(lib):
     assert f(q=A + 4) == INVALID          # codes over x
     assert f(s=3 * A + 8) == INVALID      # scale over the codes
     assert f(M=0, x=None, g=None, q=None, s=None, r=None) == OK
+
+
+def test_reduction_queries_reject_bad_arguments(lib):
+    p, n = ctypes.c_int64(7), ctypes.c_int64(7)
+    P, R = ctypes.byref(p), ctypes.byref(n)
+    q = lambda M=4, N=8, dtype=1, gemma=0, res=0, path=0, a=P, b=R: lib.rms_bwd_reduction(
+        M, N, dtype, gemma, res, path, a, b)
+    assert q(dtype=5) == INVALID
+    assert q(gemma=2) == INVALID
+    assert q(res=2) == INVALID
+    assert q(M=-1) == INVALID
+    assert q(N=0) == INVALID
+    assert q(path=5) == INVALID
+    assert q(a=None) == INVALID
+    assert q(b=None) == INVALID
+    assert q(N=1 << 40) == UNSUPPORTED
+    assert q(M=0) == OK and p.value == 0 and n.value == 0  # no rows: nothing to sum
+    lq = lambda M=4, N=8, dtype=1, path=0, a=P, b=R: lib.ln_bwd_reduction(M, N, dtype, path, a, b)
+    assert lq(dtype=9) == INVALID
+    assert lq(N=-3) == INVALID
+    assert lq(path=1) == UNSUPPORTED  # no register backward mapping
+    assert lq(path=4) == UNSUPPORTED
+    assert lq(a=None) == INVALID
+    p.value = n.value = 7
+    assert lq(M=0) == OK and p.value == 0 and n.value == 0
+
+
+def test_noalloc_answers_bad_shapes_before_its_scratch(lib):
+    # rms_bwd_noalloc(dy, x, gamma, rstd, dx, dgamma, M, N, dtype, gemma, inplace, stream):
+    # a bad shape or flag is rms_bwd's error, found before any device lookup
+    f = lambda M=4, N=8, dtype=1, gemma=0, inplace=0, dg=6 * A: lib.rms_bwd_noalloc(
+        A, 2 * A, 3 * A, 4 * A, 5 * A, dg, M, N, dtype, gemma, inplace, None)
+    assert f(M=-1) == INVALID
+    assert f(N=0) == INVALID
+    assert f(M=0, dtype=7) == INVALID
+    assert f(M=0, gemma=3) == INVALID
+    assert f(M=0, dg=None) == INVALID

@@ -83,11 +83,12 @@ def test_source_hash_ignores_comments_but_not_code():
 
 def test_cpu_baseline_times_each_direction():
     import bench
-    from synthetic import make_inputs, workload
+    from synthetic import workload
 
     w = workload("tiny_f32_64x128")
-    cb = bench.cpu_oracle_throughput(w, make_inputs(w), seconds=0.3, rows=16)
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "GB/s"
+    cb = bench.cpu_oracle_throughput(w, seconds=0.3, rows_per_worker=8, workers=2)
+    assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["unit"] == "GB/s"
+    assert "2 host cores" in cb["sample"]
     assert cb["value"] > 0 and cb["fwd_gbs"] > 0 and cb["bwd_gbs"] > 0
     # the combined rate lies between the two directions' rates
     assert min(cb["fwd_gbs"], cb["bwd_gbs"]) * 0.99 <= cb["value"] <= max(cb["fwd_gbs"],
@@ -116,3 +117,26 @@ def test_workload_spec_from_the_command_line():
                 "M=2,N=8,op=swiglu", "M=2,N8"):
         with pytest.raises(ValueError):
             bench.workload_from_spec(bad)
+
+
+def test_oracle_pool_sums_worker_partials_in_worker_order():
+    """The multi-core oracle's dgamma: each worker's rows, summed in worker
+    order, equal the oracle over all the sample's rows."""
+    import numpy as np
+
+    import bench
+    from oracle import rmsnorm_oracle as orc
+    from synthetic import make_inputs, storage_to_float64, workload
+
+    w = workload("tiny_f32_64x128")
+    pool = bench.OraclePool(w.name, 5, 3)
+    try:
+        _, dg = pool.run("bwd")
+    finally:
+        pool.close()
+    inp = make_inputs(w.with_shape(15))
+    x = storage_to_float64(inp["x"], w.dtype)
+    dy = storage_to_float64(inp["dy"], w.dtype)
+    g = storage_to_float64(inp["gamma"], w.wdtype)
+    _, ref = orc.rms_backward(x, g, dy, w.eps)
+    assert np.allclose(dg, ref, rtol=1e-13, atol=1e-13 * np.abs(ref).max())

@@ -73,22 +73,50 @@ def test_gemma_and_inplace(M, N, dtype, gemma, inplace):
 FULL = [n for n, w in WORKLOADS.items() if w.op == "rms"] if torch.cuda.is_available() else []
 
 
+# Workloads compared on every row at full size (block by block on the host);
+# the others compare sampled rows for y, rstd and dx, and dgamma in full.
+ALL_ROWS = {"tiny_f32_64x128", "llama7b_bf16_8192x4096", "wide_bf16_16384x8192",
+            "gemma_bf16_32768x3072"}
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_workload_full_size(name):
     """Every workload at its full size, in the mapping the benchmark uses."""
     w = WORKLOADS[name]
     inp = H.inputs_for(w)
     res = H.run_gpu(w, inp)
-    rows = None if w.M * w.N <= (1 << 20) else H.sample_rows(w.M)
-    H.assert_parity(w, inp, res, rows)
+    every = name in ALL_ROWS or w.M * w.N <= (1 << 20)
+    H.assert_parity(w, inp, res, None if every else H.sample_rows(w.M))
 
 
 @pytest.mark.parametrize("path", ["registers", "staged"])
 def test_headline_workload_both_mappings(path):
-    """16384 x 8192 bf16 through each vector mapping, full size."""
+    """16384 x 8192 bf16 through each vector mapping, full size, every row."""
     w = WORKLOADS["wide_bf16_16384x8192"]
     inp = H.inputs_for(w)
-    H.assert_parity(w, inp, H.run_gpu(w, inp, path=path), H.sample_rows(w.M))
+    H.assert_parity(w, inp, H.run_gpu(w, inp, path=path))
+
+
+@pytest.mark.parametrize("name", ["wide_bf16_16384x8192", "gemma_bf16_32768x3072"])
+def test_dgamma_bar_sees_dropped_rows(name):
+    """dgamma from the GPU passes the tight and normwise bars; the same
+    dgamma with one row's contribution taken out (a middle row, the last
+    row), or the last eight rows', fails the tight bar."""
+    from oracle import compare
+
+    w = WORKLOADS[name]
+    inp = H.inputs_for(w)
+    res = H.run_gpu(w, inp)
+    ref, scale = H.oracle_dgamma(w, inp)
+    got = H.to_host64(res.dgamma)
+    ok = compare.dgamma_checks(got, ref, scale, w.dtype, res.reduction)
+    assert all(c.ok for c in ok), [str(c) for c in ok]
+    for lo, hi in ((w.M // 2, w.M // 2 + 1), (w.M - 1, w.M), (w.M - 8, w.M)):
+        x = storage_to_float64(inp["x"][lo:hi], w.dtype)
+        dy = storage_to_float64(inp["dy"][lo:hi], w.dtype)
+        part = orc.rms_dgamma(x, dy, w.eps)
+        tight = compare.dgamma_checks(got - part, ref, scale, w.dtype, res.reduction)[2]
+        assert not tight.ok, f"rows {lo}..{hi - 1} dropped: {tight}"
 
 
 def test_dgamma_bitwise_reproducible():
@@ -256,7 +284,8 @@ def test_misaligned_pointers_use_scalar_path(dtype):
     ws = torch.empty(rms.rms_bwd_workspace_size(M, N), dtype=torch.uint8, device="cuda")
     rms.rms_bwd(dy, x, g, r, dx, dg, ws)
     torch.cuda.synchronize()
-    res = H.GpuResult(y, r, dx, dg, True)
+    red = rms.rms_bwd_reduction(M, N, rms.dtype_code(x, g), 0, 0, "scalar")
+    res = H.GpuResult(y, r, dx, dg, True, red)
     H.assert_parity(w, inp, res)
 
 

@@ -104,7 +104,39 @@ def pin_two_pass_variance(o):
     assert abs(1.0 / rstd[0] ** 2 - var_true) <= 1e-7 * var_true
 
 
-ALL_PINS = [pin_torch_float64, pin_finite_differences, pin_invariants, pin_two_pass_variance]
+def pin_wsum_term_scales(o):
+    """The sizes of dw's row terms, by plain loops, and what the second one
+    bounds: moving each row's mean by d (|mean| + mean|x|) and its rstd by a
+    factor (1 + d) changes dw by at most d times it (to first order)."""
+    x, w, b, dy = _case(5, 6, 31)
+    eps = 1e-5
+    s_abs, s_stat = o.ln_wsum_term_scales(x, dy, eps)
+    M, N = x.shape
+    for j in range(N):
+        a = st = 0.0
+        for i in range(M):
+            mu = sum(x[i]) / N
+            var = sum((v - mu) ** 2 for v in x[i]) / N
+            r = 1.0 / (var + eps) ** 0.5
+            xh = (x[i, j] - mu) * r
+            a += abs(dy[i, j] * xh)
+            st += abs(dy[i, j]) * (abs(xh) + (abs(mu) + sum(abs(v) for v in x[i]) / N) * r)
+        assert abs(s_abs[j] - a) <= 1e-13 * a and abs(s_stat[j] - st) <= 1e-13 * st, j
+    _, dw, _ = o.ln_backward(x, w, dy, eps)
+    assert np.all(s_abs >= np.abs(dw) * (1 - 1e-14))
+    mean, rstd = o.ln_stats(x, eps)
+    d = 1e-6
+    rng = np.random.default_rng(4)
+    for _ in range(4):
+        sg1, sg2 = rng.choice([-1.0, 1.0], M), rng.choice([-1.0, 1.0], M)
+        m2 = mean + sg1 * d * (np.abs(mean) + np.mean(np.abs(x), axis=1))
+        r2 = rstd * (1 + sg2 * d)
+        dw2 = np.sum(dy * (x - m2[:, None]) * r2[:, None], axis=0)
+        assert np.all(np.abs(dw2 - dw) <= d * s_stat * (1 + 1e-6))
+
+
+ALL_PINS = [pin_torch_float64, pin_finite_differences, pin_invariants, pin_two_pass_variance,
+            pin_wsum_term_scales]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
