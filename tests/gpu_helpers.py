@@ -315,23 +315,24 @@ def run_fused(w, inp, path="auto", fwd_path=None, bwd_path=None, h_alias=False, 
 
 def fused_checks(w, inp, res: AddResult, rows=None):
     """h bit-for-bit against the oracle's stored sum; y, rstd, dx, dgamma
-    within the bars, with the oracle evaluated on that h."""
-    rows = np.arange(w.M) if rows is None else rows
-    idx = torch.as_tensor(rows, device=res.y.device)
-    x = storage_to_float64(inp["x"][rows], w.dtype)
-    r_in = storage_to_float64(inp["residual"][rows], w.dtype)
+    within the bars, with the oracle evaluated on that h (row blocks; all
+    rows when ``rows`` is None)."""
     g = storage_to_float64(inp["gamma"], w.wdtype)
-    dy = storage_to_float64(inp["dy"][rows], w.dtype)
-    dh = storage_to_float64(inp["dh"][rows], w.dtype)
-    y_ref, r_ref, h_ref = orc.rms_forward_add(x, r_in, g, w.eps, w.gemma, w.dtype)
-    dx_ref, _, dxs, _ = orc.rms_backward_add(h_ref, g, dy, dh, w.eps, w.gemma, with_scales=True)
-    h_got = to_host64(res.h.index_select(0, idx))
-    h_bad = int(np.sum(h_got != h_ref))
-    checks = [
-        compare.check_y(to_host64(res.y.index_select(0, idx)), y_ref, w.dtype),
-        compare.check_rstd(to_host64(res.rstd.index_select(0, idx)), r_ref),
-        compare.check_dx(to_host64(res.dx.index_select(0, idx)), dx_ref, dxs, w.dtype),
-    ]
+    h_bad = 0
+    parts = {"y": [], "rstd": [], "dx": []}
+    for blk in row_blocks(w.M, w.N, rows):
+        x = storage_to_float64(inp["x"][blk], w.dtype)
+        r_in = storage_to_float64(inp["residual"][blk], w.dtype)
+        dy = storage_to_float64(inp["dy"][blk], w.dtype)
+        dh = storage_to_float64(inp["dh"][blk], w.dtype)
+        y_ref, r_ref, h_ref = orc.rms_forward_add(x, r_in, g, w.eps, w.gemma, w.dtype)
+        dx_ref, _, dxs, _ = orc.rms_backward_add(h_ref, g, dy, dh, w.eps, w.gemma,
+                                                 with_scales=True)
+        h_bad += int(np.sum(_take(res.h, blk) != h_ref))
+        parts["y"].append(compare.check_y(_take(res.y, blk), y_ref, w.dtype))
+        parts["rstd"].append(compare.check_rstd(_take(res.rstd, blk), r_ref))
+        parts["dx"].append(compare.check_dx(_take(res.dx, blk), dx_ref, dxs, w.dtype))
+    checks = [compare.merge(parts[k]) for k in ("y", "rstd", "dx")]
     # dgamma over all rows, on the oracle's h
     total = np.zeros(w.N)
     scale = np.zeros(w.N)
