@@ -85,7 +85,8 @@ typedef enum {
                              CTAs in one pass over memory; wider rows take three passes (a
                              row pass, then the outputs from a second read).  Chosen by
                              RMS_PATH_AUTO for rows the others split over a cluster or
-                             cannot take.  rms_fwd_quant: a CTA per row, three passes */
+                             cannot take.  rms_fwd_quant: rows of up to 16 x 32 KiB in
+                             one pass through a cluster, a CTA per row beyond */
 } rms_path;
 
 /*
@@ -292,9 +293,11 @@ rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const floa
  *   bits with bias 7, 3 mantissa bits, no infinities), scale [M] and
  *   rstd [M] float32 written; no output may overlap another argument.
  *   Mappings: RMS_PATH_REGISTERS (16-byte aligned rows and pointers, rows
- *   up to 32 KiB), RMS_PATH_CHUNKED (aligned rows of any width: a CTA per
- *   row, three passes over the row, the second and third served by L2) or
- *   RMS_PATH_SCALAR (any); AUTO picks the first that fits.
+ *   up to 32 KiB), RMS_PATH_CHUNKED (aligned rows of any width: up to 16
+ *   slices of 32 KiB, a cluster of CTAs per row reading it once from HBM,
+ *   the row's sum of squares and maximum |y| exchanged between them; wider
+ *   rows a CTA per row, three passes over the row, the second and third
+ *   served by L2) or RMS_PATH_SCALAR (any); AUTO picks the first that fits.
  * Source: y as rms_fwd; the fusion of the consumer's cast as "02 · 手写
  * Triton kernel:RMSNorm / RoPE / SwiGLU", sections 1-2 (neighbouring
  * elementwise work kept in registers, each tensor read or written once).

@@ -485,20 +485,30 @@ rms_status rms_fwd_quant_ex(const void* x, const void* gamma, uint8_t* q, float*
   if ((path == RMS_PATH_REGISTERS || path == RMS_PATH_CHUNKED) && !aligned)
     return RMS_ERR_ALIGNMENT;
   const bool regs = aligned && rmsi::plan_registers((int)N, dtype, false, &m) && m.threads <= 512;
+  bool wide = false;
   if (path == RMS_PATH_REGISTERS && !regs) return RMS_ERR_UNSUPPORTED;
   if (path == RMS_PATH_SCALAR || !aligned) {
     if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
     m.path = rmsi::kScalar;
   } else if (path == RMS_PATH_CHUNKED || !regs) {
-    // aligned rows too wide for the registers: a CTA per row, three passes
-    if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
-    m.path = rmsi::kChunked;
+    // aligned rows too wide for the registers: one pass in a cluster of CTAs
+    // while the row's slices fit, else a CTA per row walking it three times
+    Mapping mw;
+    if (rmsi::plan_quant_wide((int)N, dtype, &mw)) {
+      wide = true;
+      m = mw;
+    } else {
+      if (M > INT32_MAX) return RMS_ERR_UNSUPPORTED;
+      m.path = rmsi::kChunked;
+    }
   } else if ((M + m.rows_per_cta - 1) / m.rows_per_cta > INT32_MAX) {
     return RMS_ERR_UNSUPPORTED;
   }
   rmsi::QuantArgs a{x, gamma, q, scale, rstd, M, (int)N, eps, (int)dtype, gemma};
-  if (rmsi::launch_fwd_quant(a, m, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return RMS_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const cudaError_t e = wide ? rmsi::launch_fwd_quant_wide(a, m, d, g_wait_limit.load(), s)
+                             : rmsi::launch_fwd_quant(a, m, s);
+  if (e != cudaSuccess) return RMS_ERR_CUDA;
   g_launches.fetch_add(1);
   return RMS_OK;
 }

@@ -27,6 +27,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "e4m3.cuh"
 #include "internal.h"
 #include "tma.cuh"
 
@@ -278,18 +279,25 @@ __device__ __forceinline__ void wide_init(WideExchange& x, int C) {
   }
 }
 
-// This CTA's sum of one float per thread (warps in order): thread c sends it
-// to slot [buf][rank] of CTA c (thread `rank` writes its own CTA's slot and
-// arrives).  `red` alternates with buf, so the one CTA barrier here suffices.
+// This CTA's sum of one float per thread (warps in order), or with MAX its
+// maximum: thread c sends it to slot [buf][rank] of CTA c (thread `rank`
+// writes its own CTA's slot and arrives).  `red` alternates with buf, so the
+// one CTA barrier here suffices.
+template <bool MAX = false>
 __device__ __forceinline__ void wide_publish(float v, float (*red)[kWideWarps], WideExchange& x,
                                              int buf, int rank, int C) {
-  v = warp_sum(v);
+  if (MAX) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  } else {
+    v = warp_sum(v);
+  }
   if ((threadIdx.x & 31) == 0) red[buf][threadIdx.x >> 5] = v;
   __syncthreads();
   if ((int)threadIdx.x < C) {
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWideWarps; ++w) t += red[buf][w];
+    for (int w = 0; w < kWideWarps; ++w) t = MAX ? fmaxf(t, red[buf][w]) : t + red[buf][w];
     const uint32_t bar = smem_u32(&x.bars[buf]);
     if ((int)threadIdx.x == rank) {
       x.slots[buf][rank] = t;
@@ -310,6 +318,8 @@ __device__ __forceinline__ void wide_publish(float v, float (*red)[kWideWarps], 
 // parity `parity`): the slots in rank order.  A wait that runs past `limit`
 // polls raises the status word and then waits out the phase (bounded): the
 // exchange never skips a row, so every CTA keeps the same barrier phases.
+// With MAX the slots' maximum (order-free).
+template <bool MAX = false>
 __device__ __forceinline__ float wide_total(WideExchange& x, int buf, uint32_t parity, int C,
                                             long long limit) {
   const uint32_t bar = smem_u32(&x.bars[buf]);
@@ -318,7 +328,7 @@ __device__ __forceinline__ float wide_total(WideExchange& x, int buf, uint32_t p
     mbar_wait(bar, parity, kDrainPolls);
   }
   float t = 0.f;
-  for (int c = 0; c < C; ++c) t += x.slots[buf][c];
+  for (int c = 0; c < C; ++c) t = MAX ? fmaxf(t, x.slots[buf][c]) : t + x.slots[buf][c];
   return t;
 }
 
@@ -398,6 +408,118 @@ rms_fwd_wide_kernel(const WideParams p) {
       const int v = v0 + k * kWideThreads;
       if (v < NV) {
         st_stream(yr + v, Math::forward(__ldcs(src + v), gs[tid + k * kWideThreads], r));
+      }
+    }
+    row = next;
+  }
+  if (p.C > 1) cluster_sync();
+}
+
+// Forward with an FP8 E4M3 output for rows a CTA cannot hold in registers:
+// the cluster mapping of rms_fwd_wide_kernel (KV = 4, two CTAs per SM), with
+// two exchanges per row instead of one: the slice's sum of squares (giving
+// r), then the slice's maximum of |y| (giving the row's scale).  HBM is read
+// once: each thread keeps its vectors of the current row in shared memory
+// (its own slots, so no barrier) while its registers take the next row's;
+// y is formed twice from them, for the maximum and then for the codes, with
+// the same instructions and so the same values.  The exchanges of a row are consecutive steps of the one slot
+// sequence (step k uses slot and barrier k & 1), so the ordering argument of
+// WideExchange holds step by step.  q is p.out, the per-row scale p.h.
+template <typename T, typename W, bool GEMMA>
+__global__ void __launch_bounds__(kWideThreads, 2)
+rms_fwd_quant_wide_kernel(const WideParams p) {
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
+  constexpr int KV = 4;
+  constexpr int VN = Elem<T>::kPerVec;
+  constexpr int NP = Pairs<T>::n;
+  extern __shared__ __align__(16) uint8_t wide_smem[];
+  GV* gs = reinterpret_cast<GV*>(wide_smem);  // this thread's weights at [t + k*kWideThreads]
+  uint4* xs = reinterpret_cast<uint4*>(wide_smem + (size_t)p.SV * sizeof(GV));  // the row's slice
+  __shared__ float red[2][kWideWarps];
+  __shared__ WideExchange xch;
+  uint8_t* q = static_cast<uint8_t*>(p.out);
+  float* scale = static_cast<float*>(p.h);
+  const int NV = p.N / VN;
+  const int rank = p.C > 1 ? (int)cluster_rank() : 0;
+  const int64_t unit = blockIdx.x / p.C;
+  const int64_t units = gridDim.x / p.C;
+  const int tid = threadIdx.x;
+  const int v0 = rank * p.SV + tid;
+  wide_init(xch, p.C);
+  pdl_wait();
+#pragma unroll
+  for (int k = 0; k < KV; ++k) {
+    const int v = v0 + k * kWideThreads;
+    if (v < NV) gs[tid + k * kWideThreads] = GV::load(p.gamma, v);
+  }
+
+  uint4 a[KV];  // the slice of the next row, as loaded
+  auto fetch = [&](int64_t row) {
+    const uint4* xr = static_cast<const uint4*>(p.x) + row * (int64_t)NV;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = v0 + k * kWideThreads;
+      a[k] = v < NV ? __ldcg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  };
+
+  int64_t row = unit;
+  if (row < p.M) fetch(row);
+  uint32_t step = 0;  // exchanges so far
+  while (row < p.M) {
+    // First pass: the slice's sum of squares; the slice kept on chip.
+    Kahan2 ss;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      if (v0 + k * kWideThreads < NV) {
+        f32x2 t = 0ull;
+        Math::sumsq(a[k], t);
+        ss.add(t);
+        xs[tid + k * kWideThreads] = a[k];
+      }
+    }
+    wide_publish(ss.total(), red, xch, (int)(step & 1), rank, p.C);
+    const int64_t next = row + units;
+    if (next < p.M) fetch(next);  // in flight across both exchanges
+    const float tot = wide_total(xch, (int)(step & 1), (step >> 1) & 1u, p.C, p.wait_limit);
+    ++step;
+    const float r = 1.0f / sqrtf(tot / (float)p.N + p.eps);
+    // Second pass: y and its largest magnitude.
+    AbsMax<T> am;
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int i = tid + k * kWideThreads;
+      if (v0 + k * kWideThreads < NV) am.add(Math::forward(xs[i], gs[i], r));
+    }
+    wide_publish<true>(am.value(), red, xch, (int)(step & 1), rank, p.C);
+    const float amax = wide_total<true>(xch, (int)(step & 1), (step >> 1) & 1u, p.C, p.wait_limit);
+    ++step;
+    const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+    if (rank == 0 && tid == 0) {
+      p.rstd[row] = r;
+      scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    }
+    // Third pass: y again and its codes.
+    uint8_t* qr = q + row * (int64_t)p.N;
+    const f32x2 iv = splat2(inv);
+#pragma unroll
+    for (int k = 0; k < KV; ++k) {
+      const int v = v0 + k * kWideThreads;
+      if (v < NV) {
+        const uint4 yv = Math::forward(xs[tid + k * kWideThreads], gs[tid + k * kWideThreads], r);
+        uint32_t c[NP];
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+          const f32x2 pr = mul2(stored_pair<T>(yv, i), iv);
+          c[i] = f2_to_e4m3x2(lo2(pr), hi2(pr));
+        }
+        if constexpr (NP == 4) {
+          __stcs(reinterpret_cast<uint2*>(qr + (int64_t)v * VN),
+                 make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+        } else {
+          __stcs(reinterpret_cast<unsigned int*>(qr + (int64_t)v * VN), c[0] | (c[1] << 16));
+        }
       }
     }
     row = next;
@@ -698,6 +820,38 @@ static cudaError_t launch_fwd_wide(const FwdArgs& a, const Mapping& m, const Dev
     p.in2 = a.res;
     p.out = a.y;
     p.h = a.h;
+    p.rstd = a.rstd;
+    p.eps = a.eps;
+    p.wait_limit = wait_limit;
+    WideLaunch L(m, U * m.cluster, s);
+    void* args[] = {&p};
+    return cudaLaunchKernelExC(&L.cfg, k, args);
+  });
+}
+
+bool plan_quant_wide(int N, int dtype, Mapping* m) {
+  if (!plan_chunked(N, dtype, false, false, m) || !m->wide || m->kv != 4) return false;
+  m->smem += (size_t)m->sv * 16;  // the row's slice beside the weights
+  return true;
+}
+
+cudaError_t launch_fwd_quant_wide(const QuantArgs& a, const Mapping& m, const DeviceInfo& d,
+                                  long long wait_limit, cudaStream_t s) {
+  return rmsk::with_types(a.dtype, a.gemma, false,
+                         [&](auto* tp, auto* wp, auto gm, auto) -> cudaError_t {
+    using T = std::remove_pointer_t<decltype(tp)>;
+    using W = std::remove_pointer_t<decltype(wp)>;
+    constexpr bool GEMMA = decltype(gm)::value;
+    const void* k = reinterpret_cast<const void*>(&rmsk::rms_fwd_quant_wide_kernel<T, W, GEMMA>);
+    int units = 0;
+    cudaError_t e = wide_units(k, m, d, &units);
+    if (e != cudaSuccess) return e;
+    const int64_t U = std::min<int64_t>(units, a.M);
+    rmsk::WideParams p = wide_params(m, a.M, a.N);
+    p.x = a.x;
+    p.gamma = a.gamma;
+    p.out = a.q;
+    p.h = a.scale;
     p.rstd = a.rstd;
     p.eps = a.eps;
     p.wait_limit = wait_limit;

@@ -129,6 +129,12 @@ struct QuantArgs {
 // m.path kRegisters (plan_registers), kChunked (aligned rows of any width:
 // a CTA per row) or kScalar.
 cudaError_t launch_fwd_quant(const QuantArgs& a, const Mapping& m, cudaStream_t s);
+// Rows too wide for the registers whose slices of 4 x 512 vectors number at
+// most 16: a cluster of CTAs per row, one pass over HBM (chunked.cu).  false
+// when the row needs more slices.
+bool plan_quant_wide(int N, int dtype, Mapping* m);
+cudaError_t launch_fwd_quant_wide(const QuantArgs& a, const Mapping& m, const DeviceInfo& d,
+                                  long long wait_limit, cudaStream_t s);
 
 // ---- LayerNorm (layernorm.cu) ----
 struct LnFwdArgs {

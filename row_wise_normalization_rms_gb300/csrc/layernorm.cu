@@ -516,6 +516,10 @@ cudaError_t ln_occupancy(const void* k, const DeviceInfo& d, int threads, size_t
 #ifndef RMS_LN_BWD_KV2_MAX_NV
 #define RMS_LN_BWD_KV2_MAX_NV 512
 #endif
+// Most threads a backward CTA takes for its rows.
+#ifndef RMS_LN_BWD_MAX_CTA_THREADS
+#define RMS_LN_BWD_MAX_CTA_THREADS 256
+#endif
 bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInfo& d, Mapping* m,
              int64_t M) {
   const int b = dtype_bytes(dtype);
@@ -545,12 +549,14 @@ bool ln_plan(int N, int dtype, bool bwd, int path, bool aligned, const DeviceInf
     if (G <= 512) {
       int R = (int)(16384 / row_bytes);
       R = std::max(1, std::min(R, 16));
-      while (R > 1 && G * R > 256) --R;
+      while (R > 1 && G * R > RMS_LN_BWD_MAX_CTA_THREADS) --R;
       // Halve the tile while the persistent CTAs (two per SM at 256 threads,
-      // by registers) would get fewer than 20 tiles each (a ragged last
-      // wave), down to 8 KiB a tensor (smaller tiles cost more per row than
-      // the tail they save).
-      const int64_t ctas = (int64_t)(G * R <= 256 ? 2 : 1) * d.sms;
+      // four at 128, by registers) would get fewer than 20 tiles each (a
+      // ragged last wave), down to 8 KiB a tensor (smaller tiles cost more
+      // per row than the tail they save).
+      const int per_sm = (RMS_LN_BWD_MAX_CTA_THREADS <= 128 && G * R <= 128) ? 4
+                         : G * R <= 256 ? 2 : 1;
+      const int64_t ctas = (int64_t)per_sm * d.sms;
       while (R > 1 && (R / 2) * row_bytes >= 8192 && M > 0 && (M + R - 1) / R < 20 * ctas)
         R /= 2;
       const int64_t stage = 2 * (int64_t)R * row_bytes;

@@ -150,3 +150,42 @@ def test_quant_full_size_wide_rows():
     inp = H.inputs_for(w)
     q, s, r = run_quant(w, inp)
     assert_quant_parity(w, inp, q, s, r)  # every row
+
+
+@pytest.mark.parametrize("dtype,N,M", [("bf16", 65536, 37), ("bf16", 262144, 9), ("f16", 98304, 11),
+                                       ("f32", 65536, 13), ("bf16w32", 131072, 7)])
+@pytest.mark.parametrize("path", ["auto", "chunked"])
+def test_quant_cluster_mapping(dtype, N, M, path):
+    """Rows of 64 KiB to 512 KiB: a cluster of 2 to 16 CTAs per row, one read
+    of x, the sum of squares and the maximum |y| exchanged between the CTAs."""
+    w = _qw(M, N, dtype, seed=N % 991 + M)
+    inp = H.inputs_for(w)
+    assert_quant_parity(w, inp, *run_quant(w, inp, path))
+    assert rms.rms_last_device_status() == rms.RMS_OK
+
+
+@pytest.mark.parametrize("dtype,N", [("bf16", 1 << 19), ("f32", 270000)])
+def test_quant_rows_beyond_the_cluster(dtype, N):
+    """Rows needing more than 16 slices of 32 KiB (1 MiB bf16, 1.03 MiB f32)
+    fall back to a CTA per row walking the row three times."""
+    w = _qw(3, N, dtype, seed=7)
+    inp = H.inputs_for(w)
+    for path in ("auto", "chunked"):
+        assert_quant_parity(w, inp, *run_quant(w, inp, path))
+
+
+def test_quant_cluster_exchange_wait_limit_reports_status():
+    """The cluster mapping with the poll limit at 0: every exchange wait runs
+    past the limit, so the kernel raises the device status but still waits
+    each exchange out (bounded); the codes still match and the host reads
+    RMS_ERR_TIMEOUT once."""
+    w = _qw(20, 65536, "bf16", seed=21)
+    inp = H.inputs_for(w)
+    prev = rms.rms_set_wait_limit(0)
+    try:
+        q, s, r = run_quant(w, inp, "chunked")
+        assert rms.rms_last_device_status() == rms.RMS_ERR_TIMEOUT
+        assert rms.rms_last_device_status() == rms.RMS_OK  # cleared by the read
+    finally:
+        rms.rms_set_wait_limit(prev)
+    assert_quant_parity(w, inp, q, s, r)
