@@ -200,6 +200,28 @@ rms_status rms_dgamma_combine(const float* parts, int64_t ranks, int64_t N, floa
                               void* stream);
 
 /*
+ * rms_dgamma_cast — the float32 weight gradient handed back in the weight's
+ * own type, as the framework wrapper of the source does after its float32
+ * column sum: out_j = dgamma_j rounded to nearest (ties to even) in the
+ * weight type of `dtype` (bfloat16 for RMS_BF16, float16 for RMS_F16; a
+ * float32 copy for RMS_F32, RMS_BF16_W32 and RMS_F16_W32, whose weight is
+ * float32).  Works for any float32 N-vector: rms_bwd's dgamma, the total of
+ * rms_dgamma_combine, ln_bwd's dw or db.  Values beyond the type's range
+ * round to infinity (bfloat16 and float16 have no saturating cast here).
+ *   dgamma  [N] float32, read.
+ *   out     [N] weight type, written; must not overlap dgamma.
+ * The sums stay float32 everywhere else in the library; this is the one
+ * optional rounding to the weight type.
+ * Source: "Hướng dẫn Triton RMSNorm", section "Reduce dgamma không có race
+ * khi ghi" (the partial sums are reduced in float32 and the result cast to
+ * the weight's dtype by the backward wrapper).
+ * Errors: RMS_ERR_INVALID_ARG (null pointer, N < 1, dtype, overlap),
+ * RMS_ERR_CUDA.
+ */
+rms_status rms_dgamma_cast(const float* dgamma, void* out, int64_t N, rms_dtype dtype,
+                           void* stream);
+
+/*
  * rms_bwd_noalloc — rms_bwd without a caller-provided workspace.  The paper
  * has no counterpart: this entry point exists for callers, not for the
  * method.  It is for callers that cannot obtain device scratch memory

@@ -285,3 +285,23 @@ def ln_wsum_checks(got_dw, dw, dw_scale, dw_abs, dw_stat, got_db, db, db_scale, 
                 check_normwise("db_normwise", got_db, db, TOL[dtype]["dgamma"]),
                 check_sum_tight("db_tight", got_db, db, db_scale, dtype, reduction, 0.0)]
     return out
+
+
+# ---- the weight gradient rounded to the weight's type ----
+
+# Unit roundoff and smallest subnormal spacing of each weight type.
+WEIGHT_ROUNDOFF = {"bf16": (2.0 ** -8, 2.0 ** -133), "f16": (2.0 ** -11, 2.0 ** -24),
+                   "f32": (0.0, 0.0)}
+
+
+def check_weight_cast(got, ref, scale, dtype: str, wdtype: str, reduction) -> Check:
+    """dgamma after its rounding to the weight type ``wdtype``: the tight
+    float32 bar b of the column sum, then one round to nearest in the weight
+    type, |e| <= b + u_w (|ref| + b) + s_w / 2 (u_w the type's unit
+    roundoff, s_w its subnormal spacing)."""
+    ref = np.asarray(ref, np.float64)
+    b = (TOL[dtype]["dgamma"] * np.abs(ref)
+         + (sum_error_factor(reduction) + RMS_TERM_REL) * np.asarray(scale, np.float64))
+    u, s = WEIGHT_ROUNDOFF[wdtype]
+    c = _check("dgamma_cast", got, ref, b + u * (np.abs(ref) + b) + 0.5 * s)
+    return c

@@ -32,6 +32,10 @@ Sources (web pages on row-wise RMS normalisation):
   with h = x + residual as the residual stream stores it (the float32 sum
   rounded once to the I/O dtype) and dx = dRMS + dh.
 
+* The weight gradient in the weight's type ([TUT] § "Reduce dgamma không có
+  race khi ghi": reduced in fp32, then converted to gamma's dtype):
+  ``cast_to_weight_dtype``, pinned by ``tests/test_cast_oracle.py``.
+
 * Output quantised to FP8 E4M3 for the next GEMM (the same fusion principle):
   ``round_e4m3`` / ``e4m3_code`` (the format: sign, 4 exponent bits with
   bias 7, 3 mantissa bits, subnormals, no infinities, largest 448; round to
@@ -183,6 +187,24 @@ def emulate_forward_lowp(x, gamma, eps: float, gemma: int = 0, dtype: str = "bf1
         normed = rnd_w(xr)
         y = rnd(_round_f32(normed.astype(np.float64) * gf[None, :]))
     return y.astype(np.float64)
+
+
+# ---- the weight gradient in the weight's own type ------------------------------
+
+def cast_to_weight_dtype(v, wdtype: str) -> np.ndarray:
+    """float32 values rounded to the weight type ``wdtype`` ("bf16" or "f16";
+    "f32" leaves them unchanged), to nearest with ties to even; values past
+    the type's largest finite one become infinities.  Returned as float64.
+
+    [TUT] § "Reduce dgamma không có race khi ghi": the partial sums are
+    reduced in fp32, and the result is then converted to gamma's dtype.
+    """
+    f = _round_f32(v)
+    if wdtype == "bf16":
+        return _round_bf16(f).astype(np.float64)
+    if wdtype == "f16":
+        return _round_f16(f).astype(np.float64)
+    return f.astype(np.float64)
 
 
 # ---- fused residual add ------------------------------------------------------

@@ -27,7 +27,7 @@ PATHS = {"auto": RMS_PATH_AUTO, "registers": RMS_PATH_REGISTERS, "staged": RMS_P
 
 __all__ = [
     "RmsError", "lib", "rms_fwd", "rms_bwd", "rms_bwd_noalloc", "rms_bwd_workspace_size",
-    "rms_bwd_reduction", "ln_bwd_reduction", "rms_dgamma_combine",
+    "rms_bwd_reduction", "ln_bwd_reduction", "rms_dgamma_combine", "rms_dgamma_cast",
     "rms_status_string",
     "rms_last_device_status", "rms_set_wait_limit", "rms_launch_count", "dtype_code",
 ]
@@ -214,6 +214,34 @@ def rms_dgamma_combine(parts, dgamma, stream=None):
                                   _stream_handle(stream))
     if st != RMS_OK:
         raise RmsError(st, "rms_dgamma_combine")
+
+
+def rms_dgamma_cast(dgamma, out, stream=None):
+    """out (N,) = dgamma (N,) float32 rounded to out's type (bfloat16 or float16,
+    ties to even; a float32 out is a copy): the weight gradient in the weight's
+    own type."""
+    if dgamma.dim() != 1 or out.dim() != 1:
+        raise ValueError("dgamma and out must be 1-D")
+    if dgamma.dtype != _torch().float32:
+        raise ValueError("dgamma must be float32")
+    N = dgamma.numel()
+    dev = dgamma.get_device()
+    if dev < 0:
+        raise ValueError(f"dgamma must be a CUDA tensor, got one on {dgamma.device}")
+    code = {_torch().float32: RMS_F32, _torch().bfloat16: RMS_BF16,
+            _torch().float16: RMS_F16}.get(out.dtype)
+    if code is None:
+        raise ValueError(f"unsupported weight dtype {out.dtype}")
+    st = lib().rms_dgamma_cast(_ptr(dgamma), _arg(out, N * out.element_size(), "out", dev), N,
+                               code, _stream_handle(stream))
+    if st != RMS_OK:
+        raise RmsError(st, "rms_dgamma_cast")
+
+
+def _torch():
+    import torch
+
+    return torch
 
 
 def rms_fwd_add(x, residual, gamma, y, h, rstd, eps: float = 1e-6, gemma: int = 0, stream=None,

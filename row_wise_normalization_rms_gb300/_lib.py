@@ -26,6 +26,7 @@ SIGNATURES = {
                            c_int, c_int, c_int, c_vp]),
     "rms_bwd_reduction": (c_int, [c_i64, c_i64, c_int, c_int, c_int, c_int, c_vp, c_vp]),
     "rms_dgamma_combine": (c_int, [c_vp, c_i64, c_i64, c_vp, c_vp]),
+    "rms_dgamma_cast": (c_int, [c_vp, c_vp, c_i64, c_int, c_vp]),
     "rms_bwd_noalloc": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_int, c_int,
                                 c_int, c_vp]),
     "rms_fwd_add": (c_int, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i64, c_i64, c_float, c_int, c_int,

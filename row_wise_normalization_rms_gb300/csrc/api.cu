@@ -452,6 +452,20 @@ rms_status rms_dgamma_combine(const float* parts, int64_t ranks, int64_t N, floa
   return RMS_OK;
 }
 
+rms_status rms_dgamma_cast(const float* dgamma, void* out, int64_t N, rms_dtype dtype,
+                           void* stream) {
+  if (N < 1 || !dgamma || !out) return RMS_ERR_INVALID_ARG;
+  if (dtype < RMS_F32 || dtype > RMS_F16_W32) return RMS_ERR_INVALID_ARG;
+  if ((N + 3) / 4 > (int64_t)INT32_MAX * 256) return RMS_ERR_UNSUPPORTED;
+  const size_t wb = (size_t)rmsi::weight_bytes(dtype);
+  if (overlap(out, (size_t)N * wb, dgamma, (size_t)N * sizeof(float))) return RMS_ERR_INVALID_ARG;
+  if (rmsi::launch_weight_cast(dgamma, out, N, dtype, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return RMS_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return RMS_OK;
+}
+
 rms_status rms_fwd_quant_ex(const void* x, const void* gamma, uint8_t* q, float* scale,
                             float* rstd, int64_t M, int64_t N, float eps, rms_dtype dtype,
                             int gemma, rms_path path, void* stream) {
@@ -484,7 +498,7 @@ rms_status rms_fwd_quant_ex(const void* x, const void* gamma, uint8_t* q, float*
   Mapping m;
   if ((path == RMS_PATH_REGISTERS || path == RMS_PATH_CHUNKED) && !aligned)
     return RMS_ERR_ALIGNMENT;
-  const bool regs = aligned && rmsi::plan_registers((int)N, dtype, false, &m) && m.threads <= 512;
+  const bool regs = aligned && rmsi::plan_quant_registers((int)N, dtype, &m);
   bool wide = false;
   if (path == RMS_PATH_REGISTERS && !regs) return RMS_ERR_UNSUPPORTED;
   if (path == RMS_PATH_SCALAR || !aligned) {

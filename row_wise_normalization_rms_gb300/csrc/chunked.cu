@@ -287,8 +287,7 @@ template <bool MAX = false>
 __device__ __forceinline__ void wide_publish(float v, float (*red)[kWideWarps], WideExchange& x,
                                              int buf, int rank, int C) {
   if (MAX) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    asm volatile("redux.sync.max.f32 %0, %0, 0xffffffff;" : "+f"(v));  // as fmaxf over the warp
   } else {
     v = warp_sum(v);
   }
@@ -421,8 +420,8 @@ rms_fwd_wide_kernel(const WideParams p) {
 // r), then the slice's maximum of |y| (giving the row's scale).  HBM is read
 // once: each thread keeps its vectors of the current row in shared memory
 // (its own slots, so no barrier) while its registers take the next row's;
-// y is formed twice from them, for the maximum and then for the codes, with
-// the same instructions and so the same values.  The exchanges of a row are consecutive steps of the one slot
+// the pass that finds the maximum replaces them there by y, which the last
+// pass turns into codes.  The exchanges of a row are consecutive steps of the one slot
 // sequence (step k uses slot and barrier k & 1), so the ordering argument of
 // WideExchange holds step by step.  q is p.out, the per-row scale p.h.
 template <typename T, typename W, bool GEMMA>
@@ -473,9 +472,9 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
       if (v0 + k * kWideThreads < NV) {
-        f32x2 t = 0ull;
-        Math::sumsq(a[k], t);
-        ss.add(t);
+        float lo = 0.f, hi = 0.f;
+        SumSqDirect<T>::add(a[k], lo, hi);  // Math::sumsq's operations on the stored values
+        ss.add(pk2(lo, hi));
         xs[tid + k * kWideThreads] = a[k];
       }
     }
@@ -485,12 +484,17 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
     const float tot = wide_total(xch, (int)(step & 1), (step >> 1) & 1u, p.C, p.wait_limit);
     ++step;
     const float r = 1.0f / sqrtf(tot / (float)p.N + p.eps);
-    // Second pass: y and its largest magnitude.
+    // Second pass: y (kept on chip in place of the slice) and its largest
+    // magnitude.
     AbsMax<T> am;
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
       const int i = tid + k * kWideThreads;
-      if (v0 + k * kWideThreads < NV) am.add(Math::forward(xs[i], gs[i], r));
+      if (v0 + k * kWideThreads < NV) {
+        const uint4 yv = Math::forward(xs[i], gs[i], r);
+        xs[i] = yv;
+        am.add(yv);
+      }
     }
     wide_publish<true>(am.value(), red, xch, (int)(step & 1), rank, p.C);
     const float amax = wide_total<true>(xch, (int)(step & 1), (step >> 1) & 1u, p.C, p.wait_limit);
@@ -500,14 +504,14 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
       p.rstd[row] = r;
       scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
     }
-    // Third pass: y again and its codes.
+    // Third pass: the codes of the held y.
     uint8_t* qr = q + row * (int64_t)p.N;
     const f32x2 iv = splat2(inv);
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
       const int v = v0 + k * kWideThreads;
       if (v < NV) {
-        const uint4 yv = Math::forward(xs[tid + k * kWideThreads], gs[tid + k * kWideThreads], r);
+        const uint4 yv = xs[tid + k * kWideThreads];
         uint32_t c[NP];
 #pragma unroll
         for (int i = 0; i < NP; ++i) {

@@ -17,6 +17,46 @@ __device__ __forceinline__ uint32_t f2_to_e4m3x2(float lo, float hi) {
   return d;
 }
 
+// ss_lo += x_lo^2 and ss_hi += x_hi^2 over the element pairs of one vector:
+// the float32 operations of RowMath::sumsq (one fused multiply-add per
+// element on its exact float32 value), taking the 16-bit values as they are
+// stored: a mixed-precision fma (16-bit factors, float32 addend and result)
+// is exact in the product and rounds once, like the fma of the widened
+// values, and leaves no widened copy of x to hold in registers.
+template <typename T>
+struct SumSqDirect {
+  __device__ static __forceinline__ void add(const uint4& x, float& lo, float& hi) {
+    f32x2 ss = pk2(lo, hi);
+    RowMath<T, T, false>::sumsq(x, ss);
+    lo = lo2(ss);
+    hi = hi2(ss);
+  }
+};
+template <>
+struct SumSqDirect<__nv_bfloat16> {
+  __device__ static __forceinline__ void add(const uint4& x, float& lo, float& hi) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+          "fma.rn.f32.bf16 %0, a, a, %0;\n\tfma.rn.f32.bf16 %1, b, b, %1;\n\t}"
+          : "+f"(lo), "+f"(hi) : "r"(w[i]));
+    }
+  }
+};
+template <>
+struct SumSqDirect<__half> {
+  __device__ static __forceinline__ void add(const uint4& x, float& lo, float& hi) {
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+          "fma.rn.f32.f16 %0, a, a, %0;\n\tfma.rn.f32.f16 %1, b, b, %1;\n\t}"
+          : "+f"(lo), "+f"(hi) : "r"(w[i]));
+    }
+  }
+};
+
 // The stored y of one vector widened back to float32 pairs.
 template <typename T>
 __device__ __forceinline__ f32x2 stored_pair(const uint4& yv, int i) {

@@ -99,6 +99,9 @@ cudaError_t launch_colreduce2(const float* ws0, float* out0, const float* ws1, f
                               int64_t P, int N, int sms, cudaStream_t s);
 // out[j] = sum over r < R of parts[r][j], added in increasing r.
 cudaError_t launch_rank_sum(const float* parts, float* out, int64_t R, int64_t N, cudaStream_t s);
+// dst[j] = src[j] in the weight type of `dtype` (bf16 / fp16 rounded to
+// nearest even; float32 copied).
+cudaError_t launch_weight_cast(const float* src, void* dst, int64_t N, int dtype, cudaStream_t s);
 
 // ---- chunked path: rows of any width (chunked.cu) ----
 bool plan_chunked(int N, int dtype, bool bwd, bool res, Mapping* m);
@@ -128,6 +131,8 @@ struct QuantArgs {
 };
 // m.path kRegisters (plan_registers), kChunked (aligned rows of any width:
 // a CTA per row) or kScalar.
+// The register mapping of the E4M3 forward (rows up to 32 KiB).
+bool plan_quant_registers(int N, int dtype, Mapping* m);
 cudaError_t launch_fwd_quant(const QuantArgs& a, const Mapping& m, cudaStream_t s);
 // Rows too wide for the registers whose slices of 4 x 512 vectors number at
 // most 16: a cluster of CTAs per row, one pass over HBM (chunked.cu).  false

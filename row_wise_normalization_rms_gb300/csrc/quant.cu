@@ -20,10 +20,12 @@
 
 namespace rmsk {
 
+// Max over a warp in one instruction (the warp-wide float32 max reduction;
+// like fmaxf it ignores NaN operands).
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  float m;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(m) : "f"(v));
+  return m;
 }
 
 // Max over a group of G threads (as group_sum; max is order-free).
@@ -68,11 +70,11 @@ rms_fwd_quant_registers_kernel(const T* __restrict__ x, const W* __restrict__ ga
     const int j = lig + k * G;
     v[k] = (active && j < NV) ? ld_stream(xr + j) : make_uint4(0u, 0u, 0u, 0u);
   }
-  f32x2 ss2 = 0ull;
+  float ss_lo = 0.f, ss_hi = 0.f;
 #pragma unroll
-  for (int k = 0; k < KV; ++k) Math::sumsq(v[k], ss2);
-  const float ss = (KV == 1 && G < 32) ? lane_group_sum(lo2(ss2) + hi2(ss2), G)
-                                       : group_sum(lo2(ss2) + hi2(ss2), G, grp * (G >> 5), red_s);
+  for (int k = 0; k < KV; ++k) SumSqDirect<T>::add(v[k], ss_lo, ss_hi);
+  const float ss = (KV == 1 && G < 32) ? lane_group_sum(ss_lo + ss_hi, G)
+                                       : group_sum(ss_lo + ss_hi, G, grp * (G >> 5), red_s);
   const float r = 1.0f / sqrtf(ss / (float)N + eps);
   // y as the forward stores it, in place of x; its absolute maximum
   AbsMax<T> am;
@@ -102,6 +104,105 @@ rms_fwd_quant_registers_kernel(const T* __restrict__ x, const W* __restrict__ ga
       for (int i = 0; i < NP; ++i) {
         const f32x2 p = mul2(stored_pair<T>(v[k], i), iv);
         c[i] = f2_to_e4m3x2(lo2(p), hi2(p));
+      }
+      if constexpr (NP == 4) {  // 8 codes
+        *reinterpret_cast<uint2*>(qr + (int64_t)j * VN) =
+            make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+      } else {  // 4 codes
+        *reinterpret_cast<uint32_t*>(qr + (int64_t)j * VN) = c[0] | (c[1] << 16);
+      }
+    }
+  }
+}
+
+// The same row in registers with half the threads: each thread holds the
+// vectors of two of the register forward's threads (Gv threads of four
+// vectors a row; here G = Gv/2 rounded up to a warp, real thread t standing
+// for t and t + G), so every per-row step (the reductions, the square root,
+// the scale's division) is issued by half the warps.  The sum of squares
+// keeps the register forward's order exactly: each stood-for thread's
+// chain, then each stood-for warp's butterfly, then the Gv/32 warp sums in
+// order.  r, and so y, equal rms_fwd's bit for bit.
+template <typename T, typename W, bool GEMMA>
+__global__ void __launch_bounds__(256, 4)
+rms_fwd_quant_pairs_kernel(const T* __restrict__ x, const W* __restrict__ gamma,
+                           uint8_t* __restrict__ q, float* __restrict__ scale,
+                           float* __restrict__ rstd, int64_t M, int N, float eps, int G, int Gv) {
+  using Math = RowMath<T, W, GEMMA>;
+  using GV = GammaVec<T, W>;
+  using P = Pairs<T>;
+  constexpr int VN = Elem<T>::kPerVec;
+  constexpr int NP = P::n;
+  __shared__ float red_s[32], red_m[32];
+  const int NV = N / VN;
+  const int grp = threadIdx.x / G;
+  const int lig = threadIdx.x - grp * G;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / G) + grp;
+  const bool active = row < M;
+  const uint4* xr = reinterpret_cast<const uint4*>(x) + (active ? row : 0) * (int64_t)NV;
+  pdl_trigger();
+  pdl_wait();
+
+  // v[2k + h]: vector k of stood-for thread u_h = lig + h*G, column u_h + k*Gv
+  uint4 v[8];
+  bool ok[8];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int u = lig + h * G;
+      const int j = u + k * Gv;
+      ok[2 * k + h] = active && u < Gv && j < NV;
+      v[2 * k + h] = ok[2 * k + h] ? ld_stream(xr + j) : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  float s_lo[2] = {0.f, 0.f}, s_hi[2] = {0.f, 0.f};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) SumSqDirect<T>::add(v[2 * k + h], s_lo[h], s_hi[h]);
+  }
+  const int nw = G >> 5;              // real warps of a row
+  const int base = grp * 2 * nw;      // this row's slots: stood-for warps 0 .. 2*nw-1
+  const int w = (threadIdx.x >> 5) - grp * nw;
+  const float a0 = warp_sum(s_lo[0] + s_hi[0]);
+  const float a1 = warp_sum(s_lo[1] + s_hi[1]);
+  if ((threadIdx.x & 31) == 0) {
+    red_s[base + w] = a0;
+    red_s[base + nw + w] = a1;
+  }
+  __syncthreads();
+  float ss = 0.f;
+  for (int i = 0; i < (Gv >> 5); ++i) ss += red_s[base + i];
+  const float r = 1.0f / sqrtf(ss / (float)N + eps);
+  // y as the forward stores it, in place of x; its absolute maximum
+  AbsMax<T> am;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int j = lig + (i & 1) * G + (i >> 1) * Gv;
+    if (ok[i]) {
+      v[i] = Math::forward(v[i], GV::load(gamma, j), r);
+      am.add(v[i]);
+    }
+  }
+  const float amax = group_max(am.value(), G, grp * nw, red_m);
+  if (!active) return;  // no barrier follows
+  const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
+  if (lig == 0) {
+    rstd[row] = r;
+    scale[row] = amax > 0.f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+  }
+  uint8_t* qr = q + row * (int64_t)N;
+  const f32x2 iv = splat2(inv);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int j = lig + (i & 1) * G + (i >> 1) * Gv;
+    if (ok[i]) {
+      uint32_t c[NP];
+#pragma unroll
+      for (int e = 0; e < NP; ++e) {
+        const f32x2 p = mul2(stored_pair<T>(v[i], e), iv);
+        c[e] = f2_to_e4m3x2(lo2(p), hi2(p));
       }
       if constexpr (NP == 4) {  // 8 codes
         *reinterpret_cast<uint2*>(qr + (int64_t)j * VN) =
@@ -269,6 +370,32 @@ cudaError_t quant_types(int dtype, int gemma, F&& f) {
 
 namespace rmsi {
 
+// Rows of up to 32 KiB in registers.  Rows of more than 512 vectors take
+// eight vectors a thread (rms_fwd_quant_pairs_kernel: a thread for every
+// two of the register forward's Gv threads), so the per-row work of this
+// kernel (two group reductions, the square root, the scale's division) is
+// spread over twice the data.  m.kv = 8 marks it; m.sv carries Gv.
+// Measured on GB300: 16384 x 8192 bf16 74.1 -> 70.9 us; at 8192 x 4096 the
+// register forward's four vectors a thread stay faster (21.3 against
+// 22.3 us), so narrower rows keep its plan.
+#ifndef RMS_QUANT_KV8_MIN_NV
+#define RMS_QUANT_KV8_MIN_NV 513
+#endif
+bool plan_quant_registers(int N, int dtype, Mapping* m) {
+  if (!plan_registers(N, dtype, false, m)) return false;
+  if (m->threads > 512) return false;
+  const int NV = (int)(((int64_t)N * dtype_bytes(dtype)) / 16);
+  if (NV < RMS_QUANT_KV8_MIN_NV || NV <= 128) return true;
+  const int Gv = m->G;  // >= 64: four vectors a thread, NV > 128
+  const int G = (Gv / 2 + 31) / 32 * 32;
+  m->kv = 8;
+  m->sv = Gv;
+  m->G = G;
+  m->rows_per_cta = 256 / G;
+  m->threads = G * m->rows_per_cta;
+  return true;
+}
+
 cudaError_t launch_fwd_quant(const QuantArgs& a, const Mapping& m, cudaStream_t s) {
   return rmsk::quant_types(a.dtype, a.gemma, [&](auto* tp, auto* wp, auto gm) -> cudaError_t {
     using T = std::remove_pointer_t<decltype(tp)>;
@@ -281,6 +408,7 @@ cudaError_t launch_fwd_quant(const QuantArgs& a, const Mapping& m, cudaStream_t 
       switch (m.kv) {
         case 1: return rmsk::launch_pdl(rmsk::rms_fwd_quant_registers_kernel<T, W, 1, GEMMA>, grid, block, 0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, m.G);
         case 2: return rmsk::launch_pdl(rmsk::rms_fwd_quant_registers_kernel<T, W, 2, GEMMA>, grid, block, 0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, m.G);
+        case 8: return rmsk::launch_pdl(rmsk::rms_fwd_quant_pairs_kernel<T, W, GEMMA>, grid, block, 0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, m.G, m.sv);
         default: return rmsk::launch_pdl(rmsk::rms_fwd_quant_registers_kernel<T, W, 4, GEMMA>, grid, block, 0, s, x, g, a.q, a.scale, a.rstd, a.M, a.N, a.eps, m.G);
       }
     }

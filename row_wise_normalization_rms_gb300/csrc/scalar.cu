@@ -133,6 +133,9 @@ rms_dgamma_colreduce_kernel(const float* __restrict__ ws, float* __restrict__ dg
 // blockIdx.y picks one of two (ws, out) pairs so that two column sums
 // (LayerNorm's dw and db) share one launch.  The order depends only on P and
 // N, so the sums are reproducible bit for bit.
+#ifndef RMS_COLREDUCE_EARLY_TRIGGER
+#define RMS_COLREDUCE_EARLY_TRIGGER 0
+#endif
 __global__ void __launch_bounds__(512)
 rms_colreduce4_kernel(const float4* __restrict__ ws0, float4* __restrict__ out0,
                       const float4* __restrict__ ws1, float4* __restrict__ out1, int64_t P,
@@ -145,6 +148,9 @@ rms_colreduce4_kernel(const float4* __restrict__ ws0, float4* __restrict__ out0,
   const float4* ws = blockIdx.y ? ws1 : ws0;
   float4* out = blockIdx.y ? out1 : out0;
   const int64_t col4 = (int64_t)blockIdx.x * L + cx;
+#if RMS_COLREDUCE_EARLY_TRIGGER
+  pdl_trigger();
+#endif
   pdl_wait();
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col4 < N4) {
@@ -211,6 +217,30 @@ rms_rank_sum_kernel(const float* __restrict__ parts, float* __restrict__ out, in
     for (int64_t r = 1; r < R; ++r) s += parts[r * N + j];
     out[j] = s;
   }
+}
+
+
+// dst[j] = src[j] rounded to the weight type W (round to nearest even; a
+// copy for float32): the float32 column sum handed back in the weight's own
+// type.  Four columns per thread, 16-byte loads when aligned.
+template <typename W>
+__global__ void __launch_bounds__(256)
+rms_weight_cast_kernel(const float* __restrict__ src, W* __restrict__ dst, int64_t N, int vec) {
+  pdl_wait();
+  const int64_t j0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (j0 >= N) return;
+  if (vec) {  // N % 4 == 0, src 16-byte and dst 4 * sizeof(W)-byte aligned
+    const float4 v = reinterpret_cast<const float4*>(src)[j0 / 4];
+    if constexpr (sizeof(W) == 4) {
+      reinterpret_cast<float4*>(dst)[j0 / 4] = v;
+    } else {
+      const uint2 o = make_uint2(Half2Ops<W>::narrow(pk2(v.x, v.y)),
+                                 Half2Ops<W>::narrow(pk2(v.z, v.w)));
+      reinterpret_cast<uint2*>(dst)[j0 / 4] = o;
+    }
+    return;
+  }
+  for (int64_t j = j0; j < j0 + 4 && j < N; ++j) dst[j] = Elem<W>::from_f(src[j]);
 }
 
 }  // namespace rmsk
@@ -346,6 +376,25 @@ cudaError_t launch_rank_sum(const float* parts, float* out, int64_t R, int64_t N
   const int64_t threads = (N + 3) / 4;
   return rmsk::launch_pdl(rmsk::rms_rank_sum_kernel, dim3((unsigned)((threads + 255) / 256)),
                           dim3(256), 0, s, parts, out, R, N, vec);
+}
+
+cudaError_t launch_weight_cast(const float* src, void* dst, int64_t N, int dtype,
+                               cudaStream_t s) {
+  const int wb = weight_bytes(dtype);
+  const int vec = N % 4 == 0 && !((uintptr_t)src & 15u) && !((uintptr_t)dst & (4u * wb - 1u));
+  const int64_t threads = (N + 3) / 4;
+  const dim3 grid((unsigned)((threads + 255) / 256)), block(256);
+  switch (dtype) {
+    case kBF16:
+      return rmsk::launch_pdl(rmsk::rms_weight_cast_kernel<__nv_bfloat16>, grid, block, 0, s, src,
+                              static_cast<__nv_bfloat16*>(dst), N, vec);
+    case kF16:
+      return rmsk::launch_pdl(rmsk::rms_weight_cast_kernel<__half>, grid, block, 0, s, src,
+                              static_cast<__half*>(dst), N, vec);
+    default:
+      return rmsk::launch_pdl(rmsk::rms_weight_cast_kernel<float>, grid, block, 0, s, src,
+                              static_cast<float*>(dst), N, vec);
+  }
 }
 
 }  // namespace rmsi

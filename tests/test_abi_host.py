@@ -250,3 +250,18 @@ def test_noalloc_answers_bad_shapes_before_its_scratch(lib):
     assert f(M=0, dtype=7) == INVALID
     assert f(M=0, gemma=3) == INVALID
     assert f(M=0, dg=None) == INVALID
+
+
+def test_dgamma_cast_rejects_bad_arguments(lib):
+    # rms_dgamma_cast(dgamma, out, N, dtype, stream)
+    f = lambda src=A, dst=2 * A, N=8, dtype=1: lib.rms_dgamma_cast(src, dst, N, dtype, None)
+    assert f(src=None) == INVALID
+    assert f(dst=None) == INVALID
+    assert f(N=0) == INVALID
+    assert f(N=-3) == INVALID
+    assert f(dtype=-1) == INVALID
+    assert f(dtype=5) == INVALID
+    # bf16 output of 8 elements (16 bytes) inside the 32-byte float32 source
+    assert f(dst=A + 16) == INVALID
+    # a float32 output overlapping the source's tail
+    assert f(dst=A + 28, dtype=0) == INVALID

@@ -90,10 +90,14 @@ def test_quant_parity(M, N, dtype, path, gemma):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("path", ["registers", "scalar"])
-def test_quant_equals_unfused_composition(dtype, path):
+@pytest.mark.parametrize("N", [4096, 4104, 8192])
+def test_quant_equals_unfused_composition(dtype, path, N):
     """Codes and scales equal, bit for bit, rms_fwd on the same mapping followed
-    by the quantisation in torch: y * (448 / amax) in float32, then float8."""
-    w = _qw(500, 4096, dtype, seed=4)
+    by the quantisation in torch: y * (448 / amax) in float32, then float8.
+    Rows of more than 512 vectors run with half the register forward's
+    threads, each holding two threads' vectors (4104 bf16: three warps
+    standing for five), and must still sum in its order."""
+    w = _qw(500, N, dtype, seed=4)
     inp = H.inputs_for(w)
     q, s, r = run_quant(w, inp, path)
     x = H.to_device(inp["x"], dtype)
