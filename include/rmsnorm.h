@@ -306,8 +306,11 @@ rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const floa
 
 /*
  * rms_fwd_quant — the forward with its output quantised to FP8 E4M3 in the
- * same pass, for a GEMM that consumes it: y is computed exactly as rms_fwd
- * stores it (same cast order and roundings) but never written; instead
+ * same pass, for a GEMM that consumes it: y is computed as rms_fwd stores it
+ * (same cast order and roundings; r is the same float32 sum of squares,
+ * added in the order of the mapping taken, which for rows of up to 32 KiB
+ * is rms_fwd's own, so there y equals rms_fwd's bit for bit) but never
+ * written; instead
  *   amax_i = max_j |y_ij|,  scale_i = amax_i / 448  (1 for an all-zero row)
  *   q_ij   = e4m3(y_ij * (448 / amax_i))   (float32 multiply, then round to
  *            nearest even, saturating at +-448; y_ij ~ e4m3 value * scale_i)
@@ -316,10 +319,11 @@ rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const floa
  *   rstd [M] float32 written; no output may overlap another argument.
  *   Mappings: RMS_PATH_REGISTERS (16-byte aligned rows and pointers, rows
  *   up to 32 KiB), RMS_PATH_CHUNKED (aligned rows of any width: up to 16
- *   slices of 32 KiB, a cluster of CTAs per row reading it once from HBM,
- *   the row's sum of squares and maximum |y| exchanged between them; wider
- *   rows a CTA per row, three passes over the row, the second and third
- *   served by L2) or RMS_PATH_SCALAR (any); AUTO picks the first that fits.
+ *   slices of 16 KiB, or of 32 KiB for wider rows, a cluster of CTAs per
+ *   row reading it once from HBM, the row's sum of squares and maximum |y|
+ *   exchanged between them; wider rows a CTA per row, three passes over the
+ *   row, the second and third served by L2) or RMS_PATH_SCALAR (any); AUTO
+ *   picks the first that fits.
  * Source: y as rms_fwd; the fusion of the consumer's cast as "02 · 手写
  * Triton kernel:RMSNorm / RoPE / SwiGLU", sections 1-2 (neighbouring
  * elementwise work kept in registers, each tensor read or written once).

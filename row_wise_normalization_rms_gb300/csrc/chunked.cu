@@ -283,8 +283,8 @@ __device__ __forceinline__ void wide_init(WideExchange& x, int C) {
 // maximum: thread c sends it to slot [buf][rank] of CTA c (thread `rank`
 // writes its own CTA's slot and arrives).  `red` alternates with buf, so the
 // one CTA barrier here suffices.
-template <bool MAX = false>
-__device__ __forceinline__ void wide_publish(float v, float (*red)[kWideWarps], WideExchange& x,
+template <bool MAX = false, int NW = kWideWarps>
+__device__ __forceinline__ void wide_publish(float v, float (*red)[NW], WideExchange& x,
                                              int buf, int rank, int C) {
   if (MAX) {
     asm volatile("redux.sync.max.f32 %0, %0, 0xffffffff;" : "+f"(v));  // as fmaxf over the warp
@@ -296,7 +296,7 @@ __device__ __forceinline__ void wide_publish(float v, float (*red)[kWideWarps], 
   if ((int)threadIdx.x < C) {
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWideWarps; ++w) t = MAX ? fmaxf(t, red[buf][w]) : t + red[buf][w];
+    for (int w = 0; w < NW; ++w) t = MAX ? fmaxf(t, red[buf][w]) : t + red[buf][w];
     const uint32_t bar = smem_u32(&x.bars[buf]);
     if ((int)threadIdx.x == rank) {
       x.slots[buf][rank] = t;
@@ -415,7 +415,8 @@ rms_fwd_wide_kernel(const WideParams p) {
 }
 
 // Forward with an FP8 E4M3 output for rows a CTA cannot hold in registers:
-// the cluster mapping of rms_fwd_wide_kernel (KV = 4, two CTAs per SM), with
+// the cluster mapping of rms_fwd_wide_kernel (KV = 4; CTAs of TPB threads,
+// 1024 / TPB of them an SM at least), with
 // two exchanges per row instead of one: the slice's sum of squares (giving
 // r), then the slice's maximum of |y| (giving the row's scale).  HBM is read
 // once: each thread keeps its vectors of the current row in shared memory
@@ -424,8 +425,8 @@ rms_fwd_wide_kernel(const WideParams p) {
 // pass turns into codes.  The exchanges of a row are consecutive steps of the one slot
 // sequence (step k uses slot and barrier k & 1), so the ordering argument of
 // WideExchange holds step by step.  q is p.out, the per-row scale p.h.
-template <typename T, typename W, bool GEMMA>
-__global__ void __launch_bounds__(kWideThreads, 2)
+template <typename T, typename W, bool GEMMA, int TPB>
+__global__ void __launch_bounds__(TPB, 1024 / TPB)
 rms_fwd_quant_wide_kernel(const WideParams p) {
   using Math = RowMath<T, W, GEMMA>;
   using GV = GammaVec<T, W>;
@@ -433,9 +434,9 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
   constexpr int VN = Elem<T>::kPerVec;
   constexpr int NP = Pairs<T>::n;
   extern __shared__ __align__(16) uint8_t wide_smem[];
-  GV* gs = reinterpret_cast<GV*>(wide_smem);  // this thread's weights at [t + k*kWideThreads]
+  GV* gs = reinterpret_cast<GV*>(wide_smem);  // this thread's weights at [t + k*TPB]
   uint4* xs = reinterpret_cast<uint4*>(wide_smem + (size_t)p.SV * sizeof(GV));  // the row's slice
-  __shared__ float red[2][kWideWarps];
+  __shared__ float red[2][TPB / 32];
   __shared__ WideExchange xch;
   uint8_t* q = static_cast<uint8_t*>(p.out);
   float* scale = static_cast<float*>(p.h);
@@ -449,8 +450,8 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
   pdl_wait();
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
-    const int v = v0 + k * kWideThreads;
-    if (v < NV) gs[tid + k * kWideThreads] = GV::load(p.gamma, v);
+    const int v = v0 + k * TPB;
+    if (v < NV) gs[tid + k * TPB] = GV::load(p.gamma, v);
   }
 
   uint4 a[KV];  // the slice of the next row, as loaded
@@ -458,7 +459,7 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
     const uint4* xr = static_cast<const uint4*>(p.x) + row * (int64_t)NV;
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
-      const int v = v0 + k * kWideThreads;
+      const int v = v0 + k * TPB;
       a[k] = v < NV ? __ldcg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
@@ -471,14 +472,14 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
     Kahan2 ss;
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
-      if (v0 + k * kWideThreads < NV) {
+      if (v0 + k * TPB < NV) {
         float lo = 0.f, hi = 0.f;
         SumSqDirect<T>::add(a[k], lo, hi);  // Math::sumsq's operations on the stored values
         ss.add(pk2(lo, hi));
-        xs[tid + k * kWideThreads] = a[k];
+        xs[tid + k * TPB] = a[k];
       }
     }
-    wide_publish(ss.total(), red, xch, (int)(step & 1), rank, p.C);
+    wide_publish<false, TPB / 32>(ss.total(), red, xch, (int)(step & 1), rank, p.C);
     const int64_t next = row + units;
     if (next < p.M) fetch(next);  // in flight across both exchanges
     const float tot = wide_total(xch, (int)(step & 1), (step >> 1) & 1u, p.C, p.wait_limit);
@@ -489,14 +490,14 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
     AbsMax<T> am;
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
-      const int i = tid + k * kWideThreads;
-      if (v0 + k * kWideThreads < NV) {
+      const int i = tid + k * TPB;
+      if (v0 + k * TPB < NV) {
         const uint4 yv = Math::forward(xs[i], gs[i], r);
         xs[i] = yv;
         am.add(yv);
       }
     }
-    wide_publish<true>(am.value(), red, xch, (int)(step & 1), rank, p.C);
+    wide_publish<true, TPB / 32>(am.value(), red, xch, (int)(step & 1), rank, p.C);
     const float amax = wide_total<true>(xch, (int)(step & 1), (step >> 1) & 1u, p.C, p.wait_limit);
     ++step;
     const float inv = amax > 0.f ? __fdiv_rn(448.0f, amax) : 1.0f;
@@ -509,9 +510,9 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
     const f32x2 iv = splat2(inv);
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
-      const int v = v0 + k * kWideThreads;
+      const int v = v0 + k * TPB;
       if (v < NV) {
-        const uint4 yv = xs[tid + k * kWideThreads];
+        const uint4 yv = xs[tid + k * TPB];
         uint32_t c[NP];
 #pragma unroll
         for (int i = 0; i < NP; ++i) {
@@ -714,7 +715,7 @@ struct WideLaunch {
   WideLaunch(const Mapping& m, int64_t grid, cudaStream_t s) {
     cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(rmsk::kWideThreads);
+    cfg.blockDim = dim3(m.threads);
     cfg.dynamicSmemBytes = m.smem;
     cfg.stream = s;
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -767,7 +768,7 @@ static cudaError_t wide_units(const void* k, const Mapping& m, const DeviceInfo&
     WideLaunch L(m, m.cluster, nullptr);
     e = cudaOccupancyMaxActiveClusters(&n, k, &L.cfg);
   } else {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, rmsk::kWideThreads, m.smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, m.threads, m.smem);
     n *= d.sms;
   }
   if (e != cudaSuccess) return e;
@@ -833,9 +834,37 @@ static cudaError_t launch_fwd_wide(const FwdArgs& a, const Mapping& m, const Dev
   });
 }
 
+// The E4M3 cluster forward: slices of four vectors per thread in CTAs of
+// RMS_QUANT_WIDE_THREADS threads (512 when a row needs more than 16 such
+// slices), up to 16 slices a row; each CTA holds its weights and the row's
+// slice in shared memory.  Its row chain (two exchanges and three passes)
+// is long, so smaller CTAs, more of them on an SM, keep more rows in flight.
+#ifndef RMS_QUANT_WIDE_THREADS
+#define RMS_QUANT_WIDE_THREADS 256
+#endif
 bool plan_quant_wide(int N, int dtype, Mapping* m) {
-  if (!plan_chunked(N, dtype, false, false, m) || !m->wide || m->kv != 4) return false;
-  m->smem += (size_t)m->sv * 16;  // the row's slice beside the weights
+  const int64_t row_bytes = (int64_t)N * dtype_bytes(dtype);
+  if (N <= 0 || row_bytes % 16 != 0) return false;
+  const int64_t NV = row_bytes / 16;
+  int TPB = RMS_QUANT_WIDE_THREADS;
+  int64_t C = (NV + 4 * TPB - 1) / (4 * TPB);
+  if (C > rmsk::kWideMaxCluster) {
+    TPB = 512;
+    C = (NV + 4 * TPB - 1) / (4 * TPB);
+  }
+  if (C > rmsk::kWideMaxCluster) return false;  // a CTA per row
+  const int64_t sv = 4 * (int64_t)TPB;
+  const int gv_bytes = (dtype == kBF16W32 || dtype == kF16W32) ? 32 : 16;
+  m->path = kChunked;
+  m->rows_per_cta = 1;
+  m->wide = 1;
+  m->kv = 4;
+  m->threads = TPB;
+  m->G = TPB;
+  m->sv = (int)sv;
+  m->cluster = (int)C;
+  m->chunks = 0;
+  m->smem = (size_t)sv * (gv_bytes + 16);  // the weights and the row's slice
   return true;
 }
 
@@ -846,7 +875,11 @@ cudaError_t launch_fwd_quant_wide(const QuantArgs& a, const Mapping& m, const De
     using T = std::remove_pointer_t<decltype(tp)>;
     using W = std::remove_pointer_t<decltype(wp)>;
     constexpr bool GEMMA = decltype(gm)::value;
-    const void* k = reinterpret_cast<const void*>(&rmsk::rms_fwd_quant_wide_kernel<T, W, GEMMA>);
+    const void* k =
+        m.threads == 512
+            ? reinterpret_cast<const void*>(&rmsk::rms_fwd_quant_wide_kernel<T, W, GEMMA, 512>)
+            : reinterpret_cast<const void*>(
+                  &rmsk::rms_fwd_quant_wide_kernel<T, W, GEMMA, RMS_QUANT_WIDE_THREADS>);
     int units = 0;
     cudaError_t e = wide_units(k, m, d, &units);
     if (e != cudaSuccess) return e;
