@@ -195,6 +195,31 @@ __device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
   return d;
 }
 
+// The exact float32 products of two pairs of 16-bit values (one 32-bit word
+// each, low half first): one mixed-precision fma per element (16-bit factors,
+// float32 addend -0, which leaves every product, signed zeros included, as
+// the float32 multiply of the widened values gives it; the product of two
+// bf16 or two fp16 significands fits a float32 exactly).
+__device__ __forceinline__ f32x2 mul_exact2(uint32_t a, uint32_t b, const __nv_bfloat16*) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, 0f80000000;\n\tfma.rn.f32.bf16 %1, ah, bh, 0f80000000;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(a), "r"(b));
+  return pk2(lo, hi);
+}
+__device__ __forceinline__ f32x2 mul_exact2(uint32_t a, uint32_t b, const __half*) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, 0f80000000;\n\tfma.rn.f32.f16 %1, ah, bh, 0f80000000;\n\t}"
+      : "=f"(lo), "=f"(hi) : "r"(a), "r"(b));
+  return pk2(lo, hi);
+}
+
+// 32-bit word i of a 16-byte vector.
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // Pair conversion and the rounding weight multiply for the 16-bit types.
 template <typename T>
 struct Half2Ops;

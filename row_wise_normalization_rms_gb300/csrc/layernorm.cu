@@ -243,14 +243,22 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
   }
 
   // With four vectors per thread the weight is re-read through L1 at each
-  // use (the partials already take 64 registers); otherwise it is held.
+  // use (the partials already take 64 registers); otherwise it is held,
+  // widened to float32 pairs once.
   constexpr bool kHoldW = KV < 4;
-  GV wv[kHoldW ? KV : 1];
+  // Re-read 16-bit weights meet dy as stored: g = dy*w by mixed-precision fma
+  // (the same exact product), without widening either.
+  constexpr bool kMixedG = !kHoldW && sizeof(T) == 2 && sizeof(W) == 2;
+  f32x2 wf[kHoldW ? KV : 1][NP];
   f32x2 accw[KV][NP], accb[KV][NP];
 #pragma unroll
   for (int k = 0; k < KV; ++k) {
     const int v = lig + k * p.G;
-    if (kHoldW) wv[k] = v < NV ? GV::load(p.w, v) : GV::zero();
+    if (kHoldW) {
+      const GV wk = v < NV ? GV::load(p.w, v) : GV::zero();
+#pragma unroll
+      for (int i = 0; i < NP; ++i) wf[k][i] = wk.pair(i);
+    }
 #pragma unroll
     for (int i = 0; i < NP; ++i) {
       accw[k][i] = 0ull;
@@ -295,12 +303,19 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
         const int v = lig + k * p.G;
         if (v < NV) {
           const uint4 xq = lds128(xs + 16u * v), dq = lds128(ds + 16u * v);
-          const GV wk = kHoldW ? wv[k] : GV::load(p.w, v);
+          const GV wk = kHoldW ? GV::zero() : GV::load(p.w, v);
 #pragma unroll
           for (int e = 0; e < NP; ++e) {
             const f32x2 xh = fma2(P::get(xq, e), rr, nmr);
             const f32x2 d = P::get(dq, e);
-            const f32x2 g = mul2(d, wk.pair(e));
+            f32x2 g;
+            if constexpr (kHoldW) {
+              g = mul2(d, wf[k][e]);
+            } else if constexpr (kMixedG) {
+              g = mul_exact2(word_of(dq, e), wk.word(e), (const T*)nullptr);
+            } else {
+              g = mul2(d, wk.pair(e));
+            }
             s1 = fma2(xh, g, s1);
             s2 = add2(s2, g);
             accw[k][e] = fma2(d, xh, accw[k][e]);
@@ -325,9 +340,14 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
       t1 = warp_sum(v.x);
       t2 = warp_sum(v.y);
     }
-    // dx = (g - (xhat*c1 + c2))*rstd = g*rstd + (xhat*c1r + c2r) with the row
-    // constants c1r = -c1*rstd, c2r = -c2*rstd: two fused multiply-adds
-    const f32x2 c1r = splat2(-t1 * p.inv_n * rs), c2r = splat2(-t2 * p.inv_n * rs);
+    // dx = (g - (xhat*c1 + c2))*rstd = g*rstd + (xhat*c1r + c2r) with
+    // c1r = -c1*rstd, c2r = -c2*rstd, and with xhat = x*rstd - mean*rstd
+    // folded in: g*rstd + (x*ka + kb), ka = rstd*c1r, kb = -mean*rstd*c1r
+    // + c2r (row constants; two fused multiply-adds an element pair).
+    // x*ka + kb cancels like x - mean: its rounding stays within float32
+    // steps of (|x| + |mean|)*rstd*|c1r| + |c2r|.
+    const float c1r = -t1 * p.inv_n * rs, c2r = -t2 * p.inv_n * rs;
+    const f32x2 ka = splat2(rs * c1r), kb = splat2(fmaf(-mu * rs, c1r, c2r));
     if (active) {
       uint4* out = reinterpret_cast<uint4*>(p.dx) + row * (int64_t)NV;
 #pragma unroll
@@ -335,13 +355,19 @@ ln_bwd_staged_kernel(const LnStagedParams p) {
         const int v = lig + k * p.G;
         if (v < NV) {
           const uint4 xq = lds128(xs + 16u * v), dq = lds128(ds + 16u * v);
-          const GV wk = kHoldW ? wv[k] : GV::load(p.w, v);
+          const GV wk = kHoldW ? GV::zero() : GV::load(p.w, v);
           uint32_t o[4];
 #pragma unroll
           for (int e = 0; e < NP; ++e) {
-            const f32x2 xh = fma2(P::get(xq, e), rr, nmr);
-            const f32x2 g = mul2(P::get(dq, e), wk.pair(e));
-            const f32x2 dxe = fma2(g, rr, fma2(xh, c1r, c2r));
+            f32x2 g;
+            if constexpr (kHoldW) {
+              g = mul2(P::get(dq, e), wf[k][e]);
+            } else if constexpr (kMixedG) {
+              g = mul_exact2(word_of(dq, e), wk.word(e), (const T*)nullptr);
+            } else {
+              g = mul2(P::get(dq, e), wk.pair(e));
+            }
+            const f32x2 dxe = fma2(g, rr, fma2(P::get(xq, e), ka, kb));
             if constexpr (sizeof(T) == 2) {
               o[e] = Half2Ops<T>::narrow(dxe);
             } else {
