@@ -314,6 +314,9 @@ template <typename T, typename W>
 using GammaVec = typename GammaSel<T, W>::type;
 
 // ---- per-vector arithmetic ---------------------------------------------------
+#ifndef RMS_MIXED_U
+#define RMS_MIXED_U 1
+#endif
 // Shared by every vector kernel, so all mappings compute identical bits.
 // T: activation type; W: weight type (T, or float with 16-bit T).
 template <typename T, typename W, bool GEMMA>
@@ -326,6 +329,19 @@ struct RowMath {
   __device__ static __forceinline__ f32x2 weight(const G& g, int i) {
     const f32x2 w = g.pair(i);
     return GEMMA ? add2(w, splat2(1.0f)) : w;
+  }
+
+  // u = dy * weight for element pair i.  With 16-bit dy and weight (not
+  // Gemma) the exact product is taken from the stored values by
+  // mixed-precision fma, without widening either; otherwise the float32
+  // multiply of the widened values (the same bits).
+  static constexpr bool kMixedU = RMS_MIXED_U && sizeof(T) == 2 && sizeof(W) == 2 && !GEMMA;
+  __device__ static __forceinline__ f32x2 u_pair(const uint4& dy, const G& g, int i) {
+    if constexpr (kMixedU) {
+      return mul_exact2(word_of(dy, i), g.word(i), (const T*)nullptr);
+    } else {
+      return mul2(P::get(dy, i), weight(g, i));
+    }
   }
 
   // ss += x^2 over the vector.
@@ -374,7 +390,7 @@ struct RowMath {
     for (int i = 0; i < kPairs; ++i) {
       const f32x2 xn = mul2(P::get(x, i), rr);
       const f32x2 d = P::get(dy, i);
-      sux = fma2(mul2(d, weight(g, i)), xn, sux);
+      sux = fma2(kMixedU ? u_pair(dy, g, i) : mul2(d, weight(g, i)), xn, sux);
       acc[i] = fma2(d, xn, acc[i]);
     }
   }
@@ -387,7 +403,7 @@ struct RowMath {
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
       const f32x2 xn = mul2(P::get(x, i), rr);
-      sux = fma2(mul2(P::get(dy, i), weight(g, i)), xn, sux);
+      sux = fma2(u_pair(dy, g, i), xn, sux);
     }
   }
   __device__ static __forceinline__ void backward_acc(const uint4& x, const uint4& dy, float r,
@@ -406,7 +422,7 @@ struct RowMath {
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
       const f32x2 xn = mul2(P::get(x, i), rr);
-      const f32x2 u = mul2(P::get(dy, i), weight(g, i));
+      const f32x2 u = u_pair(dy, g, i);
       const f32x2 dx = mul2(fma2(xn, nk, u), rr);
       if constexpr (sizeof(T) == 2) {
         o[i] = Half2Ops<T>::narrow(dx);
@@ -429,7 +445,7 @@ struct RowMath {
 #pragma unroll
     for (int i = 0; i < kPairs; ++i) {
       const f32x2 xn = mul2(P::get(x, i), rr);
-      const f32x2 u = mul2(P::get(dy, i), weight(g, i));
+      const f32x2 u = u_pair(dy, g, i);
       const f32x2 dx = add2(mul2(fma2(xn, nk, u), rr), P::get(dh, i));
       if constexpr (sizeof(T) == 2) {
         o[i] = Half2Ops<T>::narrow(dx);
