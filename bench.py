@@ -615,9 +615,9 @@ def run_gpu(args):
 # captured with; after any change to their code the traffic reads null.  The
 # hash skips comments and whitespace, which do not reach the compiled code.
 TRAFFIC_CAPTURE = {
-    "src_sha256_16": "b928d924547d5b30",
-    "bwd": 537010688 + 233349632 + 9970176 + 0,  # staged rows kernel + column reduction
-    "fwd": 268471552 + 215364096,                # register-mapping forward
+    "src_sha256_16": "184d4cec90da10fa",
+    "bwd": 537015808 + 233428992 + 9970432 + 11520,  # staged rows kernel + column reduction
+    "fwd": 268473088 + 215949824,                    # register-mapping forward
 }
 
 
