@@ -71,6 +71,13 @@ int main(void) {
   EXPECT(rms_fwd_add(x, NULL, g, y, dy, r, 4, 8, 1e-6f, RMS_BF16, 0, NULL) ==
          RMS_ERR_INVALID_ARG);
 
+  /* the weight-type cast of dgamma: null, size, dtype and overlap checks */
+  EXPECT(rms_dgamma_cast(NULL, y, 8, RMS_BF16, NULL) == RMS_ERR_INVALID_ARG);
+  EXPECT(rms_dgamma_cast(dg, NULL, 8, RMS_BF16, NULL) == RMS_ERR_INVALID_ARG);
+  EXPECT(rms_dgamma_cast(dg, y, 0, RMS_BF16, NULL) == RMS_ERR_INVALID_ARG);
+  EXPECT(rms_dgamma_cast(dg, y, 8, (rms_dtype)5, NULL) == RMS_ERR_INVALID_ARG);
+  EXPECT(rms_dgamma_cast(dg, (char*)dg + 8, 8, RMS_BF16, NULL) == RMS_ERR_INVALID_ARG);
+
   /* sizes of nothing need no device */
   EXPECT(rms_bwd_workspace_size(0, 8) == 0);
   EXPECT(rms_bwd_workspace_size(4, 0) == 0);
