@@ -468,18 +468,18 @@ rms_fwd_quant_wide_kernel(const WideParams p) {
   if (row < p.M) fetch(row);
   uint32_t step = 0;  // exchanges so far
   while (row < p.M) {
-    // First pass: the slice's sum of squares; the slice kept on chip.
-    Kahan2 ss;
+    // First pass: the slice's sum of squares (a thread's four vectors in one
+    // chain per lane, as the register mappings add at most 32 terms a
+    // thread); the slice kept on chip.
+    float ss_lo = 0.f, ss_hi = 0.f;
 #pragma unroll
     for (int k = 0; k < KV; ++k) {
       if (v0 + k * TPB < NV) {
-        float lo = 0.f, hi = 0.f;
-        SumSqDirect<T>::add(a[k], lo, hi);  // Math::sumsq's operations on the stored values
-        ss.add(pk2(lo, hi));
+        SumSqDirect<T>::add(a[k], ss_lo, ss_hi);
         xs[tid + k * TPB] = a[k];
       }
     }
-    wide_publish<false, TPB / 32>(ss.total(), red, xch, (int)(step & 1), rank, p.C);
+    wide_publish<false, TPB / 32>(ss_lo + ss_hi, red, xch, (int)(step & 1), rank, p.C);
     const int64_t next = row + units;
     if (next < p.M) fetch(next);  // in flight across both exchanges
     const float tot = wide_total(xch, (int)(step & 1), (step >> 1) & 1u, p.C, p.wait_limit);
