@@ -31,7 +31,7 @@ def _aw(M, N, dtype, gemma=0, seed=0):
 
 
 SHAPES = [(3, 7), (17, 8), (64, 128), (31, 257), (40, 1000), (300, 2048), (65, 4096),
-          (33, 8192), (5, 16384), (2, 65536)]
+          (33, 8192), (70, 10240), (5, 16384), (2, 65536)]
 PATHS = ["auto", "registers", "staged", "scalar", "chunked"]
 
 

@@ -60,6 +60,19 @@ def test_small_shapes_full_parity(M, N, dtype, path):
     H.assert_parity(w, inp, res)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "bf16w32", "f16w32"])
+@pytest.mark.parametrize("M,N", [(400, 10240), (153, 11008), (300, 12288), (161, 5120)])
+@pytest.mark.parametrize("gemma", [0, 1])
+def test_wide_rows_one_cta_per_sm(M, N, dtype, gemma):
+    """Backward rows that leave the staged mapping one CTA per SM (16-bit rows
+    of 19-24 KiB, float32 rows of 20 KiB) take three vectors a thread; each
+    persistent CTA works through several rows."""
+    w = _w(M, N, dtype, gemma=gemma, seed=M)
+    inp = H.inputs_for(w)
+    for path in ("auto", "staged"):
+        H.assert_parity(w, inp, H.run_gpu(w, inp, path=path))
+
+
 @pytest.mark.parametrize("gemma,inplace", [(0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16", "bf16w32", "f16w32"])
 @pytest.mark.parametrize("M,N", [(257, 3072), (65, 1000), (31, 257)])
