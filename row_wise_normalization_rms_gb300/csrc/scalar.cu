@@ -133,9 +133,6 @@ rms_dgamma_colreduce_kernel(const float* __restrict__ ws, float* __restrict__ dg
 // blockIdx.y picks one of two (ws, out) pairs so that two column sums
 // (LayerNorm's dw and db) share one launch.  The order depends only on P and
 // N, so the sums are reproducible bit for bit.
-#ifndef RMS_COLREDUCE_EARLY_TRIGGER
-#define RMS_COLREDUCE_EARLY_TRIGGER 0
-#endif
 __global__ void __launch_bounds__(512)
 rms_colreduce4_kernel(const float4* __restrict__ ws0, float4* __restrict__ out0,
                       const float4* __restrict__ ws1, float4* __restrict__ out1, int64_t P,
@@ -148,9 +145,6 @@ rms_colreduce4_kernel(const float4* __restrict__ ws0, float4* __restrict__ out0,
   const float4* ws = blockIdx.y ? ws1 : ws0;
   float4* out = blockIdx.y ? out1 : out0;
   const int64_t col4 = (int64_t)blockIdx.x * L + cx;
-#if RMS_COLREDUCE_EARLY_TRIGGER
-  pdl_trigger();
-#endif
   pdl_wait();
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (col4 < N4) {

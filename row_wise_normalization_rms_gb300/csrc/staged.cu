@@ -294,9 +294,6 @@ rms_fwd_staged_kernel(const StagedParams p) {
 }
 
 // With RES, dh is staged after dy and added to dx before its rounding.
-#ifndef RMS_BWD_EARLY_TRIGGER
-#define RMS_BWD_EARLY_TRIGGER 0
-#endif
 template <typename T, typename W, int KV, bool GEMMA, bool RES>
 __global__ void __launch_bounds__(512)
 rms_bwd_staged_kernel(const StagedParams p) {
@@ -364,9 +361,6 @@ rms_bwd_staged_kernel(const StagedParams p) {
     __syncthreads();  // partial sums visible; tile i-1 fully consumed
     if (threadIdx.x == 0 && i >= 1 && issued < my_tiles && !h.abort[buf])
       issue_tile<T, RES ? 3 : 2, true>(p, h, sl, issued++, pol);
-#if RMS_BWD_EARLY_TRIGGER
-    if (i == (my_tiles > p.S ? my_tiles - p.S : 0)) pdl_trigger();  // the last tile is in flight
-#endif
     bool abort;
     const float tot = row_total(p, h, buf, first_warp, nw, sl.rank, &abort);
     if (abort) {
