@@ -308,9 +308,9 @@ rms_status rms_bwd_add_ex(void* dy, const void* h, const void* gamma, const floa
  * rms_fwd_quant — the forward with its output quantised to FP8 E4M3 in the
  * same pass, for a GEMM that consumes it: y is computed as rms_fwd stores it
  * (same cast order and roundings; r is the same float32 sum of squares,
- * added in the order of the mapping taken, which for rows of up to 32 KiB
- * is rms_fwd's own, so there y equals rms_fwd's bit for bit) but never
- * written; instead
+ * added in the order of the mapping taken, which for rows of more than
+ * 2 KiB up to 32 KiB is rms_fwd's own, so there y equals rms_fwd's bit for
+ * bit) but never written; instead
  *   amax_i = max_j |y_ij|,  scale_i = amax_i / 448  (1 for an all-zero row)
  *   q_ij   = e4m3(y_ij * (448 / amax_i))   (float32 multiply, then round to
  *            nearest even, saturating at +-448; y_ij ~ e4m3 value * scale_i)

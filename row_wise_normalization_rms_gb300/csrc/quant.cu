@@ -73,7 +73,7 @@ rms_fwd_quant_registers_kernel(const T* __restrict__ x, const W* __restrict__ ga
   float ss_lo = 0.f, ss_hi = 0.f;
 #pragma unroll
   for (int k = 0; k < KV; ++k) SumSqDirect<T>::add(v[k], ss_lo, ss_hi);
-  const float ss = (KV == 1 && G < 32) ? lane_group_sum(ss_lo + ss_hi, G)
+  const float ss = G < 32 ? lane_group_sum(ss_lo + ss_hi, G)
                                        : group_sum(ss_lo + ss_hi, G, grp * (G >> 5), red_s);
   const float r = 1.0f / sqrtf(ss / (float)N + eps);
   // y as the forward stores it, in place of x; its absolute maximum
@@ -381,17 +381,40 @@ namespace rmsi {
 #ifndef RMS_QUANT_KV8_MIN_NV
 #define RMS_QUANT_KV8_MIN_NV 513
 #endif
+// CTAs of at least this many threads (several rows a CTA when a row has
+// fewer): GB300, 8192 x 4096 bf16 with one 128-thread row a CTA 20.4 us
+// against 21.2 us with two rows in 256-thread CTAs (512: 23.0 us).
+#ifndef RMS_QUANT_MIN_CTA_THREADS
+#define RMS_QUANT_MIN_CTA_THREADS 128
+#endif
+#ifndef RMS_QUANT_NARROW_KV4
+#define RMS_QUANT_NARROW_KV4 1
+#endif
 bool plan_quant_registers(int N, int dtype, Mapping* m) {
   if (!plan_registers(N, dtype, false, m)) return false;
   if (m->threads > 512) return false;
   const int NV = (int)(((int64_t)N * dtype_bytes(dtype)) / 16);
+  if (NV <= 128 && RMS_QUANT_NARROW_KV4) {
+    // Rows of up to 128 vectors: four vectors a lane, a power-of-two group
+    // of lanes a row (several rows a warp), so the per-row work (the two
+    // reductions, the square root, the divisions) is spread over four
+    // vectors a thread instead of one or two.
+    int G = 1;
+    while (4 * G < NV) G *= 2;
+    m->kv = 4;
+    m->G = G;
+  }
+  if (m->G < 256) {
+    m->rows_per_cta = m->G >= RMS_QUANT_MIN_CTA_THREADS ? 1 : RMS_QUANT_MIN_CTA_THREADS / m->G;
+    m->threads = m->G * m->rows_per_cta;
+  }
   if (NV < RMS_QUANT_KV8_MIN_NV || NV <= 128) return true;
   const int Gv = m->G;  // >= 64: four vectors a thread, NV > 128
   const int G = (Gv / 2 + 31) / 32 * 32;
   m->kv = 8;
   m->sv = Gv;
   m->G = G;
-  m->rows_per_cta = 256 / G;
+  m->rows_per_cta = G >= RMS_QUANT_MIN_CTA_THREADS ? 1 : RMS_QUANT_MIN_CTA_THREADS / G;
   m->threads = G * m->rows_per_cta;
   return true;
 }
