@@ -615,9 +615,9 @@ def run_gpu(args):
 # captured with; after any change to their code the traffic reads null.  The
 # hash skips comments and whitespace, which do not reach the compiled code.
 TRAFFIC_CAPTURE = {
-    "src_sha256_16": "879ffc56ffb21867",
-    "bwd": 537001728 + 233359104 + 9970688 + 0,  # staged rows kernel + column reduction
-    "fwd": 268470272 + 215568896,                # register-mapping forward
+    "src_sha256_16": "bf488343656e754c",
+    "bwd": 537020416 + 233731584 + 9970176 + 0,  # staged rows kernel + column reduction
+    "fwd": 268470528 + 215786240,                # register-mapping forward
 }
 
 
